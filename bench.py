@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Benchmark: paged decode attention, us per layer-step and achieved HBM GB/s.
+
+One step = one steady decode step of the whole hot path: the metadata bind,
+then for every layer the KV append, split-KV decode attention and the partial
+merge, captured once as a CUDA graph at fixed workspace addresses and
+replayed.  Default workload: B=4, 24 layers, 32/8 heads, D=128, P=16,
+seq_lens ~ U{512..2048}, run as rounds of 64 consecutive steady steps (the
+lengths are rewound to their start values between rounds).
+
+Prints one JSON line.  ``value`` = algorithmic bytes (K+V of every cached
+token, q and out, per layer) of all timed steps on all ranks / max-over-ranks
+device time.  ``--impl reference`` times the CPU fp64 oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention µs/layer-step and achieved HBM GB/s (% of GB300 peak)"
+DEFAULT_WORKLOAD = "gqa4_b4_paged"
+ROUND = 64  # consecutive steady steps before the lengths are rewound
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1280)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--splits", type=int, default=0, help="0 = pkv_choose_splits")
+    ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+def algorithmic_bytes(lens, p, with_out=True):
+    """K+V bytes of every cached token + q (+ out) bytes, for one layer."""
+    kv = sum(lens) * p.n_kv_heads * p.head_dim * 2 * 2
+    qo = p.batch * p.n_q_heads * p.head_dim * 2
+    return kv + qo + (qo if with_out else 0)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while a region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------ oracle legs --
+
+def _oracle_problem(name, batch):
+    import pkv_inputs as W
+    return W.workload(name, batch=batch, n_layers=1, steps=1)
+
+
+def oracle_layer_step(p, lens_state, pairs):
+    """Oracle attention for the given (b, h) pairs of one layer; returns the
+    algorithmic bytes those pairs account for."""
+    import oracle.ref as R
+    import pkv_inputs as W
+    q, _, _ = W.step_inputs(p, 0, layers=1)
+    kb, vb = lens_state["kb"], lens_state["vb"]
+    R.decode_attention(R.tensor_bits(q)[0], kb, vb, 0, lens_state["slots"], p.scale,
+                       p.n_kv_heads, heads=pairs)
+    full = algorithmic_bytes(lens_state["lens"], p)
+    return full * len(pairs) / (p.batch * p.n_q_heads)
+
+
+def _oracle_state(p):
+    import oracle.ref as R
+    meta = R.bind(p.seq_lens.tolist(), req_pool_indices=p.req_pool_indices.numpy(),
+                  page_table=p.page_table.numpy(), page_size=p.page_size, mode=R.STEADY,
+                  index_mode=R.FLAT if p.index_mode == 1 else R.PAGE_TABLE)
+    lens = meta["seq_lens"]
+    if p.index_mode == 1:
+        slots = [R.token_slots(b, lens[b], index_mode=R.FLAT, kv_indptr=meta["kv_indptr"],
+                               kv_indices=meta["kv_indices"]) for b in range(p.batch)]
+    else:
+        slots = [R.token_slots(b, lens[b], page_table=p.page_table.numpy(),
+                               req_pool_indices=p.req_pool_indices.numpy(),
+                               page_size=p.page_size) for b in range(p.batch)]
+    return {"kb": R.tensor_bits(p.k_pool), "vb": R.tensor_bits(p.v_pool), "lens": lens,
+            "slots": slots}
+
+
+def cpu_baseline_worker(args):
+    """Time the oracle as it stands on one host core for ~cpu_seconds."""
+    p = _oracle_problem(args.workload, args.batch)
+    st = _oracle_state(p)
+    pairs_all = [(b, h) for b in range(p.batch) for h in range(p.n_q_heads)]
+    done_bytes = 0.0
+    n_pairs = 0
+    t0 = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t0 < args.cpu_seconds:
+        chunk = pairs_all[(i * 8) % len(pairs_all):][:8]
+        done_bytes += oracle_layer_step(p, st, chunk)
+        n_pairs += len(chunk)
+        i += 1
+    dt = time.perf_counter() - t0
+    print(json.dumps({"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": 1,
+                      "kind": "oracle",
+                      "sample": f"{n_pairs} (request, query head) attentions of one layer of "
+                                f"{args.workload} (B={p.batch}), {dt:.1f} s on 1 thread"}))
+
+
+def run_cpu_baseline(args):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker", "--workload",
+           args.workload, "--cpu-seconds", str(args.cpu_seconds)]
+    if args.batch:
+        cmd += ["--batch", str(args.batch)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
+    for line in r.stdout.splitlines()[::-1]:
+        if line.startswith("{"):
+            return json.loads(line)
+    return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "failed: " + r.stderr[-200:]}
+
+
+def run_reference(args, rank):
+    """The oracle timed as the reference arm: each step is one bounded sample
+    of (request, head) attentions of one layer of the same workload."""
+    if rank != 0:
+        return
+    p = _oracle_problem(args.workload, args.batch)
+    st = _oracle_state(p)
+    pairs_all = [(b, h) for b in range(p.batch) for h in range(p.n_q_heads)]
+    t = time.perf_counter()
+    oracle_layer_step(p, st, pairs_all[:4])
+    per_pair = max(1e-4, (time.perf_counter() - t) / 4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(len(pairs_all), budget / per_pair)))
+    for i in range(args.warmup):
+        oracle_layer_step(p, st, pairs_all[:n])
+    done = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        off = (i * n) % len(pairs_all)
+        done += oracle_layer_step(p, st, (pairs_all[off:] + pairs_all[:off])[:n])
+    dt = time.perf_counter() - t0
+    v = done / dt / 1e9
+    frac = n / len(pairs_all)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3,
+            "us_per_layer_step": dt / args.steps / frac * 1e6,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "batch": p.batch},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": v, "unit": "GB/s",
+                             "sample": f"each step: {n} of {len(pairs_all)} (request, head) "
+                                       f"attentions of one layer"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- GPU arm --
+
+def traffic_for(kernel_src_hash, workload):
+    """DRAM traffic per attention launch from a committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_attn_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_src_sha1") == kernel_src_hash:
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def kernel_src_hash():
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "paged_kv_decode_bind_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("decode") or name.endswith(".cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import pkv_inputs as W
+    from paged_kv_decode_bind_gb300 import DecodeRunner, Workspace
+    from paged_kv_decode_bind_gb300 import _abi as A
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    p = W.workload(args.workload, batch=args.batch, steps=ROUND,
+                   seed=20260000 + W.WORKLOADS.index(args.workload) + 1 + 1000 * rank)
+    B, NL = p.batch, p.n_layers
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    shape_only = A.PkvWorkspace(n_kv_heads=p.n_kv_heads, max_splits=1 << 20)
+    S = args.splits or A.pkv_choose_splits(shape_only, B, int(p.seq_lens.max()) + ROUND, sms)
+    ws = Workspace.from_problem(p, max_splits=S, device=dev)
+    run = DecodeRunner(ws, B, num_splits=S, flags=args.flags, scale=p.scale)
+    q, k, v = W.step_inputs(p, 0)
+    run.q_in.copy_(q)
+    run.k_in.copy_(k)
+    run.v_in.copy_(v)
+    lens0 = ws.seq_lens[:B].clone()
+    L0 = p.seq_lens.tolist()
+
+    # One graph per position in the round, each with its own events around
+    # every layer's attention kernel.
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext = True
+    except TypeError:
+        ext = False
+    graphs, events = [], []
+    for j in range(ROUND):
+        evs = [(torch.cuda.Event(enable_timing=True, external=ext),
+                torch.cuda.Event(enable_timing=True, external=ext)) for _ in range(NL)]
+        g = run.capture(A.PKV_BIND_STEADY, evs if ext else None)
+        graphs.append(g)
+        events.append(evs)
+    torch.cuda.synchronize()
+
+    def step(i):
+        if i % ROUND == 0:
+            ws.seq_lens[:B].copy_(lens0)
+        graphs[i % ROUND].replay()
+
+    def step_bytes(i):
+        j = i % ROUND
+        lens = [x + j + 1 for x in L0]
+        return NL * algorithmic_bytes(lens, p)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- device-timed region: inputs resident in HBM ----
+    K = args.steps
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        step(i)
+    t_end.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    barrier()
+    dt = t_start.elapsed_time(t_end) / 1e3
+    total_bytes = sum(step_bytes(i) for i in range(K))
+
+    # per-kernel durations of the attention kernel (last replay of each graph)
+    attn_ms, attn_bytes = [], []
+    if ext:
+        last_round = range(max(0, K - ROUND), K)
+        for i in last_round:
+            j = i % ROUND
+            lens = [x + j + 1 for x in L0]
+            for l in range(NL):
+                a, b = events[j][l]
+                attn_ms.append(a.elapsed_time(b))
+                attn_bytes.append(algorithmic_bytes(lens, p, with_out=(S == 1)))
+
+    # ---- end to end: pinned host inputs in, result out, every step ----
+    e2e = None
+    if not args.no_e2e:
+        qh = q.pin_memory()
+        kh = k.pin_memory()
+        vh = v.pin_memory()
+        outh = torch.empty((B, p.n_q_heads, p.head_dim), dtype=torch.bfloat16).pin_memory()
+        for i in range(args.warmup):
+            step(i)
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(K):
+            run.q_in.copy_(qh, non_blocking=True)
+            run.k_in.copy_(kh, non_blocking=True)
+            run.v_in.copy_(vh, non_blocking=True)
+            step(i)
+            outh.copy_(ws.out_bf16(B), non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+        dte = e0.elapsed_time(e1) / 1e3
+        e2e = {"dt": dte, "h2d": q.numel() * 2 + k.numel() * 2 + v.numel() * 2,
+               "d2h": outh.numel() * 2}
+
+    errbits = int(ws.err.item())
+    # max over ranks of the times, sum of the work
+    if world > 1:
+        t = torch.tensor([dt, e2e["dt"] if e2e else 0.0], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt, dte_max = t.tolist()
+        if e2e:
+            e2e["dt"] = dte_max
+        w = torch.tensor([total_bytes], device=dev, dtype=torch.float64)
+        dist.all_reduce(w)
+        total_all = float(w.item())
+    else:
+        total_all = float(total_bytes)
+    if rank != 0:
+        return
+
+    peak, peak_src = peaks()
+    value = total_all / dt / 1e9
+    layer_steps = K * NL
+    roof = None
+    if attn_ms:
+        mean_ms = statistics.fmean(attn_ms)
+        mean_bytes = statistics.fmean(attn_bytes)
+        ach = mean_bytes / (mean_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "traffic": traffic_for(kernel_src_hash(), args.workload),
+                "peak_source": peak_src, "kernel": "decode_simt_kernel",
+                "kernel_us_mean": mean_ms * 1e3, "kernel_launches_timed": len(attn_ms),
+                "algorithmic_bytes_per_launch": mean_bytes}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": dt / K * 1e3,
+        "us_per_layer_step": dt / layer_steps * 1e6,
+        "frac_of_peak": value / peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": B, "n_layers": NL,
+                   "n_q_heads": p.n_q_heads, "n_kv_heads": p.n_kv_heads,
+                   "head_dim": p.head_dim, "page_size": p.page_size,
+                   "seq_lens_start": [min(L0), max(L0), sum(L0)],
+                   "steady_steps_per_round": ROUND, "num_splits": S, "cuda_graph": True,
+                   "l2": "no flush: one step touches %.0f MB of KV, > 129 MB L2" %
+                         (step_bytes(0) / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof,
+        "gpu_launches": run.launches_per_step * K,
+        "clocks": clk,
+        "device_err_bits": errbits,
+    }
+    if e2e:
+        line["e2e"] = {"value": total_all / e2e["dt"] / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = run_cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_baseline_worker:
+        cpu_baseline_worker(args)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[v] = "1"
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * pkv.h -- C ABI of libpkv: batched paged-KV decode attention for GB300 (sm_103a).
+ *
+ * The engine this follows (AstrAI; its commit-log pages for
+ * astrai/inference/core/workspace.py, cache.py and executor.py, cited below as
+ * "<file> page, bullet n") runs one decode step as: bind the per-step metadata
+ * once (cache.py page, bullets 25, 26, 28), then per layer append the new K/V
+ * rows into the 4-D pool (cache.py page, bullets 40-41) and run the split-KV
+ * decode kernel whose partial outputs and running max / sum-exp live in
+ * caller-owned workspace buffers (workspace.py page, bullets 1, 13-18).
+ *
+ * Conventions for every entry point
+ *  - The library allocates nothing and keeps no data between calls.  Every
+ *    buffer is caller-owned device memory at an address that may stay fixed
+ *    for the life of the workspace, so a whole step can be captured once into
+ *    a CUDA graph and replayed (workspace.py page, bullets 6-7, 17-18).
+ *  - Every call is asynchronous on the given stream and never synchronises or
+ *    reads device memory on the host.
+ *  - Problems the host can see (null pointers, sizes beyond the workspace
+ *    capacity, unsupported shapes, misalignment) return a status and launch
+ *    nothing.  Problems only the device can see (an out-of-range page id or
+ *    slot, a length beyond the table's capacity, a wait that ran out) OR a
+ *    bit into the caller's sticky *err word (PKV_DEVERR_*); the affected
+ *    outputs are written as an empty result (zeros) and the kernel returns.
+ *    No kernel traps, asserts or spins without a limit.
+ *  - Element offsets into the pools are computed in 64-bit arithmetic.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID = 1,     /* null pointer, bad size or mode, misaligned buffer */
+  PKV_ERR_UNSUPPORTED = 2, /* head_dim or GQA group size without a kernel     */
+  PKV_ERR_CAPACITY = 3,    /* batch / splits / layers beyond the workspace     */
+  PKV_ERR_CUDA = 4         /* a CUDA runtime call failed (launch error)        */
+} pkv_status;
+
+/* pkv_bind_step modes */
+enum {
+  PKV_BIND_STEADY = 0,     /* position_ids <- seq_lens; seq_lens += 1; rebuild indptr/out_loc */
+  PKV_BIND_REBUILD = 1,    /* take caller-written seq_lens as the new lengths                 */
+  PKV_BIND_APPEND_ONLY = 2 /* only copy new K/V rows to pool[layer, out_loc[b]]              */
+};
+
+/* pkv_workspace.index_mode */
+enum {
+  PKV_IDX_PAGE_TABLE = 0,  /* slot(b,t) = page_table[req_pool_indices[b], t/P]*P + t%P */
+  PKV_IDX_FLAT = 1         /* P == 1: slot(b,t) = kv_indices[kv_indptr[b] + t]         */
+};
+
+/* flags for pkv_decode_attn / pkv_merge_partials */
+enum {
+  PKV_FLAG_OUT_F32 = 1,    /* write `out` as fp32 instead of bf16 (out must be sized for it) */
+  PKV_FLAG_WRITE_LSE = 2,  /* also write lse[b, h] = m + ln(l) (natural log)                */
+  PKV_FLAG_FORCE_SIMT = 4, /* use the CUDA-core kernel even where a tensor-core one exists  */
+  PKV_FLAG_FORCE_MMA = 8   /* use the tensor-core kernel (error if the shape has none)      */
+};
+
+/* bits OR-ed into *err by device code (sticky; the caller clears the word) */
+enum {
+  PKV_DEVERR_PAGE = 1,     /* page id < 0 or >= pool_slots / page_size          */
+  PKV_DEVERR_LEN = 2,      /* seq_len < 0 or > max_pages_per_req * page_size    */
+  PKV_DEVERR_TOTAL = 4,    /* flat mode: kv_indptr[b] + seq_len > max_total_tokens */
+  PKV_DEVERR_SLOT = 8,     /* a flat slot or out_loc outside [0, pool_slots)    */
+  PKV_DEVERR_TIMEOUT = 16  /* a bounded wait on an async copy ran out (~1 s)    */
+};
+
+/*
+ * The workspace: shapes plus caller-owned device buffers (the engine's
+ * InferenceWorkspace, workspace.py page, bullets 14, 17, 22).  Layouts are
+ * dense, row-major, in the element type stated.
+ */
+typedef struct pkv_workspace {
+  int32_t n_layers;          /* NL                                                   */
+  int32_t pool_slots;        /* token slots per layer in each pool ("size")          */
+  int32_t n_q_heads;         /* Hq                                                   */
+  int32_t n_kv_heads;        /* Hkv; Hq % Hkv == 0, G = Hq / Hkv in {1,2,4,8}        */
+  int32_t head_dim;          /* D in {64, 128}                                       */
+  int32_t page_size;         /* P >= 1 tokens per page; pool_slots % P == 0          */
+  int32_t index_mode;        /* PKV_IDX_*                                            */
+  int32_t max_batch;         /* capacity of every [B] buffer                         */
+  int32_t max_reqs;          /* rows of page_table                                   */
+  int32_t max_pages_per_req; /* columns of page_table (tokens per row if P == 1)     */
+  int32_t max_splits;        /* S capacity of o_part / ml_part                       */
+  int32_t max_total_tokens;  /* capacity of kv_indices (flat mode)                   */
+
+  void *k_pool;              /* bf16 [NL, pool_slots, Hkv, D], 16-byte aligned       */
+  void *v_pool;              /* bf16 [NL, pool_slots, Hkv, D], 16-byte aligned       */
+  int32_t *req_pool_indices; /* [max_batch]   page_table row of batch entry b        */
+  int32_t *page_table;       /* [max_reqs, max_pages_per_req] page ids (slots if P==1) */
+  int32_t *seq_lens;         /* [max_batch]   tokens cached incl. the newest; in/out */
+  int32_t *position_ids;     /* [max_batch]   0-based position of the newest token   */
+  int32_t *kv_indptr;        /* [max_batch+1] exclusive prefix sum of seq_lens       */
+  int32_t *out_loc;          /* [max_batch]   slot receiving the newest token        */
+  int32_t *kv_indices;       /* [max_total_tokens] flat slots (flat mode only)       */
+  float *o_part;             /* >= max_batch*Hq*max_splits*D floats; a call with S
+                                splits uses it as dense [batch, Hq, S, D]            */
+  float *ml_part;            /* >= max_batch*Hq*max_splits*2 floats; used as dense
+                                [batch, Hq, S, 2] = (max score, sum exp), ln units   */
+  void *out;                 /* [max_batch, Hq, D] bf16 (fp32 with PKV_FLAG_OUT_F32) */
+  float *lse;                /* [max_batch, Hq] or NULL                               */
+  int32_t *err;              /* one sticky int32 of PKV_DEVERR_* bits                */
+} pkv_workspace;
+
+/*
+ * Bytes the named buffer needs for the shapes in `ws` (pointers ignored).
+ * `which` is a field name ("k_pool", "o_part", "out" -- sized for fp32 --,
+ * ...).  Returns 0 for an unknown name.  Host only; no CUDA call.
+ */
+size_t pkv_workspace_bytes(const pkv_workspace *ws, const char *which);
+
+/*
+ * One per-step metadata bind and/or KV append (cache.py page, bullets 25-28,
+ * 40; workspace.py page, bullet 24).
+ *   batch        entries 0..batch-1 are live (0 <= batch <= max_batch).
+ *   mode         PKV_BIND_STEADY: position_ids[b] = seq_lens[b];
+ *                  seq_lens[b] += 1; kv_indptr = [0, cumsum(seq_lens)];
+ *                  out_loc[b] = slot(b, seq_lens[b]-1); flat mode also rebuilds
+ *                  kv_indices.  All in place, on the device.
+ *                PKV_BIND_REBUILD: as STEADY but seq_lens are taken as written
+ *                  by the caller (no +1) and position_ids = seq_lens - 1.
+ *                PKV_BIND_APPEND_ONLY: no metadata; only the appends below.
+ *   layer_begin, layer_count
+ *                layers [layer_begin, layer_begin+layer_count) receive the new
+ *                rows: K_pool[l, out_loc[b]] = k_new[l-layer_begin, b] (same
+ *                for V).  layer_count may be 0 (no append).
+ *   k_new, v_new bf16 [layer_count, batch, Hkv, D] device, 16-byte aligned;
+ *                may be NULL only when layer_count == 0.
+ * Device errors: PKV_DEVERR_PAGE (bad page id for out_loc; out_loc = -1),
+ * PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT (append skipped).
+ */
+pkv_status pkv_bind_step(const pkv_workspace *ws, int batch, int mode, int layer_begin,
+                         int layer_count, const void *k_new, const void *v_new,
+                         pkv_stream_t stream);
+
+/*
+ * Split count for a batch, host only: S = ceil(3 * num_sms / (batch * Hkv))
+ * so that the (request, KV head, split) units give about three per SM,
+ * clamped so that a split of the longest request (max_seq_len_hint tokens)
+ * holds at least 128 tokens, and to [1, max_splits].  Returns 1 for
+ * non-positive arguments.
+ */
+int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint, int num_sms);
+
+/*
+ * Split-KV GQA decode attention for one layer (workspace.py page, bullets 1,
+ * 14-16).  For every live b and query head h (KV head g = h / G):
+ *   s_t = scale * q[b,h,:] . K[layer, slot(b,t), g, :]   for t < seq_lens[b]
+ *   o   = sum_t softmax(s)_t V[layer, slot(b,t), g, :]
+ *   q           bf16 [batch, Hq, D] device, 16-byte aligned.
+ *   scale       softmax scale (fp32), usually 1/sqrt(D).
+ *   num_splits  S in [1, max_splits].  The KV axis of every request is cut
+ *               into contiguous splits of one common length
+ *               chunk = roundup(ceil(max_b seq_lens[b] / S), gran)
+ *               (gran = P if P >= 16, else the least multiple of P >= 16),
+ *               computed on the device from the live seq_lens.
+ *               S == 1: the result goes straight to `out` (and `lse`).
+ *               S > 1: split s of (b,h) writes o_part[b,h,s,:] (normalised)
+ *               and ml_part[b,h,s,:] = (max score, sum exp(s - max)); splits
+ *               past the end of a request are written empty (-inf, 0);
+ *               pkv_merge_partials then produces `out`.
+ *   flags       PKV_FLAG_* (OUT_F32 and WRITE_LSE apply when S == 1).
+ * Device errors: PKV_DEVERR_PAGE, _LEN, _TOTAL, _SLOT, _TIMEOUT; the affected
+ * (b, KV head, split) is written as empty.
+ */
+pkv_status pkv_decode_attn(const pkv_workspace *ws, int batch, int layer, const void *q,
+                           float scale, int num_splits, int flags, pkv_stream_t stream);
+
+/*
+ * Log-sum-exp merge of the S split partials into out[b,h,:] (and lse[b,h]
+ * with PKV_FLAG_WRITE_LSE):  M = max over non-empty splits of m_s,
+ * w_s = l_s exp(m_s - M), out = sum w_s o_s / sum w_s (workspace.py page,
+ * bullet 14).  A (b,h) with no non-empty split gets zeros and lse = -inf.
+ * num_splits must equal the value given to pkv_decode_attn; with
+ * num_splits == 1 this is a no-op returning PKV_OK.
+ */
+pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits, int flags,
+                              pkv_stream_t stream);
+
+/*
+ * Host steady-state test (cache.py page, bullets 1-4): non-zero when the
+ * task ids are the same, in the same order, as at the last bind and every
+ * length grew by exactly one, so a PKV_BIND_STEADY step is valid; zero means
+ * the caller must write seq_lens and bind with PKV_BIND_REBUILD.
+ * Host arrays; n_prev / n may differ (then the result is 0).
+ */
+int pkv_is_steady_increment(const int64_t *prev_ids, const int32_t *prev_lens, int n_prev,
+                            const int64_t *ids, const int32_t *lens, int n);
+
+/* Static string for a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/* Library version, e.g. "pkv 0.1 sm_103a". */
+const char *pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,191 @@
+// C-ABI entry points of libpkv (declared in include/pkv.h): host-side
+// validation, then kernel launches on the caller's stream.  Nothing here
+// allocates, synchronises or reads device memory.
+#include <cstring>
+
+#include "kernels.cuh"
+
+using namespace pkv;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by every entry point.
+pkv_status check_shape(const pkv_workspace *ws) {
+  if (!ws) return PKV_ERR_INVALID;
+  if (ws->n_layers <= 0 || ws->pool_slots <= 0 || ws->n_q_heads <= 0 || ws->n_kv_heads <= 0 ||
+      ws->head_dim <= 0 || ws->page_size <= 0 || ws->max_batch < 0 || ws->max_reqs <= 0 ||
+      ws->max_pages_per_req <= 0 || ws->max_splits <= 0)
+    return PKV_ERR_INVALID;
+  if (ws->n_q_heads % ws->n_kv_heads != 0) return PKV_ERR_INVALID;
+  if (ws->pool_slots % ws->page_size != 0) return PKV_ERR_INVALID;
+  if (ws->index_mode != PKV_IDX_PAGE_TABLE && ws->index_mode != PKV_IDX_FLAT)
+    return PKV_ERR_INVALID;
+  if (ws->index_mode == PKV_IDX_FLAT && ws->page_size != 1) return PKV_ERR_INVALID;
+  if (ws->head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+  if (!ws->err) return PKV_ERR_INVALID;
+  return PKV_OK;
+}
+
+pkv_status check_index(const pkv_workspace *ws) {
+  if (!ws->seq_lens || !ws->req_pool_indices || !ws->page_table) return PKV_ERR_INVALID;
+  if (ws->index_mode == PKV_IDX_FLAT && (!ws->kv_indptr || !ws->kv_indices || ws->max_total_tokens <= 0))
+    return PKV_ERR_INVALID;
+  return PKV_OK;
+}
+
+pkv_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  return PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_workspace_bytes(const pkv_workspace *ws, const char *which) {
+  if (!ws || !which) return 0;
+  const size_t NL = ws->n_layers > 0 ? ws->n_layers : 0;
+  const size_t slots = ws->pool_slots > 0 ? ws->pool_slots : 0;
+  const size_t hkv = ws->n_kv_heads > 0 ? ws->n_kv_heads : 0;
+  const size_t hq = ws->n_q_heads > 0 ? ws->n_q_heads : 0;
+  const size_t D = ws->head_dim > 0 ? ws->head_dim : 0;
+  const size_t B = ws->max_batch > 0 ? ws->max_batch : 0;
+  const size_t S = ws->max_splits > 0 ? ws->max_splits : 0;
+  const size_t R = ws->max_reqs > 0 ? ws->max_reqs : 0;
+  const size_t MP = ws->max_pages_per_req > 0 ? ws->max_pages_per_req : 0;
+  const size_t T = ws->max_total_tokens > 0 ? ws->max_total_tokens : 0;
+  if (!strcmp(which, "k_pool") || !strcmp(which, "v_pool")) return NL * slots * hkv * D * 2;
+  if (!strcmp(which, "req_pool_indices") || !strcmp(which, "seq_lens") ||
+      !strcmp(which, "position_ids") || !strcmp(which, "out_loc"))
+    return B * 4;
+  if (!strcmp(which, "kv_indptr")) return (B + 1) * 4;
+  if (!strcmp(which, "page_table")) return R * MP * 4;
+  if (!strcmp(which, "kv_indices")) return T * 4;
+  if (!strcmp(which, "o_part")) return B * hq * S * D * 4;
+  if (!strcmp(which, "ml_part")) return B * hq * S * 2 * 4;
+  if (!strcmp(which, "out")) return B * hq * D * 4;
+  if (!strcmp(which, "lse")) return B * hq * 4;
+  if (!strcmp(which, "err")) return 4;
+  return 0;
+}
+
+pkv_status pkv_bind_step(const pkv_workspace *ws, int batch, int mode, int layer_begin,
+                         int layer_count, const void *k_new, const void *v_new,
+                         pkv_stream_t stream) {
+  pkv_status st = check_shape(ws);
+  if (st != PKV_OK) return st;
+  if (mode != PKV_BIND_STEADY && mode != PKV_BIND_REBUILD && mode != PKV_BIND_APPEND_ONLY)
+    return PKV_ERR_INVALID;
+  if (batch < 0) return PKV_ERR_INVALID;
+  if (batch > ws->max_batch || batch > meta_max_batch()) return PKV_ERR_CAPACITY;
+  if (layer_count < 0 || layer_begin < 0) return PKV_ERR_INVALID;
+  if ((long long)layer_begin + layer_count > ws->n_layers) return PKV_ERR_CAPACITY;
+  if (mode != PKV_BIND_APPEND_ONLY) {
+    if ((st = check_index(ws)) != PKV_OK) return st;
+    if (!ws->position_ids || !ws->kv_indptr || !ws->out_loc) return PKV_ERR_INVALID;
+  }
+  if (layer_count > 0) {
+    if (!ws->k_pool || !ws->v_pool || !ws->out_loc || !k_new || !v_new) return PKV_ERR_INVALID;
+    if (!aligned16(ws->k_pool) || !aligned16(ws->v_pool) || !aligned16(k_new) ||
+        !aligned16(v_new))
+      return PKV_ERR_INVALID;
+  }
+  if (batch == 0) return PKV_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (mode != PKV_BIND_APPEND_ONLY) {
+    if ((st = from_cuda(launch_bind_meta(*ws, batch, mode, s))) != PKV_OK) return st;
+    if (ws->index_mode == PKV_IDX_FLAT)
+      if ((st = from_cuda(launch_flat_index(*ws, batch, s))) != PKV_OK) return st;
+  }
+  if (layer_count > 0)
+    return from_cuda(launch_append(*ws, batch, layer_begin, layer_count, k_new, v_new, s));
+  return PKV_OK;
+}
+
+int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint, int num_sms) {
+  if (!ws || batch <= 0 || max_seq_len_hint <= 0 || num_sms <= 0 || ws->n_kv_heads <= 0)
+    return 1;
+  const int min_chunk = 128;
+  const long long hb = (long long)batch * ws->n_kv_heads;
+  const long long target = 3ll * num_sms;
+  long long S = (target + hb - 1) / hb;
+  const long long by_len = (max_seq_len_hint + min_chunk - 1) / min_chunk;
+  if (S > by_len) S = by_len;
+  if (S > ws->max_splits) S = ws->max_splits;
+  if (S < 1) S = 1;
+  return (int)S;
+}
+
+pkv_status pkv_decode_attn(const pkv_workspace *ws, int batch, int layer, const void *q,
+                           float scale, int num_splits, int flags, pkv_stream_t stream) {
+  pkv_status st = check_shape(ws);
+  if (st != PKV_OK) return st;
+  if ((st = check_index(ws)) != PKV_OK) return st;
+  if (batch < 0 || layer < 0 || num_splits < 1) return PKV_ERR_INVALID;
+  if (layer >= ws->n_layers) return PKV_ERR_CAPACITY;
+  if (batch > ws->max_batch || num_splits > ws->max_splits) return PKV_ERR_CAPACITY;
+  const int G = ws->n_q_heads / ws->n_kv_heads;
+  if (!decode_simt_supported(ws->head_dim, G)) return PKV_ERR_UNSUPPORTED;
+  if (flags & PKV_FLAG_FORCE_MMA) return PKV_ERR_UNSUPPORTED;
+  if (!q || !ws->k_pool || !ws->v_pool || !ws->out) return PKV_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(ws->k_pool) || !aligned16(ws->v_pool) || !aligned16(ws->out))
+    return PKV_ERR_INVALID;
+  if (num_splits > 1 && (!ws->o_part || !ws->ml_part || !aligned16(ws->o_part)))
+    return PKV_ERR_INVALID;
+  if ((flags & PKV_FLAG_WRITE_LSE) && !ws->lse) return PKV_ERR_INVALID;
+  if ((long long)num_splits * batch * ws->n_kv_heads > 0x7fffffffll) return PKV_ERR_CAPACITY;
+  if (batch == 0) return PKV_OK;
+  DecodeArgs a;
+  a.ws = *ws;
+  a.batch = batch;
+  a.layer = layer;
+  a.q = q;
+  a.scale = scale;
+  a.num_splits = num_splits;
+  a.flags = flags;
+  return from_cuda(launch_decode_simt(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits, int flags,
+                              pkv_stream_t stream) {
+  pkv_status st = check_shape(ws);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || num_splits < 1) return PKV_ERR_INVALID;
+  if (batch > ws->max_batch || num_splits > ws->max_splits) return PKV_ERR_CAPACITY;
+  if (num_splits == 1 || batch == 0) return PKV_OK;
+  if (ws->head_dim != 64 && ws->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (!ws->o_part || !ws->ml_part || !ws->out) return PKV_ERR_INVALID;
+  if (!aligned16(ws->o_part) || !aligned16(ws->out)) return PKV_ERR_INVALID;
+  if ((flags & PKV_FLAG_WRITE_LSE) && !ws->lse) return PKV_ERR_INVALID;
+  return from_cuda(launch_merge(*ws, batch, num_splits, flags,
+                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pkv_is_steady_increment(const int64_t *prev_ids, const int32_t *prev_lens, int n_prev,
+                            const int64_t *ids, const int32_t *lens, int n) {
+  if (!prev_ids || !prev_lens || !ids || !lens) return 0;
+  if (n <= 0 || n != n_prev) return 0;
+  for (int i = 0; i < n; ++i) {
+    if (prev_ids[i] != ids[i]) return 0;
+    if ((long long)lens[i] != (long long)prev_lens[i] + 1) return 0;
+  }
+  return 1;
+}
+
+const char *pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape";
+    case PKV_ERR_CAPACITY: return "beyond workspace capacity";
+    case PKV_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+const char *pkv_version(void) { return "pkv 0.1 sm_103a"; }
+
+}  // extern "C"

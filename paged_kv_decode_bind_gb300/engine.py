@@ -1,0 +1,103 @@
+"""One decode step over every layer, as the engine's executor runs it.
+
+Step = metadata bind once (cache.py page, bullets 25-28), then for each layer
+the KV append (cache.py page, bullet 40), split-KV decode attention and the
+partial merge (workspace.py page, bullets 1 and 14).  Inputs live in static
+buffers owned by the runner so a whole step can be captured once into a CUDA
+graph and replayed at fixed addresses (workspace.py page, bullets 6-7; one
+graph per batch size, executor.py page, bullets 4-5, 7-8).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _abi
+from .workspace import Workspace
+
+
+class BindTracker:
+    """Host record of the last bind (the engine's _BindState; cache.py page,
+    bullets 1-4): picks STEADY when the same tasks each grew by one token."""
+
+    def __init__(self):
+        self.ids = None
+        self.lens = None
+
+    def mode(self, ids, lens):
+        steady = _abi.pkv_is_steady_increment(self.ids, self.lens, list(ids), list(lens))
+        self.ids, self.lens = list(ids), list(lens)
+        return _abi.PKV_BIND_STEADY if steady else _abi.PKV_BIND_REBUILD
+
+
+class DecodeRunner:
+    """Drives libpkv for one batch size on one stream."""
+
+    def __init__(self, ws: Workspace, batch: int, *, num_splits: int = 1, flags: int = 0,
+                 scale: float | None = None, stream: torch.cuda.Stream | None = None):
+        self.ws = ws
+        self.batch = batch
+        sh = ws.shape
+        self.num_splits = num_splits
+        self.flags = flags
+        self.scale = scale if scale is not None else sh["head_dim"] ** -0.5
+        self.stream = stream
+        NL, B = sh["n_layers"], batch
+        dev = ws.device
+        self.q_in = torch.zeros((NL, B, sh["n_q_heads"], sh["head_dim"]), dtype=torch.bfloat16,
+                                device=dev)
+        self.k_in = torch.zeros((NL, B, sh["n_kv_heads"], sh["head_dim"]), dtype=torch.bfloat16,
+                                device=dev)
+        self.v_in = torch.zeros_like(self.k_in)
+        self.graph = None
+        flat = sh["index_mode"] == _abi.PKV_IDX_FLAT
+        # kernels one step launches: bind (+ flat index build), then per layer
+        # append + attention (+ merge when split)
+        self.launches_per_step = 1 + int(flat) + NL * (2 + (1 if num_splits > 1 else 0))
+
+    # --- pieces -------------------------------------------------------------
+    def bind(self, mode=_abi.PKV_BIND_STEADY):
+        _abi.pkv_bind_step(self.ws, self.batch, mode, 0, 0, None, None, self._s())
+
+    def layer(self, l, events=None):
+        s = self._s()
+        _abi.pkv_bind_step(self.ws, self.batch, _abi.PKV_BIND_APPEND_ONLY, l, 1, self.k_in[l],
+                           self.v_in[l], s)
+        if events is not None:
+            events[0].record(s)
+        _abi.pkv_decode_attn(self.ws, self.batch, l, self.q_in[l], self.scale, self.num_splits,
+                             self.flags, s)
+        if events is not None:
+            events[1].record(s)
+        if self.num_splits > 1:
+            _abi.pkv_merge_partials(self.ws, self.batch, self.num_splits, self.flags, s)
+
+    def step(self, mode=_abi.PKV_BIND_STEADY, layer_events=None):
+        """Bind, then every layer.  ``layer_events[l]`` = (start, end) CUDA
+        events recorded around that layer's attention kernel."""
+        self.bind(mode)
+        for l in range(self.ws.shape["n_layers"]):
+            self.layer(l, None if layer_events is None else layer_events[l])
+
+    # --- CUDA graph -----------------------------------------------------------
+    def capture(self, mode=_abi.PKV_BIND_STEADY, layer_events=None):
+        """Capture one whole step (bind + all layers) into a CUDA graph.
+
+        ``layer_events[l]`` (events made with ``external=True``) become event
+        record nodes around layer l's attention kernel."""
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=self.ws.device)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                self.step(mode, layer_events)
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+
+    def _s(self):
+        if self.stream is not None:
+            return self.stream
+        return torch.cuda.current_stream()

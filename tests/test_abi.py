@@ -1,0 +1,127 @@
+"""libpkv loads, exports every symbol include/pkv.h declares, and rejects bad
+arguments on the host (no GPU needed: every call here fails validation or is
+host-only, so nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_decode_bind_gb300 as P
+from paged_kv_decode_bind_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_match_header():
+    lib = _abi.load()
+    declared = _declared()
+    assert declared, "no declarations parsed"
+    assert sorted(_abi.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_struct_layout():
+    # 12 int32 shape fields then 14 pointers, no padding on LP64.
+    assert ctypes.sizeof(_abi.PkvWorkspace) == 12 * 4 + 14 * 8
+    assert _abi.PkvWorkspace.k_pool.offset == 48
+
+
+def _ws(**kw):
+    shape = dict(n_layers=2, pool_slots=64, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                 page_size=16, index_mode=0, max_batch=4, max_reqs=8, max_pages_per_req=4,
+                 max_splits=4, max_total_tokens=0)
+    fake = 1 << 20  # non-null, 16-byte aligned; never dereferenced (validation fails first)
+    ptrs = dict(k_pool=fake, v_pool=fake, req_pool_indices=fake, page_table=fake,
+                seq_lens=fake, position_ids=fake, kv_indptr=fake, out_loc=fake,
+                kv_indices=fake, o_part=fake, ml_part=fake, out=fake, lse=fake, err=fake)
+    shape.update({k: v for k, v in kw.items() if k in shape})
+    ptrs.update({k: v for k, v in kw.items() if k in ptrs})
+    return _abi.PkvWorkspace(**shape, **ptrs)
+
+
+def test_workspace_bytes():
+    ws = _ws()
+    assert P.pkv_workspace_bytes(ws, "k_pool") == 2 * 64 * 2 * 128 * 2
+    assert P.pkv_workspace_bytes(ws, "o_part") == 4 * 8 * 4 * 128 * 4
+    assert P.pkv_workspace_bytes(ws, "ml_part") == 4 * 8 * 4 * 2 * 4
+    assert P.pkv_workspace_bytes(ws, "kv_indptr") == 5 * 4
+    assert P.pkv_workspace_bytes(ws, "page_table") == 8 * 4 * 4
+    assert P.pkv_workspace_bytes(ws, "out") == 4 * 8 * 128 * 4
+    assert P.pkv_workspace_bytes(ws, "nope") == 0
+
+
+@pytest.mark.parametrize("kw,batch,layer,splits,flags,status", [
+    (dict(head_dim=96), 1, 0, 1, 0, P.PKV_ERR_UNSUPPORTED),
+    (dict(n_q_heads=24, n_kv_heads=2), 1, 0, 1, 0, P.PKV_ERR_UNSUPPORTED),   # G = 12
+    (dict(n_q_heads=7), 1, 0, 1, 0, P.PKV_ERR_INVALID),                      # Hq % Hkv
+    (dict(), 5, 0, 1, 0, P.PKV_ERR_CAPACITY),                                # batch > max
+    (dict(), 1, 2, 1, 0, P.PKV_ERR_CAPACITY),                                # layer >= NL
+    (dict(), 1, 0, 5, 0, P.PKV_ERR_CAPACITY),                                # splits > max
+    (dict(), 1, 0, 0, 0, P.PKV_ERR_INVALID),                                 # splits < 1
+    (dict(err=None), 1, 0, 1, 0, P.PKV_ERR_INVALID),
+    (dict(k_pool=(1 << 20) + 8), 1, 0, 1, 0, P.PKV_ERR_INVALID),             # misaligned
+    (dict(o_part=None), 1, 0, 2, 0, P.PKV_ERR_INVALID),
+    (dict(lse=None), 1, 0, 1, P.PKV_FLAG_WRITE_LSE, P.PKV_ERR_INVALID),
+    (dict(index_mode=1), 1, 0, 1, 0, P.PKV_ERR_INVALID),                     # flat needs P == 1
+    (dict(pool_slots=60), 1, 0, 1, 0, P.PKV_ERR_INVALID),                    # slots % P
+    (dict(), 1, 0, 1, P.PKV_FLAG_FORCE_MMA | 0, None),
+])
+def test_decode_host_validation(kw, batch, layer, splits, flags, status):
+    ws = _ws(**kw)
+    if status is None:
+        # FORCE_MMA on a shape without a tensor-core kernel must be refused, not run.
+        ws = _ws(n_q_heads=2, n_kv_heads=2)
+        status = P.PKV_ERR_UNSUPPORTED
+    got = P.pkv_decode_attn(ws, batch, layer, 1 << 20, 0.1, splits, flags, 0, check=False)
+    assert got == status, (got, status)
+
+
+def test_bind_and_merge_host_validation():
+    ws = _ws()
+    assert P.pkv_bind_step(ws, 1, 7, 0, 0, None, None, 0, check=False) == P.PKV_ERR_INVALID
+    assert P.pkv_bind_step(ws, 9, 0, 0, 0, None, None, 0, check=False) == P.PKV_ERR_CAPACITY
+    assert P.pkv_bind_step(ws, 1, 2, 1, 2, 1 << 20, 1 << 20, 0, check=False) == \
+        P.PKV_ERR_CAPACITY
+    assert P.pkv_bind_step(ws, 1, 2, 0, 1, None, None, 0, check=False) == P.PKV_ERR_INVALID
+    assert P.pkv_bind_step(_ws(seq_lens=None), 1, 0, 0, 0, None, None, 0, check=False) == \
+        P.PKV_ERR_INVALID
+    # batch 0 and one split are valid no-ops that launch nothing
+    assert P.pkv_bind_step(ws, 0, 0, 0, 0, None, None, 0, check=False) == P.PKV_OK
+    assert P.pkv_merge_partials(ws, 2, 1, 0, 0, check=False) == P.PKV_OK
+    assert P.pkv_merge_partials(ws, 2, 9, 0, 0, check=False) == P.PKV_ERR_CAPACITY
+    assert P.pkv_decode_attn(ws, 0, 0, 1 << 20, 0.1, 1, 0, 0, check=False) == P.PKV_OK
+    assert P.pkv_merge_partials(None, 1, 2, 0, 0, check=False) == P.PKV_ERR_INVALID
+
+
+def test_choose_splits():
+    ws = _ws(max_splits=64, n_kv_heads=8, n_q_heads=32)
+    assert P.pkv_choose_splits(ws, 1, 65536, 152) == 57   # ceil(456 / 8)
+    assert P.pkv_choose_splits(ws, 4, 2048, 152) == 15    # ceil(456 / 32)
+    assert P.pkv_choose_splits(ws, 4, 1000, 152) == 8     # >= 128 tokens per split
+    assert P.pkv_choose_splits(ws, 64, 4096, 152) == 1
+    assert P.pkv_choose_splits(_ws(max_splits=4), 1, 65536, 152) == 4
+    assert P.pkv_choose_splits(ws, 0, 10, 152) == 1
+
+
+def test_steady_predicate_matches_oracle():
+    import oracle.ref as R
+    cases = [([4, 9], [10, 3], [4, 9], [11, 4]), ([4, 9], [10, 3], [9, 4], [4, 11]),
+             ([4, 9], [10, 3], [4, 9], [11, 5]), ([1], [0], [1, 2], [1, 1]),
+             (None, None, [1], [1]), ([7], [1], [7], [2])]
+    for c in cases:
+        assert P.pkv_is_steady_increment(*c) == R.is_steady_increment(*c), c
+
+
+def test_status_strings():
+    for s in range(5):
+        assert P.pkv_status_string(s)
+    assert "sm_103a" in P.pkv_version()

@@ -1,0 +1,201 @@
+"""GPU parity: libpkv against the CPU fp64 oracle on the same seeded inputs.
+
+Small cases (oracle-sized variants of every workload, several tiles and a
+ragged tail) compare every output element; full-size cases run the launch
+configuration the benchmark uses and compare metadata fully and attention on
+sampled (request, head) pairs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.ref as R
+import pkv_inputs as W
+from paged_kv_decode_bind_gb300 import DecodeRunner, Workspace
+from paged_kv_decode_bind_gb300 import _abi as A
+
+from parity import bf16_to_f64, check_attention, run_steps
+
+pytestmark = pytest.mark.gpu
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _sample_heads(p, n, seed=0):
+    rng = np.random.default_rng(seed)
+    pairs = {(int(rng.integers(p.batch)), int(rng.integers(p.n_q_heads))) for _ in range(n)}
+    pairs |= {(p.batch - 1, p.n_q_heads - 1), (0, 0)}
+    return sorted(pairs)
+
+
+# ---------------------------------------------------------------- small ----
+
+def test_single_d64_full(cuda):
+    # The whole single-request D=64 workload is oracle-sized: every element.
+    p = W.workload("single_d64", steps=1)
+    r = run_steps(p, S=1, check_pool=True)
+    assert r["max_err"] <= 1e-2
+
+
+@pytest.mark.parametrize("S", [1, 3, 8])
+def test_paged_gqa4_small(cuda, S):
+    p = W.workload("gqa4_b4_paged", shrink=8, steps=1)
+    run_steps(p, S=S, check_partials=True, check_pool=True)
+
+
+@pytest.mark.parametrize("S", [1, 5])
+def test_flat_skewed_small(cuda, S):
+    p = W.workload("gqa4_b16_flat_skewed", shrink=16, steps=1)
+    run_steps(p, S=S, check_partials=True, check_pool=True)
+
+
+@pytest.mark.parametrize("B,S", [(1, 16), (4, 7)])
+def test_long_small(cuda, B, S):
+    p = W.workload("gqa4_long_65536", batch=B, shrink=64, steps=1)
+    run_steps(p, S=S, check_partials=True)
+
+
+@pytest.mark.parametrize("B,S", [(1, 1), (4, 4), (16, 2)])
+def test_gqa8_small(cuda, B, S):
+    p = W.workload("gqa8_graph_sweep", batch=B, shrink=16, steps=1)
+    run_steps(p, S=S, check_partials=True, check_pool=True)
+
+
+@pytest.mark.parametrize("G,D", [(1, 128), (2, 64), (8, 64), (4, 64)])
+def test_group_and_head_dim_variants(cuda, G, D):
+    Hkv = 2
+    p = W.make_problem("variant", batch=3, n_layers=2, n_q_heads=G * Hkv, n_kv_heads=Hkv,
+                       head_dim=D, page_size=16, seq_lens=[1, 77, 200], seed=99, steps=1)
+    for S in (1, 4):
+        run_steps(p, S=S, check_partials=True, check_pool=True)
+
+
+@pytest.mark.parametrize("P", [1, 4, 32])
+def test_page_sizes(cuda, P):
+    p = W.make_problem("pages", batch=4, n_layers=1, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                       page_size=P, seq_lens=[33, 1, 130, 64], seed=123 + P,
+                       index_mode=W.INDEX_PAGE_TABLE, steps=1)
+    for S in (1, 3):
+        run_steps(p, S=S, check_partials=True, check_pool=True)
+
+
+def test_multi_step_steady(cuda):
+    # 64 consecutive steady steps (+1 token each); the last step is compared.
+    p = W.workload("gqa4_b4_paged", shrink=16, n_layers=1, steps=64)
+    r = run_steps(p, S=4, steps=64, check_pool=True)
+    ws = r["ws"]
+    assert ws.seq_lens[:p.batch].tolist() == [x + 64 for x in p.seq_lens.tolist()]
+
+
+def test_cross_split_agreement(cuda):
+    # fp32 outputs from different split counts agree within 1e-3.
+    p = W.workload("gqa4_long_65536", batch=2, shrink=32, steps=1)
+    outs = []
+    for S in (1, 2, 9, 32):
+        ws = Workspace.from_problem(p, max_splits=S)
+        run = DecodeRunner(ws, p.batch, num_splits=S, flags=A.PKV_FLAG_OUT_F32, scale=p.scale)
+        q, k, v = W.step_inputs(p, 0)
+        run.q_in.copy_(q), run.k_in.copy_(k), run.v_in.copy_(v)
+        run.step()
+        torch.cuda.synchronize()
+        outs.append(ws.out_f32(p.batch).cpu().numpy())
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 1e-3
+
+
+def test_lse_output(cuda):
+    p = W.workload("gqa4_b4_paged", shrink=8, n_layers=1, steps=1)
+    for S in (1, 6):
+        ws = Workspace.from_problem(p, max_splits=S)
+        run = DecodeRunner(ws, p.batch, num_splits=S, flags=A.PKV_FLAG_WRITE_LSE, scale=p.scale)
+        q, k, v = W.step_inputs(p, 0)
+        run.q_in.copy_(q), run.k_in.copy_(k), run.v_in.copy_(v)
+        run.step()
+        torch.cuda.synchronize()
+        from parity import OracleState
+        st = OracleState(p)
+        st.bind()
+        st.append(0, R.tensor_bits(k)[0], R.tensor_bits(v)[0])
+        _, lse = st.attention(0, R.tensor_bits(q)[0])
+        assert np.abs(ws.lse[:p.batch].cpu().numpy() - lse).max() <= 1e-3
+
+
+def test_graph_replay_bitexact(cuda):
+    # A captured step replays to exactly the eager result (same kernels, same plan).
+    p = W.workload("gqa8_graph_sweep", batch=8, shrink=16, steps=1)
+    q, k, v = W.step_inputs(p, 0)
+    res = []
+    for use_graph in (False, True):
+        ws = Workspace.from_problem(p, max_splits=4)
+        run = DecodeRunner(ws, p.batch, num_splits=4, scale=p.scale)
+        run.q_in.copy_(q), run.k_in.copy_(k), run.v_in.copy_(v)
+        if use_graph:
+            run.capture()
+            torch.cuda.synchronize()
+            assert ws.seq_lens[:p.batch].tolist() == p.seq_lens.tolist()  # capture ran nothing
+            run.replay()
+        else:
+            run.step()
+        torch.cuda.synchronize()
+        res.append((ws.out_bf16(p.batch).cpu().clone(), ws.seq_lens[:p.batch].cpu().clone(),
+                    ws.kv_indptr[:p.batch + 1].cpu().clone(), ws.k_pool.cpu().clone()))
+    for a, b in zip(*res):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+
+
+def test_rebuild_after_batch_change(cuda):
+    # A changed task set must be rebound with REBUILD from caller-written lengths.
+    p = W.workload("gqa4_b4_paged", shrink=16, n_layers=1, steps=4)
+    ws = Workspace.from_problem(p, max_splits=2)
+    lens = [5, 40, 17, 2]
+    ws.seq_lens[:4].copy_(torch.tensor(lens, dtype=torch.int32))
+    A.pkv_bind_step(ws, 4, A.PKV_BIND_REBUILD)
+    torch.cuda.synchronize()
+    ref = R.bind(lens, req_pool_indices=p.req_pool_indices.numpy(),
+                 page_table=p.page_table.numpy(), page_size=p.page_size, mode=R.REBUILD)
+    assert ws.seq_lens[:4].tolist() == ref["seq_lens"]
+    assert ws.position_ids[:4].tolist() == ref["position_ids"]
+    assert ws.kv_indptr[:5].tolist() == ref["kv_indptr"]
+    assert ws.out_loc[:4].tolist() == ref["out_loc"]
+
+
+def test_zero_length_request(cuda):
+    # A request with no tokens gives zeros (and lse = -inf), with no error bit.
+    p = W.make_problem("zero", batch=3, n_layers=1, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                       page_size=16, seq_lens=[10, 0, 50], seed=4)
+    for S in (1, 3):
+        ws = Workspace.from_problem(p, max_splits=S)
+        q = W.normal_bf16((3, 8, 128), 5).to("cuda")
+        A.pkv_bind_step(ws, 3, A.PKV_BIND_REBUILD)
+        A.pkv_decode_attn(ws, 3, 0, q, p.scale, S, A.PKV_FLAG_WRITE_LSE)
+        A.pkv_merge_partials(ws, 3, S, A.PKV_FLAG_WRITE_LSE)
+        torch.cuda.synchronize()
+        out = bf16_to_f64(ws.out_bf16(3))
+        assert np.all(out[1] == 0) and np.all(np.isneginf(ws.lse[1].cpu().numpy()))
+        assert int(ws.err.item()) == 0
+        st_slots = [R.token_slots(b, L, page_table=p.page_table.numpy(),
+                                  req_pool_indices=p.req_pool_indices.numpy(), page_size=16)
+                    for b, L in enumerate([10, 0, 50])]
+        ref, _ = R.decode_attention(R.tensor_bits(q.cpu()), R.tensor_bits(p.k_pool),
+                                    R.tensor_bits(p.v_pool), 0, st_slots, p.scale, 2)
+        check_attention(out, ref, f"zero-length S={S}")
+
+
+# ----------------------------------------------------------- full size ----
+
+def _bench_splits(p):
+    ws_shape = A.PkvWorkspace(n_kv_heads=p.n_kv_heads, max_splits=256)
+    return A.pkv_choose_splits(ws_shape, p.batch, int(p.seq_lens.max()) + 1, _sms())
+
+
+@pytest.mark.parametrize("name,batch", [("gqa4_b4_paged", None), ("gqa4_b16_flat_skewed", None),
+                                        ("gqa4_long_65536", 1), ("gqa4_long_65536", 4),
+                                        ("gqa8_graph_sweep", 16)])
+def test_full_size_sampled(cuda, name, batch):
+    p = W.workload(name, batch=batch, steps=1)
+    S = _bench_splits(p)
+    layers = sorted({0, p.n_layers - 1})
+    run_steps(p, S=S, check_layers=layers, heads=_sample_heads(p, 12), check_partials=True)
