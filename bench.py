@@ -266,8 +266,9 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    from paged_kv_decode_bind_gb300 import dist as D
     p = W.workload(args.workload, batch=args.batch, steps=ROUND,
-                   seed=20260000 + W.WORKLOADS.index(args.workload) + 1 + 1000 * rank)
+                   seed=D.rank_seed(20260000 + W.WORKLOADS.index(args.workload) + 1, rank))
     B, NL = p.batch, p.n_layers
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     shape_only = A.PkvWorkspace(n_kv_heads=p.n_kv_heads, max_splits=1 << 20)
@@ -375,17 +376,10 @@ def run_ours(args, rank, world, local_rank):
 
     errbits = int(ws.err.item())
     # max over ranks of the times, sum of the work
-    if world > 1:
-        t = torch.tensor([dt, e2e["dt"] if e2e else 0.0], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt, dte_max = t.tolist()
-        if e2e:
-            e2e["dt"] = dte_max
-        w = torch.tensor([total_bytes], device=dev, dtype=torch.float64)
-        dist.all_reduce(w)
-        total_all = float(w.item())
-    else:
-        total_all = float(total_bytes)
+    from paged_kv_decode_bind_gb300 import dist as D
+    dt, total_all = D.reduce_time_and_work(dt, float(total_bytes), device=dev)
+    if e2e:
+        e2e["dt"], _ = D.reduce_time_and_work(e2e["dt"], 0.0, device=dev)
     if rank != 0:
         return
 
