@@ -188,6 +188,31 @@ pkv_status pkv_decode_attn(const pkv_workspace *ws, int batch, int layer, const 
 pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits, int flags,
                               pkv_stream_t stream);
 
+/* Size of the device array behind pkv_decode_attn_static_scratch (8 MiB). */
+#define PKV_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * pkv_decode_attn followed by pkv_merge_partials, with the split partials
+ * kept in a library-owned static device array instead of ws->o_part and
+ * ws->ml_part, for callers that cannot allocate device memory (for example a
+ * plugin handed only its input and output buffers, or a loop that must not
+ * take cudaMalloc's implicit synchronisation).  The pages describe no such
+ * entry point; it has no counterpart there.
+ *   Arguments and results are those of pkv_decode_attn; ws->o_part and
+ *   ws->ml_part are ignored and may be NULL.
+ *   Limit: batch * Hq * num_splits * (D + 2) * 4 bytes must fit in
+ *   PKV_STATIC_SCRATCH_BYTES, else PKV_ERR_CAPACITY and nothing is launched.
+ *   The array exists once per GPU that loads the library, for the life of the
+ *   process.  The first call on each device looks up its device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  No call allocates or frees memory.
+ *   All calls share the array and it keeps the last call's contents; calls
+ *   whose kernels overlap on the GPU race on it, so issue them in order.
+ */
+pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, int layer,
+                                          const void *q, float scale, int num_splits,
+                                          int flags, pkv_stream_t stream);
+
 /*
  * Host steady-state test (cache.py page, bullets 1-4): non-zero when the
  * task ids are the same, in the same order, as at the last bind and every

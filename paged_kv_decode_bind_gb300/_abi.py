@@ -21,7 +21,9 @@ PKV_DEVERR_PAGE, PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT, PKV_DEVERR_T
 
 # Every symbol include/pkv.h declares (checked by the ABI test).
 EXPORTS = ("pkv_workspace_bytes", "pkv_bind_step", "pkv_choose_splits", "pkv_decode_attn",
-           "pkv_merge_partials", "pkv_is_steady_increment", "pkv_status_string", "pkv_version")
+           "pkv_merge_partials", "pkv_decode_attn_static_scratch", "pkv_is_steady_increment",
+           "pkv_status_string", "pkv_version")
+PKV_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class PkvWorkspace(ctypes.Structure):
@@ -73,6 +75,8 @@ def load(path: str = LIB_PATH):
     lib.pkv_decode_attn.restype = i32
     lib.pkv_merge_partials.argtypes = [W, i32, i32, i32, vp]
     lib.pkv_merge_partials.restype = i32
+    lib.pkv_decode_attn_static_scratch.argtypes = [W, i32, i32, vp, f32, i32, i32, vp]
+    lib.pkv_decode_attn_static_scratch.restype = i32
     p64, p32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
     lib.pkv_is_steady_increment.argtypes = [p64, p32, i32, p64, p32, i32]
     lib.pkv_is_steady_increment.restype = i32
@@ -151,6 +155,16 @@ def pkv_merge_partials(ws, batch, num_splits, flags=0, stream=None, check=True):
     s = load().pkv_merge_partials(_ws(ws), int(batch), int(num_splits), int(flags),
                                   _stream(stream))
     return _check("pkv_merge_partials", s) if check else s
+
+
+def pkv_decode_attn_static_scratch(ws, batch, layer, q, scale, num_splits=1, flags=0,
+                                   stream=None, check=True):
+    """Decode attention + merge with the partials in the library's static
+    device array (for callers that cannot allocate device memory)."""
+    s = load().pkv_decode_attn_static_scratch(_ws(ws), int(batch), int(layer), _ptr(q),
+                                              float(scale), int(num_splits), int(flags),
+                                              _stream(stream))
+    return _check("pkv_decode_attn_static_scratch", s) if check else s
 
 
 def pkv_is_steady_increment(prev_ids, prev_lens, ids, lens) -> bool:
