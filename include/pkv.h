@@ -64,7 +64,9 @@ enum {
   PKV_FLAG_OUT_F32 = 1,    /* write `out` as fp32 instead of bf16 (out must be sized for it) */
   PKV_FLAG_WRITE_LSE = 2,  /* also write lse[b, h] = m + ln(l) (natural log)                */
   PKV_FLAG_FORCE_SIMT = 4, /* use the CUDA-core kernel even where a tensor-core one exists  */
-  PKV_FLAG_FORCE_MMA = 8   /* use the tensor-core kernel (error if the shape has none)      */
+  PKV_FLAG_FORCE_MMA = 8,  /* use the tensor-core kernel (error if the shape has none)      */
+  PKV_FLAG_FORCE_GATHER = 16 /* tensor-core kernel: load K/V with cp.async gathers even where
+                                tensor-map TMA boxes apply (P % 16 == 0)                    */
 };
 
 /* bits OR-ed into *err by device code (sticky; the caller clears the word) */
@@ -111,6 +113,9 @@ typedef struct pkv_workspace {
   void *out;                 /* [max_batch, Hq, D] bf16 (fp32 with PKV_FLAG_OUT_F32) */
   float *lse;                /* [max_batch, Hq] or NULL                               */
   int32_t *err;              /* one sticky int32 of PKV_DEVERR_* bits                */
+  int32_t *split_counters;   /* [max_batch * Hkv] zero-initialised once by the caller;
+                                used and left at zero by pkv_decode_layer when S > 1;
+                                may be NULL if that entry point is not used         */
 } pkv_workspace;
 
 /*
@@ -145,13 +150,15 @@ pkv_status pkv_bind_step(const pkv_workspace *ws, int batch, int mode, int layer
                          pkv_stream_t stream);
 
 /*
- * Split count for a batch, host only: S = ceil(3 * num_sms / (batch * Hkv))
- * so that the (request, KV head, split) units give about three per SM,
- * clamped so that a split of the longest request (max_seq_len_hint tokens)
- * holds at least 128 tokens, and to [1, max_splits].  Returns 1 for
- * non-positive arguments.
+ * Split count for a batch, host only.  The target split length is
+ * chunk = max(128, ceil(Hkv * total_tokens_hint / (4 * num_sms))) tokens, so
+ * that the (request, KV head, split) units number about four per SM, and
+ * S = ceil(max_seq_len_hint / chunk), clamped to [1, max_splits].
+ * total_tokens_hint <= 0 means batch * max_seq_len_hint.  Returns 1 for
+ * non-positive batch, length or SM count.
  */
-int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint, int num_sms);
+int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint,
+                      long long total_tokens_hint, int num_sms);
 
 /*
  * Split-KV GQA decode attention for one layer (workspace.py page, bullets 1,
@@ -166,10 +173,11 @@ int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint, 
  *               (gran = P if P >= 16, else the least multiple of P >= 16),
  *               computed on the device from the live seq_lens.
  *               S == 1: the result goes straight to `out` (and `lse`).
- *               S > 1: split s of (b,h) writes o_part[b,h,s,:] (normalised)
- *               and ml_part[b,h,s,:] = (max score, sum exp(s - max)); splits
- *               past the end of a request are written empty (-inf, 0);
- *               pkv_merge_partials then produces `out`.
+ *               S > 1: split s < n_b = ceil(seq_lens[b] / chunk) of (b,h)
+ *               writes o_part[b,h,s,:] (normalised) and ml_part[b,h,s,:] =
+ *               (max score, sum exp(s - max)); splits s >= n_b are not
+ *               computed (their entries are unspecified) and
+ *               pkv_merge_partials reads only the first n_b.
  *   flags       PKV_FLAG_* (OUT_F32 and WRITE_LSE apply when S == 1).
  * Device errors: PKV_DEVERR_PAGE, _LEN, _TOTAL, _SLOT, _TIMEOUT; the affected
  * (b, KV head, split) is written as empty.
@@ -187,6 +195,27 @@ pkv_status pkv_decode_attn(const pkv_workspace *ws, int batch, int layer, const 
  */
 pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits, int flags,
                               pkv_stream_t stream);
+
+/*
+ * One layer of a decode step in a single launch: the KV append, split-KV
+ * decode attention and the split merge (workspace.py page, bullets 1, 14;
+ * cache.py page, bullet 40).  Same results as
+ *   pkv_bind_step(PKV_BIND_APPEND_ONLY, layer, 1, k_new, v_new)
+ *   pkv_decode_attn(layer, q, scale, num_splits, flags)
+ *   pkv_merge_partials(num_splits, flags)
+ * after a metadata bind has set seq_lens and out_loc.
+ *   k_new, v_new  bf16 [batch, Hkv, D] rows for this layer, or both NULL to
+ *                 skip the append.
+ *   num_splits    as pkv_decode_attn; with S > 1 ws->split_counters must be
+ *                 set (zeroed once; every call leaves it zeroed), and the last
+ *                 split to finish for each (request, KV head) merges.
+ *   flags         PKV_FLAG_*; with PKV_FLAG_FORCE_SIMT the three steps run as
+ *                 separate kernels (the CUDA-core attention has no fusion).
+ * Device errors as for pkv_bind_step and pkv_decode_attn.
+ */
+pkv_status pkv_decode_layer(const pkv_workspace *ws, int batch, int layer, const void *q,
+                            const void *k_new, const void *v_new, float scale, int num_splits,
+                            int flags, pkv_stream_t stream);
 
 /* Size of the device array behind pkv_decode_attn_static_scratch (8 MiB). */
 #define PKV_STATIC_SCRATCH_BYTES (8u << 20)

@@ -16,12 +16,14 @@ PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_CAPACITY, PKV_ERR_CUDA = r
 PKV_BIND_STEADY, PKV_BIND_REBUILD, PKV_BIND_APPEND_ONLY = 0, 1, 2
 PKV_IDX_PAGE_TABLE, PKV_IDX_FLAT = 0, 1
 PKV_FLAG_OUT_F32, PKV_FLAG_WRITE_LSE, PKV_FLAG_FORCE_SIMT, PKV_FLAG_FORCE_MMA = 1, 2, 4, 8
+PKV_FLAG_FORCE_GATHER = 16
 PKV_DEVERR_PAGE, PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT, PKV_DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16
 
 # Every symbol include/pkv.h declares (checked by the ABI test).
 EXPORTS = ("pkv_workspace_bytes", "pkv_bind_step", "pkv_choose_splits", "pkv_decode_attn",
-           "pkv_merge_partials", "pkv_decode_attn_static_scratch", "pkv_is_steady_increment",
+           "pkv_merge_partials", "pkv_decode_layer", "pkv_decode_attn_static_scratch",
+           "pkv_is_steady_increment",
            "pkv_status_string", "pkv_version")
 PKV_STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -43,6 +45,7 @@ class PkvWorkspace(ctypes.Structure):
         ("kv_indices", ctypes.c_void_p), ("o_part", ctypes.c_void_p),
         ("ml_part", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("lse", ctypes.c_void_p), ("err", ctypes.c_void_p),
+        ("split_counters", ctypes.c_void_p),
     ]
 
 
@@ -69,12 +72,14 @@ def load(path: str = LIB_PATH):
     lib.pkv_workspace_bytes.restype = ctypes.c_size_t
     lib.pkv_bind_step.argtypes = [W, i32, i32, i32, i32, vp, vp, vp]
     lib.pkv_bind_step.restype = i32
-    lib.pkv_choose_splits.argtypes = [W, i32, i32, i32]
+    lib.pkv_choose_splits.argtypes = [W, i32, i32, ctypes.c_longlong, i32]
     lib.pkv_choose_splits.restype = i32
     lib.pkv_decode_attn.argtypes = [W, i32, i32, vp, f32, i32, i32, vp]
     lib.pkv_decode_attn.restype = i32
     lib.pkv_merge_partials.argtypes = [W, i32, i32, i32, vp]
     lib.pkv_merge_partials.restype = i32
+    lib.pkv_decode_layer.argtypes = [W, i32, i32, vp, vp, vp, f32, i32, i32, vp]
+    lib.pkv_decode_layer.restype = i32
     lib.pkv_decode_attn_static_scratch.argtypes = [W, i32, i32, vp, f32, i32, i32, vp]
     lib.pkv_decode_attn_static_scratch.restype = i32
     p64, p32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
@@ -141,8 +146,9 @@ def pkv_bind_step(ws, batch, mode, layer_begin=0, layer_count=0, k_new=None, v_n
     return _check("pkv_bind_step", s) if check else s
 
 
-def pkv_choose_splits(ws, batch, max_seq_len_hint, num_sms) -> int:
-    return int(load().pkv_choose_splits(_ws(ws), int(batch), int(max_seq_len_hint), int(num_sms)))
+def pkv_choose_splits(ws, batch, max_seq_len_hint, total_tokens_hint, num_sms) -> int:
+    return int(load().pkv_choose_splits(_ws(ws), int(batch), int(max_seq_len_hint),
+                                        int(total_tokens_hint), int(num_sms)))
 
 
 def pkv_decode_attn(ws, batch, layer, q, scale, num_splits=1, flags=0, stream=None, check=True):
@@ -155,6 +161,14 @@ def pkv_merge_partials(ws, batch, num_splits, flags=0, stream=None, check=True):
     s = load().pkv_merge_partials(_ws(ws), int(batch), int(num_splits), int(flags),
                                   _stream(stream))
     return _check("pkv_merge_partials", s) if check else s
+
+
+def pkv_decode_layer(ws, batch, layer, q, k_new, v_new, scale, num_splits=1, flags=0,
+                     stream=None, check=True):
+    s = load().pkv_decode_layer(_ws(ws), int(batch), int(layer), _ptr(q), _ptr(k_new),
+                                _ptr(v_new), float(scale), int(num_splits), int(flags),
+                                _stream(stream))
+    return _check("pkv_decode_layer", s) if check else s
 
 
 def pkv_decode_attn_static_scratch(ws, batch, layer, q, scale, num_splits=1, flags=0,

@@ -1,0 +1,727 @@
+// Tensor-core split-KV GQA decode attention (workspace.py page, bullets 1 and
+// 14-16), optionally fused with the KV append (cache.py page, bullet 40) and
+// with the split merge.
+//
+// Math.  Per (request b, KV head g, split c) unit the query group is one
+// 16-row operand: S = Q_g K^T and O += P V are warp-level bf16
+// mma.m16n8k16 with fp32 accumulation (rows >= G are zero); P enters the
+// second product as P_hi + P_lo (two bf16 terms) so P V keeps ~16 mantissa
+// bits.  The K/V rows of a token are read from HBM once for all G heads.
+//
+// Block.  4 consumer warps + 1 producer warp.  A tile is 64 tokens; consumer
+// warp w owns tokens [16w, 16w+16) of each tile with its own online-softmax
+// state; the four states merge at the end of the unit.  The producer walks
+// the block's units ahead of the consumers, across unit boundaries, through a
+// 3-stage ring (`full` mbarriers complete on the landed bytes, `empty` on the
+// four consumer warps' release), fetching the next tile's index entries one
+// tile ahead so their latency overlaps the wait for a free stage.
+//
+// Units.  With batch <= kMaxCompactBatch only the non-empty (request, split)
+// pairs are units (a per-block prefix over the requests' split counts), so a
+// round-robin over units gives every block the same share.
+//
+// Shared-memory tile layout: per K (or V) tile, D/64 column halves, each
+// [64 rows][128 B] with the 128-byte swizzle (16-byte chunk c of row r sits at
+// chunk c ^ (r & 7)), so the 8 row addresses of every ldmatrix hit distinct
+// banks.  Two producers fill it:
+//   * page mode with P % 16 == 0: one tensor-map TMA box (64 cols x 1 head x
+//     16 slots, 2 KB) per 16-token page piece and column half;
+//   * any other page size and the flat (token-level) mode: cp.async 16-byte
+//     gathers written at the swizzled positions, zero-filled where a row is
+//     past the end, completing on the same mbarriers.
+//
+// Fused append: the unit that holds a request's newest token first writes the
+// new K/V row (k_new, v_new) to pool[layer, out_loc[b]], fences the async
+// proxy, then loads the tile, so the new token is attended.
+// Fused merge: a unit of a request with n > 1 splits writes its partial,
+// then takes a ticket on split_counters[b, g]; the unit that draws n - 1
+// merges all n partials and resets the counter to 0 (no waiting anywhere).
+//
+// Every wait is bounded (~1 s); a timeout raises PKV_DEVERR_TIMEOUT, marks the
+// unit empty, makes every later wait of the block return at once, and the
+// producer drains its copies in flight (again bounded) before exiting.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "decode_plan.cuh"
+#include "kernels.cuh"
+#include "merge.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kCW = 4;                   // consumer warps
+constexpr int kMThreads = (kCW + 1) * 32;
+constexpr int kMT = 16 * kCW;            // tokens per tile
+constexpr int kMStages = 3;
+
+template <int D, int G>
+struct MCfg {
+  static constexpr int HALVES = D / 64;     // 64-column (128-byte) swizzled halves
+  static constexpr int HALF = kMT * 128;    // bytes of one half of a tile
+  static constexpr int TILE = HALVES * HALF;
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int NT = D / 8;          // 8-wide output column tiles
+  static constexpr int RSTRIDE = D + 8;     // combine buffer row stride (floats)
+  // dynamic shared memory: the K/V ring (1024-aligned for the swizzle) and
+  // the combine buffer; small state lives in static shared memory.
+  static constexpr int OFF_KV = 0;
+  static constexpr int OFF_RED = OFF_KV + kMStages * 2 * TILE;  // [2][G][RSTRIDE] f32
+  static constexpr int SMEM = OFF_RED + 2 * G * RSTRIDE * 4 + 1024;  // + alignment slack
+  static_assert(G >= 1 && G <= 16, "one 16-row mma operand per group");
+  static_assert(D % 64 == 0, "whole swizzled halves");
+};
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a swizzled half.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
+                                            int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ float quad_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+// Fused append: write this (request, head)'s new K/V row to the pool when the
+// tile [tile0, tile0 + 64) of this unit holds the request's newest token
+// (warp-uniform).
+template <int D>
+__device__ __forceinline__ void append_if_newest(const DecodeArgs &a, const Unit &un, int tile0,
+                                                 int lane) {
+  if (a.k_new == nullptr || un.L <= 0) return;
+  const int t = un.L - 1;
+  if (t < tile0 || t >= min(tile0 + kMT, un.t1)) return;
+  const pkv_workspace &ws = a.ws;
+  const int loc = ws.out_loc[un.b];
+  if (loc < 0 || loc >= ws.pool_slots) {
+    if (lane == 0) atomicOr(ws.err, PKV_DEVERR_SLOT);
+    return;
+  }
+  constexpr int V16 = D / 8;  // 16-byte vectors per row
+  const long long src = ((long long)un.b * ws.n_kv_heads + un.g) * D;
+  const long long dst = (((long long)a.layer * ws.pool_slots + loc) * ws.n_kv_heads + un.g) * D;
+  for (int i = lane; i < 2 * V16; i += 32) {
+    const bool isv = i >= V16;
+    const int v = isv ? i - V16 : i;
+    const uint4 x = reinterpret_cast<const uint4 *>(
+        static_cast<const uint16_t *>(isv ? a.v_new : a.k_new) + src)[v];
+    reinterpret_cast<uint4 *>(static_cast<uint16_t *>(isv ? ws.v_pool : ws.k_pool) + dst)[v] = x;
+  }
+  // The row must be visible to the async-proxy loads issued next.
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+}
+
+// Producer, page mode: 16-token page pieces by tensor-map boxes.  Lane j < 4
+// owns piece j; `raw` is its page id, fetched one tile ahead.
+template <int D, int G>
+__device__ __forceinline__ void produce_tma(const DecodeArgs &a, const Unit &un, int tile0,
+                                            int raw, int stage, uint32_t kv_base, uint64_t *full,
+                                            int *flag, const CUtensorMap *tmk,
+                                            const CUtensorMap *tmv, int lane) {
+  using C = MCfg<D, G>;
+  const pkv_workspace &ws = a.ws;
+  const int tok0 = tile0 + 16 * lane;
+  const bool want = lane < 4 && tok0 < un.t1;
+  int kind = 0;
+  long long slot0 = -1;
+  if (want) slot0 = slot_from_raw(ws, raw, tok0, kind);  // tok0 % 16 == 0: inside one page
+  const unsigned ok = __ballot_sync(0xffffffffu, slot0 >= 0);
+  const int bad = __reduce_or_sync(0xffffffffu, kind);
+  if (lane == 0) {
+    *flag = bad;
+    if (bad) atomicOr(ws.err, bad);
+    mbar_arrive_expect_tx(full, __popc(ok) * (uint32_t)(2 * C::HALVES * 16 * 128));
+  }
+  __syncwarp();
+  if (slot0 >= 0) {
+    const uint32_t kt = kv_base + (2 * stage) * C::TILE;
+    const uint32_t vt = kt + C::TILE;
+    const int row = a.layer * ws.pool_slots + (int)slot0;
+#pragma unroll
+    for (int h = 0; h < C::HALVES; ++h) {
+      const uint32_t off = h * C::HALF + 16 * lane * 128;
+      tma_load_3d(kt + off, tmk, 64 * h, un.g, row, full);
+      tma_load_3d(vt + off, tmv, 64 * h, un.g, row, full);
+    }
+  }
+}
+
+// Producer, any page size / flat mode: cp.async 16-byte gathers.  Lane owns
+// rows lane and lane + 32 of the tile; rows past the end are zero-filled.
+template <int D, int G>
+__device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Unit &un, int tile0,
+                                                const int (&raw)[2], int stage, uint32_t kv_base,
+                                                uint64_t *full, int *flag, int lane) {
+  using C = MCfg<D, G>;
+  const pkv_workspace &ws = a.ws;
+  int kind = 0;
+  long long slot[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int tok = tile0 + lane + 32 * h;
+    slot[h] = tok < un.t1 ? slot_from_raw(ws, raw[h], tok, kind) : -1;
+  }
+  const int bad = __reduce_or_sync(0xffffffffu, kind);
+  if (lane == 0) {
+    *flag = bad;
+    if (bad) atomicOr(ws.err, bad);
+  }
+  __syncwarp();
+  const uint32_t kt = kv_base + (2 * stage) * C::TILE;
+  const uint32_t vt = kt + C::TILE;
+  const uint16_t *kp = static_cast<const uint16_t *>(ws.k_pool);
+  const uint16_t *vp = static_cast<const uint16_t *>(ws.v_pool);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = lane + 32 * h;
+    const bool ok = slot[h] >= 0;
+    const long long e =
+        ok ? (((long long)a.layer * ws.pool_slots + slot[h]) * ws.n_kv_heads + un.g) * D : 0;
+#pragma unroll
+    for (int c8 = 0; c8 < D / 8; ++c8) {
+      const uint32_t off = (c8 >> 3) * C::HALF + swz(r, c8 & 7);
+      cp_async_16(kt + off, kp + e + c8 * 8, ok ? 16 : 0);
+      cp_async_16(vt + off, vp + e + c8 * 8, ok ? 16 : 0);
+    }
+  }
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(full))
+               : "memory");
+}
+
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMThreads)
+    decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const int use_tma) {
+  using C = MCfg<D, G>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kMStages], empty[kMStages];
+  __shared__ int flags[kMStages];
+  __shared__ volatile int s_ctrl[2];  // abort flag, merge ticket
+  __shared__ float s_ml[kCW * 16 * 2];
+  __shared__ int s_bad[kCW];
+  __shared__ int s_pref[kMaxCompactBatch + 1];
+  __shared__ int s_tmp[32];
+  __shared__ int s_max_len;
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const pkv_workspace &ws = a.ws;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Hq = ws.n_q_heads;
+  volatile int *s_abort = &s_ctrl[0];
+  volatile int *s_ticket = &s_ctrl[1];
+
+  const int max_len = batch_max_len(ws, a.batch, &s_max_len);
+  // Zero the K/V ring once: pieces a tile does not load then hold finite
+  // values (zeros or earlier tokens), so masked lanes contribute 0, not NaN.
+  for (int i = tid; i < kMStages * 2 * C::TILE / 16; i += kMThreads)
+    reinterpret_cast<uint4 *>(smem + C::OFF_KV)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    for (int s = 0; s < kMStages; ++s) {
+      // TMA: one expect-tx arrival; cp.async: 32 copy-completion arrivals
+      // plus one release arrival by the lane that wrote the stage flag.
+      mbar_init(&full[s], use_tma ? 1 : 33);
+      mbar_init(&empty[s], kCW);
+    }
+    *s_abort = 0;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (tid == 0) fence_barrier_init();
+  __syncthreads();
+
+  Plan pl;
+  pl.batch = a.batch;
+  pl.hkv = ws.n_kv_heads;
+  pl.S = a.num_splits;
+  pl.chunk = split_chunk(max_len, a.num_splits, ws.page_size);
+  const bool direct = pl.S == 1;
+  const bool fused = a.fused_merge && !direct;
+  if (a.batch <= kMaxCompactBatch) {
+    const int pairs = batch_split_prefix(ws, a.batch, pl.chunk, s_pref, s_tmp);
+    pl.pref = s_pref;
+    pl.n_units = pairs * pl.hkv;
+    if (direct || fused) {
+      // Requests with no usable token have no unit: zero their outputs here.
+      for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
+        if (s_pref[b + 1] != s_pref[b]) continue;
+        for (int i = tid; i < Hq * D; i += kMThreads) {
+          const long long o = (long long)b * Hq * D + i;
+          if (a.flags & PKV_FLAG_OUT_F32) static_cast<float *>(ws.out)[o] = 0.f;
+          else static_cast<uint16_t *>(ws.out)[o] = 0;
+        }
+        if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse)
+          for (int h = tid; h < Hq; h += kMThreads) ws.lse[(long long)b * Hq + h] = -INFINITY;
+      }
+    }
+  } else {
+    pl.n_units = pl.S * pl.batch * pl.hkv;
+  }
+  const uint32_t kv_base = smem_addr(smem + C::OFF_KV);
+
+  if (warp == kCW) {
+    // ------------------------------------------------------- producer ----
+    Cursor<kMT> pc;
+    pc.seek(ws, pl, blockIdx.x);
+    ReqIndex ri;
+    int cur_u = -1;
+    int raw[2] = {-1, -1};
+    auto fetch = [&]() {  // index entries of the tile under the cursor
+      if (pc.done) return;
+      if (pc.un.u != cur_u) {
+        ri = req_index(ws, pc.un.b);
+        cur_u = pc.un.u;
+      }
+      const int tile0 = pc.un.t0 + pc.i * kMT;
+      if (use_tma) {
+        const int tok0 = tile0 + 16 * lane;
+        raw[0] = (lane < 4 && tok0 < pc.un.t1) ? raw_index(ws, ri, tok0) : -1;
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int tok = tile0 + lane + 32 * h;
+          raw[h] = tok < pc.un.t1 ? raw_index(ws, ri, tok) : -1;
+        }
+      }
+    };
+    fetch();
+    int k = 0;
+    bool aborted = false;
+    while (!pc.done) {
+      const int s = k % kMStages;
+      const int r = k / kMStages;
+      if (r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1)) {
+        aborted = true;
+        break;
+      }
+      if (*s_abort) {
+        aborted = true;
+        break;
+      }
+      const Unit un = pc.un;
+      const int tile0 = un.t0 + pc.i * kMT;
+      append_if_newest<D>(a, un, tile0, lane);
+      const int cur_raw[2] = {raw[0], raw[1]};
+      pc.advance(ws, pl);
+      fetch();  // the next tile's entries are in flight while this one is issued
+      if (use_tma) {
+        produce_tma<D, G>(a, un, tile0, cur_raw[0], s, kv_base, &full[s], &flags[s], &tmk, &tmv,
+                          lane);
+      } else {
+        produce_cpasync<D, G>(a, un, tile0, cur_raw, s, kv_base, &full[s], &flags[s], lane);
+        if (lane == 0) mbar_arrive(&full[s]);
+      }
+      ++k;
+    }
+    if (aborted) {
+      if (lane == 0) {
+        *s_abort = 1;
+        atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
+      }
+      // Drain: the last (up to kMStages) issued tiles may still be landing.
+      for (int kk = max(0, k - kMStages); kk < k; ++kk)
+        mbar_wait_bounded(&full[kk % kMStages], (kk / kMStages) & 1);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------- consumers ----
+  const int grp = lane >> 2, tig = lane & 3;
+  const int r0 = grp, r1 = grp + 8;  // the two query-head rows this lane holds
+  const float qk_scale = a.scale * kLog2e;
+  float *red = reinterpret_cast<float *>(smem + C::OFF_RED);
+  // ldmatrix lane addressing in the swizzled layout (fragment layouts of
+  // mma.m16n8k16): matrix mi = lane / 8, row rr = lane % 8 of that matrix.
+  const int mi = lane >> 3, rr = lane & 7;
+  const int rowK = 16 * warp + (mi >> 1) * 8 + rr;  // K: tokens 0-7 / 8-15 by mi / 2
+  const int rowV = 16 * warp + (mi & 1) * 8 + rr;   // V: tokens by mi % 2
+
+  int k = 0;
+  for (int u = blockIdx.x; u < pl.n_units; u += gridDim.x) {
+    const Unit un = unit_at(ws, pl, u);
+    const int hq0 = un.g * G;
+    const int n_b = un.L > 0 ? (un.L + pl.chunk - 1) / pl.chunk : 0;
+    if (un.t0 >= un.t1) {  // dense enumeration only
+      const int ct = tid;  // consumer thread 0..127
+      if (direct || fused) {
+        if (un.c == 0) {  // a request with no tokens: zero output
+          for (int i = ct; i < G * D; i += kCW * 32) {
+            const long long o = ((long long)un.b * Hq + hq0) * D + i;
+            if (a.flags & PKV_FLAG_OUT_F32) static_cast<float *>(ws.out)[o] = 0.f;
+            else static_cast<uint16_t *>(ws.out)[o] = 0;
+          }
+          if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse && ct < G)
+            ws.lse[(long long)un.b * Hq + hq0 + ct] = -INFINITY;
+        }
+      } else if (ct < G) {
+        const long long o = (((long long)un.b * Hq + hq0 + ct) * pl.S + un.c) * 2;
+        ws.ml_part[o] = -INFINITY;
+        ws.ml_part[o + 1] = 0.f;
+      }
+      continue;
+    }
+    const int ntiles = (un.t1 - un.t0 + kMT - 1) / kMT;
+
+    // Q fragments (A operand, rows = heads of the group; rows >= G are zero).
+    uint32_t qa[C::KSTEPS][4];
+    {
+      const uint32_t *q32 = static_cast<const uint32_t *>(a.q);
+      const long long row0 = ((long long)un.b * Hq + hq0 + r0) * (D / 2);
+      const long long row1 = ((long long)un.b * Hq + hq0 + r1) * (D / 2);
+#pragma unroll
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {
+        const int c = ks * 8 + tig;  // 32-bit column (two bf16)
+        qa[ks][0] = r0 < G ? q32[row0 + c] : 0u;
+        qa[ks][1] = r1 < G ? q32[row1 + c] : 0u;
+        qa[ks][2] = r0 < G ? q32[row0 + c + 4] : 0u;
+        qa[ks][3] = r1 < G ? q32[row1 + c + 4] : 0u;
+      }
+    }
+    float acc[C::NT][4];
+#pragma unroll
+    for (int j = 0; j < C::NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int bad = 0;
+
+    for (int it = 0; it < ntiles; ++it, ++k) {
+      const int s = k % kMStages;
+      bool ok = false;
+      if (!*s_abort) {
+        ok = mbar_wait_bounded(&full[s], (k / kMStages) & 1);
+        if (!ok && lane == 0) {
+          *s_abort = 1;
+          atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
+        }
+      }
+      const int nv = min(16, un.t1 - (un.t0 + it * kMT) - 16 * warp);  // my valid tokens
+      if (!ok) {
+        bad = 1;
+      } else {
+        bad |= flags[s];
+        if (nv > 0) {
+          const uint32_t kt = kv_base + (2 * s) * C::TILE;
+          const uint32_t vt = kt + C::TILE;
+          // ---- S = Q K^T: two 8-token column tiles ----
+          float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+          for (int ks = 0; ks < C::KSTEPS; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kt + (ks >> 2) * C::HALF + swz(rowK, (ks & 3) * 2 + (mi & 1)), b0, b1, b2, b3);
+            mma_bf16_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+            mma_bf16_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          }
+          // ---- online softmax (log2 units), rows r0 / r1 ----
+          float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const bool valid = nt * 8 + 2 * tig + e < nv;
+              sc[nt][e] = valid ? sc[nt][e] * qk_scale : -INFINITY;
+              sc[nt][2 + e] = valid ? sc[nt][2 + e] * qk_scale : -INFINITY;
+              t0 = fmaxf(t0, sc[nt][e]);
+              t1 = fmaxf(t1, sc[nt][2 + e]);
+            }
+          t0 = quad_max(t0);
+          t1 = quad_max(t1);
+          const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
+          const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+          m0 = mn0;
+          m1 = mn1;
+          float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              sc[nt][e] = exp2f(sc[nt][e] - mn0);
+              sc[nt][2 + e] = exp2f(sc[nt][2 + e] - mn1);
+              ps0 += sc[nt][e];
+              ps1 += sc[nt][2 + e];
+            }
+          l0 = l0 * al0 + ps0;
+          l1 = l1 * al1 + ps1;
+#pragma unroll
+          for (int j = 0; j < C::NT; ++j) {
+            acc[j][0] *= al0;
+            acc[j][1] *= al0;
+            acc[j][2] *= al1;
+            acc[j][3] *= al1;
+          }
+          // P as the A operand of O += P V (the C layout of S is the A layout
+          // of P), as P_hi + P_lo so P V keeps ~16 mantissa bits.
+          uint32_t ph[4], pl_[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float x = sc[i >> 1][(i & 1) * 2], y = sc[i >> 1][(i & 1) * 2 + 1];
+            ph[i] = pack_bf16x2(x, y);
+            pl_[i] = pack_bf16x2(x - bf16lo(ph[i]), y - bf16hi(ph[i]));
+          }
+#pragma unroll
+          for (int jj = 0; jj < C::NT / 2; ++jj) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vt + (jj >> 2) * C::HALF + swz(rowV, (jj & 3) * 2 + (mi >> 1)), b0, b1, b2, b3);
+            mma_bf16_16816(acc[2 * jj], ph[0], ph[1], ph[2], ph[3], b0, b1);
+            mma_bf16_16816(acc[2 * jj + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+            mma_bf16_16816(acc[2 * jj], pl_[0], pl_[1], pl_[2], pl_[3], b0, b1);
+            mma_bf16_16816(acc[2 * jj + 1], pl_[0], pl_[1], pl_[2], pl_[3], b2, b3);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ---- merge the four warps' states ----
+    l0 = quad_sum(l0);
+    l1 = quad_sum(l1);
+    if (tig == 0) {
+      s_ml[(warp * 16 + r0) * 2] = m0;
+      s_ml[(warp * 16 + r0) * 2 + 1] = l0;
+      s_ml[(warp * 16 + r1) * 2] = m1;
+      s_ml[(warp * 16 + r1) * 2 + 1] = l1;
+    }
+    if (lane == 0) s_bad[warp] = bad;
+    named_sync(1, kCW * 32);
+    float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) {
+      M0 = fmaxf(M0, s_ml[(w * 16 + r0) * 2]);
+      M1 = fmaxf(M1, s_ml[(w * 16 + r1) * 2]);
+    }
+    float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) {
+      const float mw0 = s_ml[(w * 16 + r0) * 2], mw1 = s_ml[(w * 16 + r1) * 2];
+      L0 += mw0 == -INFINITY ? 0.f : exp2f(mw0 - M0) * s_ml[(w * 16 + r0) * 2 + 1];
+      L1 += mw1 == -INFINITY ? 0.f : exp2f(mw1 - M1) * s_ml[(w * 16 + r1) * 2 + 1];
+    }
+    const int unit_bad = s_bad[0] | s_bad[1] | s_bad[2] | s_bad[3];
+    const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
+    const float f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
+#pragma unroll
+    for (int j = 0; j < C::NT; ++j) {
+      acc[j][0] *= f0;
+      acc[j][1] *= f0;
+      acc[j][2] *= f1;
+      acc[j][3] *= f1;
+    }
+    // tree over warps through two [G][D] buffers
+    auto store = [&](int buf) {
+#pragma unroll
+      for (int j = 0; j < C::NT; ++j) {
+        const int d = 8 * j + 2 * tig;
+        if (r0 < G)
+          *reinterpret_cast<float2 *>(red + (buf * G + r0) * C::RSTRIDE + d) =
+              make_float2(acc[j][0], acc[j][1]);
+        if (r1 < G)
+          *reinterpret_cast<float2 *>(red + (buf * G + r1) * C::RSTRIDE + d) =
+              make_float2(acc[j][2], acc[j][3]);
+      }
+    };
+    auto add = [&](int buf) {
+#pragma unroll
+      for (int j = 0; j < C::NT; ++j) {
+        const int d = 8 * j + 2 * tig;
+        if (r0 < G) {
+          const float2 v = *reinterpret_cast<const float2 *>(red + (buf * G + r0) * C::RSTRIDE + d);
+          acc[j][0] += v.x;
+          acc[j][1] += v.y;
+        }
+        if (r1 < G) {
+          const float2 v = *reinterpret_cast<const float2 *>(red + (buf * G + r1) * C::RSTRIDE + d);
+          acc[j][2] += v.x;
+          acc[j][3] += v.y;
+        }
+      }
+    };
+    if (warp >= 2) store(warp - 2);
+    named_sync(1, kCW * 32);
+    if (warp < 2) add(warp);
+    named_sync(1, kCW * 32);
+    if (warp == 1) store(0);
+    named_sync(1, kCW * 32);
+
+    // ---- write: final row, or a partial (and maybe merge them all) ----
+    const bool final_out = direct || (fused && n_b == 1);
+    if (warp == 0) {
+      add(0);
+      const float inv0 = (unit_bad || !(L0 > 0.f)) ? 0.f : 1.f / L0;
+      const float inv1 = (unit_bad || !(L1 > 0.f)) ? 0.f : 1.f / L1;
+#pragma unroll
+      for (int j = 0; j < C::NT; ++j) {
+        const int d = 8 * j + 2 * tig;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = hh ? r1 : r0;
+          if (r >= G) continue;
+          const float inv = hh ? inv1 : inv0;
+          const float x = acc[j][2 * hh] * inv, y = acc[j][2 * hh + 1] * inv;
+          if (final_out) {
+            const long long o = ((long long)un.b * Hq + hq0 + r) * D + d;
+            if (a.flags & PKV_FLAG_OUT_F32)
+              *reinterpret_cast<float2 *>(static_cast<float *>(ws.out) + o) = make_float2(x, y);
+            else
+              *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(ws.out) + o) = pack_bf16x2(x, y);
+          } else {
+            const long long o = (((long long)un.b * Hq + hq0 + r) * pl.S + un.c) * D + d;
+            *reinterpret_cast<float2 *>(ws.o_part + o) = make_float2(x, y);
+          }
+        }
+      }
+      if (tig == 0) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = hh ? r1 : r0;
+          if (r >= G) continue;
+          const float M = hh ? M1 : M0, L = hh ? L1 : L0;
+          const bool empty_out = unit_bad || !(L > 0.f);
+          if (final_out) {
+            if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse)
+              ws.lse[(long long)un.b * Hq + hq0 + r] = empty_out ? -INFINITY : M * kLn2 + logf(L);
+          } else {
+            const long long o = (((long long)un.b * Hq + hq0 + r) * pl.S + un.c) * 2;
+            ws.ml_part[o] = empty_out ? -INFINITY : M * kLn2;
+            ws.ml_part[o + 1] = empty_out ? 0.f : L;
+          }
+        }
+      }
+      if (fused && !final_out) __threadfence();  // partial visible before the ticket
+    }
+    if (fused && !final_out) {
+      named_sync(1, kCW * 32);
+      if (tid == 0) {
+        int *ctr = ws.split_counters + (long long)un.b * ws.n_kv_heads + un.g;
+        const int old = atomicAdd(ctr, 1);
+        const int last = old == n_b - 1;
+        if (last) *ctr = 0;  // ready for the next launch
+        *s_ticket = last;
+      }
+      named_sync(1, kCW * 32);
+      if (*s_ticket) {
+        __threadfence();
+        for (int h = warp; h < G; h += kCW) {
+          const long long row = (long long)un.b * Hq + hq0 + h;
+          float M, den;
+          float4 o4;
+          merge_row<D>(ws.ml_part + row * pl.S * 2, ws.o_part + row * pl.S * D, n_b, lane, M,
+                       den, o4);
+          merge_store<D>(ws, row, a.flags, lane, M, den, o4);
+        }
+      }
+    }
+    named_sync(1, kCW * 32);  // s_ml, red and the ticket are reused by the next unit
+  }
+}
+
+using TmapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+TmapEncodeFn tmap_encoder() {
+  static TmapEncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<TmapEncodeFn>(p);
+  }
+  return fn;
+}
+
+// 3-D view [NL * pool_slots][Hkv][D] of a pool; box = 16 slots x 1 head x 64 cols.
+bool encode_pool_map(CUtensorMap *m, void *base, const pkv_workspace &ws) {
+  TmapEncodeFn enc = tmap_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)ws.head_dim, (cuuint64_t)ws.n_kv_heads,
+                              (cuuint64_t)ws.n_layers * (cuuint64_t)ws.pool_slots};
+  const cuuint64_t strides[2] = {(cuuint64_t)ws.head_dim * 2,
+                                 (cuuint64_t)ws.head_dim * 2 * ws.n_kv_heads};
+  const cuuint32_t box[3] = {64, 1, 16};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
+  using C = MCfg<D, G>;
+  auto kern = decode_mma_kernel<D, G>;
+  static int occ_cache[64] = {0};
+  static int sms_cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int di = dev & 63;
+  if (occ_cache[di] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    int occ = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kMThreads, C::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms_cache[di] = sms;
+    occ_cache[di] = occ > 0 ? occ : 1;
+  }
+  CUtensorMap tmk, tmv;
+  memset(&tmk, 0, sizeof(tmk));
+  memset(&tmv, 0, sizeof(tmv));
+  const pkv_workspace &ws = a.ws;
+  int use_tma = ws.index_mode == PKV_IDX_PAGE_TABLE && ws.page_size % 16 == 0 &&
+                (long long)ws.n_layers * ws.pool_slots < 0x7fffffffll &&
+                !(a.flags & PKV_FLAG_FORCE_GATHER);
+  if (use_tma)
+    use_tma = encode_pool_map(&tmk, ws.k_pool, ws) && encode_pool_map(&tmv, ws.v_pool, ws);
+  const long long units = (long long)a.num_splits * a.batch * ws.n_kv_heads;
+  const long long cap = (long long)sms_cache[di] * occ_cache[di];
+  const int grid = (int)(units < cap ? units : cap);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, kMThreads, C::SMEM, st>>>(a, tmk, tmv, use_tma);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_mma_supported(int head_dim, int group) {
+  return (head_dim == 64 || head_dim == 128) &&
+         (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+}
+
+cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t st) {
+  const int D = a.ws.head_dim, G = a.ws.n_q_heads / a.ws.n_kv_heads;
+#define PKV_MMA_CASE(DD, GG) \
+  if (D == DD && G == GG) return launch_mma_one<DD, GG>(a, st);
+  PKV_MMA_CASE(128, 1) PKV_MMA_CASE(128, 2) PKV_MMA_CASE(128, 4) PKV_MMA_CASE(128, 8)
+  PKV_MMA_CASE(128, 16) PKV_MMA_CASE(64, 1) PKV_MMA_CASE(64, 2) PKV_MMA_CASE(64, 4)
+  PKV_MMA_CASE(64, 8) PKV_MMA_CASE(64, 16)
+#undef PKV_MMA_CASE
+  return cudaErrorNotSupported;
+}
+
+}  // namespace pkv

@@ -13,29 +13,60 @@ namespace pkv {
 
 struct Plan {
   int batch, hkv, S, chunk, n_units;
+  // Compact enumeration: exclusive prefix over requests of their split counts
+  // (shared memory, batch + 1 entries); NULL = dense enumeration.
+  const int *pref = nullptr;
 };
+
+constexpr int kMaxCompactBatch = 1024;
 
 struct Unit {
   int u, b, g, c, t0, t1;
+  int L;  // the request's (checked) length
 };
+
+// Length of request b as the kernels use it (0 if out of range).
+__device__ __forceinline__ int usable_len(const pkv_workspace &ws, int b) {
+  int L = ws.seq_lens[b];
+  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  if (L < 0 || (long long)L > cap) return 0;
+  if (ws.index_mode == PKV_IDX_FLAT && L > 0) {
+    const int base = ws.kv_indptr[b];
+    if (base < 0 || (long long)base + L > ws.max_total_tokens) return 0;
+  }
+  return L;
+}
+
+__device__ __forceinline__ int split_count(const pkv_workspace &ws, int b, int chunk) {
+  const int L = usable_len(ws, b);
+  return L > 0 ? (L + chunk - 1) / chunk : 0;
+}
 
 __device__ __forceinline__ Unit unit_at(const pkv_workspace &ws, const Plan &pl, int u) {
   Unit x;
   x.u = u;
-  const int hb = pl.batch * pl.hkv;
-  x.c = u / hb;
-  const int r = u - x.c * hb;
-  x.b = r / pl.hkv;
-  x.g = r - x.b * pl.hkv;
-  int L = ws.seq_lens[x.b];
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
-  if (L < 0 || (long long)L > cap) L = 0;  // flagged by the prologue of CTA 0
-  if (ws.index_mode == PKV_IDX_FLAT && L > 0) {
-    const int base = ws.kv_indptr[x.b];
-    if (base < 0 || (long long)base + L > ws.max_total_tokens) L = 0;
+  if (pl.pref) {
+    // u = (pair, g) over the non-empty (request, split) pairs in request order.
+    const int w = u / pl.hkv;
+    x.g = u - w * pl.hkv;
+    int lo = 0, hi = pl.batch - 1;  // last b with pref[b] <= w
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pl.pref[mid] <= w) lo = mid;
+      else hi = mid - 1;
+    }
+    x.b = lo;
+    x.c = w - pl.pref[lo];
+  } else {
+    const int hb = pl.batch * pl.hkv;
+    x.c = u / hb;
+    const int r = u - x.c * hb;
+    x.b = r / pl.hkv;
+    x.g = r - x.b * pl.hkv;
   }
+  x.L = usable_len(ws, x.b);  // out-of-range lengths are flagged by CTA 0's prologue
   x.t0 = x.c * pl.chunk;
-  x.t1 = min(x.t0 + pl.chunk, L);
+  x.t1 = min(x.t0 + pl.chunk, x.L);
   return x;
 }
 
@@ -84,6 +115,86 @@ __device__ __forceinline__ int batch_max_len(const pkv_workspace &ws, int batch,
   if ((threadIdx.x & 31) == 0) atomicMax(s_max, mx);
   __syncthreads();
   return *s_max;
+}
+
+// Block-wide exclusive prefix of the requests' split counts into
+// s_pref[0..batch] (batch <= kMaxCompactBatch); s_tmp holds 32 ints.  Every
+// thread of the block must call it; returns the number of non-empty
+// (request, split) pairs.
+__device__ __forceinline__ int batch_split_prefix(const pkv_workspace &ws, int batch, int chunk,
+                                                  int *s_pref, int *s_tmp) {
+  const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (batch + nt - 1) / nt;
+  const int lo = min(batch, tid * per), hi = min(batch, lo + per);
+  int local = 0;
+  for (int b = lo; b < hi; ++b) local += split_count(ws, b, chunk);
+  int incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) s_tmp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (nt + 31) / 32 ? s_tmp[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += v;
+    }
+    s_tmp[lane] = w;
+  }
+  __syncthreads();
+  int run = (warp > 0 ? s_tmp[warp - 1] : 0) + incl - local;
+  for (int b = lo; b < hi; ++b) {
+    s_pref[b] = run;
+    run += split_count(ws, b, chunk);
+  }
+  if (tid == nt - 1) s_pref[batch] = run;
+  __syncthreads();
+  return s_pref[batch];
+}
+
+// Where a request's index entries start: the table row (page mode) or the
+// kv_indptr offset (flat mode).  ok = false for a table row out of range.
+struct ReqIndex {
+  long long base;
+  bool ok;
+};
+
+__device__ __forceinline__ ReqIndex req_index(const pkv_workspace &ws, int b) {
+  ReqIndex r;
+  if (ws.index_mode == PKV_IDX_FLAT) {
+    r.base = ws.kv_indptr[b];
+    r.ok = true;  // usable_len already checked the range against max_total_tokens
+  } else {
+    const int row = ws.req_pool_indices[b];
+    r.ok = row >= 0 && row < ws.max_reqs;
+    r.base = r.ok ? (long long)row * ws.max_pages_per_req : 0;
+  }
+  return r;
+}
+
+// Raw index entry of token tok (flat: its slot; page mode: its page id).
+__device__ __forceinline__ int raw_index(const pkv_workspace &ws, const ReqIndex &ri, int tok) {
+  if (!ri.ok) return -1;
+  return ws.index_mode == PKV_IDX_FLAT ? ws.kv_indices[ri.base + tok]
+                                       : ws.page_table[ri.base + tok / ws.page_size];
+}
+
+// Slot from a raw entry, or -1 with *kind set to the error bit.
+__device__ __forceinline__ long long slot_from_raw(const pkv_workspace &ws, int raw, int tok,
+                                                   int &kind) {
+  if (ws.index_mode == PKV_IDX_FLAT) {
+    if (raw >= 0 && raw < ws.pool_slots) return raw;
+    kind = PKV_DEVERR_SLOT;
+    return -1;
+  }
+  const int P = ws.page_size;
+  if (raw >= 0 && raw < ws.pool_slots / P) return (long long)raw * P + tok % P;
+  kind = PKV_DEVERR_PAGE;
+  return -1;
 }
 
 // Slot of token `tok` of request b, or -1 with *kind set to the error bit.

@@ -20,12 +20,20 @@ struct DecodeArgs {
   float scale;
   int num_splits;
   int flags;
+  const void *k_new;  // fused append source (bf16 [batch, Hkv, D]) or NULL
+  const void *v_new;
+  int fused_merge;    // 1: the last split of each (request, KV head) merges
 };
 
 // CUDA-core split-KV decode.  Returns cudaErrorNotSupported for shapes
 // without an instantiation.
 cudaError_t launch_decode_simt(const DecodeArgs &a, cudaStream_t st);
 bool decode_simt_supported(int head_dim, int group);
+
+// Tensor-core (warp mma) split-KV decode; same contract as the SIMT kernel,
+// plus the fused append and merge.
+cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t st);
+bool decode_mma_supported(int head_dim, int group);
 
 cudaError_t launch_merge(const pkv_workspace &ws, int batch, int num_splits, int flags,
                          cudaStream_t st);

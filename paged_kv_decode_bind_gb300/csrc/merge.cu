@@ -2,7 +2,9 @@
 // decode_o_part / decode_ml_part buffers).  One warp per (b, query head):
 //   M = max over non-empty splits of m_s,  w_s = l_s * exp(m_s - M),
 //   out = sum_s w_s o_s / sum_s w_s,  lse = M + ln(sum_s w_s).
+#include "decode_plan.cuh"
 #include "kernels.cuh"
+#include "merge.cuh"
 
 namespace pkv {
 
@@ -13,53 +15,18 @@ constexpr int kMergeWarps = 4;
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_kernel(pkv_workspace ws, int batch, int S, int flags) {
+  __shared__ int s_max_len;
+  // Splits past a request's end were never written: merge only the first
+  // ceil(L_b / chunk), with chunk derived exactly as the attention kernel did.
+  const int chunk = split_chunk(batch_max_len(ws, batch, &s_max_len), S, ws.page_size);
   const int lane = threadIdx.x & 31;
   const long long wg = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-  const int Hq = ws.n_q_heads;
-  if (wg >= (long long)batch * Hq) return;
-  const float *ml = ws.ml_part + wg * S * 2;
-  const float *op = ws.o_part + wg * S * D;
-  constexpr int NV = D / 4;  // float4 vectors per row
-  static_assert(NV <= 32, "one float4 per lane");
-
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32)
-    if (ml[2 * s + 1] > 0.f) M = fmaxf(M, ml[2 * s]);
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, d));
-
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float l = ml[2 * s + 1];
-      if (l > 0.f) {
-        const float w = l * expf(ml[2 * s] - M);
-        den += w;
-        if (lane < NV) {
-          const float4 o = reinterpret_cast<const float4 *>(op + (long long)s * D)[lane];
-          acc.x = fmaf(w, o.x, acc.x);
-          acc.y = fmaf(w, o.y, acc.y);
-          acc.z = fmaf(w, o.z, acc.z);
-          acc.w = fmaf(w, o.w, acc.w);
-        }
-      }
-    }
-  }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  if (lane < NV) {
-    const float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (flags & PKV_FLAG_OUT_F32) {
-      reinterpret_cast<float4 *>(static_cast<float *>(ws.out) + wg * D)[lane] = r;
-    } else {
-      uint2 pk;
-      pk.x = f32_to_bf16_bits(r.x) | (f32_to_bf16_bits(r.y) << 16);
-      pk.y = f32_to_bf16_bits(r.z) | (f32_to_bf16_bits(r.w) << 16);
-      reinterpret_cast<uint2 *>(static_cast<uint16_t *>(ws.out) + wg * D)[lane] = pk;
-    }
-  }
-  if (lane == 0 && (flags & PKV_FLAG_WRITE_LSE) && ws.lse)
-    ws.lse[wg] = den > 0.f ? M + logf(den) : -INFINITY;
+  if (wg >= (long long)batch * ws.n_q_heads) return;
+  const int n = min(S, split_count(ws, (int)(wg / ws.n_q_heads), chunk));
+  float M, den;
+  float4 acc;
+  merge_row<D>(ws.ml_part + wg * S * 2, ws.o_part + wg * S * D, n, lane, M, den, acc);
+  merge_store<D>(ws, wg, flags, lane, M, den, acc);
 }
 
 }  // namespace

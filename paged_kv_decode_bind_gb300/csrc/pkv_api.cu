@@ -69,6 +69,7 @@ size_t pkv_workspace_bytes(const pkv_workspace *ws, const char *which) {
   if (!strcmp(which, "out")) return B * hq * D * 4;
   if (!strcmp(which, "lse")) return B * hq * 4;
   if (!strcmp(which, "err")) return 4;
+  if (!strcmp(which, "split_counters")) return B * hkv * 4;
   return 0;
 }
 
@@ -105,22 +106,25 @@ pkv_status pkv_bind_step(const pkv_workspace *ws, int batch, int mode, int layer
   return PKV_OK;
 }
 
-int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint, int num_sms) {
+int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint,
+                      long long total_tokens_hint, int num_sms) {
   if (!ws || batch <= 0 || max_seq_len_hint <= 0 || num_sms <= 0 || ws->n_kv_heads <= 0)
     return 1;
-  const int min_chunk = 128;
-  const long long hb = (long long)batch * ws->n_kv_heads;
-  const long long target = 3ll * num_sms;
-  long long S = (target + hb - 1) / hb;
-  const long long by_len = (max_seq_len_hint + min_chunk - 1) / min_chunk;
-  if (S > by_len) S = by_len;
+  const long long min_chunk = 128;
+  const long long total =
+      total_tokens_hint > 0 ? total_tokens_hint : (long long)batch * max_seq_len_hint;
+  const long long target_units = 4ll * num_sms;  // ~2 resident blocks x 2 units each
+  long long chunk = ((long long)ws->n_kv_heads * total + target_units - 1) / target_units;
+  if (chunk < min_chunk) chunk = min_chunk;
+  long long S = (max_seq_len_hint + chunk - 1) / chunk;
   if (S > ws->max_splits) S = ws->max_splits;
   if (S < 1) S = 1;
   return (int)S;
 }
 
-pkv_status pkv_decode_attn(const pkv_workspace *ws, int batch, int layer, const void *q,
-                           float scale, int num_splits, int flags, pkv_stream_t stream) {
+static pkv_status decode_common(const pkv_workspace *ws, int batch, int layer, const void *q,
+                                const void *k_new, const void *v_new, float scale,
+                                int num_splits, int flags, int fused, pkv_stream_t stream) {
   pkv_status st = check_shape(ws);
   if (st != PKV_OK) return st;
   if ((st = check_index(ws)) != PKV_OK) return st;
@@ -128,25 +132,47 @@ pkv_status pkv_decode_attn(const pkv_workspace *ws, int batch, int layer, const 
   if (layer >= ws->n_layers) return PKV_ERR_CAPACITY;
   if (batch > ws->max_batch || num_splits > ws->max_splits) return PKV_ERR_CAPACITY;
   const int G = ws->n_q_heads / ws->n_kv_heads;
-  if (!decode_simt_supported(ws->head_dim, G)) return PKV_ERR_UNSUPPORTED;
-  if (flags & PKV_FLAG_FORCE_MMA) return PKV_ERR_UNSUPPORTED;
+  if ((flags & PKV_FLAG_FORCE_SIMT) && (flags & (PKV_FLAG_FORCE_MMA | PKV_FLAG_FORCE_GATHER)))
+    return PKV_ERR_INVALID;
+  const bool mma_ok = decode_mma_supported(ws->head_dim, G);
+  const bool simt_ok = decode_simt_supported(ws->head_dim, G);
+  const bool use_mma = (flags & PKV_FLAG_FORCE_MMA) || (mma_ok && !(flags & PKV_FLAG_FORCE_SIMT));
+  if (use_mma ? !mma_ok : !simt_ok) return PKV_ERR_UNSUPPORTED;
   if (!q || !ws->k_pool || !ws->v_pool || !ws->out) return PKV_ERR_INVALID;
   if (!aligned16(q) || !aligned16(ws->k_pool) || !aligned16(ws->v_pool) || !aligned16(ws->out))
     return PKV_ERR_INVALID;
   if (num_splits > 1 && (!ws->o_part || !ws->ml_part || !aligned16(ws->o_part)))
     return PKV_ERR_INVALID;
   if ((flags & PKV_FLAG_WRITE_LSE) && !ws->lse) return PKV_ERR_INVALID;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new) || !ws->out_loc)) return PKV_ERR_INVALID;
+  if (fused && num_splits > 1 && !ws->split_counters) return PKV_ERR_INVALID;
   if ((long long)num_splits * batch * ws->n_kv_heads > 0x7fffffffll) return PKV_ERR_CAPACITY;
   if (batch == 0) return PKV_OK;
-  DecodeArgs a;
-  a.ws = *ws;
-  a.batch = batch;
-  a.layer = layer;
-  a.q = q;
-  a.scale = scale;
-  a.num_splits = num_splits;
-  a.flags = flags;
-  return from_cuda(launch_decode_simt(a, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!use_mma && fused) {
+    // The CUDA-core attention has no fused form: run the three steps.
+    if (k_new && (st = from_cuda(launch_append(*ws, batch, layer, 1, k_new, v_new, s))) != PKV_OK)
+      return st;
+    DecodeArgs a{*ws, batch, layer, q, scale, num_splits, flags, nullptr, nullptr, 0};
+    if ((st = from_cuda(launch_decode_simt(a, s))) != PKV_OK) return st;
+    if (num_splits > 1) return from_cuda(launch_merge(*ws, batch, num_splits, flags, s));
+    return PKV_OK;
+  }
+  DecodeArgs a{*ws, batch, layer, q, scale, num_splits, flags, k_new, v_new, fused};
+  return from_cuda(use_mma ? launch_decode_mma(a, s) : launch_decode_simt(a, s));
+}
+
+pkv_status pkv_decode_attn(const pkv_workspace *ws, int batch, int layer, const void *q,
+                           float scale, int num_splits, int flags, pkv_stream_t stream) {
+  return decode_common(ws, batch, layer, q, nullptr, nullptr, scale, num_splits, flags, 0,
+                       stream);
+}
+
+pkv_status pkv_decode_layer(const pkv_workspace *ws, int batch, int layer, const void *q,
+                            const void *k_new, const void *v_new, float scale, int num_splits,
+                            int flags, pkv_stream_t stream) {
+  return decode_common(ws, batch, layer, q, k_new, v_new, scale, num_splits, flags, 1, stream);
 }
 
 pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits, int flags,

@@ -33,7 +33,8 @@ class DecodeRunner:
     """Drives libpkv for one batch size on one stream."""
 
     def __init__(self, ws: Workspace, batch: int, *, num_splits: int = 1, flags: int = 0,
-                 scale: float | None = None, stream: torch.cuda.Stream | None = None):
+                 scale: float | None = None, stream: torch.cuda.Stream | None = None,
+                 fused: bool = True):
         self.ws = ws
         self.batch = batch
         sh = ws.shape
@@ -49,17 +50,30 @@ class DecodeRunner:
                                 device=dev)
         self.v_in = torch.zeros_like(self.k_in)
         self.graph = None
+        self.fused = fused
         flat = sh["index_mode"] == _abi.PKV_IDX_FLAT
         # kernels one step launches: bind (+ flat index build), then per layer
-        # append + attention (+ merge when split)
-        self.launches_per_step = 1 + int(flat) + NL * (2 + (1 if num_splits > 1 else 0))
+        # one fused kernel, or append + attention (+ merge when split)
+        split = num_splits > 1
+        per_layer = 1 if fused and not (flags & _abi.PKV_FLAG_FORCE_SIMT) else 2 + int(split)
+        self.launches_per_step = 1 + int(flat) + NL * per_layer
 
     # --- pieces -------------------------------------------------------------
     def bind(self, mode=_abi.PKV_BIND_STEADY):
         _abi.pkv_bind_step(self.ws, self.batch, mode, 0, 0, None, None, self._s())
 
     def layer(self, l, events=None):
+        """Layer l: one fused launch (append + attention + merge), or the
+        three separate kernels when built with fused=False."""
         s = self._s()
+        if self.fused:
+            if events is not None:
+                events[0].record(s)
+            _abi.pkv_decode_layer(self.ws, self.batch, l, self.q_in[l], self.k_in[l],
+                                  self.v_in[l], self.scale, self.num_splits, self.flags, s)
+            if events is not None:
+                events[1].record(s)
+            return
         _abi.pkv_bind_step(self.ws, self.batch, _abi.PKV_BIND_APPEND_ONLY, l, 1, self.k_in[l],
                            self.v_in[l], s)
         if events is not None:

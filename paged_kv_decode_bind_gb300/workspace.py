@@ -47,6 +47,7 @@ class Workspace:
         self.out = torch.zeros((max_batch, n_q_heads, head_dim), dtype=torch.float32, device=dev)
         self.lse = torch.zeros((max_batch, n_q_heads), dtype=torch.float32, device=dev)
         self.err = torch.zeros(1, **i32)
+        self.split_counters = torch.zeros(max(1, max_batch * n_kv_heads), **i32)
         self.struct = _abi.PkvWorkspace(
             **self.shape,
             k_pool=_abi._ptr(self.k_pool) if pools else None,
@@ -56,7 +57,8 @@ class Workspace:
             position_ids=self.position_ids.data_ptr(), kv_indptr=self.kv_indptr.data_ptr(),
             out_loc=self.out_loc.data_ptr(), kv_indices=self.kv_indices.data_ptr(),
             o_part=self.o_part.data_ptr(), ml_part=self.ml_part.data_ptr(),
-            out=self.out.data_ptr(), lse=self.lse.data_ptr(), err=self.err.data_ptr())
+            out=self.out.data_ptr(), lse=self.lse.data_ptr(), err=self.err.data_ptr(),
+            split_counters=self.split_counters.data_ptr())
 
     # typed views of the output buffer --------------------------------------
     def out_bf16(self, batch):

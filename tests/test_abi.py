@@ -30,8 +30,8 @@ def test_exports_match_header():
 
 
 def test_struct_layout():
-    # 12 int32 shape fields then 14 pointers, no padding on LP64.
-    assert ctypes.sizeof(_abi.PkvWorkspace) == 12 * 4 + 14 * 8
+    # 12 int32 shape fields then 15 pointers, no padding on LP64.
+    assert ctypes.sizeof(_abi.PkvWorkspace) == 12 * 4 + 15 * 8
     assert _abi.PkvWorkspace.k_pool.offset == 48
 
 
@@ -42,7 +42,8 @@ def _ws(**kw):
     fake = 1 << 20  # non-null, 16-byte aligned; never dereferenced (validation fails first)
     ptrs = dict(k_pool=fake, v_pool=fake, req_pool_indices=fake, page_table=fake,
                 seq_lens=fake, position_ids=fake, kv_indptr=fake, out_loc=fake,
-                kv_indices=fake, o_part=fake, ml_part=fake, out=fake, lse=fake, err=fake)
+                kv_indices=fake, o_part=fake, ml_part=fake, out=fake, lse=fake, err=fake,
+                split_counters=fake)
     shape.update({k: v for k, v in kw.items() if k in shape})
     ptrs.update({k: v for k, v in kw.items() if k in ptrs})
     return _abi.PkvWorkspace(**shape, **ptrs)
@@ -73,14 +74,14 @@ def test_workspace_bytes():
     (dict(lse=None), 1, 0, 1, P.PKV_FLAG_WRITE_LSE, P.PKV_ERR_INVALID),
     (dict(index_mode=1), 1, 0, 1, 0, P.PKV_ERR_INVALID),                     # flat needs P == 1
     (dict(pool_slots=60), 1, 0, 1, 0, P.PKV_ERR_INVALID),                    # slots % P
-    (dict(), 1, 0, 1, P.PKV_FLAG_FORCE_MMA | 0, None),
+    (dict(n_q_heads=32, n_kv_heads=2), 1, 0, 1, P.PKV_FLAG_FORCE_SIMT, P.PKV_ERR_UNSUPPORTED),
+    (dict(), 1, 0, 1, P.PKV_FLAG_FORCE_SIMT | P.PKV_FLAG_FORCE_MMA, P.PKV_ERR_INVALID),
+    (dict(), 1, 0, 1, P.PKV_FLAG_FORCE_SIMT | P.PKV_FLAG_FORCE_GATHER, P.PKV_ERR_INVALID),
+    (dict(n_q_heads=64, n_kv_heads=2), 1, 0, 1, P.PKV_FLAG_FORCE_MMA, P.PKV_ERR_UNSUPPORTED),
 ])
 def test_decode_host_validation(kw, batch, layer, splits, flags, status):
+    # Every case here must fail host validation: nothing may be launched.
     ws = _ws(**kw)
-    if status is None:
-        # FORCE_MMA on a shape without a tensor-core kernel must be refused, not run.
-        ws = _ws(n_q_heads=2, n_kv_heads=2)
-        status = P.PKV_ERR_UNSUPPORTED
     got = P.pkv_decode_attn(ws, batch, layer, 1 << 20, 0.1, splits, flags, 0, check=False)
     assert got == status, (got, status)
 
@@ -100,16 +101,29 @@ def test_bind_and_merge_host_validation():
     assert P.pkv_merge_partials(ws, 2, 9, 0, 0, check=False) == P.PKV_ERR_CAPACITY
     assert P.pkv_decode_attn(ws, 0, 0, 1 << 20, 0.1, 1, 0, 0, check=False) == P.PKV_OK
     assert P.pkv_merge_partials(None, 1, 2, 0, 0, check=False) == P.PKV_ERR_INVALID
+    # fused layer: k/v rows both or neither; split counters needed when S > 1
+    f = 1 << 20
+    assert P.pkv_decode_layer(ws, 1, 0, f, f, None, 0.1, 1, 0, 0, check=False) == \
+        P.PKV_ERR_INVALID
+    assert P.pkv_decode_layer(_ws(split_counters=None), 1, 0, f, f, f, 0.1, 2, 0, 0,
+                              check=False) == P.PKV_ERR_INVALID
+    assert P.pkv_decode_layer(ws, 5, 0, f, f, f, 0.1, 1, 0, 0, check=False) == \
+        P.PKV_ERR_CAPACITY
+    assert P.pkv_decode_layer(ws, 0, 0, f, f, f, 0.1, 2, 0, 0, check=False) == P.PKV_OK
 
 
 def test_choose_splits():
-    ws = _ws(max_splits=64, n_kv_heads=8, n_q_heads=32)
-    assert P.pkv_choose_splits(ws, 1, 65536, 152) == 57   # ceil(456 / 8)
-    assert P.pkv_choose_splits(ws, 4, 2048, 152) == 15    # ceil(456 / 32)
-    assert P.pkv_choose_splits(ws, 4, 1000, 152) == 8     # >= 128 tokens per split
-    assert P.pkv_choose_splits(ws, 64, 4096, 152) == 1
-    assert P.pkv_choose_splits(_ws(max_splits=4), 1, 65536, 152) == 4
-    assert P.pkv_choose_splits(ws, 0, 10, 152) == 1
+    ws = _ws(max_splits=128, n_kv_heads=8, n_q_heads=32)
+    # one 65536-token request: chunk = ceil(8 * 65536 / 608) = 863 -> S = 76
+    assert P.pkv_choose_splits(ws, 1, 65536, 65536, 152) == 76
+    # short batch: the 128-token floor decides
+    assert P.pkv_choose_splits(ws, 4, 2048, 6500, 152) == 16
+    # skewed batch: the total, not the longest request, sets the split length
+    assert P.pkv_choose_splits(ws, 16, 8192, 14500, 152) == 43
+    # no total given: batch * max
+    assert P.pkv_choose_splits(ws, 4, 2048, 0, 152) == 16
+    assert P.pkv_choose_splits(_ws(max_splits=4), 1, 65536, 65536, 152) == 4
+    assert P.pkv_choose_splits(ws, 0, 10, 10, 152) == 1
 
 
 def test_steady_predicate_matches_oracle():
