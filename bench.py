@@ -43,6 +43,11 @@ def parse_args(argv=None):
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--splits", type=int, default=0, help="0 = pkv_choose_splits")
     ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--unfused", action="store_true", help="separate append/attention/merge")
+    ap.add_argument("--no-kernel-events", action="store_true",
+                    help="skip the graphs with per-kernel event nodes")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -267,14 +272,16 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     from paged_kv_decode_bind_gb300 import dist as D
-    p = W.workload(args.workload, batch=args.batch, steps=ROUND,
+    p = W.workload(args.workload, batch=args.batch, steps=ROUND, n_layers=args.layers,
                    seed=D.rank_seed(20260000 + W.WORKLOADS.index(args.workload) + 1, rank))
     B, NL = p.batch, p.n_layers
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     shape_only = A.PkvWorkspace(n_kv_heads=p.n_kv_heads, max_splits=1 << 20)
-    S = args.splits or A.pkv_choose_splits(shape_only, B, int(p.seq_lens.max()) + ROUND, sms)
+    S = args.splits or A.pkv_choose_splits(shape_only, B, int(p.seq_lens.max()) + ROUND,
+                                           int(p.seq_lens.sum()) + B * ROUND // 2, sms)
     ws = Workspace.from_problem(p, max_splits=S, device=dev)
-    run = DecodeRunner(ws, B, num_splits=S, flags=args.flags, scale=p.scale)
+    run = DecodeRunner(ws, B, num_splits=S, flags=args.flags, scale=p.scale,
+                       fused=not args.unfused)
     q, k, v = W.step_inputs(p, 0)
     run.q_in.copy_(q)
     run.k_in.copy_(k)
@@ -282,26 +289,36 @@ def run_ours(args, rank, world, local_rank):
     lens0 = ws.seq_lens[:B].clone()
     L0 = p.seq_lens.tolist()
 
-    # One graph per position in the round, each with its own events around
-    # every layer's attention kernel.
+    # One graph per position in the round (the graph body is the same; the
+    # lengths advance on the device).  Plain graphs are timed for the value;
+    # graphs with event nodes around every layer's attention kernel give the
+    # event-bracketed per-kernel times (the nodes themselves cost time, so
+    # those are an upper bound); a bind-only graph gives the bind time.
     try:
         torch.cuda.Event(enable_timing=True, external=True)
-        ext = True
+        ext = not args.no_kernel_events
     except TypeError:
         ext = False
+    plain = [run.capture(A.PKV_BIND_STEADY) for _ in range(ROUND)]
     graphs, events = [], []
-    for j in range(ROUND):
-        evs = [(torch.cuda.Event(enable_timing=True, external=ext),
-                torch.cuda.Event(enable_timing=True, external=ext)) for _ in range(NL)]
-        g = run.capture(A.PKV_BIND_STEADY, evs if ext else None)
-        graphs.append(g)
-        events.append(evs)
+    if ext:
+        for j in range(ROUND):
+            evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in range(NL)]
+            graphs.append(run.capture(A.PKV_BIND_STEADY, evs))
+            events.append(evs)
+    bind_graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side), torch.cuda.graph(bind_graph, stream=side):
+        run.bind(A.PKV_BIND_STEADY)
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
 
-    def step(i):
+    def step(i, which=plain):
         if i % ROUND == 0:
             ws.seq_lens[:B].copy_(lens0)
-        graphs[i % ROUND].replay()
+        which[i % ROUND].replay()
 
     def step_bytes(i):
         j = i % ROUND
@@ -316,6 +333,16 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
+    def timed(fn, n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
     # ---- device-timed region: inputs resident in HBM ----
     K = args.steps
     clocks = ClockSampler(local_rank) if rank == 0 else None
@@ -323,29 +350,29 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if clocks:
         clocks.start()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record()
-    for i in range(K):
-        step(i)
-    t_end.record()
-    torch.cuda.synchronize()
+    dt = timed(step, K)
     clk = clocks.stop() if clocks else None
     barrier()
-    dt = t_start.elapsed_time(t_end) / 1e3
     total_bytes = sum(step_bytes(i) for i in range(K))
 
-    # per-kernel durations of the attention kernel (last replay of each graph)
-    attn_ms, attn_bytes = [], []
+    # bind alone, same rewinding, same number of replays
+    def bind_only(i):
+        if i % ROUND == 0:
+            ws.seq_lens[:B].copy_(lens0)
+        bind_graph.replay()
+    dt_bind = timed(bind_only, K)
+    ws.seq_lens[:B].copy_(lens0)
+    layer_s = (dt - dt_bind) / (K * NL)
+
+    # event-bracketed kernel times (upper bound), from the last round
+    attn_ms = []
     if ext:
-        last_round = range(max(0, K - ROUND), K)
-        for i in last_round:
-            j = i % ROUND
-            lens = [x + j + 1 for x in L0]
+        timed(lambda i: step(i, graphs), max(ROUND, (K // ROUND) * ROUND))
+        for j in range(ROUND):
             for l in range(NL):
                 a, b = events[j][l]
                 attn_ms.append(a.elapsed_time(b))
-                attn_bytes.append(algorithmic_bytes(lens, p, with_out=(S == 1)))
+    mean_layer_bytes = statistics.fmean(step_bytes(i) / NL for i in range(K))
 
     # ---- end to end: pinned host inputs in, result out, every step ----
     e2e = None
@@ -384,18 +411,23 @@ def run_ours(args, rank, world, local_rank):
         return
 
     peak, peak_src = peaks()
+    simt = bool(args.flags & A.PKV_FLAG_FORCE_SIMT)
     value = total_all / dt / 1e9
     layer_steps = K * NL
-    roof = None
+    layer_kernel = ("decode_mma_kernel (append+attention+merge, one launch per layer)"
+                    if run.fused and not simt else
+                    "append_kernel + " + ("decode_simt_kernel" if simt else "decode_mma_kernel") +
+                    (" + merge_kernel" if S > 1 else ""))
+    ach = mean_layer_bytes / layer_s / 1e9
+    roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+            "traffic": traffic_for(kernel_src_hash(), args.workload), "peak_source": peak_src,
+            "kernel": layer_kernel, "kernel_us_mean": layer_s * 1e6,
+            "kernel_time_from": "(step - bind) / layers, both timed with CUDA events over "
+                                "their own timed regions of graph replays",
+            "kernel_launches_timed": K * NL, "algorithmic_bytes_per_launch": mean_layer_bytes}
     if attn_ms:
-        mean_ms = statistics.fmean(attn_ms)
-        mean_bytes = statistics.fmean(attn_bytes)
-        ach = mean_bytes / (mean_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak, "traffic": traffic_for(kernel_src_hash(), args.workload),
-                "peak_source": peak_src, "kernel": "decode_simt_kernel",
-                "kernel_us_mean": mean_ms * 1e3, "kernel_launches_timed": len(attn_ms),
-                "algorithmic_bytes_per_launch": mean_bytes}
+        roof["attention_us_event_bracketed"] = statistics.fmean(attn_ms) * 1e3
+    roof["bind_us"] = dt_bind / K * 1e6
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": dt / K * 1e3,

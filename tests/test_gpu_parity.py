@@ -18,6 +18,14 @@ from parity import bf16_to_f64, check_attention, run_steps
 
 pytestmark = pytest.mark.gpu
 
+SIMT, MMA, GATHER = A.PKV_FLAG_FORCE_SIMT, A.PKV_FLAG_FORCE_MMA, A.PKV_FLAG_FORCE_GATHER
+# (flags, fused): the CUDA-core kernel; the tensor-core kernel with TMA boxes
+# (page sizes that are multiples of 16) or cp.async gathers; the fused layer
+# kernel (append + attention + merge in one launch) with either producer.
+PATHS = {"simt": (SIMT, False), "mma": (MMA, False), "gather": (MMA | GATHER, False),
+         "fused": (0, True), "fused_gather": (GATHER, True)}
+KERNELS = pytest.mark.parametrize("kern", list(PATHS), ids=list(PATHS))
+
 
 def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
@@ -39,52 +47,66 @@ def test_single_d64_full(cuda):
     assert r["max_err"] <= 1e-2
 
 
+@KERNELS
 @pytest.mark.parametrize("S", [1, 3, 8])
-def test_paged_gqa4_small(cuda, S):
+def test_paged_gqa4_small(cuda, S, kern):
     p = W.workload("gqa4_b4_paged", shrink=8, steps=1)
-    run_steps(p, S=S, check_partials=True, check_pool=True)
+    run_steps(p, S=S, check_partials=True, check_pool=True, flags=PATHS[kern][0],
+                  fused=PATHS[kern][1])
 
 
+@KERNELS
 @pytest.mark.parametrize("S", [1, 5])
-def test_flat_skewed_small(cuda, S):
+def test_flat_skewed_small(cuda, S, kern):
     p = W.workload("gqa4_b16_flat_skewed", shrink=16, steps=1)
-    run_steps(p, S=S, check_partials=True, check_pool=True)
+    run_steps(p, S=S, check_partials=True, check_pool=True, flags=PATHS[kern][0],
+                  fused=PATHS[kern][1])
 
 
+@KERNELS
 @pytest.mark.parametrize("B,S", [(1, 16), (4, 7)])
-def test_long_small(cuda, B, S):
+def test_long_small(cuda, B, S, kern):
     p = W.workload("gqa4_long_65536", batch=B, shrink=64, steps=1)
-    run_steps(p, S=S, check_partials=True)
+    run_steps(p, S=S, check_partials=True, flags=PATHS[kern][0], fused=PATHS[kern][1])
 
 
+@KERNELS
 @pytest.mark.parametrize("B,S", [(1, 1), (4, 4), (16, 2)])
-def test_gqa8_small(cuda, B, S):
+def test_gqa8_small(cuda, B, S, kern):
     p = W.workload("gqa8_graph_sweep", batch=B, shrink=16, steps=1)
-    run_steps(p, S=S, check_partials=True, check_pool=True)
+    run_steps(p, S=S, check_partials=True, check_pool=True, flags=PATHS[kern][0],
+                  fused=PATHS[kern][1])
 
 
-@pytest.mark.parametrize("G,D", [(1, 128), (2, 64), (8, 64), (4, 64)])
-def test_group_and_head_dim_variants(cuda, G, D):
+@KERNELS
+@pytest.mark.parametrize("G,D", [(1, 128), (2, 64), (8, 64), (4, 64), (16, 128), (16, 64)])
+def test_group_and_head_dim_variants(cuda, G, D, kern):
+    if G == 16 and kern == "simt":
+        pytest.skip("the CUDA-core kernel covers G <= 8")
     Hkv = 2
     p = W.make_problem("variant", batch=3, n_layers=2, n_q_heads=G * Hkv, n_kv_heads=Hkv,
                        head_dim=D, page_size=16, seq_lens=[1, 77, 200], seed=99, steps=1)
     for S in (1, 4):
-        run_steps(p, S=S, check_partials=True, check_pool=True)
+        run_steps(p, S=S, check_partials=True, check_pool=True, flags=PATHS[kern][0],
+                  fused=PATHS[kern][1])
 
 
+@KERNELS
 @pytest.mark.parametrize("P", [1, 4, 32])
-def test_page_sizes(cuda, P):
+def test_page_sizes(cuda, P, kern):
     p = W.make_problem("pages", batch=4, n_layers=1, n_q_heads=8, n_kv_heads=2, head_dim=128,
                        page_size=P, seq_lens=[33, 1, 130, 64], seed=123 + P,
                        index_mode=W.INDEX_PAGE_TABLE, steps=1)
     for S in (1, 3):
-        run_steps(p, S=S, check_partials=True, check_pool=True)
+        run_steps(p, S=S, check_partials=True, check_pool=True, flags=PATHS[kern][0],
+                  fused=PATHS[kern][1])
 
 
-def test_multi_step_steady(cuda):
+@pytest.mark.parametrize("fused", [False, True])
+def test_multi_step_steady(cuda, fused):
     # 64 consecutive steady steps (+1 token each); the last step is compared.
     p = W.workload("gqa4_b4_paged", shrink=16, n_layers=1, steps=64)
-    r = run_steps(p, S=4, steps=64, check_pool=True)
+    r = run_steps(p, S=4, steps=64, check_pool=True, fused=fused)
     ws = r["ws"]
     assert ws.seq_lens[:p.batch].tolist() == [x + 64 for x in p.seq_lens.tolist()]
 
@@ -93,9 +115,10 @@ def test_cross_split_agreement(cuda):
     # fp32 outputs from different split counts agree within 1e-3.
     p = W.workload("gqa4_long_65536", batch=2, shrink=32, steps=1)
     outs = []
-    for S in (1, 2, 9, 32):
+    for S, fused in ((1, False), (2, False), (9, False), (32, False), (9, True), (32, True)):
         ws = Workspace.from_problem(p, max_splits=S)
-        run = DecodeRunner(ws, p.batch, num_splits=S, flags=A.PKV_FLAG_OUT_F32, scale=p.scale)
+        run = DecodeRunner(ws, p.batch, num_splits=S, flags=A.PKV_FLAG_OUT_F32, scale=p.scale,
+                           fused=fused)
         q, k, v = W.step_inputs(p, 0)
         run.q_in.copy_(q), run.k_in.copy_(k), run.v_in.copy_(v)
         run.step()
@@ -122,14 +145,15 @@ def test_lse_output(cuda):
         assert np.abs(ws.lse[:p.batch].cpu().numpy() - lse).max() <= 1e-3
 
 
-def test_graph_replay_bitexact(cuda):
+@pytest.mark.parametrize("fused", [False, True])
+def test_graph_replay_bitexact(cuda, fused):
     # A captured step replays to exactly the eager result (same kernels, same plan).
     p = W.workload("gqa8_graph_sweep", batch=8, shrink=16, steps=1)
     q, k, v = W.step_inputs(p, 0)
     res = []
     for use_graph in (False, True):
         ws = Workspace.from_problem(p, max_splits=4)
-        run = DecodeRunner(ws, p.batch, num_splits=4, scale=p.scale)
+        run = DecodeRunner(ws, p.batch, num_splits=4, scale=p.scale, fused=fused)
         run.q_in.copy_(q), run.k_in.copy_(k), run.v_in.copy_(v)
         if use_graph:
             run.capture()
@@ -166,12 +190,15 @@ def test_zero_length_request(cuda):
     # A request with no tokens gives zeros (and lse = -inf), with no error bit.
     p = W.make_problem("zero", batch=3, n_layers=1, n_q_heads=8, n_kv_heads=2, head_dim=128,
                        page_size=16, seq_lens=[10, 0, 50], seed=4)
-    for S in (1, 3):
+    for S, fused in ((1, False), (3, False), (1, True), (3, True)):
         ws = Workspace.from_problem(p, max_splits=S)
         q = W.normal_bf16((3, 8, 128), 5).to("cuda")
         A.pkv_bind_step(ws, 3, A.PKV_BIND_REBUILD)
-        A.pkv_decode_attn(ws, 3, 0, q, p.scale, S, A.PKV_FLAG_WRITE_LSE)
-        A.pkv_merge_partials(ws, 3, S, A.PKV_FLAG_WRITE_LSE)
+        if fused:
+            A.pkv_decode_layer(ws, 3, 0, q, None, None, p.scale, S, A.PKV_FLAG_WRITE_LSE)
+        else:
+            A.pkv_decode_attn(ws, 3, 0, q, p.scale, S, A.PKV_FLAG_WRITE_LSE)
+            A.pkv_merge_partials(ws, 3, S, A.PKV_FLAG_WRITE_LSE)
         torch.cuda.synchronize()
         out = bf16_to_f64(ws.out_bf16(3))
         assert np.all(out[1] == 0) and np.all(np.isneginf(ws.lse[1].cpu().numpy()))
@@ -188,7 +215,8 @@ def test_zero_length_request(cuda):
 
 def _bench_splits(p):
     ws_shape = A.PkvWorkspace(n_kv_heads=p.n_kv_heads, max_splits=256)
-    return A.pkv_choose_splits(ws_shape, p.batch, int(p.seq_lens.max()) + 1, _sms())
+    return A.pkv_choose_splits(ws_shape, p.batch, int(p.seq_lens.max()) + 1,
+                               int(p.seq_lens.sum()) + p.batch, _sms())
 
 
 @pytest.mark.parametrize("name,batch", [("gqa4_b4_paged", None), ("gqa4_b16_flat_skewed", None),
@@ -198,4 +226,24 @@ def test_full_size_sampled(cuda, name, batch):
     p = W.workload(name, batch=batch, steps=1)
     S = _bench_splits(p)
     layers = sorted({0, p.n_layers - 1})
-    run_steps(p, S=S, check_layers=layers, heads=_sample_heads(p, 12), check_partials=True)
+    # the fused layer kernel the benchmark times, then the unfused tensor-core path
+    for flags, fused in ((0, True), (MMA, False)):
+        run_steps(p, S=S, check_layers=layers, heads=_sample_heads(p, 12), check_partials=True,
+                  flags=flags, fused=fused)
+
+
+def test_kernels_agree(cuda):
+    # fp32 outputs of the CUDA-core and both tensor-core producers, same inputs.
+    p = W.workload("gqa8_graph_sweep", batch=4, shrink=8, steps=1)
+    outs = []
+    for kern in (SIMT, MMA, MMA | GATHER):
+        ws = Workspace.from_problem(p, max_splits=3)
+        run = DecodeRunner(ws, p.batch, num_splits=3, flags=kern | A.PKV_FLAG_OUT_F32,
+                           scale=p.scale)
+        q, k, v = W.step_inputs(p, 0)
+        run.q_in.copy_(q), run.k_in.copy_(k), run.v_in.copy_(v)
+        run.step()
+        torch.cuda.synchronize()
+        outs.append(ws.out_f32(p.batch).cpu().numpy())
+    assert np.abs(outs[0] - outs[1]).max() <= 1e-3
+    assert np.abs(outs[0] - outs[2]).max() <= 1e-3
