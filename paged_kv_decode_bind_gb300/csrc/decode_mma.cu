@@ -2,11 +2,15 @@
 // 14-16), optionally fused with the KV append (cache.py page, bullet 40) and
 // with the split merge.
 //
-// Math.  Per (request b, KV head g, split c) unit the query group is one
-// 16-row operand: S = Q_g K^T and O += P V are warp-level bf16
-// mma.m16n8k16 with fp32 accumulation (rows >= G are zero); P enters the
-// second product as P_hi + P_lo (two bf16 terms) so P V keeps ~16 mantissa
-// bits.  The K/V rows of a token are read from HBM once for all G heads.
+// Math.  Per (request b, KV head g, split c) unit both products keep the
+// token axis on the 16-row side of warp-level bf16 mma.m16n8k16 (fp32
+// accumulation) and the query group on the 8-wide side, so a group of up to
+// 8 heads needs no padding:  S^T = K Q_g^T (16 tokens x 8 heads per k-step of
+// 16 dims) and O^T += V^T P^T (16 dims x 8 heads per 16 tokens).  The C
+// fragment of S^T becomes the B fragment of P^T with one movmatrix transpose
+// per 8x8 block.  P enters as P_hi + P_lo (two bf16 terms) so P V keeps ~16
+// mantissa bits.  The K/V rows of a token are read from HBM once for all G
+// heads.
 //
 // Block.  4 consumer warps + 1 producer warp.  A tile is 64 tokens; consumer
 // warp w owns tokens [16w, 16w+16) of each tile with its own online-softmax
@@ -63,8 +67,9 @@ struct MCfg {
   static constexpr int HALF = kMT * 128;    // bytes of one half of a tile
   static constexpr int TILE = HALVES * HALF;
   static constexpr int KSTEPS = D / 16;
-  static constexpr int NT = D / 8;          // 8-wide output column tiles
-  static constexpr int RSTRIDE = D + 8;     // combine buffer row stride (floats)
+  static constexpr int NH = (G + 7) / 8;    // 8-wide head tiles
+  static constexpr int MT = D / 16;         // 16-row output (head_dim) tiles
+  static constexpr int RSTRIDE = D + 4;     // combine buffer row stride (floats)
   // dynamic shared memory: the K/V ring (1024-aligned for the swizzle) and
   // the combine buffer; small state lives in static shared memory.
   static constexpr int OFF_KV = 0;
@@ -347,14 +352,14 @@ __global__ void __launch_bounds__(kMThreads)
 
   // ---------------------------------------------------------- consumers ----
   const int grp = lane >> 2, tig = lane & 3;
-  const int r0 = grp, r1 = grp + 8;  // the two query-head rows this lane holds
+  // This lane's B/C columns are heads 2*tig + e (+ 8*n for the n-th head tile).
   const float qk_scale = a.scale * kLog2e;
   float *red = reinterpret_cast<float *>(smem + C::OFF_RED);
-  // ldmatrix lane addressing in the swizzled layout (fragment layouts of
-  // mma.m16n8k16): matrix mi = lane / 8, row rr = lane % 8 of that matrix.
+  // ldmatrix lane addressing in the swizzled layout: matrix mi = lane / 8,
+  // row rr = lane % 8 of that matrix.
   const int mi = lane >> 3, rr = lane & 7;
-  const int rowK = 16 * warp + (mi >> 1) * 8 + rr;  // K: tokens 0-7 / 8-15 by mi / 2
-  const int rowV = 16 * warp + (mi & 1) * 8 + rr;   // V: tokens by mi % 2
+  const int rowK = 16 * warp + (mi & 1) * 8 + rr;   // K as A: tokens 0-7 / 8-15 by mi % 2
+  const int rowV = 16 * warp + (mi >> 1) * 8 + rr;  // V^T as A: tokens by mi / 2
 
   int k = 0;
   for (int u = blockIdx.x; u < pl.n_units; u += gridDim.x) {
@@ -382,25 +387,34 @@ __global__ void __launch_bounds__(kMThreads)
     }
     const int ntiles = (un.t1 - un.t0 + kMT - 1) / kMT;
 
-    // Q fragments (A operand, rows = heads of the group; rows >= G are zero).
-    uint32_t qa[C::KSTEPS][4];
+    // Q^T as the B operand: b0 = Q[h][d0 + 2 tig ..], b1 = Q[h][d0 + 8 + 2 tig ..]
+    // for h = grp + 8 n (heads >= G are zero).
+    uint32_t qb[C::NH][C::KSTEPS][2];
     {
       const uint32_t *q32 = static_cast<const uint32_t *>(a.q);
-      const long long row0 = ((long long)un.b * Hq + hq0 + r0) * (D / 2);
-      const long long row1 = ((long long)un.b * Hq + hq0 + r1) * (D / 2);
 #pragma unroll
-      for (int ks = 0; ks < C::KSTEPS; ++ks) {
-        const int c = ks * 8 + tig;  // 32-bit column (two bf16)
-        qa[ks][0] = r0 < G ? q32[row0 + c] : 0u;
-        qa[ks][1] = r1 < G ? q32[row1 + c] : 0u;
-        qa[ks][2] = r0 < G ? q32[row0 + c + 4] : 0u;
-        qa[ks][3] = r1 < G ? q32[row1 + c + 4] : 0u;
+      for (int n = 0; n < C::NH; ++n) {
+        const int h = grp + 8 * n;
+        const long long row = ((long long)un.b * Hq + hq0 + h) * (D / 2);
+#pragma unroll
+        for (int ks = 0; ks < C::KSTEPS; ++ks) {
+          qb[n][ks][0] = h < G ? q32[row + ks * 8 + tig] : 0u;
+          qb[n][ks][1] = h < G ? q32[row + ks * 8 + tig + 4] : 0u;
+        }
       }
     }
-    float acc[C::NT][4];
+    // O^T accumulators: acc[n][mt] = O[h = 8n + 2 tig + {0,1}][d = 16 mt + grp (+8)]
+    float acc[C::NH][C::MT][4];
 #pragma unroll
-    for (int j = 0; j < C::NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int n = 0; n < C::NH; ++n)
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt) acc[n][mt][0] = acc[n][mt][1] = acc[n][mt][2] = acc[n][mt][3] = 0.f;
+    float m_run[C::NH][2], l_run[C::NH][2];
+#pragma unroll
+    for (int n = 0; n < C::NH; ++n) {
+      m_run[n][0] = m_run[n][1] = -INFINITY;
+      l_run[n][0] = l_run[n][1] = 0.f;
+    }
     int bad = 0;
 
     for (int it = 0; it < ntiles; ++it, ++k) {
@@ -421,69 +435,66 @@ __global__ void __launch_bounds__(kMThreads)
         if (nv > 0) {
           const uint32_t kt = kv_base + (2 * s) * C::TILE;
           const uint32_t vt = kt + C::TILE;
-          // ---- S = Q K^T: two 8-token column tiles ----
-          float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          // ---- S^T = K Q^T: rows = tokens grp / grp + 8, cols = heads ----
+          float sc[C::NH][4];
+#pragma unroll
+          for (int n = 0; n < C::NH; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
           for (int ks = 0; ks < C::KSTEPS; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kt + (ks >> 2) * C::HALF + swz(rowK, (ks & 3) * 2 + (mi & 1)), b0, b1, b2, b3);
-            mma_bf16_16816(sc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-            mma_bf16_16816(sc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-          }
-          // ---- online softmax (log2 units), rows r0 / r1 ----
-          float t0 = -INFINITY, t1 = -INFINITY;
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kt + (ks >> 2) * C::HALF + swz(rowK, (ks & 3) * 2 + (mi >> 1)), a0, a1, a2, a3);
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+            for (int n = 0; n < C::NH; ++n)
+              mma_bf16_16816(sc[n], a0, a1, a2, a3, qb[n][ks][0], qb[n][ks][1]);
+          }
+          // ---- online softmax over the tokens, per head (log2 units) ----
+          const bool v0 = grp < nv, v1 = grp + 8 < nv;
+          uint32_t bh[C::NH][2], bl[C::NH][2];  // P^T as B: tokens 0-7 / 8-15
+#pragma unroll
+          for (int n = 0; n < C::NH; ++n) {
+            float al[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const bool valid = nt * 8 + 2 * tig + e < nv;
-              sc[nt][e] = valid ? sc[nt][e] * qk_scale : -INFINITY;
-              sc[nt][2 + e] = valid ? sc[nt][2 + e] * qk_scale : -INFINITY;
-              t0 = fmaxf(t0, sc[nt][e]);
-              t1 = fmaxf(t1, sc[nt][2 + e]);
+              const float s0 = v0 ? sc[n][e] * qk_scale : -INFINITY;
+              const float s1 = v1 ? sc[n][2 + e] * qk_scale : -INFINITY;
+              float t = fmaxf(s0, s1);
+              t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 4));
+              t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 8));
+              t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 16));
+              const float mn = fmaxf(m_run[n][e], t);
+              al[e] = exp2f(m_run[n][e] - mn);
+              m_run[n][e] = mn;
+              const float p0 = exp2f(s0 - mn), p1 = exp2f(s1 - mn);
+              l_run[n][e] = l_run[n][e] * al[e] + p0 + p1;
+              sc[n][e] = p0;
+              sc[n][2 + e] = p1;
             }
-          t0 = quad_max(t0);
-          t1 = quad_max(t1);
-          const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
-          const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-          m0 = mn0;
-          m1 = mn1;
-          float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              sc[nt][e] = exp2f(sc[nt][e] - mn0);
-              sc[nt][2 + e] = exp2f(sc[nt][2 + e] - mn1);
-              ps0 += sc[nt][e];
-              ps1 += sc[nt][2 + e];
+            for (int mt = 0; mt < C::MT; ++mt) {
+              acc[n][mt][0] *= al[0];
+              acc[n][mt][1] *= al[1];
+              acc[n][mt][2] *= al[0];
+              acc[n][mt][3] *= al[1];
             }
-          l0 = l0 * al0 + ps0;
-          l1 = l1 * al1 + ps1;
 #pragma unroll
-          for (int j = 0; j < C::NT; ++j) {
-            acc[j][0] *= al0;
-            acc[j][1] *= al0;
-            acc[j][2] *= al1;
-            acc[j][3] *= al1;
+            for (int hlf = 0; hlf < 2; ++hlf) {
+              const float x = sc[n][2 * hlf], y = sc[n][2 * hlf + 1];
+              const uint32_t hi = pack_bf16x2(x, y);
+              const uint32_t lo = pack_bf16x2(x - bf16lo(hi), y - bf16hi(hi));
+              bh[n][hlf] = movmatrix_t(hi);
+              bl[n][hlf] = movmatrix_t(lo);
+            }
           }
-          // P as the A operand of O += P V (the C layout of S is the A layout
-          // of P), as P_hi + P_lo so P V keeps ~16 mantissa bits.
-          uint32_t ph[4], pl_[4];
+          // ---- O^T += V^T P^T: 16 head_dim rows per mma ----
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float x = sc[i >> 1][(i & 1) * 2], y = sc[i >> 1][(i & 1) * 2 + 1];
-            ph[i] = pack_bf16x2(x, y);
-            pl_[i] = pack_bf16x2(x - bf16lo(ph[i]), y - bf16hi(ph[i]));
-          }
+          for (int mt = 0; mt < C::MT; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vt + (mt >> 2) * C::HALF + swz(rowV, (mt & 3) * 2 + (mi & 1)), a0, a1, a2, a3);
 #pragma unroll
-          for (int jj = 0; jj < C::NT / 2; ++jj) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vt + (jj >> 2) * C::HALF + swz(rowV, (jj & 3) * 2 + (mi >> 1)), b0, b1, b2, b3);
-            mma_bf16_16816(acc[2 * jj], ph[0], ph[1], ph[2], ph[3], b0, b1);
-            mma_bf16_16816(acc[2 * jj + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
-            mma_bf16_16816(acc[2 * jj], pl_[0], pl_[1], pl_[2], pl_[3], b0, b1);
-            mma_bf16_16816(acc[2 * jj + 1], pl_[0], pl_[1], pl_[2], pl_[3], b2, b3);
+            for (int n = 0; n < C::NH; ++n) {
+              mma_bf16_16816(acc[n][mt], a0, a1, a2, a3, bh[n][0], bh[n][1]);
+              mma_bf16_16816(acc[n][mt], a0, a1, a2, a3, bl[n][0], bl[n][1]);
+            }
           }
         }
       }
@@ -492,67 +503,78 @@ __global__ void __launch_bounds__(kMThreads)
     }
 
     // ---- merge the four warps' states ----
-    l0 = quad_sum(l0);
-    l1 = quad_sum(l1);
-    if (tig == 0) {
-      s_ml[(warp * 16 + r0) * 2] = m0;
-      s_ml[(warp * 16 + r0) * 2 + 1] = l0;
-      s_ml[(warp * 16 + r1) * 2] = m1;
-      s_ml[(warp * 16 + r1) * 2 + 1] = l1;
-    }
+#pragma unroll
+    for (int n = 0; n < C::NH; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float l = l_run[n][e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        l_run[n][e] = l;
+        if (grp == 0) {
+          const int h = 8 * n + 2 * tig + e;
+          s_ml[(warp * 16 + h) * 2] = m_run[n][e];
+          s_ml[(warp * 16 + h) * 2 + 1] = l;
+        }
+      }
     if (lane == 0) s_bad[warp] = bad;
     named_sync(1, kCW * 32);
-    float M0 = -INFINITY, M1 = -INFINITY;
+    float Mh[C::NH][2], Lh[C::NH][2];
 #pragma unroll
-    for (int w = 0; w < kCW; ++w) {
-      M0 = fmaxf(M0, s_ml[(w * 16 + r0) * 2]);
-      M1 = fmaxf(M1, s_ml[(w * 16 + r1) * 2]);
-    }
-    float L0 = 0.f, L1 = 0.f;
+    for (int n = 0; n < C::NH; ++n)
 #pragma unroll
-    for (int w = 0; w < kCW; ++w) {
-      const float mw0 = s_ml[(w * 16 + r0) * 2], mw1 = s_ml[(w * 16 + r1) * 2];
-      L0 += mw0 == -INFINITY ? 0.f : exp2f(mw0 - M0) * s_ml[(w * 16 + r0) * 2 + 1];
-      L1 += mw1 == -INFINITY ? 0.f : exp2f(mw1 - M1) * s_ml[(w * 16 + r1) * 2 + 1];
-    }
+      for (int e = 0; e < 2; ++e) {
+        const int h = 8 * n + 2 * tig + e;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) M = fmaxf(M, s_ml[(w * 16 + h) * 2]);
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCW; ++w) {
+          const float mw = s_ml[(w * 16 + h) * 2];
+          L += mw == -INFINITY ? 0.f : exp2f(mw - M) * s_ml[(w * 16 + h) * 2 + 1];
+        }
+        Mh[n][e] = M;
+        Lh[n][e] = L;
+        const float f = m_run[n][e] == -INFINITY ? 0.f : exp2f(m_run[n][e] - M);
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+          acc[n][mt][e] *= f;
+          acc[n][mt][2 + e] *= f;
+        }
+      }
     const int unit_bad = s_bad[0] | s_bad[1] | s_bad[2] | s_bad[3];
-    const float f0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
-    const float f1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
-#pragma unroll
-    for (int j = 0; j < C::NT; ++j) {
-      acc[j][0] *= f0;
-      acc[j][1] *= f0;
-      acc[j][2] *= f1;
-      acc[j][3] *= f1;
-    }
-    // tree over warps through two [G][D] buffers
+    // tree over warps through two [G][RSTRIDE] buffers
     auto store = [&](int buf) {
 #pragma unroll
-      for (int j = 0; j < C::NT; ++j) {
-        const int d = 8 * j + 2 * tig;
-        if (r0 < G)
-          *reinterpret_cast<float2 *>(red + (buf * G + r0) * C::RSTRIDE + d) =
-              make_float2(acc[j][0], acc[j][1]);
-        if (r1 < G)
-          *reinterpret_cast<float2 *>(red + (buf * G + r1) * C::RSTRIDE + d) =
-              make_float2(acc[j][2], acc[j][3]);
-      }
+      for (int n = 0; n < C::NH; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 8 * n + 2 * tig + e;
+          if (h >= G) continue;
+          float *rowp = red + (buf * G + h) * C::RSTRIDE;
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) {
+            rowp[16 * mt + grp] = acc[n][mt][e];
+            rowp[16 * mt + grp + 8] = acc[n][mt][2 + e];
+          }
+        }
     };
     auto add = [&](int buf) {
 #pragma unroll
-      for (int j = 0; j < C::NT; ++j) {
-        const int d = 8 * j + 2 * tig;
-        if (r0 < G) {
-          const float2 v = *reinterpret_cast<const float2 *>(red + (buf * G + r0) * C::RSTRIDE + d);
-          acc[j][0] += v.x;
-          acc[j][1] += v.y;
+      for (int n = 0; n < C::NH; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 8 * n + 2 * tig + e;
+          if (h >= G) continue;
+          const float *rowp = red + (buf * G + h) * C::RSTRIDE;
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) {
+            acc[n][mt][e] += rowp[16 * mt + grp];
+            acc[n][mt][2 + e] += rowp[16 * mt + grp + 8];
+          }
         }
-        if (r1 < G) {
-          const float2 v = *reinterpret_cast<const float2 *>(red + (buf * G + r1) * C::RSTRIDE + d);
-          acc[j][2] += v.x;
-          acc[j][3] += v.y;
-        }
-      }
     };
     if (warp >= 2) store(warp - 2);
     named_sync(1, kCW * 32);
@@ -565,46 +587,41 @@ __global__ void __launch_bounds__(kMThreads)
     const bool final_out = direct || (fused && n_b == 1);
     if (warp == 0) {
       add(0);
-      const float inv0 = (unit_bad || !(L0 > 0.f)) ? 0.f : 1.f / L0;
-      const float inv1 = (unit_bad || !(L1 > 0.f)) ? 0.f : 1.f / L1;
 #pragma unroll
-      for (int j = 0; j < C::NT; ++j) {
-        const int d = 8 * j + 2 * tig;
+      for (int n = 0; n < C::NH; ++n)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = hh ? r1 : r0;
-          if (r >= G) continue;
-          const float inv = hh ? inv1 : inv0;
-          const float x = acc[j][2 * hh] * inv, y = acc[j][2 * hh + 1] * inv;
-          if (final_out) {
-            const long long o = ((long long)un.b * Hq + hq0 + r) * D + d;
-            if (a.flags & PKV_FLAG_OUT_F32)
-              *reinterpret_cast<float2 *>(static_cast<float *>(ws.out) + o) = make_float2(x, y);
-            else
-              *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(ws.out) + o) = pack_bf16x2(x, y);
-          } else {
-            const long long o = (((long long)un.b * Hq + hq0 + r) * pl.S + un.c) * D + d;
-            *reinterpret_cast<float2 *>(ws.o_part + o) = make_float2(x, y);
-          }
-        }
-      }
-      if (tig == 0) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = hh ? r1 : r0;
-          if (r >= G) continue;
-          const float M = hh ? M1 : M0, L = hh ? L1 : L0;
+        for (int e = 0; e < 2; ++e) {
+          const int h = 8 * n + 2 * tig + e;
+          if (h >= G) continue;
+          const float M = Mh[n][e], L = Lh[n][e];
           const bool empty_out = unit_bad || !(L > 0.f);
-          if (final_out) {
-            if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse)
-              ws.lse[(long long)un.b * Hq + hq0 + r] = empty_out ? -INFINITY : M * kLn2 + logf(L);
-          } else {
-            const long long o = (((long long)un.b * Hq + hq0 + r) * pl.S + un.c) * 2;
-            ws.ml_part[o] = empty_out ? -INFINITY : M * kLn2;
-            ws.ml_part[o + 1] = empty_out ? 0.f : L;
+          const float inv = empty_out ? 0.f : 1.f / L;
+          const long long qrow = (long long)un.b * Hq + hq0 + h;
+#pragma unroll
+          for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int d = 16 * mt + grp + 8 * hh;
+              const float x = acc[n][mt][2 * hh + e] * inv;
+              if (final_out) {
+                if (a.flags & PKV_FLAG_OUT_F32) static_cast<float *>(ws.out)[qrow * D + d] = x;
+                else static_cast<uint16_t *>(ws.out)[qrow * D + d] = (uint16_t)f32_to_bf16_bits(x);
+              } else {
+                ws.o_part[(qrow * pl.S + un.c) * D + d] = x;
+              }
+            }
+          }
+          if (grp == 0) {
+            if (final_out) {
+              if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse)
+                ws.lse[qrow] = empty_out ? -INFINITY : M * kLn2 + logf(L);
+            } else {
+              const long long o = (qrow * pl.S + un.c) * 2;
+              ws.ml_part[o] = empty_out ? -INFINITY : M * kLn2;
+              ws.ml_part[o + 1] = empty_out ? 0.f : L;
+            }
           }
         }
-      }
       if (fused && !final_out) __threadfence();  // partial visible before the ticket
     }
     if (fused && !final_out) {
