@@ -150,12 +150,17 @@ pkv_status pkv_bind_step(const pkv_workspace *ws, int batch, int mode, int layer
                          pkv_stream_t stream);
 
 /*
- * Split count for a batch, host only.  The target split length is
- * chunk = max(128, ceil(Hkv * total_tokens_hint / (4 * num_sms))) tokens, so
- * that the (request, KV head, split) units number about four per SM, and
- * S = ceil(max_seq_len_hint / chunk), clamped to [1, max_splits].
- * total_tokens_hint <= 0 means batch * max_seq_len_hint.  Returns 1 for
- * non-positive batch, length or SM count.
+ * Split count for a batch, host only.  Work units are (request, KV head,
+ * split) and the tensor-core kernel keeps 2 blocks per SM resident, so the
+ * time is modelled as waves * (chunk + 96), chunk = ceil(max_seq_len_hint /
+ * S) rounded to 16 tokens; the S in [1, max_splits] with the lowest modelled
+ * time is returned (splits shorter than 128 tokens are not considered).
+ * Near-uniform lengths (total_tokens_hint >= 95% of batch *
+ * max_seq_len_hint): units = batch * Hkv * S, waves = ceil(units / (2 *
+ * num_sms)).  Otherwise units = Hkv * (ceil(total / chunk) + batch / 2) and
+ * waves = units / (2 * num_sms) + 1/2 (unequal last splits).  total_tokens_hint <= 0 means
+ * batch * max_seq_len_hint.  Returns 1 for non-positive batch, length or SM
+ * count.
  */
 int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint,
                       long long total_tokens_hint, int num_sms);

@@ -110,16 +110,33 @@ int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint,
                       long long total_tokens_hint, int num_sms) {
   if (!ws || batch <= 0 || max_seq_len_hint <= 0 || num_sms <= 0 || ws->n_kv_heads <= 0)
     return 1;
-  const long long min_chunk = 128;
+  const long long hkv = ws->n_kv_heads, L = max_seq_len_hint;
   const long long total =
       total_tokens_hint > 0 ? total_tokens_hint : (long long)batch * max_seq_len_hint;
-  const long long target_units = 4ll * num_sms;  // ~2 resident blocks x 2 units each
-  long long chunk = ((long long)ws->n_kv_heads * total + target_units - 1) / target_units;
-  if (chunk < min_chunk) chunk = min_chunk;
-  long long S = (max_seq_len_hint + chunk - 1) / chunk;
-  if (S > ws->max_splits) S = ws->max_splits;
-  if (S < 1) S = 1;
-  return (int)S;
+  const bool uniform = total * 100 >= (long long)batch * L * 95;
+  const long long slots = 2ll * num_sms;  // resident blocks of the tensor-core kernel
+  const long long unit_cost = 96;         // per-unit fixed cost, in tokens of streaming
+  long long best_t = -1;
+  int best_s = 1;
+  for (int S = 1; S <= ws->max_splits && S <= 4096; ++S) {
+    long long chunk = (L + S - 1) / S;
+    chunk = (chunk + 15) / 16 * 16;
+    if (S > 1 && chunk < 128) break;
+    const long long per_req = (L + chunk - 1) / chunk;
+    if (per_req < S) continue;  // same split length as a smaller S
+    const long long units = uniform ? (long long)batch * hkv * per_req
+                                    : hkv * ((total + chunk - 1) / chunk + batch / 2);
+    // uniform lengths: whole waves; mixed lengths (unequal last splits): the
+    // fluid share plus half a wave of imbalance.  Fixed point, x1000.
+    const long long waves_x1000 =
+        uniform ? (units + slots - 1) / slots * 1000 : units * 1000 / slots + 500;
+    const long long t = waves_x1000 * (chunk + unit_cost);
+    if (best_t < 0 || t < best_t) {
+      best_t = t;
+      best_s = S;
+    }
+  }
+  return best_s;
 }
 
 static pkv_status decode_common(const pkv_workspace *ws, int batch, int layer, const void *q,

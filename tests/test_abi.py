@@ -114,14 +114,16 @@ def test_bind_and_merge_host_validation():
 
 def test_choose_splits():
     ws = _ws(max_splits=128, n_kv_heads=8, n_q_heads=32)
-    # one 65536-token request: chunk = ceil(8 * 65536 / 608) = 863 -> S = 76
-    assert P.pkv_choose_splits(ws, 1, 65536, 65536, 152) == 76
-    # short batch: the 128-token floor decides
-    assert P.pkv_choose_splits(ws, 4, 2048, 6500, 152) == 16
-    # skewed batch: the total, not the longest request, sets the split length
-    assert P.pkv_choose_splits(ws, 16, 8192, 14500, 152) == 43
-    # no total given: batch * max
-    assert P.pkv_choose_splits(ws, 4, 2048, 0, 152) == 16
+    # one 65536-token request: 38 splits x 8 heads = 304 units, one per
+    # resident block of 152 SMs x 2
+    assert P.pkv_choose_splits(ws, 1, 65536, 65536, 152) == 38
+    # four such requests: 19 splits -> 608 units = exactly two waves
+    assert P.pkv_choose_splits(ws, 4, 65600, 4 * 65568, 152) == 19
+    # mixed lengths: fluid share plus half a wave decides
+    assert P.pkv_choose_splits(ws, 4, 2048, 6500, 152) == 12
+    assert P.pkv_choose_splits(ws, 16, 8192, 14500, 152) == 37
+    # no total given: batch * max, treated as uniform
+    assert P.pkv_choose_splits(ws, 4, 2048, 0, 152) == 9
     assert P.pkv_choose_splits(_ws(max_splits=4), 1, 65536, 65536, 152) == 4
     assert P.pkv_choose_splits(ws, 0, 10, 10, 152) == 1
 
