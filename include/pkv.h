@@ -9,6 +9,12 @@
  * decode kernel whose partial outputs and running max / sum-exp live in
  * caller-owned workspace buffers (workspace.py page, bullets 1, 13-18).
  *
+ * Launch overlap: the tensor-core decode kernel is launched with programmatic
+ * stream serialization, so it may start while the previous kernel on the
+ * stream drains; it waits for that kernel (griddepcontrol.wait) before reading
+ * anything another kernel may still be writing, and lets its own successor
+ * start only after that wait.
+ *
  * Conventions for every entry point
  *  - The library allocates nothing and keeps no data between calls.  Every
  *    buffer is caller-owned device memory at an address that may stay fixed
@@ -65,8 +71,15 @@ enum {
   PKV_FLAG_WRITE_LSE = 2,  /* also write lse[b, h] = m + ln(l) (natural log)                */
   PKV_FLAG_FORCE_SIMT = 4, /* use the CUDA-core kernel even where a tensor-core one exists  */
   PKV_FLAG_FORCE_MMA = 8,  /* use the tensor-core kernel (error if the shape has none)      */
-  PKV_FLAG_FORCE_GATHER = 16 /* tensor-core kernel: load K/V with cp.async gathers even where
-                                tensor-map TMA boxes apply (P % 16 == 0)                    */
+  PKV_FLAG_FORCE_GATHER = 16, /* tensor-core kernel: load K/V with cp.async gathers even where
+                                 tensor-map TMA boxes apply (P % 16 == 0)                   */
+  PKV_FLAG_PLAN_EARLY = 32   /* tensor-core kernel: the caller guarantees that seq_lens,
+                                kv_indptr, kv_indices, req_pool_indices, page_table and
+                                out_loc were last written at least two launches earlier
+                                on this stream (or by the host), so the kernel may read
+                                them and start loading K/V before the previous kernel
+                                finishes (programmatic dependent launch); q, k_new and
+                                all outputs are still touched only after it finishes  */
 };
 
 /* bits OR-ed into *err by device code (sticky; the caller clears the word) */

@@ -16,7 +16,7 @@ PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_CAPACITY, PKV_ERR_CUDA = r
 PKV_BIND_STEADY, PKV_BIND_REBUILD, PKV_BIND_APPEND_ONLY = 0, 1, 2
 PKV_IDX_PAGE_TABLE, PKV_IDX_FLAT = 0, 1
 PKV_FLAG_OUT_F32, PKV_FLAG_WRITE_LSE, PKV_FLAG_FORCE_SIMT, PKV_FLAG_FORCE_MMA = 1, 2, 4, 8
-PKV_FLAG_FORCE_GATHER = 16
+PKV_FLAG_FORCE_GATHER, PKV_FLAG_PLAN_EARLY = 16, 32
 PKV_DEVERR_PAGE, PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT, PKV_DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16
 

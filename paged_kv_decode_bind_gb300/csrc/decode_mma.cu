@@ -236,6 +236,10 @@ __global__ void __launch_bounds__(kMThreads)
   const int Hq = ws.n_q_heads;
   volatile int *s_abort = &s_ctrl[0];
   volatile int *s_ticket = &s_ctrl[1];
+  // Without PKV_FLAG_PLAN_EARLY nothing is read before the previous kernel
+  // on the stream has finished.
+  const bool early = (a.flags & PKV_FLAG_PLAN_EARLY) != 0;
+  if (!early) pdl_wait();
 
   const int max_len = batch_max_len(ws, a.batch, &s_max_len);
   // Zero the K/V ring once: pieces a tile does not load then hold finite
@@ -266,19 +270,6 @@ __global__ void __launch_bounds__(kMThreads)
     const int pairs = batch_split_prefix(ws, a.batch, pl.chunk, s_pref, s_tmp);
     pl.pref = s_pref;
     pl.n_units = pairs * pl.hkv;
-    if (direct || fused) {
-      // Requests with no usable token have no unit: zero their outputs here.
-      for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
-        if (s_pref[b + 1] != s_pref[b]) continue;
-        for (int i = tid; i < Hq * D; i += kMThreads) {
-          const long long o = (long long)b * Hq * D + i;
-          if (a.flags & PKV_FLAG_OUT_F32) static_cast<float *>(ws.out)[o] = 0.f;
-          else static_cast<uint16_t *>(ws.out)[o] = 0;
-        }
-        if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse)
-          for (int h = tid; h < Hq; h += kMThreads) ws.lse[(long long)b * Hq + h] = -INFINITY;
-      }
-    }
   } else {
     pl.n_units = pl.S * pl.batch * pl.hkv;
   }
@@ -312,6 +303,8 @@ __global__ void __launch_bounds__(kMThreads)
     fetch();
     int k = 0;
     bool aborted = false;
+    bool waited = !early;
+    if (waited) pdl_trigger();
     while (!pc.done) {
       const int s = k % kMStages;
       const int r = k / kMStages;
@@ -325,6 +318,12 @@ __global__ void __launch_bounds__(kMThreads)
       }
       const Unit un = pc.un;
       const int tile0 = un.t0 + pc.i * kMT;
+      if (!waited && a.k_new != nullptr && un.L > 0 && un.L - 1 >= tile0 &&
+          un.L - 1 < min(tile0 + kMT, un.t1)) {
+        pdl_wait();  // k_new comes from the previous kernel
+        pdl_trigger();
+        waited = true;
+      }
       append_if_newest<D>(a, un, tile0, lane);
       const int cur_raw[2] = {raw[0], raw[1]};
       pc.advance(ws, pl);
@@ -360,6 +359,24 @@ __global__ void __launch_bounds__(kMThreads)
   const int mi = lane >> 3, rr = lane & 7;
   const int rowK = 16 * warp + (mi & 1) * 8 + rr;   // K as A: tokens 0-7 / 8-15 by mi % 2
   const int rowV = 16 * warp + (mi >> 1) * 8 + rr;  // V^T as A: tokens by mi / 2
+
+  // q and every output belong to the current stream order: wait here, then
+  // let the next kernel on the stream be scheduled.
+  if (early) pdl_wait();
+  pdl_trigger();
+  if (pl.pref && (direct || fused)) {
+    // Requests with no usable token have no unit: zero their outputs here.
+    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
+      if (s_pref[b + 1] != s_pref[b]) continue;
+      for (int i = tid; i < Hq * D; i += kCW * 32) {
+        const long long o = (long long)b * Hq * D + i;
+        if (a.flags & PKV_FLAG_OUT_F32) static_cast<float *>(ws.out)[o] = 0.f;
+        else static_cast<uint16_t *>(ws.out)[o] = 0;
+      }
+      if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse)
+        for (int h = tid; h < Hq; h += kCW * 32) ws.lse[(long long)b * Hq + h] = -INFINITY;
+    }
+  }
 
   int k = 0;
   for (int u = blockIdx.x; u < pl.n_units; u += gridDim.x) {
@@ -719,8 +736,17 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
   const long long cap = (long long)sms_cache[di] * occ_cache[di];
   const int grid = (int)(units < cap ? units : cap);
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, kMThreads, C::SMEM, st>>>(a, tmk, tmv, use_tma);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, tmk, tmv, use_tma);
 }
 
 }  // namespace

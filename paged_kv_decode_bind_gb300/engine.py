@@ -69,8 +69,12 @@ class DecodeRunner:
         if self.fused:
             if events is not None:
                 events[0].record(s)
+            # Layers after the first read metadata the step's bind wrote two or
+            # more launches earlier, so they may start before layer l-1 ends.
+            early = _abi.PKV_FLAG_PLAN_EARLY if (l > 0 and events is None) else 0
             _abi.pkv_decode_layer(self.ws, self.batch, l, self.q_in[l], self.k_in[l],
-                                  self.v_in[l], self.scale, self.num_splits, self.flags, s)
+                                  self.v_in[l], self.scale, self.num_splits, self.flags | early,
+                                  s)
             if events is not None:
                 events[1].record(s)
             return
