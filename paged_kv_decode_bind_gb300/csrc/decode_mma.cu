@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(kMThreads)
   __shared__ float s_ml[kCW * 16 * 2];
   __shared__ int s_bad[kCW];
   __shared__ int s_pref[kMaxCompactBatch + 1];
+  __shared__ int s_len[kMaxCompactBatch];
   __shared__ int s_tmp[32];
   __shared__ int s_max_len;
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -241,11 +242,6 @@ __global__ void __launch_bounds__(kMThreads)
   const bool early = (a.flags & PKV_FLAG_PLAN_EARLY) != 0;
   if (!early) pdl_wait();
 
-  const int max_len = batch_max_len(ws, a.batch, &s_max_len);
-  // Zero the K/V ring once: pieces a tile does not load then hold finite
-  // values (zeros or earlier tokens), so masked lanes contribute 0, not NaN.
-  for (int i = tid; i < kMStages * 2 * C::TILE / 16; i += kMThreads)
-    reinterpret_cast<uint4 *>(smem + C::OFF_KV)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
     for (int s = 0; s < kMStages; ++s) {
       // TMA: one expect-tx arrival; cp.async: 32 copy-completion arrivals
@@ -263,14 +259,16 @@ __global__ void __launch_bounds__(kMThreads)
   pl.batch = a.batch;
   pl.hkv = ws.n_kv_heads;
   pl.S = a.num_splits;
-  pl.chunk = split_chunk(max_len, a.num_splits, ws.page_size);
   const bool direct = pl.S == 1;
   const bool fused = a.fused_merge && !direct;
   if (a.batch <= kMaxCompactBatch) {
-    const int pairs = batch_split_prefix(ws, a.batch, pl.chunk, s_pref, s_tmp);
+    const int pairs =
+        batch_plan_compact(ws, a.batch, pl.S, s_len, s_pref, s_tmp, &s_max_len, &pl.chunk);
     pl.pref = s_pref;
+    pl.lens = s_len;
     pl.n_units = pairs * pl.hkv;
   } else {
+    pl.chunk = split_chunk(batch_max_len(ws, a.batch, &s_max_len), pl.S, ws.page_size);
     pl.n_units = pl.S * pl.batch * pl.hkv;
   }
   const uint32_t kv_base = smem_addr(smem + C::OFF_KV);
@@ -453,16 +451,37 @@ __global__ void __launch_bounds__(kMThreads)
           const uint32_t kt = kv_base + (2 * s) * C::TILE;
           const uint32_t vt = kt + C::TILE;
           // ---- S^T = K Q^T: rows = tokens grp / grp + 8, cols = heads ----
-          float sc[C::NH][4];
+          // two independent accumulation chains (even / odd k-steps)
+          float sc[C::NH][4], sc2[C::NH][4];
 #pragma unroll
-          for (int n = 0; n < C::NH; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+          for (int n = 0; n < C::NH; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sc[n][i] = sc2[n][i] = 0.f;
 #pragma unroll
           for (int ks = 0; ks < C::KSTEPS; ++ks) {
             uint32_t a0, a1, a2, a3;
             ldsm_x4(kt + (ks >> 2) * C::HALF + swz(rowK, (ks & 3) * 2 + (mi >> 1)), a0, a1, a2, a3);
 #pragma unroll
             for (int n = 0; n < C::NH; ++n)
-              mma_bf16_16816(sc[n], a0, a1, a2, a3, qb[n][ks][0], qb[n][ks][1]);
+              mma_bf16_16816((ks & 1) ? sc2[n] : sc[n], a0, a1, a2, a3, qb[n][ks][0], qb[n][ks][1]);
+          }
+#pragma unroll
+          for (int n = 0; n < C::NH; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sc[n][i] += sc2[n][i];
+          if (nv < 16) {
+            // Rows past the end of this warp's piece may hold anything the
+            // pool held (even NaN bit patterns); P is 0 there, so clear them.
+            for (int i = lane; i < (16 - nv) * 16; i += 32) {
+              const int r = 16 * warp + nv + (i >> 4), c8 = i & 15;
+              if (c8 < D / 8)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                                 vt + (c8 >> 3) * C::HALF + swz(r, c8 & 7)),
+                             "r"(0u)
+                             : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
           }
           // ---- online softmax over the tokens, per head (log2 units) ----
           const bool v0 = grp < nv, v1 = grp + 8 < nv;
@@ -619,7 +638,7 @@ __global__ void __launch_bounds__(kMThreads)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               const int d = 16 * mt + grp + 8 * hh;
-              const float x = acc[n][mt][2 * hh + e] * inv;
+              const float x = empty_out ? 0.f : acc[n][mt][2 * hh + e] * inv;
               if (final_out) {
                 if (a.flags & PKV_FLAG_OUT_F32) static_cast<float *>(ws.out)[qrow * D + d] = x;
                 else static_cast<uint16_t *>(ws.out)[qrow * D + d] = (uint16_t)f32_to_bf16_bits(x);
@@ -639,11 +658,11 @@ __global__ void __launch_bounds__(kMThreads)
             }
           }
         }
-      if (fused && !final_out) __threadfence();  // partial visible before the ticket
     }
     if (fused && !final_out) {
       named_sync(1, kCW * 32);
       if (tid == 0) {
+        __threadfence();  // the block's partial (ordered by the barrier) before the ticket
         int *ctr = ws.split_counters + (long long)un.b * ws.n_kv_heads + un.g;
         const int old = atomicAdd(ctr, 1);
         const int last = old == n_b - 1;
@@ -653,14 +672,11 @@ __global__ void __launch_bounds__(kMThreads)
       named_sync(1, kCW * 32);
       if (*s_ticket) {
         __threadfence();
-        for (int h = warp; h < G; h += kCW) {
-          const long long row = (long long)un.b * Hq + hq0 + h;
-          float M, den;
-          float4 o4;
-          merge_row<D>(ws.ml_part + row * pl.S * 2, ws.o_part + row * pl.S * D, n_b, lane, M,
-                       den, o4);
-          merge_store<D>(ws, row, a.flags, lane, M, den, o4);
-        }
+        // warp w merges query heads w, w + 4, ... of the group
+        constexpr int RPW = G >= kCW ? G / kCW : 1;
+        if (warp < G)
+          merge_rows_batched<D, RPW>(ws, (long long)un.b * Hq + hq0 + warp, kCW, pl.S, n_b,
+                                     a.flags, lane);
       }
     }
     named_sync(1, kCW * 32);  // s_ml, red and the ticket are reused by the next unit

@@ -14,11 +14,13 @@ namespace pkv {
 struct Plan {
   int batch, hkv, S, chunk, n_units;
   // Compact enumeration: exclusive prefix over requests of their split counts
-  // (shared memory, batch + 1 entries); NULL = dense enumeration.
+  // and their usable lengths (shared memory, batch + 1 / batch entries);
+  // NULL = dense enumeration.
   const int *pref = nullptr;
+  const int *lens = nullptr;
 };
 
-constexpr int kMaxCompactBatch = 1024;
+constexpr int kMaxCompactBatch = 512;
 
 struct Unit {
   int u, b, g, c, t0, t1;
@@ -64,7 +66,7 @@ __device__ __forceinline__ Unit unit_at(const pkv_workspace &ws, const Plan &pl,
     x.b = r / pl.hkv;
     x.g = r - x.b * pl.hkv;
   }
-  x.L = usable_len(ws, x.b);  // out-of-range lengths are flagged by CTA 0's prologue
+  x.L = pl.lens ? pl.lens[x.b] : usable_len(ws, x.b);  // bad lengths flagged by CTA 0
   x.t0 = x.c * pl.chunk;
   x.t1 = min(x.t0 + pl.chunk, x.L);
   return x;
@@ -150,6 +152,74 @@ __device__ __forceinline__ int batch_split_prefix(const pkv_workspace &ws, int b
   for (int b = lo; b < hi; ++b) {
     s_pref[b] = run;
     run += split_count(ws, b, chunk);
+  }
+  if (tid == nt - 1) s_pref[batch] = run;
+  __syncthreads();
+  return s_pref[batch];
+}
+
+// Block prologue for compact enumeration (batch <= kMaxCompactBatch): one
+// pass reads every request's usable length into s_len (CTA 0 raises the
+// length error bits), then the split length and the exclusive prefix of the
+// split counts follow from shared memory.  Every thread of the block must
+// call it; returns the number of non-empty (request, split) pairs and sets
+// *chunk_out.
+__device__ __forceinline__ int batch_plan_compact(const pkv_workspace &ws, int batch, int S,
+                                                  int *s_len, int *s_pref, int *s_tmp,
+                                                  int *s_max, int *chunk_out) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) *s_max = 0;
+  __syncthreads();
+  int mx = 0;
+  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  for (int b = tid; b < batch; b += blockDim.x) {
+    const int raw = ws.seq_lens[b];
+    int L = raw;
+    if (L < 0 || (long long)L > cap) {
+      if (blockIdx.x == 0) atomicOr(ws.err, PKV_DEVERR_LEN);
+      L = 0;
+    } else if (ws.index_mode == PKV_IDX_FLAT && L > 0) {
+      const int base = ws.kv_indptr[b];
+      if (base < 0 || (long long)base + L > ws.max_total_tokens) {
+        if (blockIdx.x == 0) atomicOr(ws.err, PKV_DEVERR_TOTAL);
+        L = 0;
+      }
+    }
+    s_len[b] = L;
+    mx = max(mx, L);
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) atomicMax(s_max, mx);
+  __syncthreads();
+  const int chunk = split_chunk(*s_max, S, ws.page_size);
+  *chunk_out = chunk;
+  const int nt = blockDim.x;
+  const int per = (batch + nt - 1) / nt;
+  const int lo = min(batch, tid * per), hi = min(batch, lo + per);
+  int local = 0;
+  for (int b = lo; b < hi; ++b) local += (s_len[b] + chunk - 1) / chunk;
+  int incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) s_tmp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < (nt + 31) / 32 ? s_tmp[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += v;
+    }
+    s_tmp[lane] = w;
+  }
+  __syncthreads();
+  int run = (warp > 0 ? s_tmp[warp - 1] : 0) + incl - local;
+  for (int b = lo; b < hi; ++b) {
+    s_pref[b] = run;
+    run += (s_len[b] + chunk - 1) / chunk;
   }
   if (tid == nt - 1) s_pref[batch] = run;
   __syncthreads();

@@ -85,4 +85,79 @@ __device__ __forceinline__ void merge_store(const pkv_workspace &ws, long long r
     ws.lse[row] = den > 0.f ? M + logf(den) : -INFINITY;
 }
 
+// Merge of the n split partials of NH query-head rows (row0 + j * rstep,
+// j < NH) by one warp, with all of a batch of partial-row loads in flight:
+// lane s holds split s's weight for every row, then up to 8 splits x NH rows
+// of float4 loads are issued before any is used.
+template <int D, int NH>
+__device__ __forceinline__ void merge_rows_batched(const pkv_workspace &ws, long long row0,
+                                                   long long rstep, int S, int n, int flags,
+                                                   int lane) {
+  constexpr int NV = D / 4;
+  float M[NH], den[NH];
+  float4 acc[NH];
+#pragma unroll
+  for (int j = 0; j < NH; ++j) {
+    M[j] = -INFINITY;
+    den[j] = 0.f;
+    acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    // (m, l) of split s0 + lane for every row
+    float2 ml[NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j)
+      ml[j] = s0 + lane < n
+                  ? __ldcg(reinterpret_cast<const float2 *>(ws.ml_part + (row0 + j * rstep) * S * 2) + s0 + lane)
+                  : make_float2(-INFINITY, 0.f);
+    float w[NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+      float mx = ml[j].y > 0.f ? ml[j].x : -INFINITY;
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+      const float Mn = fmaxf(M[j], mx);
+      // rescale what was accumulated against the old maximum
+      const float r = M[j] == -INFINITY ? 0.f : expf(M[j] - Mn);
+      den[j] *= r;
+      acc[j].x *= r;
+      acc[j].y *= r;
+      acc[j].z *= r;
+      acc[j].w *= r;
+      M[j] = Mn;
+      w[j] = (ml[j].y > 0.f && Mn != -INFINITY) ? ml[j].y * expf(ml[j].x - Mn) : 0.f;
+      float ws_ = w[j];
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) ws_ += __shfl_xor_sync(0xffffffffu, ws_, d);
+      den[j] += ws_;
+    }
+    const int m = min(32, n - s0);
+    for (int t0 = 0; t0 < m; t0 += 8) {
+      float4 o[8][NH];
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int j = 0; j < NH; ++j)
+          o[t][j] = (t0 + t < m && lane < NV)
+                        ? __ldcg(reinterpret_cast<const float4 *>(
+                                     ws.o_part + ((row0 + j * rstep) * S + s0 + t0 + t) * D) + lane)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int j = 0; j < NH; ++j) {
+          const float wt = __shfl_sync(0xffffffffu, w[j], (t0 + t) & 31);
+          if (t0 + t < m && wt > 0.f) {
+            acc[j].x = fmaf(wt, o[t][j].x, acc[j].x);
+            acc[j].y = fmaf(wt, o[t][j].y, acc[j].y);
+            acc[j].z = fmaf(wt, o[t][j].z, acc[j].z);
+            acc[j].w = fmaf(wt, o[t][j].w, acc[j].w);
+          }
+        }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NH; ++j) merge_store<D>(ws, row0 + j * rstep, flags, lane, M[j], den[j], acc[j]);
+}
+
 }  // namespace pkv
