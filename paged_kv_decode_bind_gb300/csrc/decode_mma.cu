@@ -17,8 +17,8 @@
 // state; the four states merge at the end of the unit.  The producer walks
 // the block's units ahead of the consumers, across unit boundaries, through a
 // 3-stage ring (`full` mbarriers complete on the landed bytes, `empty` on the
-// four consumer warps' release), fetching the next tile's index entries one
-// tile ahead so their latency overlaps the wait for a free stage.
+// four consumer warps' release), fetching index entries up to 8 tiles ahead
+// (a second cursor) so their latency overlaps the issue of earlier tiles.
 //
 // Units.  With batch <= kMaxCompactBatch only the non-empty (request, split)
 // pairs are units (a per-block prefix over the requests' split counts), so a
@@ -139,7 +139,7 @@ __device__ __forceinline__ void append_if_newest(const DecodeArgs &a, const Unit
 }
 
 // Producer, page mode: 16-token page pieces by tensor-map boxes.  Lane j < 4
-// owns piece j; `raw` is its page id, fetched one tile ahead.
+// owns piece j; `raw` is its page id, fetched ahead.
 template <int D, int G>
 __device__ __forceinline__ void produce_tma(const DecodeArgs &a, const Unit &un, int tile0,
                                             int raw, int stage, uint32_t kv_base, uint64_t *full,
@@ -229,6 +229,7 @@ __global__ void __launch_bounds__(kMThreads)
   __shared__ int s_bad[kCW];
   __shared__ int s_pref[kMaxCompactBatch + 1];
   __shared__ int s_len[kMaxCompactBatch];
+  __shared__ int s_base[kMaxCompactBatch];
   __shared__ int s_tmp[32];
   __shared__ int s_max_len;
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(kMThreads)
   const bool fused = a.fused_merge && !direct;
   if (a.batch <= kMaxCompactBatch) {
     const int pairs =
-        batch_plan_compact(ws, a.batch, pl.S, s_len, s_pref, s_tmp, &s_max_len, &pl.chunk);
+        batch_plan_compact(ws, a.batch, pl.S, s_len, s_base, s_pref, s_tmp, &s_max_len, &pl.chunk);
     pl.pref = s_pref;
     pl.lens = s_len;
     pl.n_units = pairs * pl.hkv;
@@ -277,28 +278,47 @@ __global__ void __launch_bounds__(kMThreads)
     // ------------------------------------------------------- producer ----
     Cursor<kMT> pc;
     pc.seek(ws, pl, blockIdx.x);
-    ReqIndex ri;
-    int cur_u = -1;
-    int raw[2] = {-1, -1};
-    auto fetch = [&]() {  // index entries of the tile under the cursor
-      if (pc.done) return;
-      if (pc.un.u != cur_u) {
-        ri = req_index(ws, pc.un.b);
-        cur_u = pc.un.u;
-      }
-      const int tile0 = pc.un.t0 + pc.i * kMT;
-      if (use_tma) {
-        const int tok0 = tile0 + 16 * lane;
-        raw[0] = (lane < 4 && tok0 < pc.un.t1) ? raw_index(ws, ri, tok0) : -1;
-      } else {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int tok = tile0 + lane + 32 * h;
-          raw[h] = tok < pc.un.t1 ? raw_index(ws, ri, tok) : -1;
-        }
+    // Index entries are fetched by a second cursor running ahead of pc, so
+    // their load latency overlaps the issue of earlier tiles.  TMA path:
+    // lane l holds the page id of piece l % 4 of tile k + l / 4 (8 tiles of
+    // lookahead in one register); gather path: a queue of 3 tiles, 2 rows
+    // per lane each.
+    Cursor<kMT> pf = pc;
+    int pf_u = -1;
+    ReqIndex pf_ri;
+    auto pf_index = [&]() {
+      if (pf.un.u != pf_u) {
+        pf_ri = pl.pref ? req_index_cached(ws, s_base, pf.un.b) : req_index(ws, pf.un.b);
+        pf_u = pf.un.u;
       }
     };
-    fetch();
+    int win = -1;
+    int rq[3][2];
+    if (use_tma) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (!pf.done) {
+          pf_index();
+          const int tok0 = pf.un.t0 + pf.i * kMT + 16 * (lane & 3);
+          if ((lane >> 2) == j) win = tok0 < pf.un.t1 ? raw_index(ws, pf_ri, tok0) : -1;
+          pf.advance(ws, pl);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        rq[j][0] = rq[j][1] = -1;
+        if (!pf.done) {
+          pf_index();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int tok = pf.un.t0 + pf.i * kMT + lane + 32 * h;
+            rq[j][h] = tok < pf.un.t1 ? raw_index(ws, pf_ri, tok) : -1;
+          }
+          pf.advance(ws, pl);
+        }
+      }
+    }
     int k = 0;
     bool aborted = false;
     bool waited = !early;
@@ -323,14 +343,37 @@ __global__ void __launch_bounds__(kMThreads)
         waited = true;
       }
       append_if_newest<D>(a, un, tile0, lane);
-      const int cur_raw[2] = {raw[0], raw[1]};
       pc.advance(ws, pl);
-      fetch();  // the next tile's entries are in flight while this one is issued
       if (use_tma) {
-        produce_tma<D, G>(a, un, tile0, cur_raw[0], s, kv_base, &full[s], &flags[s], &tmk, &tmv,
-                          lane);
+        const int cur = win;  // lanes 0..3: this tile's pieces
+        win = __shfl_down_sync(0xffffffffu, win, 4);
+        if (!pf.done) {
+          pf_index();
+          const int tok0 = pf.un.t0 + pf.i * kMT + 16 * (lane & 3);
+          if (lane >= 28) win = tok0 < pf.un.t1 ? raw_index(ws, pf_ri, tok0) : -1;
+          pf.advance(ws, pl);
+        } else if (lane >= 28) {
+          win = -1;
+        }
+        produce_tma<D, G>(a, un, tile0, cur, s, kv_base, &full[s], &flags[s], &tmk, &tmv, lane);
       } else {
-        produce_cpasync<D, G>(a, un, tile0, cur_raw, s, kv_base, &full[s], &flags[s], lane);
+        const int cur[2] = {rq[0][0], rq[0][1]};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          rq[0][h] = rq[1][h];
+          rq[1][h] = rq[2][h];
+          rq[2][h] = -1;
+        }
+        if (!pf.done) {
+          pf_index();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int tok = pf.un.t0 + pf.i * kMT + lane + 32 * h;
+            rq[2][h] = tok < pf.un.t1 ? raw_index(ws, pf_ri, tok) : -1;
+          }
+          pf.advance(ws, pl);
+        }
+        produce_cpasync<D, G>(a, un, tile0, cur, s, kv_base, &full[s], &flags[s], lane);
         if (lane == 0) mbar_arrive(&full[s]);
       }
       ++k;

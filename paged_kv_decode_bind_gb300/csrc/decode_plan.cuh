@@ -160,13 +160,14 @@ __device__ __forceinline__ int batch_split_prefix(const pkv_workspace &ws, int b
 
 // Block prologue for compact enumeration (batch <= kMaxCompactBatch): one
 // pass reads every request's usable length into s_len (CTA 0 raises the
-// length error bits), then the split length and the exclusive prefix of the
-// split counts follow from shared memory.  Every thread of the block must
+// length error bits) and its index base into s_base (the table row in page
+// mode, the kv_indptr offset in flat mode), then the split length and the
+// exclusive prefix of the split counts follow from shared memory.  Every thread of the block must
 // call it; returns the number of non-empty (request, split) pairs and sets
 // *chunk_out.
 __device__ __forceinline__ int batch_plan_compact(const pkv_workspace &ws, int batch, int S,
-                                                  int *s_len, int *s_pref, int *s_tmp,
-                                                  int *s_max, int *chunk_out) {
+                                                  int *s_len, int *s_base, int *s_pref,
+                                                  int *s_tmp, int *s_max, int *chunk_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) *s_max = 0;
   __syncthreads();
@@ -174,6 +175,7 @@ __device__ __forceinline__ int batch_plan_compact(const pkv_workspace &ws, int b
   const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
   for (int b = tid; b < batch; b += blockDim.x) {
     const int raw = ws.seq_lens[b];
+    s_base[b] = ws.index_mode == PKV_IDX_FLAT ? ws.kv_indptr[b] : ws.req_pool_indices[b];
     int L = raw;
     if (L < 0 || (long long)L > cap) {
       if (blockIdx.x == 0) atomicOr(ws.err, PKV_DEVERR_LEN);
@@ -232,6 +234,21 @@ struct ReqIndex {
   long long base;
   bool ok;
 };
+
+// As req_index, from the bases cached by batch_plan_compact.
+__device__ __forceinline__ ReqIndex req_index_cached(const pkv_workspace &ws, const int *s_base,
+                                                     int b) {
+  ReqIndex r;
+  if (ws.index_mode == PKV_IDX_FLAT) {
+    r.base = s_base[b];
+    r.ok = true;
+  } else {
+    const int row = s_base[b];
+    r.ok = row >= 0 && row < ws.max_reqs;
+    r.base = r.ok ? (long long)row * ws.max_pages_per_req : 0;
+  }
+  return r;
+}
 
 __device__ __forceinline__ ReqIndex req_index(const pkv_workspace &ws, int b) {
   ReqIndex r;
