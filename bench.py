@@ -41,7 +41,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--batch", type=int, default=None)
-    ap.add_argument("--splits", type=int, default=0, help="0 = pkv_choose_splits")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="0 = pkv_choose_pieces (fused) / pkv_choose_splits (fixed chunks)")
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--unfused", action="store_true", help="separate append/attention/merge")
     ap.add_argument("--no-kernel-events", action="store_true",
@@ -277,8 +278,12 @@ def run_ours(args, rank, world, local_rank):
     B, NL = p.batch, p.n_layers
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     shape_only = A.PkvWorkspace(n_kv_heads=p.n_kv_heads, max_splits=1 << 20)
-    S = args.splits or A.pkv_choose_splits(shape_only, B, int(p.seq_lens.max()) + ROUND,
-                                           int(p.seq_lens.sum()) + B * ROUND // 2, sms)
+    # the fused layer kernel cuts balanced pieces (S caps them per request and
+    # head); the separate calls and PKV_FLAG_FIXED_CHUNK cut fixed chunks
+    balanced = not args.unfused and not (args.flags & A.PKV_FLAG_FIXED_CHUNK)
+    choose = A.pkv_choose_pieces if balanced else A.pkv_choose_splits
+    S = args.splits or choose(shape_only, B, int(p.seq_lens.max()) + ROUND,
+                              int(p.seq_lens.sum()) + B * ROUND // 2, sms)
     ws = Workspace.from_problem(p, max_splits=S, device=dev)
     run = DecodeRunner(ws, B, num_splits=S, flags=args.flags, scale=p.scale,
                        fused=not args.unfused)

@@ -73,13 +73,15 @@ enum {
   PKV_FLAG_FORCE_MMA = 8,  /* use the tensor-core kernel (error if the shape has none)      */
   PKV_FLAG_FORCE_GATHER = 16, /* tensor-core kernel: load K/V with cp.async gathers even where
                                  tensor-map TMA boxes apply (P % 16 == 0)                   */
-  PKV_FLAG_PLAN_EARLY = 32   /* tensor-core kernel: the caller guarantees that seq_lens,
+  PKV_FLAG_PLAN_EARLY = 32,  /* tensor-core kernel: the caller guarantees that seq_lens,
                                 kv_indptr, kv_indices, req_pool_indices, page_table and
                                 out_loc were last written at least two launches earlier
                                 on this stream (or by the host), so the kernel may read
                                 them and start loading K/V before the previous kernel
                                 finishes (programmatic dependent launch); q, k_new and
                                 all outputs are still touched only after it finishes  */
+  PKV_FLAG_FIXED_CHUNK = 64  /* pkv_decode_layer, tensor-core kernel: cut the KV axis into
+                                pkv_decode_attn's fixed chunks instead of balanced pieces */
 };
 
 /* bits OR-ed into *err by device code (sticky; the caller clears the word) */
@@ -179,6 +181,22 @@ int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint,
                       long long total_tokens_hint, int num_sms);
 
 /*
+ * Piece cap S for pkv_decode_layer's balanced pieces, host only.  The kernel
+ * gives each of its (up to 2 * num_sms) resident blocks W = max(share,
+ * (L - 1) / (S - 1) + 1) positions (integer division) of the line of
+ * (request, KV head) token ranges, share = T / blocks, T = Hkv * total; the
+ * value returned
+ * is one more than the least S whose cap term does not exceed the share, so
+ * a few steps of length growth past the hints keep the blocks balanced:
+ *   share = max(ceil(Hkv * total_tokens_hint / (2 * num_sms)), 128)
+ *   S     = min(3 + (max_seq_len_hint - 1) / share, max_splits).
+ * total_tokens_hint <= 0 means batch * max_seq_len_hint.  Returns 1 for
+ * non-positive batch, length or SM count, or max_splits < 2.
+ */
+int pkv_choose_pieces(const pkv_workspace *ws, int batch, int max_seq_len_hint,
+                      long long total_tokens_hint, int num_sms);
+
+/*
  * Split-KV GQA decode attention for one layer (workspace.py page, bullets 1,
  * 14-16).  For every live b and query head h (KV head g = h / G):
  *   s_t = scale * q[b,h,:] . K[layer, slot(b,t), g, :]   for t < seq_lens[b]
@@ -227,6 +245,15 @@ pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits
  *   num_splits    as pkv_decode_attn; with S > 1 ws->split_counters must be
  *                 set (zeroed once; every call leaves it zeroed), and the last
  *                 split to finish for each (request, KV head) merges.
+ *                 With S > 1 and batch <= 256 the tensor-core kernel cuts the
+ *                 KV axis into balanced pieces instead of fixed chunks: the
+ *                 (request, KV head) token ranges are laid end to end and each
+ *                 resident block takes an equal share of that line, cut inside
+ *                 a range at multiples of 64 tokens and into at most S pieces;
+ *                 the pieces are merged as splits are (o_part / ml_part slots
+ *                 0 .. pieces - 1).  The result equals the fixed-chunk one up to
+ *                 floating-point rounding order; PKV_FLAG_FIXED_CHUNK keeps
+ *                 the fixed chunks.
  *   flags         PKV_FLAG_*; with PKV_FLAG_FORCE_SIMT the three steps run as
  *                 separate kernels (the CUDA-core attention has no fusion).
  * Device errors as for pkv_bind_step and pkv_decode_attn.

@@ -16,12 +16,13 @@ PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_CAPACITY, PKV_ERR_CUDA = r
 PKV_BIND_STEADY, PKV_BIND_REBUILD, PKV_BIND_APPEND_ONLY = 0, 1, 2
 PKV_IDX_PAGE_TABLE, PKV_IDX_FLAT = 0, 1
 PKV_FLAG_OUT_F32, PKV_FLAG_WRITE_LSE, PKV_FLAG_FORCE_SIMT, PKV_FLAG_FORCE_MMA = 1, 2, 4, 8
-PKV_FLAG_FORCE_GATHER, PKV_FLAG_PLAN_EARLY = 16, 32
+PKV_FLAG_FORCE_GATHER, PKV_FLAG_PLAN_EARLY, PKV_FLAG_FIXED_CHUNK = 16, 32, 64
 PKV_DEVERR_PAGE, PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT, PKV_DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16
 
 # Every symbol include/pkv.h declares (checked by the ABI test).
-EXPORTS = ("pkv_workspace_bytes", "pkv_bind_step", "pkv_choose_splits", "pkv_decode_attn",
+EXPORTS = ("pkv_workspace_bytes", "pkv_bind_step", "pkv_choose_splits", "pkv_choose_pieces",
+           "pkv_decode_attn",
            "pkv_merge_partials", "pkv_decode_layer", "pkv_decode_attn_static_scratch",
            "pkv_is_steady_increment",
            "pkv_status_string", "pkv_version")
@@ -74,6 +75,8 @@ def load(path: str = LIB_PATH):
     lib.pkv_bind_step.restype = i32
     lib.pkv_choose_splits.argtypes = [W, i32, i32, ctypes.c_longlong, i32]
     lib.pkv_choose_splits.restype = i32
+    lib.pkv_choose_pieces.argtypes = [W, i32, i32, ctypes.c_longlong, i32]
+    lib.pkv_choose_pieces.restype = i32
     lib.pkv_decode_attn.argtypes = [W, i32, i32, vp, f32, i32, i32, vp]
     lib.pkv_decode_attn.restype = i32
     lib.pkv_merge_partials.argtypes = [W, i32, i32, i32, vp]
@@ -148,6 +151,11 @@ def pkv_bind_step(ws, batch, mode, layer_begin=0, layer_count=0, k_new=None, v_n
 
 def pkv_choose_splits(ws, batch, max_seq_len_hint, total_tokens_hint, num_sms) -> int:
     return int(load().pkv_choose_splits(_ws(ws), int(batch), int(max_seq_len_hint),
+                                        int(total_tokens_hint), int(num_sms)))
+
+
+def pkv_choose_pieces(ws, batch, max_seq_len_hint, total_tokens_hint, num_sms) -> int:
+    return int(load().pkv_choose_pieces(_ws(ws), int(batch), int(max_seq_len_hint),
                                         int(total_tokens_hint), int(num_sms)))
 
 

@@ -17,8 +17,9 @@
 // state; the four states merge at the end of the unit.  The producer walks
 // the block's units ahead of the consumers, across unit boundaries, through a
 // 3-stage ring (`full` mbarriers complete on the landed bytes, `empty` on the
-// four consumer warps' release), fetching index entries up to 8 tiles ahead
-// (a second cursor) so their latency overlaps the issue of earlier tiles.
+// four consumer warps' release), fetching index entries 8 tiles ahead (a
+// second cursor, cp.async into a shared ring) so their latency overlaps the
+// issue of earlier tiles.
 //
 // Units.  With batch <= kMaxCompactBatch only the non-empty (request, split)
 // pairs are units (a per-block prefix over the requests' split counts), so a
@@ -60,12 +61,13 @@ constexpr int kCW = 4;                   // consumer warps
 constexpr int kMThreads = (kCW + 1) * 32;
 constexpr int kMT = 16 * kCW;            // tokens per tile
 constexpr int kMStages = 3;
+constexpr int kLA = 8;  // tiles of index lookahead (shared-memory ring of slots)
 
 template <int D, int G>
 struct MCfg {
   static constexpr int HALVES = D / 64;     // 64-column (128-byte) swizzled halves
-  static constexpr int HALF = kMT * 128;    // bytes of one half of a tile
-  static constexpr int TILE = HALVES * HALF;
+  static constexpr int PIECE = 16 * HALVES * 128;  // bytes of a 16-token page piece
+  static constexpr int TILE = (kMT / 16) * PIECE;
   static constexpr int KSTEPS = D / 16;
   static constexpr int NH = (G + 7) / 8;    // 8-wide head tiles
   static constexpr int MT = D / 16;         // 16-row output (head_dim) tiles
@@ -79,17 +81,27 @@ struct MCfg {
   static_assert(D % 64 == 0, "whole swizzled halves");
 };
 
-// Byte offset of 16-byte chunk c (0..7) of row r inside a swizzled half.
+// Byte offset of 16-byte chunk c (0..7) of 128-byte row r, 128B-swizzled.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
-                                            int c2, uint64_t *bar) {
+// A K or V tile in shared memory: 16-token pieces of HALVES x 16 rows of 128
+// bytes ([piece][half][token % 16][64 columns], the box order of the pool
+// tensor map), so token t, half h is row (t / 16) * 16 * HALVES + 16 h + t % 16
+// and rows of consecutive tokens stay consecutive (conflict-free ldmatrix).
+template <int HALVES>
+__device__ __forceinline__ uint32_t kv_off(int t, int h, int c) {
+  return swz((t >> 4) * (16 * HALVES) + h * 16 + (t & 15), c);
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
+                                            int c2, int c3, uint64_t *bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
-      "[%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -99,14 +111,6 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, int s
                : "memory");
 }
 
-__device__ __forceinline__ float quad_max(float x) {
-  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
-  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
-}
-__device__ __forceinline__ float quad_sum(float x) {
-  x += __shfl_xor_sync(0xffffffffu, x, 1);
-  return x + __shfl_xor_sync(0xffffffffu, x, 2);
-}
 
 // Fused append: write this (request, head)'s new K/V row to the pool when the
 // tile [tile0, tile0 + 64) of this unit holds the request's newest token
@@ -138,12 +142,13 @@ __device__ __forceinline__ void append_if_newest(const DecodeArgs &a, const Unit
   __syncwarp();
 }
 
-// Producer, page mode: 16-token page pieces by tensor-map boxes.  Lane j < 4
-// owns piece j; `raw` is its page id, fetched ahead.
+// Producer, page mode: one tensor-map box per 16-token page piece and pool
+// (both halves of the row).  Lane j < 4 resolves piece j (`raw` is its page
+// id, fetched ahead); lanes 0-3 then load the K pieces, lanes 4-7 the V ones.
 template <int D, int G>
-__device__ __forceinline__ void produce_tma(const DecodeArgs &a, const Unit &un, int tile0,
-                                            int raw, int stage, uint32_t kv_base, uint64_t *full,
-                                            int *flag, const CUtensorMap *tmk,
+__device__ __forceinline__ void produce_tma(const DecodeArgs &a, const Plan &pl, const Unit &un,
+                                            int tile0, int raw, int stage, uint32_t kv_base,
+                                            uint64_t *full, int *flag, const CUtensorMap *tmk,
                                             const CUtensorMap *tmv, int lane) {
   using C = MCfg<D, G>;
   const pkv_workspace &ws = a.ws;
@@ -151,32 +156,27 @@ __device__ __forceinline__ void produce_tma(const DecodeArgs &a, const Unit &un,
   const bool want = lane < 4 && tok0 < un.t1;
   int kind = 0;
   long long slot0 = -1;
-  if (want) slot0 = slot_from_raw(ws, raw, tok0, kind);  // tok0 % 16 == 0: inside one page
+  if (want) slot0 = slot_from_raw(ws, pl, raw, tok0, kind);  // tok0 % 16 == 0: inside one page
   const unsigned ok = __ballot_sync(0xffffffffu, slot0 >= 0);
   const int bad = __reduce_or_sync(0xffffffffu, kind);
+  const int row = __shfl_sync(0xffffffffu, a.layer * ws.pool_slots + (int)slot0, lane & 3);
   if (lane == 0) {
     *flag = bad;
     if (bad) atomicOr(ws.err, bad);
-    mbar_arrive_expect_tx(full, __popc(ok) * (uint32_t)(2 * C::HALVES * 16 * 128));
+    mbar_arrive_expect_tx(full, __popc(ok) * (uint32_t)(2 * C::PIECE));
   }
   __syncwarp();
-  if (slot0 >= 0) {
-    const uint32_t kt = kv_base + (2 * stage) * C::TILE;
-    const uint32_t vt = kt + C::TILE;
-    const int row = a.layer * ws.pool_slots + (int)slot0;
-#pragma unroll
-    for (int h = 0; h < C::HALVES; ++h) {
-      const uint32_t off = h * C::HALF + 16 * lane * 128;
-      tma_load_3d(kt + off, tmk, 64 * h, un.g, row, full);
-      tma_load_3d(vt + off, tmv, 64 * h, un.g, row, full);
-    }
+  if (lane < 8 && ((ok >> (lane & 3)) & 1)) {
+    const uint32_t dst = kv_base + (2 * stage + (lane >> 2)) * C::TILE + (lane & 3) * C::PIECE;
+    tma_load_4d(dst, lane < 4 ? tmk : tmv, 0, row, 0, un.g, full);
   }
 }
 
 // Producer, any page size / flat mode: cp.async 16-byte gathers.  Lane owns
 // rows lane and lane + 32 of the tile; rows past the end are zero-filled.
 template <int D, int G>
-__device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Unit &un, int tile0,
+__device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Plan &pl,
+                                                const Unit &un, int tile0,
                                                 const int (&raw)[2], int stage, uint32_t kv_base,
                                                 uint64_t *full, int *flag, int lane) {
   using C = MCfg<D, G>;
@@ -186,7 +186,7 @@ __device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Unit 
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int tok = tile0 + lane + 32 * h;
-    slot[h] = tok < un.t1 ? slot_from_raw(ws, raw[h], tok, kind) : -1;
+    slot[h] = tok < un.t1 ? slot_from_raw(ws, pl, raw[h], tok, kind) : -1;
   }
   const int bad = __reduce_or_sync(0xffffffffu, kind);
   if (lane == 0) {
@@ -206,7 +206,7 @@ __device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Unit 
         ok ? (((long long)a.layer * ws.pool_slots + slot[h]) * ws.n_kv_heads + un.g) * D : 0;
 #pragma unroll
     for (int c8 = 0; c8 < D / 8; ++c8) {
-      const uint32_t off = (c8 >> 3) * C::HALF + swz(r, c8 & 7);
+      const uint32_t off = kv_off<C::HALVES>(r, c8 >> 3, c8 & 7);
       cp_async_16(kt + off, kp + e + c8 * 8, ok ? 16 : 0);
       cp_async_16(vt + off, vp + e + c8 * 8, ok ? 16 : 0);
     }
@@ -217,7 +217,7 @@ __device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Unit 
 
 
 template <int D, int G>
-__global__ void __launch_bounds__(kMThreads)
+__global__ void __launch_bounds__(kMThreads, 2)
     decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, const int use_tma) {
   using C = MCfg<D, G>;
@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(kMThreads)
   __shared__ int s_pref[kMaxCompactBatch + 1];
   __shared__ int s_len[kMaxCompactBatch];
   __shared__ int s_base[kMaxCompactBatch];
+  __shared__ __align__(16) int s_idx[kLA][64];  // index entries of tiles k .. k + kLA - 1
   __shared__ int s_tmp[32];
   __shared__ int s_max_len;
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -241,6 +242,11 @@ __global__ void __launch_bounds__(kMThreads)
   // Without PKV_FLAG_PLAN_EARLY nothing is read before the previous kernel
   // on the stream has finished.
   const bool early = (a.flags & PKV_FLAG_PLAN_EARLY) != 0;
+  if (use_tma && tid == kCW * 32) {
+    // fetch both descriptors while the plan is built
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmk) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmv) : "memory");
+  }
   if (!early) pdl_wait();
 
   if (tid == 0) {
@@ -257,68 +263,104 @@ __global__ void __launch_bounds__(kMThreads)
   __syncthreads();
 
   Plan pl;
+  pl.set_pages(ws);
   pl.batch = a.batch;
   pl.hkv = ws.n_kv_heads;
   pl.S = a.num_splits;
   const bool direct = pl.S == 1;
   const bool fused = a.fused_merge && !direct;
   if (a.batch <= kMaxCompactBatch) {
-    const int pairs =
-        batch_plan_compact(ws, a.batch, pl.S, s_len, s_base, s_pref, s_tmp, &s_max_len, &pl.chunk);
+    const bool balanced = a.balanced && fused;  // the launcher also checked batch and S
+    const int total = batch_plan_compact(ws, a.batch, pl.S, balanced, s_len, s_base, s_pref,
+                                         s_tmp, &s_max_len, &pl.chunk);
     pl.pref = s_pref;
     pl.lens = s_len;
-    pl.n_units = pairs * pl.hkv;
+    if (balanced) {
+      // W: an equal share of the line for every block, but large enough that
+      // no segment is cut into more than S pieces (a segment of L tokens has
+      // at most floor((L - 1) / W) + 2 of them).
+      pl.balanced = true;
+      pl.T = pl.hkv * total;
+      const int share = (int)(((long long)pl.T + gridDim.x - 1) / gridDim.x);
+      const int by_cap = max(s_max_len - 1, 0) / (pl.S - 1) + 1;
+      pl.W = max(max(share, by_cap), kMinPiece);
+      pl.n_units = 0;
+    } else {
+      pl.n_units = total * pl.hkv;
+    }
   } else {
     pl.chunk = split_chunk(batch_max_len(ws, a.batch, &s_max_len), pl.S, ws.page_size);
     pl.n_units = pl.S * pl.batch * pl.hkv;
   }
   const uint32_t kv_base = smem_addr(smem + C::OFF_KV);
 
+  // Index entries of the block's first kLA tiles, fetched by the whole block
+  // in one round trip (each thread walks its own cursor to its tile), so the
+  // producer can issue tile 0 right away.  TMA path: entries 0..3 of a ring
+  // slot are the page ids of the tile's 16-token pieces; gather path: entries
+  // 0..63 are the slots / page ids of its rows; -1 where there is none.
+  {
+    const int per = use_tma ? 4 : kMT;
+    Cursor<kMT> c;
+    int at = -1;
+    for (int e = tid; e < kLA * per; e += kMThreads) {
+      const int tile = e / per, r = e - tile * per;
+      if (at < 0) {
+        c.start(ws, pl);
+        at = 0;
+      }
+      c.advance_by(ws, pl, tile - at);
+      at = tile;
+      int v = -1;
+      if (!c.done) {
+        const Unit &u = c.it.un;
+        const int tok = u.t0 + c.i * kMT + (use_tma ? 16 * r : r);
+        const ReqIndex ri = pl.pref ? req_index_cached(ws, s_base, u.b) : req_index(ws, u.b);
+        if (tok < u.t1 && ri.ok) v = *index_src(ws, pl, ri, tok);
+      }
+      s_idx[tile][r] = v;
+    }
+  }
+  __syncthreads();
+
   if (warp == kCW) {
     // ------------------------------------------------------- producer ----
     Cursor<kMT> pc;
-    pc.seek(ws, pl, blockIdx.x);
-    // Index entries are fetched by a second cursor running ahead of pc, so
-    // their load latency overlaps the issue of earlier tiles.  TMA path:
-    // lane l holds the page id of piece l % 4 of tile k + l / 4 (8 tiles of
-    // lookahead in one register); gather path: a queue of 3 tiles, 2 rows
-    // per lane each.
+    pc.start(ws, pl);
+    // Later index entries are fetched by a second cursor running kLA tiles
+    // ahead of pc, with 4-byte cp.async copies into the ring (one commit group
+    // per tile, issued at iteration k for tile k + kLA), so no register ever
+    // waits on an index load: at iteration k, tile k's entries are complete
+    // once at most kLA - 1 newer groups pend (and tiles 0 .. kLA - 1 came in
+    // with the block's fetch above).
     Cursor<kMT> pf = pc;
+    pf.advance_by(ws, pl, kLA);
     int pf_u = -1;
-    ReqIndex pf_ri;
-    auto pf_index = [&]() {
-      if (pf.un.u != pf_u) {
-        pf_ri = pl.pref ? req_index_cached(ws, s_base, pf.un.b) : req_index(ws, pf.un.b);
-        pf_u = pf.un.u;
+    ReqIndex pf_ri{0, false};
+    auto prefetch = [&](int slot) {  // entries of the tile under pf into s_idx[slot]
+      const Unit &fu = pf.it.un;
+      if (!pf.done && fu.u != pf_u) {
+        pf_ri = pl.pref ? req_index_cached(ws, s_base, fu.b) : req_index(ws, fu.b);
+        pf_u = fu.u;
       }
+      const int tile0 = pf.done ? 0 : fu.t0 + pf.i * kMT;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        const int tok = use_tma ? tile0 + 16 * r : tile0 + r;
+        const bool want = (use_tma ? r < 4 : true) && !pf.done && tok < fu.t1 && pf_ri.ok;
+        int *dst = &s_idx[slot][r];
+        if (want) {
+          const int *src = index_src(ws, pl, pf_ri, tok);
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+                       : "memory");
+        } else {
+          *dst = -1;
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (!pf.done) pf.advance(ws, pl);
     };
-    int win = -1;
-    int rq[3][2];
-    if (use_tma) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (!pf.done) {
-          pf_index();
-          const int tok0 = pf.un.t0 + pf.i * kMT + 16 * (lane & 3);
-          if ((lane >> 2) == j) win = tok0 < pf.un.t1 ? raw_index(ws, pf_ri, tok0) : -1;
-          pf.advance(ws, pl);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        rq[j][0] = rq[j][1] = -1;
-        if (!pf.done) {
-          pf_index();
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int tok = pf.un.t0 + pf.i * kMT + lane + 32 * h;
-            rq[j][h] = tok < pf.un.t1 ? raw_index(ws, pf_ri, tok) : -1;
-          }
-          pf.advance(ws, pl);
-        }
-      }
-    }
     int k = 0;
     bool aborted = false;
     bool waited = !early;
@@ -334,7 +376,7 @@ __global__ void __launch_bounds__(kMThreads)
         aborted = true;
         break;
       }
-      const Unit un = pc.un;
+      const Unit un = pc.it.un;
       const int tile0 = un.t0 + pc.i * kMT;
       if (!waited && a.k_new != nullptr && un.L > 0 && un.L - 1 >= tile0 &&
           un.L - 1 < min(tile0 + kMT, un.t1)) {
@@ -344,38 +386,20 @@ __global__ void __launch_bounds__(kMThreads)
       }
       append_if_newest<D>(a, un, tile0, lane);
       pc.advance(ws, pl);
+      asm volatile("cp.async.wait_group %0;" ::"n"(kLA - 1) : "memory");
+      const int slot = k % kLA;
+      const int cur[2] = {s_idx[slot][lane], s_idx[slot][lane + 32]};
+      __syncwarp();
       if (use_tma) {
-        const int cur = win;  // lanes 0..3: this tile's pieces
-        win = __shfl_down_sync(0xffffffffu, win, 4);
-        if (!pf.done) {
-          pf_index();
-          const int tok0 = pf.un.t0 + pf.i * kMT + 16 * (lane & 3);
-          if (lane >= 28) win = tok0 < pf.un.t1 ? raw_index(ws, pf_ri, tok0) : -1;
-          pf.advance(ws, pl);
-        } else if (lane >= 28) {
-          win = -1;
-        }
-        produce_tma<D, G>(a, un, tile0, cur, s, kv_base, &full[s], &flags[s], &tmk, &tmv, lane);
+        produce_tma<D, G>(a, pl, un, tile0, cur[0], s, kv_base, &full[s], &flags[s], &tmk, &tmv,
+                          lane);
       } else {
-        const int cur[2] = {rq[0][0], rq[0][1]};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          rq[0][h] = rq[1][h];
-          rq[1][h] = rq[2][h];
-          rq[2][h] = -1;
-        }
-        if (!pf.done) {
-          pf_index();
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int tok = pf.un.t0 + pf.i * kMT + lane + 32 * h;
-            rq[2][h] = tok < pf.un.t1 ? raw_index(ws, pf_ri, tok) : -1;
-          }
-          pf.advance(ws, pl);
-        }
-        produce_cpasync<D, G>(a, un, tile0, cur, s, kv_base, &full[s], &flags[s], lane);
+        // Issued before the next index copies: the stage's copy-completion
+        // arrival covers every earlier cp.async of the lane.
+        produce_cpasync<D, G>(a, pl, un, tile0, cur, s, kv_base, &full[s], &flags[s], lane);
         if (lane == 0) mbar_arrive(&full[s]);
       }
+      prefetch(slot);  // tile k + kLA reuses the slot just read
       ++k;
     }
     if (aborted) {
@@ -387,6 +411,7 @@ __global__ void __launch_bounds__(kMThreads)
       for (int kk = max(0, k - kMStages); kk < k; ++kk)
         mbar_wait_bounded(&full[kk % kMStages], (kk / kMStages) & 1);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // index copies still in flight
     return;
   }
 
@@ -420,10 +445,12 @@ __global__ void __launch_bounds__(kMThreads)
   }
 
   int k = 0;
-  for (int u = blockIdx.x; u < pl.n_units; u += gridDim.x) {
-    const Unit un = unit_at(ws, pl, u);
+  UnitIter ui;
+  ui.first(ws, pl);
+  for (; !ui.done; ui.next(ws, pl)) {
+    const Unit un = ui.un;
     const int hq0 = un.g * G;
-    const int n_b = un.L > 0 ? (un.L + pl.chunk - 1) / pl.chunk : 0;
+    const int n_b = un.n;
     if (un.t0 >= un.t1) {  // dense enumeration only
       const int ct = tid;  // consumer thread 0..127
       if (direct || fused) {
@@ -503,7 +530,8 @@ __global__ void __launch_bounds__(kMThreads)
 #pragma unroll
           for (int ks = 0; ks < C::KSTEPS; ++ks) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(kt + (ks >> 2) * C::HALF + swz(rowK, (ks & 3) * 2 + (mi >> 1)), a0, a1, a2, a3);
+            ldsm_x4(kt + kv_off<C::HALVES>(rowK, ks >> 2, (ks & 3) * 2 + (mi >> 1)), a0, a1, a2,
+                    a3);
 #pragma unroll
             for (int n = 0; n < C::NH; ++n)
               mma_bf16_16816((ks & 1) ? sc2[n] : sc[n], a0, a1, a2, a3, qb[n][ks][0], qb[n][ks][1]);
@@ -519,7 +547,7 @@ __global__ void __launch_bounds__(kMThreads)
               const int r = 16 * warp + nv + (i >> 4), c8 = i & 15;
               if (c8 < D / 8)
                 asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
-                                 vt + (c8 >> 3) * C::HALF + swz(r, c8 & 7)),
+                                 vt + kv_off<C::HALVES>(r, c8 >> 3, c8 & 7)),
                              "r"(0u)
                              : "memory");
             }
@@ -568,7 +596,8 @@ __global__ void __launch_bounds__(kMThreads)
 #pragma unroll
           for (int mt = 0; mt < C::MT; ++mt) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(vt + (mt >> 2) * C::HALF + swz(rowV, (mt & 3) * 2 + (mi & 1)), a0, a1, a2, a3);
+            ldsm_x4_t(vt + kv_off<C::HALVES>(rowV, mt >> 2, (mt & 3) * 2 + (mi & 1)), a0, a1, a2,
+                      a3);
 #pragma unroll
             for (int n = 0; n < C::NH; ++n) {
               mma_bf16_16816(acc[n][mt], a0, a1, a2, a3, bh[n][0], bh[n][1]);
@@ -705,16 +734,16 @@ __global__ void __launch_bounds__(kMThreads)
     if (fused && !final_out) {
       named_sync(1, kCW * 32);
       if (tid == 0) {
-        __threadfence();  // the block's partial (ordered by the barrier) before the ticket
+        // the block's partial (ordered by the barrier) is released with the
+        // ticket; the last taker acquires every other block's
         int *ctr = ws.split_counters + (long long)un.b * ws.n_kv_heads + un.g;
-        const int old = atomicAdd(ctr, 1);
+        const int old = atomic_add_acq_rel_gpu(ctr, 1);
         const int last = old == n_b - 1;
         if (last) *ctr = 0;  // ready for the next launch
         *s_ticket = last;
       }
       named_sync(1, kCW * 32);
       if (*s_ticket) {
-        __threadfence();
         // warp w merges query heads w, w + 4, ... of the group
         constexpr int RPW = G >= kCW ? G / kCW : 1;
         if (warp < G)
@@ -746,17 +775,20 @@ TmapEncodeFn tmap_encoder() {
   return fn;
 }
 
-// 3-D view [NL * pool_slots][Hkv][D] of a pool; box = 16 slots x 1 head x 64 cols.
+// 4-D view of a pool [NL * pool_slots, Hkv, D] as (64 columns, slot, 64-column
+// half, KV head), strides 2 B, Hkv * D * 2, 128, D * 2: a box of 64 x 16 x
+// halves x 1 lands in shared memory as [half][slot][64 columns], one page
+// piece of one head with both halves of its rows.  Every element a box can
+// address lies inside the pool.
 bool encode_pool_map(CUtensorMap *m, void *base, const pkv_workspace &ws) {
   TmapEncodeFn enc = tmap_encoder();
   if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)ws.head_dim, (cuuint64_t)ws.n_kv_heads,
-                              (cuuint64_t)ws.n_layers * (cuuint64_t)ws.pool_slots};
-  const cuuint64_t strides[2] = {(cuuint64_t)ws.head_dim * 2,
-                                 (cuuint64_t)ws.head_dim * 2 * ws.n_kv_heads};
-  const cuuint32_t box[3] = {64, 1, 16};
-  const cuuint32_t elem[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, elem,
+  const cuuint64_t D = (cuuint64_t)ws.head_dim, H = (cuuint64_t)ws.n_kv_heads;
+  const cuuint64_t dims[4] = {64, (cuuint64_t)ws.n_layers * (cuuint64_t)ws.pool_slots, D / 64, H};
+  const cuuint64_t strides[3] = {H * D * 2, 128, D * 2};
+  const cuuint32_t box[4] = {64, 16, (cuuint32_t)(D / 64), 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, elem,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -795,6 +827,13 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
   const long long cap = (long long)sms_cache[di] * occ_cache[di];
   const int grid = (int)(units < cap ? units : cap);
   if (grid <= 0) return cudaSuccess;
+  // Balanced pieces need the compact plan, and their line positions (Hkv x
+  // the summed lengths) must fit in an int.
+  DecodeArgs args = a;
+  args.balanced = a.fused_merge && a.num_splits > 1 && a.batch <= kMaxCompactBatch &&
+                  !(a.flags & PKV_FLAG_FIXED_CHUNK) &&
+                  (long long)a.batch * ws.max_pages_per_req * ws.page_size * ws.n_kv_heads <
+                      0x7fffffffll;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kMThreads);
@@ -805,7 +844,7 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, tmk, tmv, use_tma);
+  return cudaLaunchKernelEx(&cfg, kern, args, tmk, tmv, use_tma);
 }
 
 }  // namespace

@@ -86,9 +86,10 @@ __device__ __forceinline__ void merge_store(const pkv_workspace &ws, long long r
 }
 
 // Merge of the n split partials of NH query-head rows (row0 + j * rstep,
-// j < NH) by one warp, with all of a batch of partial-row loads in flight:
-// lane s holds split s's weight for every row, then up to 8 splits x NH rows
-// of float4 loads are issued before any is used.
+// j < NH) by one warp, with all of a group of partial-row loads in flight:
+// lane s holds split s's weight for every row, and GS splits x NH rows of
+// float4 loads are issued before any is used (the first group together with
+// the weights' loads).
 template <int D, int NH>
 __device__ __forceinline__ void merge_rows_batched(const pkv_workspace &ws, long long row0,
                                                    long long rstep, int S, int n, int flags,
@@ -102,14 +103,29 @@ __device__ __forceinline__ void merge_rows_batched(const pkv_workspace &ws, long
     den[j] = 0.f;
     acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  constexpr int GS = NH >= 4 ? 4 : 8;  // splits per group of row loads (registers)
+  auto load_rows = [&](float4 (&o)[GS][NH], int s, int m) {  // splits s .. s + GS - 1 (< m)
+#pragma unroll
+    for (int t = 0; t < GS; ++t)
+#pragma unroll
+      for (int j = 0; j < NH; ++j)
+        o[t][j] = (t < m && lane < NV)
+                      ? __ldcg(reinterpret_cast<const float4 *>(
+                                   ws.o_part + ((row0 + j * rstep) * S + s + t) * D) + lane)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
   for (int s0 = 0; s0 < n; s0 += 32) {
-    // (m, l) of split s0 + lane for every row
+    // (m, l) of split s0 + lane for every row, with the first GS splits' rows
+    // (independent of the weights) already in flight
     float2 ml[NH];
 #pragma unroll
     for (int j = 0; j < NH; ++j)
       ml[j] = s0 + lane < n
                   ? __ldcg(reinterpret_cast<const float2 *>(ws.ml_part + (row0 + j * rstep) * S * 2) + s0 + lane)
                   : make_float2(-INFINITY, 0.f);
+    const int m = min(32, n - s0);
+    float4 o[GS][NH];
+    load_rows(o, s0, m);
     float w[NH];
 #pragma unroll
     for (int j = 0; j < NH; ++j) {
@@ -131,19 +147,10 @@ __device__ __forceinline__ void merge_rows_batched(const pkv_workspace &ws, long
       for (int d = 16; d >= 1; d >>= 1) ws_ += __shfl_xor_sync(0xffffffffu, ws_, d);
       den[j] += ws_;
     }
-    const int m = min(32, n - s0);
-    for (int t0 = 0; t0 < m; t0 += 8) {
-      float4 o[8][NH];
+    for (int t0 = 0; t0 < m; t0 += GS) {
+      if (t0 > 0) load_rows(o, s0 + t0, m - t0);
 #pragma unroll
-      for (int t = 0; t < 8; ++t)
-#pragma unroll
-        for (int j = 0; j < NH; ++j)
-          o[t][j] = (t0 + t < m && lane < NV)
-                        ? __ldcg(reinterpret_cast<const float4 *>(
-                                     ws.o_part + ((row0 + j * rstep) * S + s0 + t0 + t) * D) + lane)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
+      for (int t = 0; t < GS; ++t)
 #pragma unroll
         for (int j = 0; j < NH; ++j) {
           const float wt = __shfl_sync(0xffffffffu, w[j], (t0 + t) & 31);

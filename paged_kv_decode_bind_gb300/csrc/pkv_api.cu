@@ -139,6 +139,20 @@ int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint,
   return best_s;
 }
 
+int pkv_choose_pieces(const pkv_workspace *ws, int batch, int max_seq_len_hint,
+                      long long total_tokens_hint, int num_sms) {
+  if (!ws || batch <= 0 || max_seq_len_hint <= 0 || num_sms <= 0 || ws->n_kv_heads <= 0 ||
+      ws->max_splits < 2)
+    return 1;
+  const long long L = max_seq_len_hint;
+  const long long total = total_tokens_hint > 0 ? total_tokens_hint : (long long)batch * L;
+  const long long blocks = 2ll * num_sms;  // resident blocks of the tensor-core kernel
+  long long share = (ws->n_kv_heads * total + blocks - 1) / blocks;
+  if (share < 128) share = 128;  // two tiles: shorter pieces cost more in merging
+  const long long S = 3 + (L - 1) / share;
+  return (int)(S < ws->max_splits ? S : ws->max_splits);
+}
+
 static pkv_status decode_common(const pkv_workspace *ws, int batch, int layer, const void *q,
                                 const void *k_new, const void *v_new, float scale,
                                 int num_splits, int flags, int fused, pkv_stream_t stream) {
@@ -171,12 +185,12 @@ static pkv_status decode_common(const pkv_workspace *ws, int batch, int layer, c
     // The CUDA-core attention has no fused form: run the three steps.
     if (k_new && (st = from_cuda(launch_append(*ws, batch, layer, 1, k_new, v_new, s))) != PKV_OK)
       return st;
-    DecodeArgs a{*ws, batch, layer, q, scale, num_splits, flags, nullptr, nullptr, 0};
+    DecodeArgs a{*ws, batch, layer, q, scale, num_splits, flags, nullptr, nullptr, 0, 0};
     if ((st = from_cuda(launch_decode_simt(a, s))) != PKV_OK) return st;
     if (num_splits > 1) return from_cuda(launch_merge(*ws, batch, num_splits, flags, s));
     return PKV_OK;
   }
-  DecodeArgs a{*ws, batch, layer, q, scale, num_splits, flags, k_new, v_new, fused};
+  DecodeArgs a{*ws, batch, layer, q, scale, num_splits, flags, k_new, v_new, fused, 0};
   return from_cuda(use_mma ? launch_decode_mma(a, s) : launch_decode_simt(a, s));
 }
 

@@ -128,6 +128,23 @@ def test_choose_splits():
     assert P.pkv_choose_splits(ws, 0, 10, 10, 152) == 1
 
 
+def test_choose_pieces():
+    ws = _ws(max_splits=128, n_kv_heads=8, n_q_heads=32)
+    # share = ceil(8 * 65536 / 304) = 1725 -> 3 + 65535 // 1725
+    assert P.pkv_choose_pieces(ws, 1, 65536, 65536, 152) == 40
+    # share = ceil(8 * 262272 / 304) = 6902 -> 3 + 65599 // 6902
+    assert P.pkv_choose_pieces(ws, 4, 65600, 4 * 65568, 152) == 12
+    # skewed: share = ceil(8 * 14500 / 304) = 382 -> 3 + 8191 // 382
+    assert P.pkv_choose_pieces(ws, 16, 8192, 14500, 152) == 24
+    # share = ceil(8 * 6500 / 304) = 172 -> 3 + 2047 // 172
+    assert P.pkv_choose_pieces(ws, 4, 2048, 6500, 152) == 14
+    # tiny: the share floor of 128 tokens
+    assert P.pkv_choose_pieces(ws, 1, 100, 100, 152) == 3
+    assert P.pkv_choose_pieces(_ws(max_splits=4), 1, 65536, 65536, 152) == 4
+    assert P.pkv_choose_pieces(_ws(max_splits=1), 1, 65536, 65536, 152) == 1
+    assert P.pkv_choose_pieces(ws, 0, 10, 10, 152) == 1
+
+
 def test_steady_predicate_matches_oracle():
     import oracle.ref as R
     cases = [([4, 9], [10, 3], [4, 9], [11, 4]), ([4, 9], [10, 3], [9, 4], [4, 11]),

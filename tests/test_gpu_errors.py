@@ -21,7 +21,8 @@ pytestmark = pytest.mark.gpu
 
 PATHS = {"simt": (A.PKV_FLAG_FORCE_SIMT, False), "mma": (A.PKV_FLAG_FORCE_MMA, False),
          "gather": (A.PKV_FLAG_FORCE_MMA | A.PKV_FLAG_FORCE_GATHER, False),
-         "fused": (0, True), "fused_gather": (A.PKV_FLAG_FORCE_GATHER, True)}
+         "fused": (0, True), "fused_gather": (A.PKV_FLAG_FORCE_GATHER, True),
+         "fused_fixed": (A.PKV_FLAG_FIXED_CHUNK, True)}
 
 
 def _setup(p, S, kern):

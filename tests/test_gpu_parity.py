@@ -19,11 +19,13 @@ from parity import bf16_to_f64, check_attention, run_steps
 pytestmark = pytest.mark.gpu
 
 SIMT, MMA, GATHER = A.PKV_FLAG_FORCE_SIMT, A.PKV_FLAG_FORCE_MMA, A.PKV_FLAG_FORCE_GATHER
+FIXED = A.PKV_FLAG_FIXED_CHUNK
 # (flags, fused): the CUDA-core kernel; the tensor-core kernel with TMA boxes
 # (page sizes that are multiples of 16) or cp.async gathers; the fused layer
-# kernel (append + attention + merge in one launch) with either producer.
+# kernel (append + attention + merge in one launch) with either producer and
+# balanced pieces, and with the fixed chunks of the unfused call.
 PATHS = {"simt": (SIMT, False), "mma": (MMA, False), "gather": (MMA | GATHER, False),
-         "fused": (0, True), "fused_gather": (GATHER, True)}
+         "fused": (0, True), "fused_gather": (GATHER, True), "fused_fixed": (FIXED, True)}
 KERNELS = pytest.mark.parametrize("kern", list(PATHS), ids=list(PATHS))
 
 
@@ -115,10 +117,11 @@ def test_cross_split_agreement(cuda):
     # fp32 outputs from different split counts agree within 1e-3.
     p = W.workload("gqa4_long_65536", batch=2, shrink=32, steps=1)
     outs = []
-    for S, fused in ((1, False), (2, False), (9, False), (32, False), (9, True), (32, True)):
+    for S, fused, fl in ((1, False, 0), (2, False, 0), (9, False, 0), (32, False, 0),
+                         (2, True, 0), (9, True, 0), (32, True, 0), (9, True, FIXED)):
         ws = Workspace.from_problem(p, max_splits=S)
-        run = DecodeRunner(ws, p.batch, num_splits=S, flags=A.PKV_FLAG_OUT_F32, scale=p.scale,
-                           fused=fused)
+        run = DecodeRunner(ws, p.batch, num_splits=S, flags=A.PKV_FLAG_OUT_F32 | fl,
+                           scale=p.scale, fused=fused)
         q, k, v = W.step_inputs(p, 0)
         run.q_in.copy_(q), run.k_in.copy_(k), run.v_in.copy_(v)
         run.step()
@@ -213,10 +216,10 @@ def test_zero_length_request(cuda):
 
 # ----------------------------------------------------------- full size ----
 
-def _bench_splits(p):
+def _bench_splits(p, chooser=A.pkv_choose_splits):
     ws_shape = A.PkvWorkspace(n_kv_heads=p.n_kv_heads, max_splits=256)
-    return A.pkv_choose_splits(ws_shape, p.batch, int(p.seq_lens.max()) + 1,
-                               int(p.seq_lens.sum()) + p.batch, _sms())
+    return chooser(ws_shape, p.batch, int(p.seq_lens.max()) + 1,
+                   int(p.seq_lens.sum()) + p.batch, _sms())
 
 
 @pytest.mark.parametrize("name,batch", [("gqa4_b4_paged", None), ("gqa4_b16_flat_skewed", None),
@@ -224,10 +227,12 @@ def _bench_splits(p):
                                         ("gqa8_graph_sweep", 16)])
 def test_full_size_sampled(cuda, name, batch):
     p = W.workload(name, batch=batch, steps=1)
-    S = _bench_splits(p)
     layers = sorted({0, p.n_layers - 1})
-    # the fused layer kernel the benchmark times, then the unfused tensor-core path
-    for flags, fused in ((0, True), (MMA, False)):
+    # the fused layer kernel the benchmark times (balanced pieces, S from
+    # pkv_choose_pieces), then the unfused tensor-core path
+    for flags, fused, chooser in ((0, True, A.pkv_choose_pieces),
+                                  (MMA, False, A.pkv_choose_splits)):
+        S = _bench_splits(p, chooser)
         run_steps(p, S=S, check_layers=layers, heads=_sample_heads(p, 12), check_partials=True,
                   flags=flags, fused=fused)
 
