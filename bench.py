@@ -278,10 +278,10 @@ def run_ours(args, rank, world, local_rank):
     B, NL = p.batch, p.n_layers
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     shape_only = A.PkvWorkspace(n_kv_heads=p.n_kv_heads, max_splits=1 << 20)
-    # the fused layer kernel cuts balanced pieces (S caps them per request and
+    # the fused layer kernel cuts apportioned splits (S caps them per request and
     # head); the separate calls and PKV_FLAG_FIXED_CHUNK cut fixed chunks
-    balanced = not args.unfused and not (args.flags & A.PKV_FLAG_FIXED_CHUNK)
-    choose = A.pkv_choose_pieces if balanced else A.pkv_choose_splits
+    apportioned = not args.unfused and not (args.flags & A.PKV_FLAG_FIXED_CHUNK)
+    choose = A.pkv_choose_pieces if apportioned else A.pkv_choose_splits
     S = args.splits or choose(shape_only, B, int(p.seq_lens.max()) + ROUND,
                               int(p.seq_lens.sum()) + B * ROUND // 2, sms)
     ws = Workspace.from_problem(p, max_splits=S, device=dev)

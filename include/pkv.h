@@ -81,7 +81,8 @@ enum {
                                 finishes (programmatic dependent launch); q, k_new and
                                 all outputs are still touched only after it finishes  */
   PKV_FLAG_FIXED_CHUNK = 64  /* pkv_decode_layer, tensor-core kernel: cut the KV axis into
-                                pkv_decode_attn's fixed chunks instead of balanced pieces */
+                                pkv_decode_attn's fixed chunks instead of apportioned
+                                splits */
 };
 
 /* bits OR-ed into *err by device code (sticky; the caller clears the word) */
@@ -181,13 +182,11 @@ int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint,
                       long long total_tokens_hint, int num_sms);
 
 /*
- * Piece cap S for pkv_decode_layer's balanced pieces, host only.  The kernel
- * gives each of its (up to 2 * num_sms) resident blocks W = max(share,
- * (L - 1) / (S - 1) + 1) positions (integer division) of the line of
- * (request, KV head) token ranges, share = T / blocks, T = Hkv * total; the
- * value returned
- * is one more than the least S whose cap term does not exceed the share, so
- * a few steps of length growth past the hints keep the blocks balanced:
+ * Split cap S for pkv_decode_layer's apportioned splits, host only.  The
+ * kernel gives a request of L tokens about L / share splits, share = Hkv *
+ * total / blocks over its (up to 2 * num_sms) resident blocks; the value
+ * returned leaves headroom over the longest request's share, so a few steps
+ * of length growth past the hints do not hit the cap:
  *   share = max(ceil(Hkv * total_tokens_hint / (2 * num_sms)), 128)
  *   S     = min(3 + (max_seq_len_hint - 1) / share, max_splits).
  * total_tokens_hint <= 0 means batch * max_seq_len_hint.  Returns 1 for
@@ -246,14 +245,15 @@ pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits
  *                 set (zeroed once; every call leaves it zeroed), and the last
  *                 split to finish for each (request, KV head) merges.
  *                 With S > 1 and batch <= 256 the tensor-core kernel cuts the
- *                 KV axis into balanced pieces instead of fixed chunks: the
- *                 (request, KV head) token ranges are laid end to end and each
- *                 resident block takes an equal share of that line, cut inside
- *                 a range at multiples of 64 tokens and into at most S pieces;
- *                 the pieces are merged as splits are (o_part / ml_part slots
- *                 0 .. pieces - 1).  The result equals the fixed-chunk one up to
- *                 floating-point rounding order; PKV_FLAG_FIXED_CHUNK keeps
- *                 the fixed chunks.
+ *                 KV axis into apportioned splits instead of fixed chunks: its
+ *                 resident blocks are shared out among the requests in
+ *                 proportion to their lengths, request b getting n_b splits
+ *                 (1 <= n_b <= min(S, ceil(L_b / 128))) of one chunk of its
+ *                 own, a multiple of 64 tokens, per KV head, with Hkv * sum n_b
+ *                 at most the blocks whenever Hkv * (requests) is; the splits
+ *                 are merged as usual (o_part / ml_part slots 0 .. n_b - 1).
+ *                 The result equals the fixed-chunk one up to floating-point
+ *                 rounding order; PKV_FLAG_FIXED_CHUNK keeps the fixed chunks.
  *   flags         PKV_FLAG_*; with PKV_FLAG_FORCE_SIMT the three steps run as
  *                 separate kernels (the CUDA-core attention has no fusion).
  * Device errors as for pkv_bind_step and pkv_decode_attn.

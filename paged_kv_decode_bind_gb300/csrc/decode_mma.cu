@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
   __shared__ int s_pref[kMaxCompactBatch + 1];
   __shared__ int s_len[kMaxCompactBatch];
   __shared__ int s_base[kMaxCompactBatch];
+  __shared__ int s_chunk[kMaxCompactBatch];
   __shared__ __align__(16) int s_idx[kLA][64];  // index entries of tiles k .. k + kLA - 1
   __shared__ int s_tmp[32];
   __shared__ int s_max_len;
@@ -270,24 +271,13 @@ __global__ void __launch_bounds__(kMThreads, 2)
   const bool direct = pl.S == 1;
   const bool fused = a.fused_merge && !direct;
   if (a.batch <= kMaxCompactBatch) {
-    const bool balanced = a.balanced && fused;  // the launcher also checked batch and S
-    const int total = batch_plan_compact(ws, a.batch, pl.S, balanced, s_len, s_base, s_pref,
-                                         s_tmp, &s_max_len, &pl.chunk);
+    const int budget = a.apportion && fused ? (int)gridDim.x : 0;
+    const int pairs = batch_plan_compact(ws, a.batch, pl.S, budget, s_len, s_base, s_pref,
+                                         s_chunk, s_tmp, &s_max_len, &pl.chunk);
     pl.pref = s_pref;
     pl.lens = s_len;
-    if (balanced) {
-      // W: an equal share of the line for every block, but large enough that
-      // no segment is cut into more than S pieces (a segment of L tokens has
-      // at most floor((L - 1) / W) + 2 of them).
-      pl.balanced = true;
-      pl.T = pl.hkv * total;
-      const int share = (int)(((long long)pl.T + gridDim.x - 1) / gridDim.x);
-      const int by_cap = max(s_max_len - 1, 0) / (pl.S - 1) + 1;
-      pl.W = max(max(share, by_cap), kMinPiece);
-      pl.n_units = 0;
-    } else {
-      pl.n_units = total * pl.hkv;
-    }
+    pl.chunks = budget > 0 ? s_chunk : nullptr;
+    pl.n_units = pairs * pl.hkv;
   } else {
     pl.chunk = split_chunk(batch_max_len(ws, a.batch, &s_max_len), pl.S, ws.page_size);
     pl.n_units = pl.S * pl.batch * pl.hkv;
@@ -827,13 +817,12 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
   const long long cap = (long long)sms_cache[di] * occ_cache[di];
   const int grid = (int)(units < cap ? units : cap);
   if (grid <= 0) return cudaSuccess;
-  // Balanced pieces need the compact plan, and their line positions (Hkv x
-  // the summed lengths) must fit in an int.
+  // Apportioned splits need the compact plan, and the summed lengths must
+  // fit in an int.
   DecodeArgs args = a;
-  args.balanced = a.fused_merge && a.num_splits > 1 && a.batch <= kMaxCompactBatch &&
-                  !(a.flags & PKV_FLAG_FIXED_CHUNK) &&
-                  (long long)a.batch * ws.max_pages_per_req * ws.page_size * ws.n_kv_heads <
-                      0x7fffffffll;
+  args.apportion = a.fused_merge && a.num_splits > 1 && a.batch <= kMaxCompactBatch &&
+                   !(a.flags & PKV_FLAG_FIXED_CHUNK) &&
+                   (long long)a.batch * ws.max_pages_per_req * ws.page_size < 0x7fffffffll;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kMThreads);

@@ -7,13 +7,12 @@
 // the live maximum length (split_chunk), so no request needs more than S
 // splits.  Compact enumeration skips the splits past each request's end.
 //
-// Balanced pieces (fused merge only): the (request, KV head) segments of the
-// batch are laid end to end, b-major, and block i takes the positions
-// [i*W, (i+1)*W) of that line, W = ceil(T / blocks) for T positions in all;
-// inside a segment the cut points are rounded up to a multiple of
-// kPieceAlign tokens.  Every block then streams the same number of tokens
-// (to within a tile per segment it touches) whatever the length mix, and a
-// segment's pieces are its splits, numbered from 0 in token order.
+// Apportioned splits (fused merge only): the resident blocks are shared out
+// among the requests in proportion to their lengths, request b getting n_b
+// splits of one per-request chunk (a multiple of kChunkAlign tokens) for each
+// of its KV heads, with Hkv * sum n_b never above the blocks: every block
+// then has at most one unit, and the units are as even as whole tiles allow
+// whatever the length mix.
 #pragma once
 
 #include "common.cuh"
@@ -25,13 +24,11 @@ struct Plan {
   // Compact enumeration: exclusive prefix over requests of their split counts
   // and their usable lengths (shared memory, batch + 1 / batch entries);
   // NULL = dense enumeration.
-  // Balanced pieces: pref is the exclusive prefix of the usable lengths,
-  // W the positions per block, T = hkv * pref[batch].
-  // Both fit in 31 bits (the launcher checks Hkv * batch * capacity).
+  // Apportioned splits: chunks[b] is request b's chunk (else NULL: the one
+  // chunk above).
   const int *pref = nullptr;
   const int *lens = nullptr;
-  bool balanced = false;
-  int W = 0, T = 0;
+  const int *chunks = nullptr;
   // Page geometry, so that the per-tile index arithmetic needs no division
   // when the page size is a power of two.
   int P = 1, pshift = 0, n_pages = 0;
@@ -50,8 +47,8 @@ struct Plan {
 };
 
 constexpr int kMaxCompactBatch = 256;
-constexpr int kPieceAlign = 64;  // balanced cut points: multiples of this many tokens
-constexpr int kMinPiece = 128;   // balanced share floor: shorter pieces cost more to merge
+constexpr int kChunkAlign = 64;  // apportioned chunks: multiples of this many tokens
+constexpr int kMinChunk = 128;   // no apportioned split shorter (more merging than streaming)
 
 struct Unit {
   int u, b, g, c, t0, t1;
@@ -91,6 +88,7 @@ __device__ __forceinline__ Unit unit_at(const pkv_workspace &ws, const Plan &pl,
     }
     x.b = lo;
     x.c = w - pl.pref[lo];
+    x.n = pl.pref[lo + 1] - pl.pref[lo];
   } else {
     const int hb = pl.batch * pl.hkv;
     x.c = u / hb;
@@ -99,90 +97,28 @@ __device__ __forceinline__ Unit unit_at(const pkv_workspace &ws, const Plan &pl,
     x.g = r - x.b * pl.hkv;
   }
   x.L = pl.lens ? pl.lens[x.b] : usable_len(ws, x.b);  // bad lengths flagged by CTA 0
-  x.t0 = x.c * pl.chunk;
-  x.t1 = min(x.t0 + pl.chunk, x.L);
-  x.n = x.L > 0 ? (x.L + pl.chunk - 1) / pl.chunk : 0;
+  const int chunk = pl.chunks ? pl.chunks[x.b] : pl.chunk;
+  x.t0 = x.c * chunk;
+  x.t1 = min(x.t0 + chunk, x.L);
+  if (!pl.pref) x.n = x.L > 0 ? (x.L + chunk - 1) / chunk : 0;
   return x;
 }
 
-// Balanced pieces: cut point at line position x inside a segment of L tokens.
-__device__ __forceinline__ int piece_edge(long long x, int L) {
-  if (x <= 0) return 0;
-  const long long r = (x + kPieceAlign - 1) / kPieceAlign * kPieceAlign;
-  return r < L ? (int)r : L;
-}
-
-// This block's piece of segment (b, g) (empty if the rounded cut points meet).
-// The segment starts at line position o inside block o / W's range, which
-// owns its piece 0; the piece count follows from the last cut point below L.
-__device__ __forceinline__ Unit piece_at(const Plan &pl, int b, int g) {
-  Unit x;
-  x.b = b;
-  x.g = g;
-  x.u = b * pl.hkv + g;
-  x.L = pl.lens[b];
-  const int o = pl.hkv * pl.pref[b] + g * x.L;  // < T
-  const long long lo = (long long)blockIdx.x * pl.W;
-  x.t0 = piece_edge(lo - o, x.L);
-  x.t1 = piece_edge(lo + pl.W - o, x.L);
-  const int first = o / pl.W;
-  x.c = (int)blockIdx.x - first;
-  const int last_cut = (x.L - 1) / kPieceAlign * kPieceAlign;
-  x.n = (o + last_cut) / pl.W - first + 1;  // o + last_cut < T
-  return x;
-}
-
-// The units one block processes, in order (uniform in the block).  Fixed
-// chunks: every gridDim.x-th unit, empty ones included; balanced pieces: the
-// non-empty pieces of the segments meeting the block's range.
+// The units one block processes, in order (uniform in the block): every
+// gridDim.x-th unit, empty ones included.
 struct UnitIter {
   Unit un;
   bool done;
 
-  __device__ __forceinline__ void strided(const pkv_workspace &ws, const Plan &pl, int u) {
+  __device__ __forceinline__ void at(const pkv_workspace &ws, const Plan &pl, int u) {
     done = u >= pl.n_units;
     if (!done) un = unit_at(ws, pl, u);
   }
   __device__ __forceinline__ void first(const pkv_workspace &ws, const Plan &pl) {
-    if (!pl.balanced) {
-      strided(ws, pl, blockIdx.x);
-      return;
-    }
-    const long long lo = (long long)blockIdx.x * pl.W;
-    done = lo >= pl.T;
-    if (done) return;
-    // the request holding position lo: the last b with hkv * pref[b] <= lo
-    // (its length is > 0 because lo < T)
-    int l = 0, h = pl.batch - 1;
-    while (l < h) {
-      const int mid = (l + h + 1) >> 1;
-      if (pl.hkv * pl.pref[mid] <= lo) l = mid;
-      else h = mid - 1;
-    }
-    const int L = pl.lens[l];
-    if (L <= 0) {
-      done = true;
-      return;
-    }
-    un = piece_at(pl, l, ((int)lo - pl.hkv * pl.pref[l]) / L);
-    // only the first segment's piece can be empty (its cut points rounded
-    // past the segment's end: the next block owns that tail)
-    if (un.t0 >= un.t1) next(ws, pl);
+    at(ws, pl, blockIdx.x);
   }
   __device__ __forceinline__ void next(const pkv_workspace &ws, const Plan &pl) {
-    if (!pl.balanced) {
-      strided(ws, pl, un.u + gridDim.x);
-      return;
-    }
-    int b = un.b, g = un.g + 1;
-    if (g == pl.hkv) {
-      g = 0;
-      do ++b;
-      while (b < pl.batch && pl.lens[b] == 0);
-    }
-    done = b >= pl.batch ||
-           pl.hkv * pl.pref[b] + g * pl.lens[b] >= (long long)(blockIdx.x + 1) * pl.W;
-    if (!done) un = piece_at(pl, b, g);
+    at(ws, pl, un.u + gridDim.x);
   }
 };
 
@@ -249,19 +185,50 @@ __device__ __forceinline__ int batch_max_len(const pkv_workspace &ws, int batch,
   return *s_max;
 }
 
+// Apportioned splits: the search for the common split length X (a multiple
+// of kChunkAlign, at least kMinChunk and maxL / S) starts from the even share
+// Hkv * sum L / budget and grows by about 1/16 per step until
+// Hkv * sum ceil(L_b / X) fits the budget (bounded: after kSearchSteps steps,
+// or past the longest request, X is one split per request).  Request b's own chunk then evens its
+// ceil(L_b / X) splits out: ceil(L_b / n_b) rounded up to kChunkAlign.
+constexpr int kSearchSteps = 48;
+
+__device__ __forceinline__ int align_chunk(long long c) {
+  return (int)((c + kChunkAlign - 1) / kChunkAlign * kChunkAlign);
+}
+
+__device__ __forceinline__ int apportion_start(long long sum_len, int max_len, int hkv,
+                                               int budget, int S) {
+  long long x = ((long long)hkv * sum_len + budget - 1) / budget;
+  x = max(x, (long long)(max_len + S - 1) / S);
+  return max(align_chunk(x), kMinChunk);
+}
+
+__device__ __forceinline__ int apportion_step(int x) {
+  return x + max(kChunkAlign, align_chunk(x / 16));
+}
+
+__device__ __forceinline__ int apportioned_chunk(int L, int x) {
+  const int n = (L + x - 1) / x;
+  return align_chunk((L + n - 1) / n);
+}
+
 // Block prologue for compact enumeration (batch <= kMaxCompactBatch): one
 // pass reads every request's usable length into s_len (CTA 0 raises the
 // length error bits) and its index base into s_base (the table row in page
-// mode, the kv_indptr offset in flat mode), then the split length and an
-// exclusive prefix into s_pref follow from shared memory: of the split counts
-// (fixed chunks), or of the lengths themselves (by_len, balanced pieces).
-// Every thread of the block must call it; returns s_pref[batch] and sets
-// *chunk_out (the longest usable length stays in *s_max).
+// mode, the kv_indptr offset in flat mode); the split counts then follow from
+// shared memory and their exclusive prefix goes to s_pref.  budget == 0:
+// fixed chunks (one chunk from the longest length and S); budget > 0:
+// apportioned splits over `budget` blocks, each request's chunk in s_chunk.
+// Every thread of the block must call it; returns the number of non-empty
+// (request, split) pairs and sets *chunk_out (the longest usable length stays
+// in *s_max).
 __device__ __forceinline__ int batch_plan_compact(const pkv_workspace &ws, int batch, int S,
-                                                  bool by_len, int *s_len, int *s_base,
-                                                  int *s_pref, int *s_tmp, int *s_max,
-                                                  int *chunk_out) {
+                                                  int budget, int *s_len, int *s_base,
+                                                  int *s_pref, int *s_chunk, int *s_tmp,
+                                                  int *s_max, int *chunk_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int hkv = ws.n_kv_heads;
   const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
   // request b's usable length (and its index base into s_base[b])
   auto read_req = [&](int b) {
@@ -280,13 +247,35 @@ __device__ __forceinline__ int batch_plan_compact(const pkv_workspace &ws, int b
     s_len[b] = L;
     return L;
   };
+  // splits of request b (length L): fixed chunks, or apportioned with split
+  // length x (recording its chunk)
+  auto splits = [&](int b, int L, int chunk, int x) {
+    if (L <= 0) return 0;
+    if (budget == 0) return (L + chunk - 1) / chunk;
+    const int c = apportioned_chunk(L, x);
+    s_chunk[b] = c;
+    return (L + c - 1) / c;
+  };
   if (batch <= 32) {
-    // one warp: maximum and prefix by shuffles, one block barrier
+    // one warp: sums, maximum and prefix by shuffles, one block barrier
     if (warp == 0) {
       const int L = lane < batch ? read_req(lane) : 0;
       const int mx = __reduce_max_sync(0xffffffffu, L);
       const int chunk = split_chunk(mx, S, ws.page_size);
-      const int cnt = by_len ? L : (L + chunk - 1) / chunk;
+      int x = 0;
+      if (budget > 0 && mx > 0) {
+        const long long sum_len = __reduce_add_sync(0xffffffffu, (unsigned)L);
+        x = apportion_start(sum_len, mx, hkv, budget, S);
+        for (int step = 0; x < mx; ++step, x = apportion_step(x)) {
+          const int n = L > 0 ? (L + x - 1) / x : 0;
+          if ((long long)hkv * __reduce_add_sync(0xffffffffu, (unsigned)n) <= budget) break;
+          if (step == kSearchSteps) {
+            x = align_chunk(mx);
+            break;
+          }
+        }
+      }
+      const int cnt = splits(lane, L, chunk, x);
       int incl = cnt;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -304,21 +293,53 @@ __device__ __forceinline__ int batch_plan_compact(const pkv_workspace &ws, int b
     *chunk_out = s_tmp[0];
     return s_pref[batch];
   }
-  if (tid == 0) *s_max = 0;
+  if (tid == 0) {
+    *s_max = 0;
+    s_tmp[0] = 0;  // sum of the lengths
+  }
   __syncthreads();
-  int mx = 0;
-  for (int b = tid; b < batch; b += blockDim.x) mx = max(mx, read_req(b));
+  int mx = 0, sum = 0;
+  for (int b = tid; b < batch; b += blockDim.x) {
+    const int L = read_req(b);
+    mx = max(mx, L);
+    sum += L;
+  }
   mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) atomicMax(s_max, mx);
+  sum = (int)__reduce_add_sync(0xffffffffu, (unsigned)sum);
+  if (lane == 0) {
+    atomicMax(s_max, mx);
+    atomicAdd(&s_tmp[0], sum);
+  }
   __syncthreads();
   const int chunk = split_chunk(*s_max, S, ws.page_size);
   *chunk_out = chunk;
+  int x = 0;
+  const int mxl = *s_max;
+  if (budget > 0 && mxl > 0) {
+    x = apportion_start(s_tmp[0], mxl, hkv, budget, S);
+    __syncthreads();  // everyone has read s_tmp[0]
+    for (int step = 0; x < mxl; ++step, x = apportion_step(x)) {
+      int n = 0;
+      for (int b = tid; b < batch; b += blockDim.x) n += (s_len[b] + x - 1) / x;
+      n = (int)__reduce_add_sync(0xffffffffu, (unsigned)n);
+      if (tid == 0) s_tmp[2 + (step & 1)] = 0;  // this step's counter (the other one was last read a barrier ago)
+      __syncthreads();
+      if (lane == 0) atomicAdd(&s_tmp[2 + (step & 1)], n);
+      __syncthreads();
+      const bool fits = (long long)hkv * s_tmp[2 + (step & 1)] <= budget;
+      if (fits) break;
+      if (step == kSearchSteps) {
+        x = align_chunk(mxl);
+        break;
+      }
+    }
+    __syncthreads();  // s_tmp is reused by the scan below
+  }
   const int nt = blockDim.x;
   const int per = (batch + nt - 1) / nt;
   const int lo = min(batch, tid * per), hi = min(batch, lo + per);
-  auto count = [&](int b) { return by_len ? s_len[b] : (s_len[b] + chunk - 1) / chunk; };
   int local = 0;
-  for (int b = lo; b < hi; ++b) local += count(b);
+  for (int b = lo; b < hi; ++b) local += splits(b, s_len[b], chunk, x);
   int incl = local;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -340,7 +361,9 @@ __device__ __forceinline__ int batch_plan_compact(const pkv_workspace &ws, int b
   int run = (warp > 0 ? s_tmp[warp - 1] : 0) + incl - local;
   for (int b = lo; b < hi; ++b) {
     s_pref[b] = run;
-    run += count(b);
+    run += (s_len[b] <= 0) ? 0
+           : (budget == 0 ? (s_len[b] + chunk - 1) / chunk
+                          : (s_len[b] + s_chunk[b] - 1) / s_chunk[b]);
   }
   if (tid == nt - 1) s_pref[batch] = run;
   __syncthreads();

@@ -23,7 +23,7 @@ struct DecodeArgs {
   const void *k_new;  // fused append source (bf16 [batch, Hkv, D]) or NULL
   const void *v_new;
   int fused_merge;    // 1: the last split of each (request, KV head) merges
-  int balanced;       // tensor-core kernel: balanced pieces (set by its launcher)
+  int apportion;      // tensor-core kernel: apportioned splits (set by its launcher)
 };
 
 // CUDA-core split-KV decode.  Returns cudaErrorNotSupported for shapes

@@ -148,7 +148,7 @@ int pkv_choose_pieces(const pkv_workspace *ws, int batch, int max_seq_len_hint,
   const long long total = total_tokens_hint > 0 ? total_tokens_hint : (long long)batch * L;
   const long long blocks = 2ll * num_sms;  // resident blocks of the tensor-core kernel
   long long share = (ws->n_kv_heads * total + blocks - 1) / blocks;
-  if (share < 128) share = 128;  // two tiles: shorter pieces cost more in merging
+  if (share < 128) share = 128;  // two tiles: shorter splits cost more in merging
   const long long S = 3 + (L - 1) / share;
   return (int)(S < ws->max_splits ? S : ws->max_splits);
 }

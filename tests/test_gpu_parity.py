@@ -23,7 +23,7 @@ FIXED = A.PKV_FLAG_FIXED_CHUNK
 # (flags, fused): the CUDA-core kernel; the tensor-core kernel with TMA boxes
 # (page sizes that are multiples of 16) or cp.async gathers; the fused layer
 # kernel (append + attention + merge in one launch) with either producer and
-# balanced pieces, and with the fixed chunks of the unfused call.
+# apportioned splits, and with the fixed chunks of the unfused call.
 PATHS = {"simt": (SIMT, False), "mma": (MMA, False), "gather": (MMA | GATHER, False),
          "fused": (0, True), "fused_gather": (GATHER, True), "fused_fixed": (FIXED, True)}
 KERNELS = pytest.mark.parametrize("kern", list(PATHS), ids=list(PATHS))
@@ -228,7 +228,7 @@ def _bench_splits(p, chooser=A.pkv_choose_splits):
 def test_full_size_sampled(cuda, name, batch):
     p = W.workload(name, batch=batch, steps=1)
     layers = sorted({0, p.n_layers - 1})
-    # the fused layer kernel the benchmark times (balanced pieces, S from
+    # the fused layer kernel the benchmark times (apportioned splits, S from
     # pkv_choose_pieces), then the unfused tensor-core path
     for flags, fused, chooser in ((0, True, A.pkv_choose_pieces),
                                   (MMA, False, A.pkv_choose_splits)):
