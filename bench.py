@@ -236,16 +236,18 @@ def run_reference(args, rank):
 
 # --------------------------------------------------------------- GPU arm --
 
-def traffic_for(kernel_src_hash, workload):
+def traffic_for(kernel_src_hash, workload, algorithmic_bytes):
     """DRAM traffic per attention launch from a committed ncu summary, if it
-    was taken on the current kernel source; else None."""
+    was taken on the current kernel source; else None.  The capture may be of
+    a smaller case of the same workload (fewer layers): its traffic is scaled
+    by the algorithmic bytes of the two launches."""
     path = os.path.join(ROOT, "profiles", "decode_attn_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(workload)
         if e and e.get("kernel_src_sha1") == kernel_src_hash:
-            return e.get("dram_bytes_per_launch")
+            return e["dram_bytes_per_launch"] * algorithmic_bytes / e["algorithmic_bytes_per_launch"]
     except Exception:
         pass
     return None
@@ -425,7 +427,9 @@ def run_ours(args, rank, world, local_rank):
                     (" + merge_kernel" if S > 1 else ""))
     ach = mean_layer_bytes / layer_s / 1e9
     roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "traffic": traffic_for(kernel_src_hash(), args.workload), "peak_source": peak_src,
+            "traffic": (traffic_for(kernel_src_hash(), args.workload, mean_layer_bytes)
+                        if run.fused and not args.flags and not args.splits else None),
+            "peak_source": peak_src,
             "kernel": layer_kernel, "kernel_us_mean": layer_s * 1e6,
             "kernel_time_from": "(step - bind) / layers, both timed with CUDA events over "
                                 "their own timed regions of graph replays",
