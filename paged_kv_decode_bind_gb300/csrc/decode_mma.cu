@@ -250,7 +250,9 @@ __global__ void __launch_bounds__(kMThreads, 2)
   }
   if (!early) pdl_wait();
 
-  if (tid == 0) {
+  // The producer's lane 0 sets up the barriers while warp 0 plans; the plan's
+  // block barrier publishes them before any use.
+  if (tid == kCW * 32) {
     for (int s = 0; s < kMStages; ++s) {
       // TMA: one expect-tx arrival; cp.async: 32 copy-completion arrivals
       // plus one release arrival by the lane that wrote the stage flag.
@@ -260,8 +262,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
     *s_abort = 0;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  if (tid == 0) fence_barrier_init();
-  __syncthreads();
+  if (tid == kCW * 32) fence_barrier_init();
 
   Plan pl;
   pl.set_pages(ws);
@@ -311,20 +312,23 @@ __global__ void __launch_bounds__(kMThreads, 2)
       s_idx[tile][r] = v;
     }
   }
+  // The producer's cursors, while the block's index loads are in flight:
+  // pc walks the tiles to issue; pf runs kLA tiles ahead and fetches later
+  // index entries with 4-byte cp.async copies into the ring (one commit group
+  // per tile, issued at iteration k for tile k + kLA), so no register ever
+  // waits on an index load: at iteration k, tile k's entries are complete once
+  // at most kLA - 1 newer groups pend (tiles 0 .. kLA - 1 came in with the
+  // block's fetch above).
+  Cursor<kMT> pc, pf;
+  if (warp == kCW) {
+    pc.start(ws, pl);
+    pf = pc;
+    pf.advance_by(ws, pl, kLA);
+  }
   __syncthreads();
 
   if (warp == kCW) {
     // ------------------------------------------------------- producer ----
-    Cursor<kMT> pc;
-    pc.start(ws, pl);
-    // Later index entries are fetched by a second cursor running kLA tiles
-    // ahead of pc, with 4-byte cp.async copies into the ring (one commit group
-    // per tile, issued at iteration k for tile k + kLA), so no register ever
-    // waits on an index load: at iteration k, tile k's entries are complete
-    // once at most kLA - 1 newer groups pend (and tiles 0 .. kLA - 1 came in
-    // with the block's fetch above).
-    Cursor<kMT> pf = pc;
-    pf.advance_by(ws, pl, kLA);
     int pf_u = -1;
     ReqIndex pf_ri{0, false};
     auto prefetch = [&](int slot) {  // entries of the tile under pf into s_idx[slot]
@@ -375,7 +379,6 @@ __global__ void __launch_bounds__(kMThreads, 2)
         waited = true;
       }
       append_if_newest<D>(a, un, tile0, lane);
-      pc.advance(ws, pl);
       asm volatile("cp.async.wait_group %0;" ::"n"(kLA - 1) : "memory");
       const int slot = k % kLA;
       const int cur[2] = {s_idx[slot][lane], s_idx[slot][lane + 32]};
@@ -389,6 +392,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
         produce_cpasync<D, G>(a, pl, un, tile0, cur, s, kv_base, &full[s], &flags[s], lane);
         if (lane == 0) mbar_arrive(&full[s]);
       }
+      pc.advance(ws, pl);
       prefetch(slot);  // tile k + kLA reuses the slot just read
       ++k;
     }
@@ -674,52 +678,68 @@ __global__ void __launch_bounds__(kMThreads, 2)
           }
         }
     };
+    // (w0 + w2) and (w1 + w3) land in the two buffers; every consumer thread
+    // then writes four consecutive elements of their sum (coalesced).
     if (warp >= 2) store(warp - 2);
     named_sync(1, kCW * 32);
-    if (warp < 2) add(warp);
-    named_sync(1, kCW * 32);
-    if (warp == 1) store(0);
+    if (warp < 2) {
+      add(warp);
+      store(warp);
+    }
     named_sync(1, kCW * 32);
 
     // ---- write: final row, or a partial (and maybe merge them all) ----
     const bool final_out = direct || (fused && n_b == 1);
-    if (warp == 0) {
-      add(0);
+    // (M, L) of query head h of the group from the warps' states
+    auto head_ml = [&](int h, float &M, float &L) {
+      M = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < C::NH; ++n)
+      for (int w = 0; w < kCW; ++w) M = fmaxf(M, s_ml[(w * 16 + h) * 2]);
+      L = 0.f;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int h = 8 * n + 2 * tig + e;
-          if (h >= G) continue;
-          const float M = Mh[n][e], L = Lh[n][e];
-          const bool empty_out = unit_bad || !(L > 0.f);
-          const float inv = empty_out ? 0.f : 1.f / L;
-          const long long qrow = (long long)un.b * Hq + hq0 + h;
+      for (int w = 0; w < kCW; ++w) {
+        const float mw = s_ml[(w * 16 + h) * 2];
+        L += mw == -INFINITY ? 0.f : exp2f(mw - M) * s_ml[(w * 16 + h) * 2 + 1];
+      }
+    };
 #pragma unroll
-          for (int mt = 0; mt < C::MT; ++mt) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int d = 16 * mt + grp + 8 * hh;
-              const float x = empty_out ? 0.f : acc[n][mt][2 * hh + e] * inv;
-              if (final_out) {
-                if (a.flags & PKV_FLAG_OUT_F32) static_cast<float *>(ws.out)[qrow * D + d] = x;
-                else static_cast<uint16_t *>(ws.out)[qrow * D + d] = (uint16_t)f32_to_bf16_bits(x);
-              } else {
-                ws.o_part[(qrow * pl.S + un.c) * D + d] = x;
-              }
-            }
-          }
-          if (grp == 0) {
-            if (final_out) {
-              if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse)
-                ws.lse[qrow] = empty_out ? -INFINITY : M * kLn2 + logf(L);
-            } else {
-              const long long o = (qrow * pl.S + un.c) * 2;
-              ws.ml_part[o] = empty_out ? -INFINITY : M * kLn2;
-              ws.ml_part[o + 1] = empty_out ? 0.f : L;
-            }
-          }
+    for (int i = tid * 4; i < G * D; i += kCW * 32 * 4) {
+      const int h = i / D, d = i - h * D;
+      float M, L;
+      head_ml(h, M, L);
+      const bool empty_out = unit_bad || !(L > 0.f);
+      const float inv = empty_out ? 0.f : 1.f / L;
+      const float4 x0 = *reinterpret_cast<const float4 *>(red + h * C::RSTRIDE + d);
+      const float4 x1 = *reinterpret_cast<const float4 *>(red + (G + h) * C::RSTRIDE + d);
+      const float4 x = make_float4((x0.x + x1.x) * inv, (x0.y + x1.y) * inv,
+                                   (x0.z + x1.z) * inv, (x0.w + x1.w) * inv);
+      const long long qrow = (long long)un.b * Hq + hq0 + h;
+      if (final_out) {
+        if (a.flags & PKV_FLAG_OUT_F32) {
+          *reinterpret_cast<float4 *>(static_cast<float *>(ws.out) + qrow * D + d) = x;
+        } else {
+          uint2 pk;
+          pk.x = f32_to_bf16_bits(x.x) | (f32_to_bf16_bits(x.y) << 16);
+          pk.y = f32_to_bf16_bits(x.z) | (f32_to_bf16_bits(x.w) << 16);
+          *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(ws.out) + qrow * D + d) = pk;
         }
+      } else {
+        *reinterpret_cast<float4 *>(ws.o_part + (qrow * pl.S + un.c) * D + d) = x;
+      }
+    }
+    if (tid < G) {
+      float M, L;
+      head_ml(tid, M, L);
+      const bool empty_out = unit_bad || !(L > 0.f);
+      const long long qrow = (long long)un.b * Hq + hq0 + tid;
+      if (final_out) {
+        if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse)
+          ws.lse[qrow] = empty_out ? -INFINITY : M * kLn2 + logf(L);
+      } else {
+        const long long o = (qrow * pl.S + un.c) * 2;
+        ws.ml_part[o] = empty_out ? -INFINITY : M * kLn2;
+        ws.ml_part[o + 1] = empty_out ? 0.f : L;
+      }
     }
     if (fused && !final_out) {
       named_sync(1, kCW * 32);
