@@ -67,7 +67,7 @@ template <int D, int G>
 struct MCfg {
   static constexpr int HALVES = D / 64;     // 64-column (128-byte) swizzled halves
   static constexpr int PIECE = 16 * HALVES * 128;  // bytes of a 16-token page piece
-  static constexpr int TILE = (kMT / 16) * PIECE;
+  static constexpr int TILE = (kMT / 16) * PIECE;    // bytes of K (or V) of a tile
   static constexpr int KSTEPS = D / 16;
   static constexpr int NH = (G + 7) / 8;    // 8-wide head tiles
   static constexpr int MT = D / 16;         // 16-row output (head_dim) tiles
@@ -86,13 +86,14 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-// A K or V tile in shared memory: 16-token pieces of HALVES x 16 rows of 128
-// bytes ([piece][half][token % 16][64 columns], the box order of the pool
-// tensor map), so token t, half h is row (t / 16) * 16 * HALVES + 16 h + t % 16
-// and rows of consecutive tokens stay consecutive (conflict-free ldmatrix).
+// A ring stage in shared memory holds, per 16-token page piece, the piece's K
+// then its V (the box order of the pool tensor map): each is HALVES x 16 rows
+// of 128 bytes, [half][token % 16][64 columns].  Offset of chunk c of token t,
+// half h inside the stage's K (or, from the V base, V) data: rows of
+// consecutive tokens stay consecutive (conflict-free ldmatrix).
 template <int HALVES>
 __device__ __forceinline__ uint32_t kv_off(int t, int h, int c) {
-  return swz((t >> 4) * (16 * HALVES) + h * 16 + (t & 15), c);
+  return (uint32_t)((t >> 4) * (2 * 16 * 128 * HALVES)) + swz(h * 16 + (t & 15), c);
 }
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
@@ -143,33 +144,36 @@ __device__ __forceinline__ void append_if_newest(const DecodeArgs &a, const Unit
 }
 
 // Producer, page mode: one tensor-map box per 16-token page piece and pool
-// (both halves of the row).  Lane j < 4 resolves piece j (`raw` is its page
-// id, fetched ahead); lanes 0-3 then load the K pieces, lanes 4-7 the V ones.
+// (both halves of the rows).  Lanes j and j + 4 (j < 4) both resolve piece j
+// from its page id `raw` (fetched ahead) and load its K and its V; lane j
+// records the piece's error bit.  A bad page id loads an in-range dummy piece
+// instead (its unit is written empty), so the byte count follows from the
+// tile's length alone and no warp vote is needed.
 template <int D, int G>
 __device__ __forceinline__ void produce_tma(const DecodeArgs &a, const Plan &pl, const Unit &un,
                                             int tile0, int raw, int stage, uint32_t kv_base,
-                                            uint64_t *full, int *flag, const CUtensorMap *tmk,
+                                            uint64_t *full, int *flag4, const CUtensorMap *tmk,
                                             const CUtensorMap *tmv, int lane) {
   using C = MCfg<D, G>;
   const pkv_workspace &ws = a.ws;
-  const int tok0 = tile0 + 16 * lane;
-  const bool want = lane < 4 && tok0 < un.t1;
-  int kind = 0;
-  long long slot0 = -1;
-  if (want) slot0 = slot_from_raw(ws, pl, raw, tok0, kind);  // tok0 % 16 == 0: inside one page
-  const unsigned ok = __ballot_sync(0xffffffffu, slot0 >= 0);
-  const int bad = __reduce_or_sync(0xffffffffu, kind);
-  const int row = __shfl_sync(0xffffffffu, a.layer * ws.pool_slots + (int)slot0, lane & 3);
-  if (lane == 0) {
-    *flag = bad;
-    if (bad) atomicOr(ws.err, bad);
-    mbar_arrive_expect_tx(full, __popc(ok) * (uint32_t)(2 * C::PIECE));
+  if (lane < 8) {
+    const int j = lane & 3;
+    const int tok0 = tile0 + 16 * j;
+    int kind = 0;
+    if (tok0 < un.t1) {
+      long long slot0 = slot_from_raw(ws, pl, raw, tok0, kind);  // tok0 % 16 == 0: one page
+      if (kind) {
+        if (lane < 4) atomicOr(ws.err, kind);
+        slot0 = 0;
+      }
+      tma_load_4d(kv_base + stage * 2 * C::TILE + j * 2 * C::PIECE + (lane >> 2) * C::PIECE,
+                  lane < 4 ? tmk : tmv, 0, a.layer * ws.pool_slots + (int)slot0, 0, un.g, full);
+    }
+    if (lane < 4) flag4[lane] = kind;
   }
-  __syncwarp();
-  if (lane < 8 && ((ok >> (lane & 3)) & 1)) {
-    const uint32_t dst = kv_base + (2 * stage + (lane >> 2)) * C::TILE + (lane & 3) * C::PIECE;
-    tma_load_4d(dst, lane < 4 ? tmk : tmv, 0, row, 0, un.g, full);
-  }
+  __syncwarp();  // the lanes' flags before the arrival that publishes the stage
+  if (lane == 0)
+    mbar_arrive_expect_tx(full, min(4, (un.t1 - tile0 + 15) / 16) * (uint32_t)(2 * C::PIECE));
 }
 
 // Producer, any page size / flat mode: cp.async 16-byte gathers.  Lane owns
@@ -178,7 +182,7 @@ template <int D, int G>
 __device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Plan &pl,
                                                 const Unit &un, int tile0,
                                                 const int (&raw)[2], int stage, uint32_t kv_base,
-                                                uint64_t *full, int *flag, int lane) {
+                                                uint64_t *full, int *flag4, int lane) {
   using C = MCfg<D, G>;
   const pkv_workspace &ws = a.ws;
   int kind = 0;
@@ -189,13 +193,11 @@ __device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Plan 
     slot[h] = tok < un.t1 ? slot_from_raw(ws, pl, raw[h], tok, kind) : -1;
   }
   const int bad = __reduce_or_sync(0xffffffffu, kind);
-  if (lane == 0) {
-    *flag = bad;
-    if (bad) atomicOr(ws.err, bad);
-  }
+  if (lane < 4) flag4[lane] = lane == 0 ? bad : 0;
+  if (lane == 0 && bad) atomicOr(ws.err, bad);
   __syncwarp();
-  const uint32_t kt = kv_base + (2 * stage) * C::TILE;
-  const uint32_t vt = kt + C::TILE;
+  const uint32_t kt = kv_base + stage * 2 * C::TILE;  // K then V per 16-token piece
+  const uint32_t vt = kt + C::PIECE;
   const uint16_t *kp = static_cast<const uint16_t *>(ws.k_pool);
   const uint16_t *vp = static_cast<const uint16_t *>(ws.v_pool);
 #pragma unroll
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
   using C = MCfg<D, G>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kMStages], empty[kMStages];
-  __shared__ int flags[kMStages];
+  __shared__ int flags[kMStages][4];  // per stage: error bits of the tile's four pieces
   __shared__ volatile int s_ctrl[2];  // abort flag, merge ticket
   __shared__ float s_ml[kCW * 16 * 2];
   __shared__ int s_bad[kCW];
@@ -381,15 +383,16 @@ __global__ void __launch_bounds__(kMThreads, 2)
       append_if_newest<D>(a, un, tile0, lane);
       asm volatile("cp.async.wait_group %0;" ::"n"(kLA - 1) : "memory");
       const int slot = k % kLA;
-      const int cur[2] = {s_idx[slot][lane], s_idx[slot][lane + 32]};
+      // TMA: lanes j and j + 4 both need piece j's page id
+      const int cur[2] = {s_idx[slot][use_tma ? (lane & 3) : lane], s_idx[slot][lane + 32]};
       __syncwarp();
       if (use_tma) {
-        produce_tma<D, G>(a, pl, un, tile0, cur[0], s, kv_base, &full[s], &flags[s], &tmk, &tmv,
+        produce_tma<D, G>(a, pl, un, tile0, cur[0], s, kv_base, &full[s], flags[s], &tmk, &tmv,
                           lane);
       } else {
         // Issued before the next index copies: the stage's copy-completion
         // arrival covers every earlier cp.async of the lane.
-        produce_cpasync<D, G>(a, pl, un, tile0, cur, s, kv_base, &full[s], &flags[s], lane);
+        produce_cpasync<D, G>(a, pl, un, tile0, cur, s, kv_base, &full[s], flags[s], lane);
         if (lane == 0) mbar_arrive(&full[s]);
       }
       pc.advance(ws, pl);
@@ -510,10 +513,10 @@ __global__ void __launch_bounds__(kMThreads, 2)
       if (!ok) {
         bad = 1;
       } else {
-        bad |= flags[s];
+        bad |= flags[s][0] | flags[s][1] | flags[s][2] | flags[s][3];
         if (nv > 0) {
-          const uint32_t kt = kv_base + (2 * s) * C::TILE;
-          const uint32_t vt = kt + C::TILE;
+          const uint32_t kt = kv_base + s * 2 * C::TILE;  // K then V per 16-token piece
+          const uint32_t vt = kt + C::PIECE;
           // ---- S^T = K Q^T: rows = tokens grp / grp + 8, cols = heads ----
           // two independent accumulation chains (even / odd k-steps)
           float sc[C::NH][4], sc2[C::NH][4];
@@ -711,8 +714,11 @@ __global__ void __launch_bounds__(kMThreads, 2)
       const float inv = empty_out ? 0.f : 1.f / L;
       const float4 x0 = *reinterpret_cast<const float4 *>(red + h * C::RSTRIDE + d);
       const float4 x1 = *reinterpret_cast<const float4 *>(red + (G + h) * C::RSTRIDE + d);
-      const float4 x = make_float4((x0.x + x1.x) * inv, (x0.y + x1.y) * inv,
-                                   (x0.z + x1.z) * inv, (x0.w + x1.w) * inv);
+      // an empty or failed unit is written as zeros whatever its tiles held
+      // (a bad page's dummy piece may hold NaN bit patterns)
+      const float4 x = empty_out ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                 : make_float4((x0.x + x1.x) * inv, (x0.y + x1.y) * inv,
+                                               (x0.z + x1.z) * inv, (x0.w + x1.w) * inv);
       const long long qrow = (long long)un.b * Hq + hq0 + h;
       if (final_out) {
         if (a.flags & PKV_FLAG_OUT_F32) {
@@ -789,7 +795,9 @@ TmapEncodeFn tmap_encoder() {
 // half, KV head), strides 2 B, Hkv * D * 2, 128, D * 2: a box of 64 x 16 x
 // halves x 1 lands in shared memory as [half][slot][64 columns], one page
 // piece of one head with both halves of its rows.  Every element a box can
-// address lies inside the pool.
+// address lies inside the pool.  (One map over both pools, with their distance
+// as a fifth stride, halves the copies per tile but ran the 65536-token single
+// request ~1.5x slower.)
 bool encode_pool_map(CUtensorMap *m, void *base, const pkv_workspace &ws) {
   TmapEncodeFn enc = tmap_encoder();
   if (!enc) return false;
