@@ -176,21 +176,27 @@ __device__ __forceinline__ void produce_tma(const DecodeArgs &a, const Plan &pl,
     mbar_arrive_expect_tx(full, min(4, (un.t1 - tile0 + 15) / 16) * (uint32_t)(2 * C::PIECE));
 }
 
-// Producer, any page size / flat mode: cp.async 16-byte gathers.  Lane owns
-// rows lane and lane + 32 of the tile; rows past the end are zero-filled.
+// Producer, any page size / flat mode: cp.async 16-byte gathers.  Lane
+// validates rows lane and lane + 32 of the tile and writes their pool slots
+// (-1: none) back over the ring slot's raw entries; the copies then go two or
+// four rows per warp instruction, D / 8 consecutive lanes per row (whole
+// 128-byte lines), each row's slot read back from shared memory.  Rows past
+// the end are zero-filled.
 template <int D, int G>
 __device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Plan &pl,
                                                 const Unit &un, int tile0,
-                                                const int (&raw)[2], int stage, uint32_t kv_base,
-                                                uint64_t *full, int *flag4, int lane) {
+                                                const int (&raw)[2], int *ring, int stage,
+                                                uint32_t kv_base, uint64_t *full, int *flag4,
+                                                int lane) {
   using C = MCfg<D, G>;
+  constexpr int CH = D / 8;     // 16-byte chunks per row
+  constexpr int RPI = 32 / CH;  // rows per warp instruction
   const pkv_workspace &ws = a.ws;
   int kind = 0;
-  long long slot[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int tok = tile0 + lane + 32 * h;
-    slot[h] = tok < un.t1 ? slot_from_raw(ws, pl, raw[h], tok, kind) : -1;
+    ring[lane + 32 * h] = tok < un.t1 ? (int)slot_from_raw(ws, pl, raw[h], tok, kind) : -1;
   }
   const int bad = __reduce_or_sync(0xffffffffu, kind);
   if (lane < 4) flag4[lane] = lane == 0 ? bad : 0;
@@ -198,25 +204,23 @@ __device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Plan 
   __syncwarp();
   const uint32_t kt = kv_base + stage * 2 * C::TILE;  // K then V per 16-token piece
   const uint32_t vt = kt + C::PIECE;
-  const uint16_t *kp = static_cast<const uint16_t *>(ws.k_pool);
-  const uint16_t *vp = static_cast<const uint16_t *>(ws.v_pool);
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = lane + 32 * h;
-    const bool ok = slot[h] >= 0;
-    const long long e =
-        ok ? (((long long)a.layer * ws.pool_slots + slot[h]) * ws.n_kv_heads + un.g) * D : 0;
-#pragma unroll
-    for (int c8 = 0; c8 < D / 8; ++c8) {
-      const uint32_t off = kv_off<C::HALVES>(r, c8 >> 3, c8 & 7);
-      cp_async_16(kt + off, kp + e + c8 * 8, ok ? 16 : 0);
-      cp_async_16(vt + off, vp + e + c8 * 8, ok ? 16 : 0);
-    }
+  const int sub = lane / CH, ch = lane % CH;
+  const long long head0 = ((long long)a.layer * ws.pool_slots * ws.n_kv_heads + un.g) * D + ch * 8;
+  const uint16_t *kb = static_cast<const uint16_t *>(ws.k_pool) + head0;
+  const uint16_t *vb = static_cast<const uint16_t *>(ws.v_pool) + head0;
+  const long long slot_elems = (long long)ws.n_kv_heads * D;
+#pragma unroll 8
+  for (int i = 0; i < kMT / RPI; ++i) {
+    const int r = i * RPI + sub;
+    const int sl = ring[r];
+    const long long e = sl >= 0 ? sl * slot_elems : 0;
+    const uint32_t off = kv_off<C::HALVES>(r, ch >> 3, ch & 7);
+    cp_async_16(kt + off, kb + e, sl >= 0 ? 16 : 0);
+    cp_async_16(vt + off, vb + e, sl >= 0 ? 16 : 0);
   }
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(full))
                : "memory");
 }
-
 
 template <int D, int G>
 __global__ void __launch_bounds__(kMThreads, 2)
@@ -392,7 +396,8 @@ __global__ void __launch_bounds__(kMThreads, 2)
       } else {
         // Issued before the next index copies: the stage's copy-completion
         // arrival covers every earlier cp.async of the lane.
-        produce_cpasync<D, G>(a, pl, un, tile0, cur, s, kv_base, &full[s], flags[s], lane);
+        produce_cpasync<D, G>(a, pl, un, tile0, cur, s_idx[slot], s, kv_base, &full[s], flags[s],
+                              lane);
         if (lane == 0) mbar_arrive(&full[s]);
       }
       pc.advance(ws, pl);
