@@ -319,8 +319,10 @@ def run_ours(args, rank, world, local_rank):
     bind_graph = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
+    # the metadata bind alone: the step's split plan (pkv_plan_step, part of
+    # run.bind) stays in the layers' share of the step time
     with torch.cuda.stream(side), torch.cuda.graph(bind_graph, stream=side):
-        run.bind(A.PKV_BIND_STEADY)
+        A.pkv_bind_step(ws, B, A.PKV_BIND_STEADY, 0, 0, None, None, side)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
 
@@ -450,7 +452,8 @@ def run_ours(args, rank, world, local_rank):
                         if run.fused and not args.flags and not args.splits else None),
             "peak_source": peak_src,
             "kernel": layer_kernel, "kernel_us_mean": layer_s * 1e6,
-            "kernel_time_from": "(step - bind) / layers, both timed with CUDA events over "
+            "kernel_time_from": "(step - metadata bind) / layers (the step's split plan counts "
+                                "in the layers), both timed with CUDA events over "
                                 "their own timed regions of graph replays",
             "kernel_launches_timed": K * NL, "algorithmic_bytes_per_launch": mean_layer_bytes}
     if attn_ms:

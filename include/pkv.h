@@ -74,15 +74,20 @@ enum {
   PKV_FLAG_FORCE_GATHER = 16, /* tensor-core kernel: load K/V with cp.async gathers even where
                                  tensor-map TMA boxes apply (P % 16 == 0)                   */
   PKV_FLAG_PLAN_EARLY = 32,  /* tensor-core kernel: the caller guarantees that seq_lens,
-                                kv_indptr, kv_indices, req_pool_indices, page_table and
-                                out_loc were last written at least two launches earlier
+                                kv_indptr, kv_indices, req_pool_indices, page_table,
+                                out_loc and work_plan were last written at least two
+                                launches earlier
                                 on this stream (or by the host), so the kernel may read
                                 them and start loading K/V before the previous kernel
                                 finishes (programmatic dependent launch); q, k_new and
                                 all outputs are still touched only after it finishes  */
-  PKV_FLAG_FIXED_CHUNK = 64  /* pkv_decode_layer, tensor-core kernel: cut the KV axis into
-                                pkv_decode_attn's fixed chunks instead of apportioned
-                                splits */
+  PKV_FLAG_FIXED_CHUNK = 64,  /* pkv_decode_layer, tensor-core kernel: cut the KV axis
+                                 into pkv_decode_attn's fixed chunks instead of
+                                 apportioned splits */
+  PKV_FLAG_USE_PLAN = 128     /* pkv_decode_layer: take the split plan and the first page
+                                 ids from ws->work_plan (pkv_plan_step) when it was made
+                                 for this batch size, split count and flags; else plan
+                                 as without the flag */
 };
 
 /* bits OR-ed into *err by device code (sticky; the caller clears the word) */
@@ -132,6 +137,10 @@ typedef struct pkv_workspace {
   int32_t *split_counters;   /* [max_batch * Hkv] zero-initialised once by the caller;
                                 used and left at zero by pkv_decode_layer when S > 1;
                                 may be NULL if that entry point is not used         */
+  int32_t *work_plan;        /* pkv_workspace_bytes(ws, "work_plan") bytes: the step's
+                                split plan written by pkv_plan_step and read by
+                                pkv_decode_layer with PKV_FLAG_USE_PLAN; may be
+                                NULL if those are not used                          */
 } pkv_workspace;
 
 /*
@@ -261,6 +270,23 @@ pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits
 pkv_status pkv_decode_layer(const pkv_workspace *ws, int batch, int layer, const void *q,
                             const void *k_new, const void *v_new, float scale, int num_splits,
                             int flags, pkv_stream_t stream);
+
+/*
+ * The split plan of a step, once for all its layers: what every
+ * pkv_decode_layer launch with this batch, num_splits and flags would derive
+ * from seq_lens, req_pool_indices / kv_indptr and the page table (usable
+ * lengths, index bases, the split length of every request) plus the page ids
+ * of each block's first tiles, written to ws->work_plan.  Call it after the
+ * step's metadata bind (pkv_bind_step) and before its layers; a layer called
+ * with PKV_FLAG_USE_PLAN then reads the plan in one round trip instead of
+ * deriving it.  The plan is valid until seq_lens, the request rows, kv_indptr /
+ * kv_indices or the page table change (the next bind).  A plan made for other
+ * arguments is recognised and ignored.  Nothing is launched (PKV_OK) for
+ * batch 0, batch > 256 or shapes without the tensor-core kernel.
+ * Device errors: PKV_DEVERR_LEN, PKV_DEVERR_TOTAL.
+ */
+pkv_status pkv_plan_step(const pkv_workspace *ws, int batch, int num_splits, int flags,
+                         pkv_stream_t stream);
 
 /* Size of the device array behind pkv_decode_attn_static_scratch (8 MiB). */
 #define PKV_STATIC_SCRATCH_BYTES (8u << 20)

@@ -17,13 +17,15 @@ PKV_BIND_STEADY, PKV_BIND_REBUILD, PKV_BIND_APPEND_ONLY = 0, 1, 2
 PKV_IDX_PAGE_TABLE, PKV_IDX_FLAT = 0, 1
 PKV_FLAG_OUT_F32, PKV_FLAG_WRITE_LSE, PKV_FLAG_FORCE_SIMT, PKV_FLAG_FORCE_MMA = 1, 2, 4, 8
 PKV_FLAG_FORCE_GATHER, PKV_FLAG_PLAN_EARLY, PKV_FLAG_FIXED_CHUNK = 16, 32, 64
+PKV_FLAG_USE_PLAN = 128
 PKV_DEVERR_PAGE, PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT, PKV_DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16
 
 # Every symbol include/pkv.h declares (checked by the ABI test).
 EXPORTS = ("pkv_workspace_bytes", "pkv_bind_step", "pkv_choose_splits", "pkv_choose_pieces",
            "pkv_decode_attn",
-           "pkv_merge_partials", "pkv_decode_layer", "pkv_decode_attn_static_scratch",
+           "pkv_merge_partials", "pkv_decode_layer", "pkv_plan_step",
+           "pkv_decode_attn_static_scratch",
            "pkv_is_steady_increment",
            "pkv_status_string", "pkv_version")
 PKV_STATIC_SCRATCH_BYTES = 8 << 20
@@ -46,7 +48,7 @@ class PkvWorkspace(ctypes.Structure):
         ("kv_indices", ctypes.c_void_p), ("o_part", ctypes.c_void_p),
         ("ml_part", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("lse", ctypes.c_void_p), ("err", ctypes.c_void_p),
-        ("split_counters", ctypes.c_void_p),
+        ("split_counters", ctypes.c_void_p), ("work_plan", ctypes.c_void_p),
     ]
 
 
@@ -83,6 +85,8 @@ def load(path: str = LIB_PATH):
     lib.pkv_merge_partials.restype = i32
     lib.pkv_decode_layer.argtypes = [W, i32, i32, vp, vp, vp, f32, i32, i32, vp]
     lib.pkv_decode_layer.restype = i32
+    lib.pkv_plan_step.argtypes = [W, i32, i32, i32, vp]
+    lib.pkv_plan_step.restype = i32
     lib.pkv_decode_attn_static_scratch.argtypes = [W, i32, i32, vp, f32, i32, i32, vp]
     lib.pkv_decode_attn_static_scratch.restype = i32
     p64, p32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
@@ -177,6 +181,11 @@ def pkv_decode_layer(ws, batch, layer, q, k_new, v_new, scale, num_splits=1, fla
                                 _ptr(v_new), float(scale), int(num_splits), int(flags),
                                 _stream(stream))
     return _check("pkv_decode_layer", s) if check else s
+
+
+def pkv_plan_step(ws, batch, num_splits=1, flags=0, stream=None, check=True):
+    s = load().pkv_plan_step(_ws(ws), int(batch), int(num_splits), int(flags), _stream(stream))
+    return _check("pkv_plan_step", s) if check else s
 
 
 def pkv_decode_attn_static_scratch(ws, batch, layer, q, scale, num_splits=1, flags=0,

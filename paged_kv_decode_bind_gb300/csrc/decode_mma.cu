@@ -62,6 +62,7 @@ constexpr int kMThreads = (kCW + 1) * 32;
 constexpr int kMT = 16 * kCW;            // tokens per tile
 constexpr int kMStages = 3;
 constexpr int kLA = 8;  // tiles of index lookahead (shared-memory ring of slots)
+static_assert(kLA == kPlanTiles, "the step's plan holds the first ring's worth of page ids");
 
 template <int D, int G>
 struct MCfg {
@@ -277,64 +278,113 @@ __global__ void __launch_bounds__(kMThreads, 2)
   pl.S = a.num_splits;
   const bool direct = pl.S == 1;
   const bool fused = a.fused_merge && !direct;
-  if (a.batch <= kMaxCompactBatch) {
-    const int budget = a.apportion && fused ? (int)gridDim.x : 0;
-    const int pairs = batch_plan_compact(ws, a.batch, pl.S, budget, s_len, s_base, s_pref,
-                                         s_chunk, s_tmp, &s_max_len, &pl.chunk);
-    pl.pref = s_pref;
-    pl.lens = s_len;
-    pl.chunks = budget > 0 ? s_chunk : nullptr;
-    pl.n_units = pairs * pl.hkv;
-  } else {
-    pl.chunk = split_chunk(batch_max_len(ws, a.batch, &s_max_len), pl.S, ws.page_size);
-    pl.n_units = pl.S * pl.batch * pl.hkv;
+  // The step's plan (PKV_FLAG_USE_PLAN): every thread reads the header and
+  // its share of the arrays in one round trip, and they are used only if the
+  // header was written for exactly this launch; else the block plans below.
+  bool planned = false;
+  if ((a.flags & PKV_FLAG_USE_PLAN) && ws.work_plan && a.batch <= kMaxCompactBatch &&
+      gridDim.x <= kPlanMaxGrid) {
+    const int *P = ws.work_plan;
+    const int apportioned = a.apportion && fused ? 1 : 0;
+    int h[10];
+#pragma unroll
+    for (int i = 0; i < 10; ++i) h[i] = __ldcg(P + i);
+    constexpr int kPer = (kMaxCompactBatch + kMThreads - 1) / kMThreads;
+    int vp[kPer], vl[kPer], vb[kPer], vc[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int b = tid + j * kMThreads;
+      if (b <= a.batch) vp[j] = __ldcg(P + kPlanPref + b);
+      if (b < a.batch) {
+        vl[j] = __ldcg(P + kPlanLen + b);
+        vb[j] = __ldcg(P + kPlanBase + b);
+        vc[j] = __ldcg(P + kPlanChunk + b);
+      }
+    }
+    const int first =
+        use_tma && tid < kLA * 4 ? __ldcg(P + kPlanFirst + blockIdx.x * kLA * 4 + tid) : -1;
+    planned = h[kHMagic] == kPlanMagic && h[kHBatch] == a.batch && h[kHSplits] == pl.S &&
+              h[kHGrid] == (int)gridDim.x && h[kHApportion] == apportioned &&
+              h[kHTma] == (use_tma ? 1 : 0) && h[kHHkv] == pl.hkv;
+    if (planned) {
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int b = tid + j * kMThreads;
+        if (b <= a.batch) s_pref[b] = vp[j];
+        if (b < a.batch) {
+          s_len[b] = vl[j];
+          s_base[b] = vb[j];
+          s_chunk[b] = vc[j];
+        }
+      }
+      if (use_tma && tid < kLA * 4) s_idx[tid >> 2][tid & 3] = first;
+      pl.pref = s_pref;
+      pl.lens = s_len;
+      pl.chunks = apportioned ? s_chunk : nullptr;
+      pl.chunk = h[kHChunk];
+      pl.n_units = h[kHUnits];
+    }
+    __syncthreads();  // also publishes the barriers set up above
+  }
+  if (!planned) {
+    if (a.batch <= kMaxCompactBatch) {
+      const int budget = a.apportion && fused ? (int)gridDim.x : 0;
+      const int pairs = batch_plan_compact(ws, a.batch, pl.S, budget, s_len, s_base, s_pref,
+                                           s_chunk, s_tmp, &s_max_len, &pl.chunk);
+      pl.pref = s_pref;
+      pl.lens = s_len;
+      pl.chunks = budget > 0 ? s_chunk : nullptr;
+      pl.n_units = pairs * pl.hkv;
+    } else {
+      pl.chunk = split_chunk(batch_max_len(ws, a.batch, &s_max_len), pl.S, ws.page_size);
+      pl.n_units = pl.S * pl.batch * pl.hkv;
+    }
   }
   const uint32_t kv_base = smem_addr(smem + C::OFF_KV);
 
-  // Index entries of the block's first kLA tiles, fetched by the whole block
-  // in one round trip (each thread walks its own cursor to its tile), so the
-  // producer can issue tile 0 right away.  TMA path: entries 0..3 of a ring
-  // slot are the page ids of the tile's 16-token pieces; gather path: entries
-  // 0..63 are the slots / page ids of its rows; -1 where there is none.
-  {
-    const int per = use_tma ? 4 : kMT;
-    Cursor<kMT> c;
-    int at = -1;
-    for (int e = tid; e < kLA * per; e += kMThreads) {
-      const int tile = e / per, r = e - tile * per;
-      if (at < 0) {
-        c.start(ws, pl);
-        at = 0;
-      }
-      c.advance_by(ws, pl, tile - at);
-      at = tile;
-      int v = -1;
-      if (!c.done) {
-        const Unit &u = c.it.un;
-        const int tok = u.t0 + c.i * kMT + (use_tma ? 16 * r : r);
-        const ReqIndex ri = pl.pref ? req_index_cached(ws, s_base, u.b) : req_index(ws, u.b);
-        if (tok < u.t1 && ri.ok) v = *index_src(ws, pl, ri, tok);
-      }
-      s_idx[tile][r] = v;
-    }
-  }
-  // The producer's cursors, while the block's index loads are in flight:
-  // pc walks the tiles to issue; pf runs kLA tiles ahead and fetches later
-  // index entries with 4-byte cp.async copies into the ring (one commit group
-  // per tile, issued at iteration k for tile k + kLA), so no register ever
-  // waits on an index load: at iteration k, tile k's entries are complete once
-  // at most kLA - 1 newer groups pend (tiles 0 .. kLA - 1 came in with the
-  // block's fetch above).
-  Cursor<kMT> pc, pf;
-  if (warp == kCW) {
-    pc.start(ws, pl);
-    pf = pc;
-    pf.advance_by(ws, pl, kLA);
-  }
-  __syncthreads();
-
   if (warp == kCW) {
     // ------------------------------------------------------- producer ----
+    // pc walks the tiles to issue.  The index entries of the first kLA tiles
+    // are fetched at once, lane-strided, with 4-byte cp.async copies (each
+    // lane walks a copy of pc to its entry's tile); pf then runs kLA tiles
+    // ahead and fetches later entries the same way into the ring, one commit
+    // group per tile issued at iteration k for tile k + kLA, so no register
+    // ever waits on an index load: at iteration k, tile k's entries are
+    // complete once at most kLA - 1 newer groups pend.  TMA path: entries
+    // 0..3 of a ring slot are the page ids of the tile's 16-token pieces;
+    // gather path: entries 0..63 are the slots / page ids of its rows; -1
+    // where there is none.
+    Cursor<kMT> pc;
+    pc.start(ws, pl);
+    if (!(planned && use_tma)) {
+      const int per = use_tma ? 4 : kMT;
+      Cursor<kMT> c = pc;
+      int at = 0;
+      for (int e = lane; e < kLA * per; e += 32) {
+        const int tile = e / per, r = e - tile * per;
+        c.advance_by(ws, pl, tile - at);
+        at = tile;
+        int *dst = &s_idx[tile][r];
+        bool want = false;
+        const int *src = nullptr;
+        if (!c.done) {
+          const Unit &u = c.it.un;
+          const int tok = u.t0 + c.i * kMT + (use_tma ? 16 * r : r);
+          const ReqIndex ri = pl.pref ? req_index_cached(ws, s_base, u.b) : req_index(ws, u.b);
+          want = tok < u.t1 && ri.ok;
+          if (want) src = index_src(ws, pl, ri, tok);
+        }
+        if (want)
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+                       : "memory");
+        else
+          *dst = -1;
+      }
+    }
+    Cursor<kMT> pf = pc;
+    pf.advance_by(ws, pl, kLA);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
     int pf_u = -1;
     ReqIndex pf_ri{0, false};
     auto prefetch = [&](int slot) {  // entries of the tile under pf into s_idx[slot]
@@ -816,8 +866,15 @@ bool encode_pool_map(CUtensorMap *m, void *base, const pkv_workspace &ws) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch shape of the tensor-core decode kernel for a call: resident-block
+// grid, whether its splits are apportioned, and whether TMA boxes apply (the
+// tensor maps still have to encode).  The step's plan is made for the same.
+struct MmaShape {
+  int grid, apportion, tma;
+};
+
 template <int D, int G>
-cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
+cudaError_t mma_shape(const DecodeArgs &a, MmaShape *sh) {
   using C = MCfg<D, G>;
   auto kern = decode_mma_kernel<D, G>;
   static int occ_cache[64] = {0};
@@ -837,27 +894,39 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
     sms_cache[di] = sms;
     occ_cache[di] = occ > 0 ? occ : 1;
   }
+  const pkv_workspace &ws = a.ws;
+  const long long units = (long long)a.num_splits * a.batch * ws.n_kv_heads;
+  const long long cap = (long long)sms_cache[di] * occ_cache[di];
+  sh->grid = (int)(units < cap ? units : cap);
+  // Apportioned splits need the compact plan, and the summed lengths must
+  // fit in an int.
+  sh->apportion = a.fused_merge && a.num_splits > 1 && a.batch <= kMaxCompactBatch &&
+                  !(a.flags & PKV_FLAG_FIXED_CHUNK) &&
+                  (long long)a.batch * ws.max_pages_per_req * ws.page_size < 0x7fffffffll;
+  sh->tma = ws.index_mode == PKV_IDX_PAGE_TABLE && ws.page_size % 16 == 0 &&
+            (long long)ws.n_layers * ws.pool_slots < 0x7fffffffll &&
+            !(a.flags & PKV_FLAG_FORCE_GATHER);
+  return cudaSuccess;
+}
+
+template <int D, int G>
+cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
+  using C = MCfg<D, G>;
+  MmaShape sh;
+  cudaError_t e = mma_shape<D, G>(a, &sh);
+  if (e != cudaSuccess) return e;
+  if (sh.grid <= 0) return cudaSuccess;
   CUtensorMap tmk, tmv;
   memset(&tmk, 0, sizeof(tmk));
   memset(&tmv, 0, sizeof(tmv));
   const pkv_workspace &ws = a.ws;
-  int use_tma = ws.index_mode == PKV_IDX_PAGE_TABLE && ws.page_size % 16 == 0 &&
-                (long long)ws.n_layers * ws.pool_slots < 0x7fffffffll &&
-                !(a.flags & PKV_FLAG_FORCE_GATHER);
+  int use_tma = sh.tma;
   if (use_tma)
     use_tma = encode_pool_map(&tmk, ws.k_pool, ws) && encode_pool_map(&tmv, ws.v_pool, ws);
-  const long long units = (long long)a.num_splits * a.batch * ws.n_kv_heads;
-  const long long cap = (long long)sms_cache[di] * occ_cache[di];
-  const int grid = (int)(units < cap ? units : cap);
-  if (grid <= 0) return cudaSuccess;
-  // Apportioned splits need the compact plan, and the summed lengths must
-  // fit in an int.
   DecodeArgs args = a;
-  args.apportion = a.fused_merge && a.num_splits > 1 && a.batch <= kMaxCompactBatch &&
-                   !(a.flags & PKV_FLAG_FIXED_CHUNK) &&
-                   (long long)a.batch * ws.max_pages_per_req * ws.page_size < 0x7fffffffll;
+  args.apportion = sh.apportion;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(sh.grid);
   cfg.blockDim = dim3(kMThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
@@ -866,7 +935,90 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args, tmk, tmv, use_tma);
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, G>, args, tmk, tmv, use_tma);
+}
+
+// The step's plan (see pkv_plan_step): the compact plan every decode block
+// would derive, and the TMA page ids of every block's first kPlanTiles tiles
+// (one thread per (block, tile)).  Block 0 writes the header and the arrays.
+constexpr int kPlanThreads = 256;
+
+__global__ void __launch_bounds__(kPlanThreads)
+    plan_kernel(const __grid_constant__ pkv_workspace ws, int batch, int S, int grid,
+                int apportion, int tma) {
+  __shared__ int s_len[kMaxCompactBatch], s_base[kMaxCompactBatch], s_chunk[kMaxCompactBatch];
+  __shared__ int s_pref[kMaxCompactBatch + 1];
+  __shared__ int s_tmp[32];
+  __shared__ int s_max;
+  Plan pl;
+  pl.set_pages(ws);
+  pl.batch = batch;
+  pl.hkv = ws.n_kv_heads;
+  pl.S = S;
+  const int budget = apportion ? grid : 0;
+  const int pairs =
+      batch_plan_compact(ws, batch, S, budget, s_len, s_base, s_pref, s_chunk, s_tmp, &s_max,
+                         &pl.chunk);
+  pl.pref = s_pref;
+  pl.lens = s_len;
+  pl.chunks = budget > 0 ? s_chunk : nullptr;
+  pl.n_units = pairs * pl.hkv;
+  int *P = ws.work_plan;
+  const int tid = threadIdx.x;
+  if (tma) {
+    for (int item = blockIdx.x * blockDim.x + tid; item < grid * kPlanTiles;
+         item += gridDim.x * blockDim.x) {
+      const int blk = item / kPlanTiles, t = item - blk * kPlanTiles;
+      Cursor<kMT> c;
+      c.start(ws, pl, blk, grid);
+      c.advance_by(ws, pl, t);
+      int v[4] = {-1, -1, -1, -1};
+      if (!c.done) {
+        const Unit &u = c.it.un;
+        const ReqIndex ri = req_index_cached(ws, s_base, u.b);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int tok = u.t0 + c.i * kMT + 16 * r;
+          if (tok < u.t1 && ri.ok) v[r] = *index_src(ws, pl, ri, tok);
+        }
+      }
+      *reinterpret_cast<int4 *>(P + kPlanFirst + item * 4) = make_int4(v[0], v[1], v[2], v[3]);
+    }
+  }
+  if (blockIdx.x == 0) {
+    for (int b = tid; b < batch; b += blockDim.x) {
+      P[kPlanPref + b] = s_pref[b];
+      P[kPlanLen + b] = s_len[b];
+      P[kPlanBase + b] = s_base[b];
+      P[kPlanChunk + b] = budget > 0 ? s_chunk[b] : 0;
+    }
+    if (tid == 0) {
+      P[kPlanPref + batch] = s_pref[batch];
+      P[kHBatch] = batch;
+      P[kHSplits] = S;
+      P[kHGrid] = grid;
+      P[kHUnits] = pl.n_units;
+      P[kHChunk] = pl.chunk;
+      P[kHMaxLen] = s_max;
+      P[kHApportion] = budget > 0;
+      P[kHTma] = tma;
+      P[kHHkv] = pl.hkv;
+      P[kHMagic] = kPlanMagic;
+    }
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_plan_one(const DecodeArgs &a, cudaStream_t st) {
+  MmaShape sh;
+  cudaError_t e = mma_shape<D, G>(a, &sh);
+  if (e != cudaSuccess) return e;
+  if (sh.grid <= 0 || sh.grid > kPlanMaxGrid || a.batch > kMaxCompactBatch) return cudaSuccess;
+  const int items = sh.tma ? sh.grid * kPlanTiles : 1;
+  const int blocks = (items + kPlanThreads - 1) / kPlanThreads;
+  plan_kernel<<<blocks, kPlanThreads, 0, st>>>(a.ws, a.batch, a.num_splits, sh.grid,
+                                                sh.apportion, sh.tma);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -874,6 +1026,19 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
 bool decode_mma_supported(int head_dim, int group) {
   return (head_dim == 64 || head_dim == 128) &&
          (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+}
+
+size_t plan_bytes() { return (size_t)kPlanInts * 4; }
+
+cudaError_t launch_plan(const DecodeArgs &a, cudaStream_t st) {
+  const int D = a.ws.head_dim, G = a.ws.n_q_heads / a.ws.n_kv_heads;
+#define PKV_PLAN_CASE(DD, GG) \
+  if (D == DD && G == GG) return launch_plan_one<DD, GG>(a, st);
+  PKV_PLAN_CASE(128, 1) PKV_PLAN_CASE(128, 2) PKV_PLAN_CASE(128, 4) PKV_PLAN_CASE(128, 8)
+  PKV_PLAN_CASE(128, 16) PKV_PLAN_CASE(64, 1) PKV_PLAN_CASE(64, 2) PKV_PLAN_CASE(64, 4)
+  PKV_PLAN_CASE(64, 8) PKV_PLAN_CASE(64, 16)
+#undef PKV_PLAN_CASE
+  return cudaErrorNotSupported;
 }
 
 cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t st) {

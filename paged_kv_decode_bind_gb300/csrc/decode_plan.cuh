@@ -47,6 +47,21 @@ struct Plan {
 };
 
 constexpr int kMaxCompactBatch = 256;
+
+// Layout of ws.work_plan (int32 offsets), written by the step's plan kernel
+// and read by the decode kernel: a header, the compact plan's arrays, and the
+// TMA page ids of the first kPlanTiles tiles of every block.
+constexpr int kPlanMagic = 0x706b7631;
+constexpr int kPlanTiles = 8;
+constexpr int kPlanMaxGrid = 1024;
+enum PlanHdr { kHMagic, kHBatch, kHSplits, kHGrid, kHUnits, kHChunk, kHMaxLen, kHApportion,
+               kHTma, kHHkv, kPlanHdr = 16 };
+constexpr int kPlanPref = kPlanHdr;                          // batch + 1 entries
+constexpr int kPlanLen = kPlanPref + kMaxCompactBatch + 4;
+constexpr int kPlanBase = kPlanLen + kMaxCompactBatch;
+constexpr int kPlanChunk = kPlanBase + kMaxCompactBatch;
+constexpr int kPlanFirst = kPlanChunk + kMaxCompactBatch;    // [block][tile][4]
+constexpr int kPlanInts = kPlanFirst + kPlanMaxGrid * kPlanTiles * 4;
 constexpr int kChunkAlign = 64;  // apportioned chunks: multiples of this many tokens
 constexpr int kMinChunk = 128;   // no apportioned split shorter (more merging than streaming)
 
@@ -104,21 +119,27 @@ __device__ __forceinline__ Unit unit_at(const pkv_workspace &ws, const Plan &pl,
   return x;
 }
 
-// The units one block processes, in order (uniform in the block): every
-// gridDim.x-th unit, empty ones included.
+// The units block blk of nblk processes, in order (uniform in the block):
+// every nblk-th unit from blk, empty ones included.
 struct UnitIter {
   Unit un;
   bool done;
+  int nblk;
 
   __device__ __forceinline__ void at(const pkv_workspace &ws, const Plan &pl, int u) {
     done = u >= pl.n_units;
     if (!done) un = unit_at(ws, pl, u);
   }
+  __device__ __forceinline__ void first(const pkv_workspace &ws, const Plan &pl, int blk,
+                                        int n) {
+    nblk = n;
+    at(ws, pl, blk);
+  }
   __device__ __forceinline__ void first(const pkv_workspace &ws, const Plan &pl) {
-    at(ws, pl, blockIdx.x);
+    first(ws, pl, blockIdx.x, gridDim.x);
   }
   __device__ __forceinline__ void next(const pkv_workspace &ws, const Plan &pl) {
-    at(ws, pl, un.u + gridDim.x);
+    at(ws, pl, un.u + nblk);
   }
 };
 
@@ -141,6 +162,11 @@ struct Cursor {
   }
   __device__ __forceinline__ void start(const pkv_workspace &ws, const Plan &pl) {
     it.first(ws, pl);
+    skip_empty(ws, pl);
+  }
+  // as block blk of a grid of n
+  __device__ __forceinline__ void start(const pkv_workspace &ws, const Plan &pl, int blk, int n) {
+    it.first(ws, pl, blk, n);
     skip_empty(ws, pl);
   }
   __device__ __forceinline__ void advance(const pkv_workspace &ws, const Plan &pl) {
@@ -199,7 +225,8 @@ __device__ __forceinline__ int align_chunk(long long c) {
 
 __device__ __forceinline__ int apportion_start(long long sum_len, int max_len, int hkv,
                                                int budget, int S) {
-  long long x = ((long long)hkv * sum_len + budget - 1) / budget;
+  // the even share (a float estimate is enough: the search only grows it)
+  long long x = (long long)__fdividef((float)hkv * (float)sum_len, (float)budget);
   x = max(x, (long long)(max_len + S - 1) / S);
   return max(align_chunk(x), kMinChunk);
 }

@@ -34,6 +34,10 @@ bool decode_simt_supported(int head_dim, int group);
 // Tensor-core (warp mma) split-KV decode; same contract as the SIMT kernel,
 // plus the fused append and merge.
 cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t st);
+// The step's split plan for the tensor-core kernel (pkv_plan_step) and the
+// size of ws.work_plan it needs.
+cudaError_t launch_plan(const DecodeArgs &a, cudaStream_t st);
+size_t plan_bytes();
 bool decode_mma_supported(int head_dim, int group);
 
 cudaError_t launch_merge(const pkv_workspace &ws, int batch, int num_splits, int flags,

@@ -103,7 +103,7 @@ __device__ __forceinline__ void merge_rows_batched(const pkv_workspace &ws, long
     den[j] = 0.f;
     acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  constexpr int GS = NH >= 4 ? 4 : 8;  // splits per group of row loads (registers)
+  constexpr int GS = NH >= 4 ? 4 : (NH == 1 ? 16 : 8);  // splits per group of row loads
   auto load_rows = [&](float4 (&o)[GS][NH], int s, int m) {  // splits s .. s + GS - 1 (< m)
 #pragma unroll
     for (int t = 0; t < GS; ++t)

@@ -70,6 +70,7 @@ size_t pkv_workspace_bytes(const pkv_workspace *ws, const char *which) {
   if (!strcmp(which, "lse")) return B * hq * 4;
   if (!strcmp(which, "err")) return 4;
   if (!strcmp(which, "split_counters")) return B * hkv * 4;
+  if (!strcmp(which, "work_plan")) return plan_bytes();
   return 0;
 }
 
@@ -204,6 +205,22 @@ pkv_status pkv_decode_layer(const pkv_workspace *ws, int batch, int layer, const
                             const void *k_new, const void *v_new, float scale, int num_splits,
                             int flags, pkv_stream_t stream) {
   return decode_common(ws, batch, layer, q, k_new, v_new, scale, num_splits, flags, 1, stream);
+}
+
+pkv_status pkv_plan_step(const pkv_workspace *ws, int batch, int num_splits, int flags,
+                         pkv_stream_t stream) {
+  pkv_status st = check_shape(ws);
+  if (st != PKV_OK) return st;
+  if ((st = check_index(ws)) != PKV_OK) return st;
+  if (batch < 0 || num_splits < 1) return PKV_ERR_INVALID;
+  if (batch > ws->max_batch || num_splits > ws->max_splits) return PKV_ERR_CAPACITY;
+  if (!ws->work_plan || !aligned16(ws->work_plan) || !ws->seq_lens) return PKV_ERR_INVALID;
+  if ((long long)num_splits * batch * ws->n_kv_heads > 0x7fffffffll) return PKV_ERR_CAPACITY;
+  const int G = ws->n_q_heads / ws->n_kv_heads;
+  if (batch == 0 || (flags & PKV_FLAG_FORCE_SIMT) || !decode_mma_supported(ws->head_dim, G))
+    return PKV_OK;  // no tensor-core launch would read a plan
+  DecodeArgs a{*ws, batch, 0, nullptr, 0.f, num_splits, flags, nullptr, nullptr, 1, 0};
+  return from_cuda(launch_plan(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits, int flags,

@@ -34,7 +34,7 @@ class DecodeRunner:
 
     def __init__(self, ws: Workspace, batch: int, *, num_splits: int = 1, flags: int = 0,
                  scale: float | None = None, stream: torch.cuda.Stream | None = None,
-                 fused: bool = True):
+                 fused: bool = True, plan: bool = False):
         self.ws = ws
         self.batch = batch
         sh = ws.shape
@@ -55,12 +55,22 @@ class DecodeRunner:
         # kernels one step launches: bind (+ flat index build), then per layer
         # one fused kernel, or append + attention (+ merge when split)
         split = num_splits > 1
-        per_layer = 1 if fused and not (flags & _abi.PKV_FLAG_FORCE_SIMT) else 2 + int(split)
-        self.launches_per_step = 1 + int(flat) + NL * per_layer
+        mma = (not (flags & _abi.PKV_FLAG_FORCE_SIMT) and sh["head_dim"] in (64, 128)
+               and sh["n_q_heads"] // sh["n_kv_heads"] in (1, 2, 4, 8, 16))
+        # plan=True: the fused layers take the step's split plan, made once after
+        # the bind (pkv_plan_step).  Off by default: with the layers pipelined by
+        # programmatic dependent launch the plan saves no time, and a one-layer
+        # step pays for the extra launch.
+        self.use_plan = plan and fused and mma and ws.work_plan is not None
+        per_layer = 1 if fused and mma else 2 + int(split)
+        self.launches_per_step = (1 + int(flat) + int(self.use_plan and 0 < batch <= 256) +
+                                  NL * per_layer)
 
     # --- pieces -------------------------------------------------------------
     def bind(self, mode=_abi.PKV_BIND_STEADY):
         _abi.pkv_bind_step(self.ws, self.batch, mode, 0, 0, None, None, self._s())
+        if self.use_plan:
+            _abi.pkv_plan_step(self.ws, self.batch, self.num_splits, self.flags, self._s())
 
     def layer(self, l, events=None):
         """Layer l: one fused launch (append + attention + merge), or the
@@ -72,9 +82,10 @@ class DecodeRunner:
             # Layers after the first read metadata the step's bind wrote two or
             # more launches earlier, so they may start before layer l-1 ends.
             early = _abi.PKV_FLAG_PLAN_EARLY if (l > 0 and events is None) else 0
+            use = _abi.PKV_FLAG_USE_PLAN if self.use_plan else 0
             _abi.pkv_decode_layer(self.ws, self.batch, l, self.q_in[l], self.k_in[l],
-                                  self.v_in[l], self.scale, self.num_splits, self.flags | early,
-                                  s)
+                                  self.v_in[l], self.scale, self.num_splits,
+                                  self.flags | early | use, s)
             if events is not None:
                 events[1].record(s)
             return

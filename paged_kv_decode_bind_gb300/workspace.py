@@ -48,6 +48,7 @@ class Workspace:
         self.lse = torch.zeros((max_batch, n_q_heads), dtype=torch.float32, device=dev)
         self.err = torch.zeros(1, **i32)
         self.split_counters = torch.zeros(max(1, max_batch * n_kv_heads), **i32)
+        self.work_plan = None  # sized below from the library's layout
         self.struct = _abi.PkvWorkspace(
             **self.shape,
             k_pool=_abi._ptr(self.k_pool) if pools else None,
@@ -59,6 +60,9 @@ class Workspace:
             o_part=self.o_part.data_ptr(), ml_part=self.ml_part.data_ptr(),
             out=self.out.data_ptr(), lse=self.lse.data_ptr(), err=self.err.data_ptr(),
             split_counters=self.split_counters.data_ptr())
+        plan_bytes = _abi.pkv_workspace_bytes(self.struct, "work_plan")
+        self.work_plan = torch.zeros(max(1, plan_bytes // 4), **i32)
+        self.struct.work_plan = self.work_plan.data_ptr()
 
     # typed views of the output buffer --------------------------------------
     def out_bf16(self, batch):

@@ -30,8 +30,8 @@ def test_exports_match_header():
 
 
 def test_struct_layout():
-    # 12 int32 shape fields then 15 pointers, no padding on LP64.
-    assert ctypes.sizeof(_abi.PkvWorkspace) == 12 * 4 + 15 * 8
+    # 12 int32 shape fields then 16 pointers, no padding on LP64.
+    assert ctypes.sizeof(_abi.PkvWorkspace) == 12 * 4 + 16 * 8
     assert _abi.PkvWorkspace.k_pool.offset == 48
 
 
@@ -43,7 +43,7 @@ def _ws(**kw):
     ptrs = dict(k_pool=fake, v_pool=fake, req_pool_indices=fake, page_table=fake,
                 seq_lens=fake, position_ids=fake, kv_indptr=fake, out_loc=fake,
                 kv_indices=fake, o_part=fake, ml_part=fake, out=fake, lse=fake, err=fake,
-                split_counters=fake)
+                split_counters=fake, work_plan=fake)
     shape.update({k: v for k, v in kw.items() if k in shape})
     ptrs.update({k: v for k, v in kw.items() if k in ptrs})
     return _abi.PkvWorkspace(**shape, **ptrs)

@@ -252,3 +252,47 @@ def test_kernels_agree(cuda):
         outs.append(ws.out_f32(p.batch).cpu().numpy())
     assert np.abs(outs[0] - outs[1]).max() <= 1e-3
     assert np.abs(outs[0] - outs[2]).max() <= 1e-3
+
+
+# ------------------------------------------------------------ step plan ----
+
+def _fused_out(p, S, flags=0, plan=True, plan_args=None):
+    ws = Workspace.from_problem(p, max_splits=max(S, 8))
+    run = DecodeRunner(ws, p.batch, num_splits=S, flags=flags | A.PKV_FLAG_OUT_F32,
+                       scale=p.scale, plan=plan)
+    q, k, v = W.step_inputs(p, 0)
+    run.q_in.copy_(q), run.k_in.copy_(k), run.v_in.copy_(v)
+    if plan_args is not None:
+        # a plan made for other arguments: the layers must ignore it
+        A.pkv_bind_step(ws, p.batch, A.PKV_BIND_STEADY, 0, 0, None, None)
+        A.pkv_plan_step(ws, *plan_args)
+        for l in range(p.n_layers):
+            A.pkv_decode_layer(ws, p.batch, l, run.q_in[l], run.k_in[l], run.v_in[l], p.scale,
+                               S, flags | A.PKV_FLAG_OUT_F32 | A.PKV_FLAG_USE_PLAN)
+    else:
+        run.step()
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) == 0
+    assert int(ws.split_counters.abs().sum().item()) == 0
+    return ws.out_f32(p.batch).cpu().numpy().copy()
+
+
+@pytest.mark.parametrize("name,batch", [("gqa4_b4_paged", None), ("gqa8_graph_sweep", 16),
+                                        ("gqa4_b16_flat_skewed", None)])
+def test_step_plan_bitexact(cuda, name, batch):
+    # Layers that read the step's plan compute exactly what layers that plan
+    # for themselves compute (same splits, same arithmetic).
+    p = W.workload(name, batch=batch, shrink=4, steps=1)
+    S = _bench_splits(p, A.pkv_choose_pieces)
+    a = _fused_out(p, S, plan=True)
+    b = _fused_out(p, S, plan=False)
+    assert np.array_equal(a, b)
+
+
+def test_step_plan_for_other_arguments_is_ignored(cuda):
+    p = W.workload("gqa4_b4_paged", shrink=8, steps=1)
+    ref = _fused_out(p, 4, plan=False)
+    for other in ((p.batch, 3, 0), (p.batch - 1, 4, 0), (p.batch, 4, A.PKV_FLAG_FIXED_CHUNK),
+                  (p.batch, 4, A.PKV_FLAG_FORCE_GATHER)):
+        got = _fused_out(p, 4, plan_args=other)
+        assert np.array_equal(got, ref), other
