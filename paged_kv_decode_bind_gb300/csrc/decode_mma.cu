@@ -342,6 +342,32 @@ __global__ void __launch_bounds__(kMThreads, 2)
   }
   const uint32_t kv_base = smem_addr(smem + C::OFF_KV);
 
+  // Gather path: the 64 index entries of each of the first kLA tiles are
+  // fetched by the whole block at once (each thread walks its own cursor to
+  // its entries' tile); the TMA path's 4 per tile are left to the producer.
+  if (!use_tma) {
+    Cursor<kMT> c;
+    int at = -1;
+    for (int e = tid; e < kLA * kMT; e += kMThreads) {
+      const int tile = e / kMT, r = e - tile * kMT;
+      if (at < 0) {
+        c.start(ws, pl);
+        at = 0;
+      }
+      c.advance_by(ws, pl, tile - at);
+      at = tile;
+      int v = -1;
+      if (!c.done) {
+        const Unit &u = c.it.un;
+        const int tok = u.t0 + c.i * kMT + r;
+        const ReqIndex ri = pl.pref ? req_index_cached(ws, s_base, u.b) : req_index(ws, u.b);
+        if (tok < u.t1 && ri.ok) v = *index_src(ws, pl, ri, tok);
+      }
+      s_idx[tile][r] = v;
+    }
+    __syncthreads();
+  }
+
   if (warp == kCW) {
     // ------------------------------------------------------- producer ----
     // pc walks the tiles to issue.  The index entries of the first kLA tiles
@@ -356,8 +382,8 @@ __global__ void __launch_bounds__(kMThreads, 2)
     // where there is none.
     Cursor<kMT> pc;
     pc.start(ws, pl);
-    if (!(planned && use_tma)) {
-      const int per = use_tma ? 4 : kMT;
+    if (use_tma && !planned) {
+      const int per = 4;
       Cursor<kMT> c = pc;
       int at = 0;
       for (int e = lane; e < kLA * per; e += 32) {
@@ -369,7 +395,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
         const int *src = nullptr;
         if (!c.done) {
           const Unit &u = c.it.un;
-          const int tok = u.t0 + c.i * kMT + (use_tma ? 16 * r : r);
+          const int tok = u.t0 + c.i * kMT + 16 * r;
           const ReqIndex ri = pl.pref ? req_index_cached(ws, s_base, u.b) : req_index(ws, u.b);
           want = tok < u.t1 && ri.ok;
           if (want) src = index_src(ws, pl, ri, tok);
