@@ -189,6 +189,19 @@ def test_rebuild_after_batch_change(cuda):
     assert ws.out_loc[:4].tolist() == ref["out_loc"]
 
 
+@pytest.mark.parametrize("kern", ["mma", "fused", "fused_gather"])
+def test_batch_beyond_compact_plan(cuda, kern):
+    # More requests than the blocks plan compactly (256): every unit is
+    # enumerated, splits of requests shorter than the chunk are empty.
+    rng = np.random.default_rng(11)
+    lens = [int(x) for x in rng.integers(1, 97, size=300)]
+    lens[5] = 0
+    p = W.make_problem("wide", batch=300, n_layers=1, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                       page_size=16, seq_lens=lens, steps=1, seed=12)
+    run_steps(p, S=3, heads=_sample_heads(p, 40), check_partials=True, check_pool=True,
+              flags=PATHS[kern][0], fused=PATHS[kern][1])
+
+
 def test_zero_length_request(cuda):
     # A request with no tokens gives zeros (and lse = -inf), with no error bit.
     p = W.make_problem("zero", batch=3, n_layers=1, n_q_heads=8, n_kv_heads=2, head_dim=128,
