@@ -8,7 +8,7 @@ Sources (the engine's commit-log pages, AstrAI by ViperEkura; cited as
   * cache.py page      -- commit cbc5844, astrai/inference/core/cache.py
   * executor.py page   -- commit e0f7fa8, astrai/inference/core/executor.py
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * query head h reads KV head h // G, G = Hq / Hkv (contiguous groups);
   * the new token is appended before attention, so it is attended;
   * a steady step sets position_ids to the old length, then adds 1 to
