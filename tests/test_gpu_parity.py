@@ -309,3 +309,19 @@ def test_step_plan_for_other_arguments_is_ignored(cuda):
                   (p.batch, 4, A.PKV_FLAG_FORCE_GATHER)):
         got = _fused_out(p, 4, plan_args=other)
         assert np.array_equal(got, ref), other
+
+
+# ------------------------------------------------------ token-level pages ----
+
+@pytest.mark.parametrize("D,G,Hkv,P", [(128, 4, 8, 1), (128, 2, 4, 1), (64, 1, 4, 1),
+                                       (64, 4, 8, 8), (128, 1, 8, 1)])
+@pytest.mark.parametrize("S", [1, 3])
+def test_token_level_variants(cuda, D, G, Hkv, P, S):
+    # Flat token-level indices and pages shorter than a 16-token box, over head
+    # dims, group sizes and KV head counts: the fused layer's gather producer
+    # (and the flat bind / append around it).
+    rng = np.random.default_rng(D + G + Hkv + P)
+    lens = [int(x) for x in rng.integers(1, 300, size=5)]
+    p = W.make_problem("rows", batch=5, n_layers=2, n_q_heads=G * Hkv, n_kv_heads=Hkv,
+                       head_dim=D, page_size=P, seq_lens=lens, steps=1, seed=13)
+    run_steps(p, S=S, check_pool=True, fused=True)
