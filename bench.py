@@ -128,6 +128,11 @@ class ClockSampler:
 
 # ------------------------------------------------------------ oracle legs --
 
+# layers of each workload (the oracle arm times one; the layers are alike)
+WORKLOAD_LAYERS = {"single_d64": 1, "gqa4_b4_paged": 24, "gqa4_b16_flat_skewed": 24,
+                   "gqa4_long_65536": 1, "gqa8_graph_sweep": 24}
+
+
 def _oracle_problem(name, batch):
     import pkv_inputs as W
     return W.workload(name, batch=batch, n_layers=1, steps=1)
@@ -227,7 +232,14 @@ def run_reference(args, rank):
             "ms_per_step": dt / args.steps * 1e3,
             "us_per_layer_step": dt / args.steps / frac * 1e6,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload, "batch": p.batch},
+            "data": "synthetic",
+            "config": {"workload": args.workload, "batch": p.batch,
+                       "n_layers": args.layers or WORKLOAD_LAYERS[args.workload],
+                       "n_q_heads": p.n_q_heads, "n_kv_heads": p.n_kv_heads,
+                       "head_dim": p.head_dim, "page_size": p.page_size,
+                       "seq_lens_start": [int(p.seq_lens.min()), int(p.seq_lens.max()),
+                                          int(p.seq_lens.sum())],
+                       "timed": "one layer per step (the layers are alike)"},
             "cpu_baseline": {"kind": "oracle", "cores": 1, "value": v, "unit": "GB/s",
                              "sample": f"each step: {n} of {len(pairs_all)} (request, head) "
                                        f"attentions of one layer"},
