@@ -84,10 +84,15 @@ enum {
   PKV_FLAG_FIXED_CHUNK = 64,  /* pkv_decode_layer, tensor-core kernel: cut the KV axis
                                  into pkv_decode_attn's fixed chunks instead of
                                  apportioned splits */
-  PKV_FLAG_USE_PLAN = 128     /* pkv_decode_layer: take the split plan and the first page
+  PKV_FLAG_USE_PLAN = 128,    /* pkv_decode_layer: take the split plan and the first page
                                  ids from ws->work_plan (pkv_plan_step) when it was made
                                  for this batch size, split count and flags; else plan
                                  as without the flag */
+  PKV_FLAG_TEST_SKIP_FIRST_TILE = 256  /* test hook, tensor-core kernel: every block's
+                                 producer leaves its first tile unloaded, so the bounded
+                                 wait for it runs out (~1 s): the launch sets
+                                 PKV_DEVERR_TIMEOUT, writes those units empty and
+                                 returns, and the context stays usable */
 };
 
 /* bits OR-ed into *err by device code (sticky; the caller clears the word) */

@@ -18,6 +18,7 @@ PKV_IDX_PAGE_TABLE, PKV_IDX_FLAT = 0, 1
 PKV_FLAG_OUT_F32, PKV_FLAG_WRITE_LSE, PKV_FLAG_FORCE_SIMT, PKV_FLAG_FORCE_MMA = 1, 2, 4, 8
 PKV_FLAG_FORCE_GATHER, PKV_FLAG_PLAN_EARLY, PKV_FLAG_FIXED_CHUNK = 16, 32, 64
 PKV_FLAG_USE_PLAN = 128
+PKV_FLAG_TEST_SKIP_FIRST_TILE = 256
 PKV_DEVERR_PAGE, PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT, PKV_DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16
 

@@ -466,7 +466,9 @@ __global__ void __launch_bounds__(kMThreads, 2)
       // TMA: lanes j and j + 4 both need piece j's page id
       const int cur[2] = {s_idx[slot][use_tma ? (lane & 3) : lane], s_idx[slot][lane + 32]};
       __syncwarp();
-      if (use_tma) {
+      if (k == 0 && (a.flags & PKV_FLAG_TEST_SKIP_FIRST_TILE)) {
+        // test hook: the stage is never armed, the consumers' wait runs out
+      } else if (use_tma) {
         produce_tma<D, G>(a, pl, un, tile0, cur[0], s, kv_base, &full[s], flags[s], &tmk, &tmv,
                           lane);
       } else {

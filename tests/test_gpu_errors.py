@@ -117,3 +117,22 @@ def test_err_word_is_sticky_and_cleared_by_caller(cuda):
     run.step()
     torch.cuda.synchronize()
     assert int(ws.err.item()) == 0
+
+
+@pytest.mark.parametrize("kern", ["fused", "fused_gather"])
+def test_bounded_wait_runs_out(cuda, kern):
+    # The test hook leaves every block's first tile unloaded, so the
+    # consumers' bounded wait for it runs out (~1 s): the launch sets
+    # PKV_DEVERR_TIMEOUT and returns with empty (finite) outputs and its split
+    # counters back at zero, and the context stays usable.
+    from parity import run_steps
+    p = W.workload("gqa4_b4_paged", shrink=8, n_layers=1, steps=1)
+    ws, run, q, k, v = _setup(p, 2, kern)
+    run.bind()
+    A.pkv_decode_layer(ws, p.batch, 0, run.q_in[0], run.k_in[0], run.v_in[0], p.scale, 2,
+                       PATHS[kern][0] | A.PKV_FLAG_TEST_SKIP_FIRST_TILE)
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) & A.PKV_DEVERR_TIMEOUT
+    assert np.all(np.isfinite(bf16_to_f64(ws.out_bf16(p.batch))))
+    assert int(ws.split_counters.abs().sum().item()) == 0
+    run_steps(p, S=2, flags=PATHS[kern][0], fused=True)  # a normal launch afterwards
