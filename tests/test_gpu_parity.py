@@ -325,3 +325,35 @@ def test_token_level_variants(cuda, D, G, Hkv, P, S):
     p = W.make_problem("rows", batch=5, n_layers=2, n_q_heads=G * Hkv, n_kv_heads=Hkv,
                        head_dim=D, page_size=P, seq_lens=lens, steps=1, seed=13)
     run_steps(p, S=S, check_pool=True, fused=True)
+
+
+# ------------------------------------------------- cache layouts (next) ----
+
+@pytest.mark.parametrize("P", [2048, 1040])
+def test_contiguous_cache(cuda, P):
+    # One page per request holding its whole context (page size = capacity):
+    # a contiguous cache as a special case of the page table.  1040 is a
+    # multiple of 16 but no power of two (the page arithmetic divides).
+    lens = [1500, 7, 1023, 2000] if P == 2048 else [1000, 7, 1023, 640]
+    p = W.make_problem("contig", batch=4, n_layers=1, n_q_heads=16, n_kv_heads=4,
+                       head_dim=128, page_size=P, seq_lens=lens, steps=1, seed=21)
+    assert p.max_pages_per_req == 1
+    for S, kern in ((1, "fused"), (4, "fused"), (4, "mma"), (4, "fused_gather")):
+        run_steps(p, S=S, check_pool=True, check_partials=kern == "mma",
+                  flags=PATHS[kern][0], fused=PATHS[kern][1])
+
+
+def test_shared_prefix_pages(cuda):
+    # Requests whose tables alias the same physical pages for a common prefix
+    # (each appends into a page of its own): every request attends to the
+    # shared prefix's K/V.
+    lens = [200, 150, 180, 170]
+    p = W.make_problem("prefix", batch=4, n_layers=2, n_q_heads=16, n_kv_heads=4,
+                       head_dim=128, page_size=16, seq_lens=lens, steps=1, seed=22)
+    rows = p.req_pool_indices.tolist()
+    shared = p.page_table[rows[0], :5].clone()
+    for b in range(1, 4):
+        p.page_table[rows[b], :5] = shared
+    for kern in ("fused", "mma", "fused_gather"):
+        run_steps(p, S=3, check_pool=True, check_partials=kern == "mma",
+                  flags=PATHS[kern][0], fused=PATHS[kern][1])
