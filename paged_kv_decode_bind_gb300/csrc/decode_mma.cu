@@ -12,11 +12,12 @@
 // mantissa bits.  The K/V rows of a token are read from HBM once for all G
 // heads.
 //
-// Block.  4 consumer warps + 1 producer warp.  A tile is 64 tokens; consumer
-// warp w owns tokens [16w, 16w+16) of each tile with its own online-softmax
-// state; the four states merge at the end of the unit.  The producer walks
-// the block's units ahead of the consumers, across unit boundaries, through a
-// 3-stage ring (`full` mbarriers complete on the landed bytes, `empty` on the
+// Block.  4 consumer warps + 2 producer warps (one issues the TMA boxes; the
+// cp.async gathers are shared round-robin by both).  A tile is 64 tokens;
+// consumer warp w owns tokens [16w, 16w+16) of each tile with its own
+// online-softmax state; the four states merge at the end of the unit.  The
+// producers walk the block's units ahead of the consumers, across unit
+// boundaries, through a 3-stage ring (`full` mbarriers complete on the landed bytes, `empty` on the
 // four consumer warps' release), fetching index entries 8 tiles ahead (a
 // second cursor, cp.async into a shared ring) so their latency overlaps the
 // issue of earlier tiles.
@@ -58,11 +59,14 @@ namespace pkv {
 namespace {
 
 constexpr int kCW = 4;                   // consumer warps
-constexpr int kMThreads = (kCW + 1) * 32;
+constexpr int kMaxProducers = 2;         // producer warps (a launch has 1 or 2)
+constexpr int kMThreads = (kCW + kMaxProducers) * 32;  // largest block
+constexpr int kMMinThreads = (kCW + 1) * 32;           // smallest block
 constexpr int kMT = 16 * kCW;            // tokens per tile
 constexpr int kMStages = 3;
 constexpr int kLA = 8;  // tiles of index lookahead (shared-memory ring of slots)
 static_assert(kLA == kPlanTiles, "the step's plan holds the first ring's worth of page ids");
+static_assert(kLA % kMaxProducers == 0, "each index ring slot belongs to one producer");
 
 template <int D, int G>
 struct MCfg {
@@ -223,10 +227,14 @@ __device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Plan 
                : "memory");
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kMThreads, 2)
+// TMA: the page-mode producer (one warp); else the cp.async gathers (two
+// warps).  The block has kCW + nprod warps.
+template <int D, int G, bool TMA>
+__global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
     decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
-                      const __grid_constant__ CUtensorMap tmv, const int use_tma) {
+                      const __grid_constant__ CUtensorMap tmv) {
+  constexpr bool use_tma = TMA;
+  constexpr int nprod = TMA ? 1 : kMaxProducers;
   using C = MCfg<D, G>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kMStages], empty[kMStages];
@@ -289,11 +297,12 @@ __global__ void __launch_bounds__(kMThreads, 2)
     int h[10];
 #pragma unroll
     for (int i = 0; i < 10; ++i) h[i] = __ldcg(P + i);
-    constexpr int kPer = (kMaxCompactBatch + kMThreads - 1) / kMThreads;
+    constexpr int kPer = (kMaxCompactBatch + kMMinThreads) / kMMinThreads;  // batch + 1 entries
+    const int nthr = blockDim.x;
     int vp[kPer], vl[kPer], vb[kPer], vc[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int b = tid + j * kMThreads;
+      const int b = tid + j * nthr;
       if (b <= a.batch) vp[j] = __ldcg(P + kPlanPref + b);
       if (b < a.batch) {
         vl[j] = __ldcg(P + kPlanLen + b);
@@ -309,7 +318,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
     if (planned) {
 #pragma unroll
       for (int j = 0; j < kPer; ++j) {
-        const int b = tid + j * kMThreads;
+        const int b = tid + j * nthr;
         if (b <= a.batch) s_pref[b] = vp[j];
         if (b < a.batch) {
           s_len[b] = vl[j];
@@ -348,7 +357,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
   if (!use_tma) {
     Cursor<kMT> c;
     int at = -1;
-    for (int e = tid; e < kLA * kMT; e += kMThreads) {
+    for (int e = tid; e < kLA * kMT; e += blockDim.x) {
       const int tile = e / kMT, r = e - tile * kMT;
       if (at < 0) {
         c.start(ws, pl);
@@ -368,18 +377,23 @@ __global__ void __launch_bounds__(kMThreads, 2)
     __syncthreads();
   }
 
-  if (warp == kCW) {
-    // ------------------------------------------------------- producer ----
-    // pc walks the tiles to issue.  The index entries of the first kLA tiles
-    // are fetched at once, lane-strided, with 4-byte cp.async copies (each
-    // lane walks a copy of pc to its entry's tile); pf then runs kLA tiles
-    // ahead and fetches later entries the same way into the ring, one commit
-    // group per tile issued at iteration k for tile k + kLA, so no register
-    // ever waits on an index load: at iteration k, tile k's entries are
-    // complete once at most kLA - 1 newer groups pend.  TMA path: entries
+  if (warp >= kCW) {
+    // ------------------------------------------------------ producers ----
+    // nprod warps issue the tiles round-robin: producer pw issues the tiles
+    // k with k % nprod == pw, so the issue work of the gathers
+    // (one cp.async per 16 bytes) is split over two warps.  Each producer
+    // walks all the tiles with its cursor pc.  The index entries of the
+    // first kLA tiles are fetched at once, lane-strided, with 4-byte cp.async
+    // copies (each lane walks a copy of pc to its entry's tile); pf then runs
+    // kLA tiles ahead and fetches later entries the same way into the ring,
+    // one commit group per own tile issued at iteration k for tile k + kLA
+    // (the same producer's: kLA is a multiple of nprod), so no register ever
+    // waits on an index load: at iteration k, tile k's entries are complete
+    // once at most kLA / nprod - 1 newer groups pend.  TMA path: entries
     // 0..3 of a ring slot are the page ids of the tile's 16-token pieces;
     // gather path: entries 0..63 are the slots / page ids of its rows; -1
     // where there is none.
+    const int pw = warp - kCW;
     Cursor<kMT> pc;
     pc.start(ws, pl);
     if (use_tma && !planned) {
@@ -388,6 +402,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
       int at = 0;
       for (int e = lane; e < kLA * per; e += 32) {
         const int tile = e / per, r = e - tile * per;
+        if ((tile & (nprod - 1)) != pw) continue;  // the other producer's tile
         c.advance_by(ws, pl, tile - at);
         at = tile;
         int *dst = &s_idx[tile][r];
@@ -413,8 +428,14 @@ __global__ void __launch_bounds__(kMThreads, 2)
     __syncwarp();
     int pf_u = -1;
     ReqIndex pf_ri{0, false};
-    auto prefetch = [&](int slot) {  // entries of the tile under pf into s_idx[slot]
+    // entries of the tile under pf into s_idx[slot] when it is this
+    // producer's (mine), then pf moves on
+    auto prefetch = [&](int slot, bool mine) {
       const Unit &fu = pf.it.un;
+      if (!mine) {
+        if (!pf.done) pf.advance(ws, pl);
+        return;
+      }
       if (!pf.done && fu.u != pf_u) {
         pf_ri = pl.pref ? req_index_cached(ws, s_base, fu.b) : req_index(ws, fu.b);
         pf_u = fu.u;
@@ -442,6 +463,12 @@ __global__ void __launch_bounds__(kMThreads, 2)
     bool waited = !early;
     if (waited) pdl_trigger();
     while (!pc.done) {
+      if ((k & (nprod - 1)) != pw) {  // the other producer's tile
+        pc.advance(ws, pl);
+        prefetch(k % kLA, false);
+        ++k;
+        continue;
+      }
       const int s = k % kMStages;
       const int r = k / kMStages;
       if (r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1)) {
@@ -461,7 +488,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
         waited = true;
       }
       append_if_newest<D>(a, un, tile0, lane);
-      asm volatile("cp.async.wait_group %0;" ::"n"(kLA - 1) : "memory");
+      asm volatile("cp.async.wait_group %0;" ::"n"(kLA / nprod - 1) : "memory");
       const int slot = k % kLA;
       // TMA: lanes j and j + 4 both need piece j's page id
       const int cur[2] = {s_idx[slot][use_tma ? (lane & 3) : lane], s_idx[slot][lane + 32]};
@@ -479,7 +506,7 @@ __global__ void __launch_bounds__(kMThreads, 2)
         if (lane == 0) mbar_arrive(&full[s]);
       }
       pc.advance(ws, pl);
-      prefetch(slot);  // tile k + kLA reuses the slot just read
+      prefetch(slot, true);  // tile k + kLA reuses the slot just read
       ++k;
     }
     if (aborted) {
@@ -487,9 +514,11 @@ __global__ void __launch_bounds__(kMThreads, 2)
         *s_abort = 1;
         atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
       }
-      // Drain: the last (up to kMStages) issued tiles may still be landing.
+      // Drain: this producer's tiles among the last kMStages may still be
+      // landing.
       for (int kk = max(0, k - kMStages); kk < k; ++kk)
-        mbar_wait_bounded(&full[kk % kMStages], (kk / kMStages) & 1);
+        if ((kk & (nprod - 1)) == pw)
+          mbar_wait_bounded(&full[kk % kMStages], (kk / kMStages) & 1);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // index copies still in flight
     return;
@@ -904,7 +933,6 @@ struct MmaShape {
 template <int D, int G>
 cudaError_t mma_shape(const DecodeArgs &a, MmaShape *sh) {
   using C = MCfg<D, G>;
-  auto kern = decode_mma_kernel<D, G>;
   static int occ_cache[64] = {0};
   static int sms_cache[64] = {0};
   int dev = 0;
@@ -912,11 +940,19 @@ cudaError_t mma_shape(const DecodeArgs &a, MmaShape *sh) {
   if (e != cudaSuccess) return e;
   const int di = dev & 63;
   if (occ_cache[di] == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    // both producer paths: a launch may fall back from TMA to the gathers
+    auto kt = decode_mma_kernel<D, G, true>;
+    auto kg = decode_mma_kernel<D, G, false>;
+    e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    int occ = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kMThreads, C::SMEM);
+    e = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    int occ = 0, occ_g = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kt, kMMinThreads, C::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_g, kg, kMThreads, C::SMEM);
+    if (e != cudaSuccess) return e;
+    occ = occ < occ_g ? occ : occ_g;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     sms_cache[di] = sms;
@@ -953,9 +989,11 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
     use_tma = encode_pool_map(&tmk, ws.k_pool, ws) && encode_pool_map(&tmv, ws.v_pool, ws);
   DecodeArgs args = a;
   args.apportion = sh.apportion;
+  // The gathers issue one copy per 16 bytes: two producer warps share them.
+  static_assert(kMaxProducers == 2, "producers take tiles by the low bits of the tile index");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sh.grid);
-  cfg.blockDim = dim3(kMThreads);
+  cfg.blockDim = dim3(use_tma ? kMMinThreads : kMThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -963,7 +1001,8 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, G>, args, tmk, tmv, use_tma);
+  if (use_tma) return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, G, true>, args, tmk, tmv);
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, G, false>, args, tmk, tmv);
 }
 
 // The step's plan (see pkv_plan_step): the compact plan every decode block
