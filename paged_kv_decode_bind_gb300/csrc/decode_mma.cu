@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
   __shared__ int flags[kMStages][4];  // per stage: error bits of the tile's four pieces
   __shared__ volatile int s_ctrl[2];  // abort flag, merge ticket
   __shared__ float s_ml[kCW * 16 * 2];
+  __shared__ float s_hml[16][2];  // (M, L) of each query head of the unit's group
   __shared__ int s_bad[kCW];
   __shared__ int s_pref[kMaxCompactBatch + 1];
   __shared__ int s_len[kMaxCompactBatch];
@@ -737,7 +738,6 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
       }
     if (lane == 0) s_bad[warp] = bad;
     named_sync(1, kCW * 32);
-    float Mh[C::NH][2], Lh[C::NH][2];
 #pragma unroll
     for (int n = 0; n < C::NH; ++n)
 #pragma unroll
@@ -752,8 +752,10 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
           const float mw = s_ml[(w * 16 + h) * 2];
           L += mw == -INFINITY ? 0.f : exp2f(mw - M) * s_ml[(w * 16 + h) * 2 + 1];
         }
-        Mh[n][e] = M;
-        Lh[n][e] = L;
+        if (warp == 0 && grp == 0 && h < G) {  // lanes 0-3 of warp 0 hold every head once
+          s_hml[h][0] = M;
+          s_hml[h][1] = L;
+        }
         const float f = m_run[n][e] == -INFINITY ? 0.f : exp2f(m_run[n][e] - M);
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
@@ -805,23 +807,10 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
 
     // ---- write: final row, or a partial (and maybe merge them all) ----
     const bool final_out = direct || (fused && n_b == 1);
-    // (M, L) of query head h of the group from the warps' states
-    auto head_ml = [&](int h, float &M, float &L) {
-      M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kCW; ++w) M = fmaxf(M, s_ml[(w * 16 + h) * 2]);
-      L = 0.f;
-#pragma unroll
-      for (int w = 0; w < kCW; ++w) {
-        const float mw = s_ml[(w * 16 + h) * 2];
-        L += mw == -INFINITY ? 0.f : exp2f(mw - M) * s_ml[(w * 16 + h) * 2 + 1];
-      }
-    };
 #pragma unroll
     for (int i = tid * 4; i < G * D; i += kCW * 32 * 4) {
       const int h = i / D, d = i - h * D;
-      float M, L;
-      head_ml(h, M, L);
+      const float L = s_hml[h][1];
       const bool empty_out = unit_bad || !(L > 0.f);
       const float inv = empty_out ? 0.f : 1.f / L;
       const float4 x0 = *reinterpret_cast<const float4 *>(red + h * C::RSTRIDE + d);
@@ -846,8 +835,7 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
       }
     }
     if (tid < G) {
-      float M, L;
-      head_ml(tid, M, L);
+      const float M = s_hml[tid][0], L = s_hml[tid][1];
       const bool empty_out = unit_bad || !(L > 0.f);
       const long long qrow = (long long)un.b * Hq + hq0 + tid;
       if (final_out) {
