@@ -204,7 +204,9 @@ int pkv_choose_splits(const pkv_workspace *ws, int batch, int max_seq_len_hint,
  *   share = max(ceil(Hkv * total_tokens_hint / (2 * num_sms)), 128)
  *   S     = min(3 + (max_seq_len_hint - 1) / share, max_splits).
  * total_tokens_hint <= 0 means batch * max_seq_len_hint.  Returns 1 for
- * non-positive batch, length or SM count, or max_splits < 2.
+ * non-positive batch, length or SM count, for max_splits < 2, and for
+ * max_seq_len_hint <= 256 (four 64-token tiles: the merge of a split costs
+ * more than the streaming it saves).
  */
 int pkv_choose_pieces(const pkv_workspace *ws, int batch, int max_seq_len_hint,
                       long long total_tokens_hint, int num_sms);

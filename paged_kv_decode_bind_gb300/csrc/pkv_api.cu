@@ -146,6 +146,8 @@ int pkv_choose_pieces(const pkv_workspace *ws, int batch, int max_seq_len_hint,
       ws->max_splits < 2)
     return 1;
   const long long L = max_seq_len_hint;
+  // Four tiles or fewer: a split saves less streaming than its merge costs.
+  if (L <= 256) return 1;
   const long long total = total_tokens_hint > 0 ? total_tokens_hint : (long long)batch * L;
   const long long blocks = 2ll * num_sms;  // resident blocks of the tensor-core kernel
   long long share = (ws->n_kv_heads * total + blocks - 1) / blocks;

@@ -138,8 +138,11 @@ def test_choose_pieces():
     assert P.pkv_choose_pieces(ws, 16, 8192, 14500, 152) == 24
     # share = ceil(8 * 6500 / 304) = 172 -> 3 + 2047 // 172
     assert P.pkv_choose_pieces(ws, 4, 2048, 6500, 152) == 14
-    # tiny: the share floor of 128 tokens
-    assert P.pkv_choose_pieces(ws, 1, 100, 100, 152) == 3
+    # the share floor of 128 tokens
+    assert P.pkv_choose_pieces(ws, 1, 300, 300, 152) == 5
+    # four tiles or fewer: no split
+    assert P.pkv_choose_pieces(ws, 1, 256, 256, 152) == 1
+    assert P.pkv_choose_pieces(ws, 64, 192, 64 * 192, 152) == 1
     assert P.pkv_choose_pieces(_ws(max_splits=4), 1, 65536, 65536, 152) == 4
     assert P.pkv_choose_pieces(_ws(max_splits=1), 1, 65536, 65536, 152) == 1
     assert P.pkv_choose_pieces(ws, 0, 10, 10, 152) == 1
