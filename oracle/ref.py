@@ -20,7 +20,9 @@ Readings taken where the pages are silent:
   * split partials hold the normalised partial output and (m, l) in natural
     log units; splits are contiguous token ranges of one common length that
     is a multiple of the split granularity; an empty split has m = -inf,
-    l = 0 and is skipped by the merge.
+    l = 0 and is skipped by the merge;
+  * extend (prefill) attention is causal: a request's n new tokens are the
+    last n of its context and each attends to its own position and earlier.
 
 Everything is written out as loops over requests, heads and tokens; numpy
 only supplies elementwise exp / log, sums and dot products.
@@ -281,6 +283,62 @@ def merge_partials(o_part, ml_part):
             out[b, h], lse[b, h] = merge(list(ml_part[b, h, :, 0]), list(ml_part[b, h, :, 1]),
                                          list(o_part[b, h]))
     return out, lse
+
+
+# ---------------------------------------------------------------------------
+# Extend (prefill) attention: the step before decode, whose per-request query
+# offsets qo_indptr the workspace holds (workspace.py page, bullet 19).  The
+# pages give no formula; reading: the standard causal prefill.  Request b holds
+# L_b tokens in the pool, the last n_b of them new; new token i sits at
+# position L_b - n_b + i and attends tokens 0 .. L_b - n_b + i.
+# ---------------------------------------------------------------------------
+
+def extend_positions(seq_len, n_new):
+    """Positions of a request's n_new newest tokens in its context of
+    seq_len tokens."""
+    return [seq_len - n_new + i for i in range(n_new)]
+
+
+def extend_attention(q_bits, k_pool_bits, v_pool_bits, layer, slots_per_req, qo_lens, scale,
+                     n_kv_heads, rows=None):
+    """Causal attention of each request's new tokens over its context.
+
+    q_bits: uint16 (sum n_b, Hq, D), the new tokens' queries in request
+    order; slots_per_req[b]: physical slots of tokens 0..L_b-1 (new ones
+    included); qo_lens[b] = n_b.  ``rows``: optional list of (query row, h)
+    to compute (others stay 0).  Returns o (sum n_b, Hq, D) float64 and lse
+    (sum n_b, Hq)."""
+    q = bf16_bits_to_f64(q_bits)
+    T, Hq, D = q.shape
+    scale = float(np.float32(scale))
+    o = np.zeros((T, Hq, D))
+    lse = np.full((T, Hq), -math.inf)
+    owner = []  # query row -> (request, position)
+    for b, n in enumerate(qo_lens):
+        for pos in extend_positions(len(slots_per_req[b]), int(n)):
+            owner.append((b, pos))
+    assert len(owner) == T, "q rows do not match the new-token counts"
+    want = rows if rows is not None else [(r, h) for r in range(T) for h in range(Hq)]
+    for r, h in want:
+        b, pos = owner[r]
+        g = kv_head_of(h, Hq, n_kv_heads)
+        sl = np.asarray(slots_per_req[b][:pos + 1], dtype=np.int64)
+        K = bf16_bits_to_f64(k_pool_bits[layer, sl, g]) if sl.size else np.zeros((0, D))
+        V = bf16_bits_to_f64(v_pool_bits[layer, sl, g]) if sl.size else np.zeros((0, D))
+        o[r, h], lse[r, h] = attend(q[r, h], K, V, scale)
+    return o, lse
+
+
+def extend_append(pool_bits, layer, slots_per_req, qo_lens, new_bits):
+    """Extend append: the new tokens' rows (new_bits (sum n_b, Hkv, D), in
+    request order) go to the slots of the last n_b positions of each request."""
+    out = pool_bits.copy()
+    r = 0
+    for b, n in enumerate(qo_lens):
+        for pos in extend_positions(len(slots_per_req[b]), int(n)):
+            out[layer, slots_per_req[b][pos]] = new_bits[r]
+            r += 1
+    return out
 
 
 # ---------------------------------------------------------------------------

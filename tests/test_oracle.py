@@ -303,6 +303,119 @@ def pin_bf16_decode():
     assert list(v) == [1.0, -2.0, 0.5, 2.0 ** -133]
 
 
+def _extend_case(seed=11, B=3, Hq=4, Hkv=2, D=8, P=4, lens=(6, 3, 9), qo=(2, 3, 4), NL=2):
+    p = W.make_problem("tiny_extend", batch=B, n_layers=NL, n_q_heads=Hq, n_kv_heads=Hkv,
+                       head_dim=D, page_size=P, seq_lens=list(lens), seed=seed)
+    slots = [R.token_slots(b, int(p.seq_lens[b]), page_table=p.page_table.numpy(),
+                           req_pool_indices=p.req_pool_indices.numpy(), page_size=P)
+             for b in range(B)]
+    q = W.normal_bf16((sum(qo), Hq, D), seed + 200)
+    return p, slots, list(qo), q
+
+
+def pin_extend_one_new_token_is_decode():
+    # One new token per request: extend reduces to decode attention.
+    p, q, slots, layer = _tiny_problem()
+    kb, vb = R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool)
+    od, ld = R.decode_attention(R.tensor_bits(q), kb, vb, layer, slots, p.scale, p.n_kv_heads)
+    oe, le = R.extend_attention(R.tensor_bits(q), kb, vb, layer, slots, [1] * p.batch, p.scale,
+                                p.n_kv_heads)
+    assert np.array_equal(od, oe) and np.array_equal(ld, le)
+
+
+def pin_extend_dense_causal():
+    # Dense form: per request and head, S = Q K^T * scale with the positions
+    # past each query masked, row softmax, times V, as whole matrices.
+    p, slots, qo, q = _extend_case()
+    layer = 1
+    kb, vb = R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool)
+    o, lse = R.extend_attention(R.tensor_bits(q), kb, vb, layer, slots, qo, p.scale,
+                                p.n_kv_heads)
+    qf = q.to(torch.float64).numpy()
+    kf = p.k_pool.to(torch.float64).numpy()
+    vf = p.v_pool.to(torch.float64).numpy()
+    G = p.n_q_heads // p.n_kv_heads
+    scale = float(np.float32(p.scale))
+    r0 = 0
+    for b, n in enumerate(qo):
+        L = len(slots[b])
+        sl = np.asarray(slots[b])
+        for h in range(p.n_q_heads):
+            K, V = kf[layer, sl, h // G], vf[layer, sl, h // G]
+            Q = qf[r0:r0 + n, h]
+            S = (Q @ K.T) * scale
+            pos = np.arange(L - n, L)[:, None]
+            S = np.where(np.arange(L)[None, :] > pos, -np.inf, S)
+            Pm = np.exp(S - S.max(axis=1, keepdims=True))
+            ref = (Pm @ V) / Pm.sum(axis=1, keepdims=True)
+            assert np.allclose(o[r0:r0 + n, h], ref, rtol=0, atol=1e-12)
+            ref_lse = S.max(axis=1) + np.log(Pm.sum(axis=1))
+            assert np.allclose(lse[r0:r0 + n, h], ref_lse, rtol=0, atol=1e-12)
+        r0 += n
+
+
+def pin_extend_prefill_matches_sdpa():
+    # Whole-context prefill (every token new) equals the float64 library
+    # routine with its causal mask, K/V heads repeated for the groups.
+    p, slots, _, _ = _extend_case(lens=(5, 8, 3))
+    qo = [len(s) for s in slots]
+    q = W.normal_bf16((sum(qo), p.n_q_heads, p.head_dim), 321)
+    layer = 0
+    o, _ = R.extend_attention(R.tensor_bits(q), R.tensor_bits(p.k_pool),
+                              R.tensor_bits(p.v_pool), layer, slots, qo, p.scale,
+                              p.n_kv_heads)
+    G = p.n_q_heads // p.n_kv_heads
+    r0 = 0
+    for b, n in enumerate(qo):
+        sl = torch.tensor(slots[b])
+        K = p.k_pool[layer, sl].to(torch.float64).transpose(0, 1).repeat_interleave(G, 0)
+        V = p.v_pool[layer, sl].to(torch.float64).transpose(0, 1).repeat_interleave(G, 0)
+        Q = q[r0:r0 + n].to(torch.float64).transpose(0, 1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            Q, K, V, is_causal=True, scale=float(np.float32(p.scale)))
+        assert np.allclose(o[r0:r0 + n], ref.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
+        r0 += n
+
+
+def pin_extend_causality():
+    # A new token's output ignores rows after its position and depends on
+    # the row at its position.
+    p, slots, qo, q = _extend_case()
+    layer = 1
+    kb, vb = R.tensor_bits(p.k_pool).copy(), R.tensor_bits(p.v_pool).copy()
+    qb = R.tensor_bits(q)
+    o0, _ = R.extend_attention(qb, kb, vb, layer, slots, qo, p.scale, p.n_kv_heads)
+    b = 2  # L = 9, new tokens at positions 5..8 -> query rows 5..8
+    r_first = sum(qo[:b])
+    k2, v2 = kb.copy(), vb.copy()
+    for t in range(6, 9):  # after the first new token's position (5)
+        k2[layer, slots[b][t]] ^= np.uint16(0x4000)
+        v2[layer, slots[b][t]] ^= np.uint16(0x4000)
+    o1, _ = R.extend_attention(qb, k2, v2, layer, slots, qo, p.scale, p.n_kv_heads)
+    assert np.array_equal(o0[r_first], o1[r_first])
+    assert not np.allclose(o0[r_first + 1], o1[r_first + 1])
+    k3 = kb.copy()
+    k3[layer, slots[b][5]] ^= np.uint16(0x4000)
+    o2, _ = R.extend_attention(qb, k3, vb, layer, slots, qo, p.scale, p.n_kv_heads)
+    assert not np.allclose(o0[r_first], o2[r_first])
+
+
+def pin_extend_append():
+    p, slots, qo, _ = _extend_case()
+    kb = R.tensor_bits(p.k_pool)
+    new = np.arange(sum(qo) * p.n_kv_heads * p.head_dim, dtype=np.uint16).reshape(
+        sum(qo), p.n_kv_heads, p.head_dim)
+    out = R.extend_append(kb, 1, slots, qo, new)
+    changed = {(1, int(s)) for b, n in enumerate(qo) for s in slots[b][len(slots[b]) - n:]}
+    r = 0
+    for b, n in enumerate(qo):
+        for t in range(len(slots[b]) - n, len(slots[b])):
+            assert np.array_equal(out[1, slots[b][t]], new[r])
+            r += 1
+    diff = np.argwhere(np.any(out != kb, axis=(2, 3)))
+    assert {(int(a), int(c)) for a, c in diff} <= changed
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
@@ -355,6 +468,14 @@ def _mut_bf16(bits):
     return b.view(np.float32).astype(np.float64)
 
 
+def _mut_positions_late(seq_len, n_new):
+    return [min(seq_len - 1, seq_len - n_new + i + 1) for i in range(n_new)]
+
+
+def _mut_positions_all(seq_len, n_new):
+    return [seq_len - 1] * n_new
+
+
 _orig = {"attend": R.attend, "bind": R.bind}
 
 MUTATIONS = {
@@ -366,6 +487,8 @@ MUTATIONS = {
     "merge_without_max_shift": ("merge", _mut_merge_unweighted),
     "indptr_inclusive": ("bind", _mut_bind_inclusive),
     "bf16_shift": ("bf16_bits_to_f64", _mut_bf16),
+    "extend_position_shifted": ("extend_positions", _mut_positions_late),
+    "extend_not_causal": ("extend_positions", _mut_positions_all),
 }
 
 
