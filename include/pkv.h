@@ -321,6 +321,51 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
                                           int flags, pkv_stream_t stream);
 
 /*
+ * Paged extend (prefill) attention, the step before decode: each request's
+ * newest tokens attend causally over its cached context (the engine keeps
+ * the prefill step's qo_indptr in its workspace: workspace.py page, bullet
+ * 19; the causal rule is the standard prefill, which the pages do not
+ * spell out).
+ *   qo_indptr   device int32 [batch + 1]: request b's new tokens are query
+ *               rows qo_indptr[b] .. qo_indptr[b + 1] - 1.  They are the last
+ *               n_b = qo_indptr[b + 1] - qo_indptr[b] of its seq_lens[b]
+ *               tokens, whose K/V are already in the pool (pkv_extend_append);
+ *               new token i sits at position p = seq_lens[b] - n_b + i and
+ *               attends to positions 0 .. p (query head h reads KV head h / G).
+ *   max_qo_len  host upper bound on every n_b (sizes the grid).
+ *   q           device bf16 [qo_indptr[batch], Hq, D], 16-byte aligned.
+ *   out         device bf16 [qo_indptr[batch], Hq, D] (fp32 with
+ *               PKV_FLAG_OUT_F32), 16-byte aligned; the only buffer written.
+ *   flags       PKV_FLAG_OUT_F32 or 0.
+ * Reads seq_lens and either req_pool_indices + page_table (page mode) or
+ * kv_indptr + kv_indices (flat mode: bind with PKV_BIND_REBUILD first).
+ * Host errors: PKV_ERR_INVALID (null pointer, misalignment, batch < 0,
+ * max_qo_len < 0, another flag), PKV_ERR_CAPACITY (batch > max_batch, layer
+ * >= n_layers), PKV_ERR_UNSUPPORTED (head_dim not 64 / 128, or G not 1, 2,
+ * 4, 8, 16).  Device errors: PKV_DEVERR_LEN (n_b < 0, n_b > seq_lens[b],
+ * n_b > max_qo_len or a length out of range: that request's rows are not
+ * written), PKV_DEVERR_PAGE / _SLOT (a bad index entry: the affected rows are
+ * written as zeros), PKV_DEVERR_TIMEOUT.  Nothing is allocated; the call is
+ * asynchronous on `stream` and graph-capturable.
+ */
+pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
+                           const int32_t *qo_indptr, int max_qo_len, const void *q, void *out,
+                           float scale, int flags, pkv_stream_t stream);
+
+/*
+ * Extend append: the new tokens' K and V rows into the pool.  k_new, v_new:
+ * device bf16 [qo_indptr[batch], Hkv, D], 16-byte aligned; row
+ * qo_indptr[b] + i goes to layer `layer`, slot of position
+ * seq_lens[b] - n_b + i (page-table walk, or kv_indices in flat mode).
+ * Same request checks as pkv_extend_attn (PKV_DEVERR_LEN: the request is
+ * skipped); a bad page id or slot raises PKV_DEVERR_PAGE / _SLOT and that
+ * row is skipped.  Host errors as pkv_extend_attn.
+ */
+pkv_status pkv_extend_append(const pkv_workspace *ws, int batch, int layer,
+                             const int32_t *qo_indptr, int max_qo_len, const void *k_new,
+                             const void *v_new, pkv_stream_t stream);
+
+/*
  * Host steady-state test (cache.py page, bullets 1-4): non-zero when the
  * task ids are the same, in the same order, as at the last bind and every
  * length grew by exactly one, so a PKV_BIND_STEADY step is valid; zero means

@@ -27,6 +27,7 @@ EXPORTS = ("pkv_workspace_bytes", "pkv_bind_step", "pkv_choose_splits", "pkv_cho
            "pkv_decode_attn",
            "pkv_merge_partials", "pkv_decode_layer", "pkv_plan_step",
            "pkv_decode_attn_static_scratch",
+           "pkv_extend_attn", "pkv_extend_append",
            "pkv_is_steady_increment",
            "pkv_status_string", "pkv_version")
 PKV_STATIC_SCRATCH_BYTES = 8 << 20
@@ -90,6 +91,10 @@ def load(path: str = LIB_PATH):
     lib.pkv_plan_step.restype = i32
     lib.pkv_decode_attn_static_scratch.argtypes = [W, i32, i32, vp, f32, i32, i32, vp]
     lib.pkv_decode_attn_static_scratch.restype = i32
+    lib.pkv_extend_attn.argtypes = [W, i32, i32, vp, i32, vp, vp, f32, i32, vp]
+    lib.pkv_extend_attn.restype = i32
+    lib.pkv_extend_append.argtypes = [W, i32, i32, vp, i32, vp, vp, vp]
+    lib.pkv_extend_append.restype = i32
     p64, p32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
     lib.pkv_is_steady_increment.argtypes = [p64, p32, i32, p64, p32, i32]
     lib.pkv_is_steady_increment.restype = i32
@@ -197,6 +202,23 @@ def pkv_decode_attn_static_scratch(ws, batch, layer, q, scale, num_splits=1, fla
                                               float(scale), int(num_splits), int(flags),
                                               _stream(stream))
     return _check("pkv_decode_attn_static_scratch", s) if check else s
+
+
+def pkv_extend_attn(ws, batch, layer, qo_indptr, max_qo_len, q, out, scale, flags=0,
+                    stream=None, check=True):
+    """Causal extend attention of each request's newest tokens (device
+    qo_indptr int32 [batch + 1], q and out [total, Hq, D])."""
+    s = load().pkv_extend_attn(_ws(ws), int(batch), int(layer), _ptr(qo_indptr),
+                               int(max_qo_len), _ptr(q), _ptr(out), float(scale), int(flags),
+                               _stream(stream))
+    return _check("pkv_extend_attn", s) if check else s
+
+
+def pkv_extend_append(ws, batch, layer, qo_indptr, max_qo_len, k_new, v_new, stream=None,
+                      check=True):
+    s = load().pkv_extend_append(_ws(ws), int(batch), int(layer), _ptr(qo_indptr),
+                                 int(max_qo_len), _ptr(k_new), _ptr(v_new), _stream(stream))
+    return _check("pkv_extend_append", s) if check else s
 
 
 def pkv_is_steady_increment(prev_ids, prev_lens, ids, lens) -> bool:

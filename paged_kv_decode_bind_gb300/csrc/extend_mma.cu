@@ -1,0 +1,512 @@
+// Paged extend (prefill) attention on the tensor cores, and the append of the
+// new tokens' K/V.  The per-request query offsets qo_indptr are the ones the
+// engine keeps in its workspace for the prefill step (workspace.py page,
+// bullet 19).  Request b holds L_b tokens in the pool, the last n_b of them
+// new (qo_indptr[b + 1] - qo_indptr[b]); new token i sits at position
+// L_b - n_b + i and attends causally to tokens 0 .. L_b - n_b + i.
+//
+// Math.  A block computes 64 query rows of one (request, KV head): rows are
+// (new token, query head of the group) pairs, 64 / G tokens x G heads, so a
+// key tile is read once for the whole group.  Each of four consumer warps
+// owns 16 rows: S = Q K^T with warp-level bf16 mma.m16n8k16 (query rows on
+// the 16-row side, 8 keys per n-tile, fp32 accumulation), the causal mask
+// and an online softmax in fp32 (exp2), then O += P V with P entering as a
+// bf16 high part plus its bf16 remainder (~16 mantissa bits, as in the decode
+// kernel).  The accumulator fragment of S is the A fragment of P as it
+// stands, so no transpose is needed.
+//
+// Pipeline.  One producer warp gathers each 64-key tile's K and V rows with
+// 16-byte cp.async (any page size, page-table or flat indices) into 128-byte
+// swizzled rows of a 3-stage ring with full / empty mbarriers; the next
+// tile's index entries are loaded while the current tile's copies are
+// issued.  Every wait is bounded (~1 s) and raises PKV_DEVERR_TIMEOUT.
+//
+// Work.  Units are (request, KV head, query block j), visited in order of
+// decreasing j so that the longest causal ranges start first; a persistent
+// grid strides over them.  Invalid requests (n_b < 0, n_b > L_b,
+// n_b > max_qo_len, rows past qo_indptr[batch], L_b out of range) raise
+// PKV_DEVERR_LEN and get no output rows; a bad page id or flat slot raises its bit and writes the unit's rows
+// as zeros.
+#include "decode_plan.cuh"
+
+namespace pkv {
+
+cudaError_t launch_extend(const pkv_workspace &ws, int batch, int layer, const int *qo_indptr,
+                          int max_qo_len, const void *q, void *out, float scale, int flags,
+                          cudaStream_t st);
+cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
+                                 const int *qo_indptr, int max_qo_len, const void *k_new,
+                                 const void *v_new, cudaStream_t st);
+bool extend_supported(int head_dim, int group);
+
+namespace {
+
+constexpr int kXW = 4;                  // consumer warps
+constexpr int kXThreads = (kXW + 1) * 32;
+constexpr int kXT = 64;                 // keys per tile
+constexpr int kXRows = 16 * kXW;        // query rows per block
+constexpr int kXStages = 3;
+
+template <int D>
+struct XCfg {
+  static constexpr int HALF = kXT * 128;        // one 64-column half of a K (or V) tile
+  static constexpr int TILE = (D / 64) * HALF;  // K (or V) of a tile
+  static constexpr int STAGE = 2 * TILE;        // K then V
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int ND = D / 8;              // 8-column output tiles
+  static constexpr int SMEM = kXStages * STAGE + 1024;  // + alignment slack
+  static_assert(D % 64 == 0 && KSTEPS % 2 == 0, "whole swizzled halves, paired k-steps");
+};
+
+// Byte offset of 16-byte chunk ch (0 .. D/8 - 1) of key row t inside a K or
+// V tile: [half][row][128 B], chunk c of row r at c ^ (r & 7).
+template <int D>
+__device__ __forceinline__ uint32_t xoff(int t, int ch) {
+  return (uint32_t)((ch >> 3) * XCfg<D>::HALF + t * 128 + (((ch & 7) ^ (t & 7)) << 4));
+}
+
+__device__ __forceinline__ void xcp16(uint32_t dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+struct XArgs {
+  pkv_workspace ws;
+  int batch, layer, max_qo_len, flags;
+  const int *qo_indptr;
+  const void *q;
+  void *out;
+  float scale;
+};
+
+// One unit: request b's query block j for KV head g.
+struct XUnit {
+  int b, g, j;
+  int n;      // new tokens of the request
+  int L;      // its cached length (new tokens included)
+  int q0;     // qo_indptr[b]
+  int kend;   // keys 0 .. kend - 1 are read
+  bool live;  // valid request and a non-empty block
+};
+
+// Request b's new-token count and length, checked; raises PKV_DEVERR_LEN
+// (once per request, by the unit with g == 0 and j == 0).
+__device__ __forceinline__ XUnit xunit(const XArgs &a, int u, int tq, int jmax) {
+  const pkv_workspace &ws = a.ws;
+  const int bh = a.batch * ws.n_kv_heads;
+  XUnit x;
+  const int jj = u / bh, r = u - jj * bh;
+  x.b = r / ws.n_kv_heads;
+  x.g = r - x.b * ws.n_kv_heads;
+  x.j = jmax - 1 - jj;
+  x.q0 = a.qo_indptr[x.b];
+  x.n = a.qo_indptr[x.b + 1] - x.q0;
+  x.L = ws.seq_lens[x.b];
+  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  bool ok = x.n >= 0 && x.n <= x.L && x.n <= a.max_qo_len && x.q0 >= 0 &&
+            x.q0 + x.n <= a.qo_indptr[a.batch] && (long long)x.L <= cap;
+  if (ok && ws.index_mode == PKV_IDX_FLAT) {
+    const int base = ws.kv_indptr[x.b];
+    ok = base >= 0 && (long long)base + x.L <= ws.max_total_tokens;
+  }
+  if (!ok && x.g == 0 && x.j == 0 && (threadIdx.x & 31) == 0) atomicOr(ws.err, PKV_DEVERR_LEN);
+  x.live = ok && x.j * tq < x.n;
+  x.kend = x.live ? x.L - x.n + min(x.n, (x.j + 1) * tq) : 0;
+  return x;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kXThreads, 2)
+    extend_mma_kernel(const __grid_constant__ XArgs a) {
+  using C = XCfg<D>;
+  constexpr int TQ = kXRows / G;  // new tokens per block
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kXStages], empty[kXStages];
+  __shared__ int flags[kXStages];
+  __shared__ int s_slot[kXStages][kXT];
+  __shared__ volatile int s_abort;
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const pkv_workspace &ws = a.ws;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Hq = ws.n_q_heads;
+  const int jmax = (a.max_qo_len + TQ - 1) / TQ;
+  const int units = jmax * a.batch * ws.n_kv_heads;
+  if (tid == kXW * 32) {
+    for (int s = 0; s < kXStages; ++s) {
+      mbar_init(&full[s], 33);  // 32 copy-completion arrivals + the flag writer's
+      mbar_init(&empty[s], kXW);
+    }
+    s_abort = 0;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (tid == kXW * 32) fence_barrier_init();
+  __syncthreads();
+  const uint32_t ring = smem_addr(smem);
+
+  if (warp == kXW) {
+    // ------------------------------------------------------- producer ----
+    Plan pl;
+    pl.set_pages(ws);
+    constexpr int CH = D / 8;     // 16-byte chunks per row
+    constexpr int RPI = 32 / CH;  // rows per warp instruction
+    const int sub = lane / CH, ch = lane % CH;
+    const long long slot_elems = (long long)ws.n_kv_heads * D;
+    int k = 0;
+    bool aborted = false;
+    for (int u = blockIdx.x; u < units && !aborted; u += gridDim.x) {
+      const XUnit x = xunit(a, u, TQ, jmax);
+      if (!x.live) continue;
+      long long base = 0;
+      bool row_ok = true;
+      if (ws.index_mode == PKV_IDX_FLAT) {
+        base = ws.kv_indptr[x.b];
+      } else {
+        const int row = ws.req_pool_indices[x.b];
+        row_ok = row >= 0 && row < ws.max_reqs;
+        base = row_ok ? (long long)row * ws.max_pages_per_req : 0;
+      }
+      const int *idx = ws.index_mode == PKV_IDX_FLAT ? ws.kv_indices : ws.page_table;
+      auto raw_at = [&](int t) {
+        if (t >= x.kend || !row_ok) return -1;
+        return idx[base + (ws.index_mode == PKV_IDX_FLAT ? t : pl.page_of(t))];
+      };
+      const long long head0 = ((long long)a.layer * ws.pool_slots * ws.n_kv_heads + x.g) * D + ch * 8;
+      const uint16_t *kb = static_cast<const uint16_t *>(ws.k_pool) + head0;
+      const uint16_t *vb = static_cast<const uint16_t *>(ws.v_pool) + head0;
+      const int ntiles = (x.kend + kXT - 1) / kXT;
+      int raw[2] = {raw_at(lane), raw_at(lane + 32)};
+      for (int tile = 0; tile < ntiles; ++tile, ++k) {
+        const int s = k % kXStages, r = k / kXStages;
+        if ((r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1)) || s_abort) {
+          aborted = true;
+          break;
+        }
+        const int t0 = tile * kXT;
+        int kind = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = t0 + lane + 32 * h;
+          // a bad table row reads as raw -1: a page error
+          const int sl = t < x.kend ? (int)slot_from_raw(ws, pl, raw[h], t, kind) : -1;
+          s_slot[s][lane + 32 * h] = sl;
+        }
+        // the next tile's index entries load while this tile's copies issue
+        const int nx[2] = {raw_at(t0 + kXT + lane), raw_at(t0 + kXT + lane + 32)};
+        const int bad = __reduce_or_sync(0xffffffffu, kind);
+        if (lane == 0) {
+          flags[s] = bad;
+          if (bad) atomicOr(ws.err, bad);
+        }
+        __syncwarp();
+        const uint32_t kt = ring + s * C::STAGE, vt = kt + C::TILE;
+#pragma unroll 8
+        for (int i = 0; i < kXT / RPI; ++i) {
+          const int row = i * RPI + sub;
+          const int sl = s_slot[s][row];
+          const long long e = sl >= 0 ? sl * slot_elems : 0;
+          const uint32_t off = xoff<D>(row, ch);
+          xcp16(kt + off, kb + e, sl >= 0 ? 16 : 0);
+          xcp16(vt + off, vb + e, sl >= 0 ? 16 : 0);
+        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                         smem_addr(&full[s]))
+                     : "memory");
+        if (lane == 0) mbar_arrive(&full[s]);
+        raw[0] = nx[0];
+        raw[1] = nx[1];
+      }
+    }
+    if (aborted) {
+      if (lane == 0) {
+        s_abort = 1;
+        atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
+      }
+      for (int kk = max(0, k - kXStages); kk < k; ++kk)
+        mbar_wait_bounded(&full[kk % kXStages], (kk / kXStages) & 1);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+
+  // ---------------------------------------------------------- consumers ----
+  const int grp = lane >> 2, tig = lane & 3;
+  const float qk_scale = a.scale * kLog2e;
+  const int mi = lane >> 3, rr = lane & 7;
+  int k = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const XUnit x = xunit(a, u, TQ, jmax);
+    if (!x.live) continue;
+    // this lane's two rows (grp, grp + 8 of the warp's 16)
+    int pos[2], qrow[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int row = 16 * warp + grp + 8 * e;
+      const int i = x.j * TQ + row / G;
+      const bool valid = i < x.n;
+      pos[e] = valid ? x.L - x.n + i : -1;
+      qrow[e] = valid ? (x.q0 + i) * Hq + x.g * G + row % G : -1;
+    }
+    // the warp's last attended key: tiles past it are skipped
+    int wpos = max(pos[0], pos[1]);
+    wpos = __reduce_max_sync(0xffffffffu, wpos);
+    // Q as the A operand: qa[ks] = {Q[r0][c..], Q[r1][c..], Q[r0][c+8..], Q[r1][c+8..]},
+    // c = 16 ks + 2 tig
+    uint32_t qa[C::KSTEPS][4];
+    {
+      const uint32_t *q32 = static_cast<const uint32_t *>(a.q);
+#pragma unroll
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {
+        const int c2 = (16 * ks + 2 * tig) / 2;
+        qa[ks][0] = qrow[0] >= 0 ? q32[(long long)qrow[0] * (D / 2) + c2] : 0u;
+        qa[ks][1] = qrow[1] >= 0 ? q32[(long long)qrow[1] * (D / 2) + c2] : 0u;
+        qa[ks][2] = qrow[0] >= 0 ? q32[(long long)qrow[0] * (D / 2) + c2 + 4] : 0u;
+        qa[ks][3] = qrow[1] >= 0 ? q32[(long long)qrow[1] * (D / 2) + c2 + 4] : 0u;
+      }
+    }
+    float oacc[C::ND][4];
+#pragma unroll
+    for (int nd = 0; nd < C::ND; ++nd) oacc[nd][0] = oacc[nd][1] = oacc[nd][2] = oacc[nd][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    int bad = 0;
+    const int ntiles = (x.kend + kXT - 1) / kXT;
+    for (int tile = 0; tile < ntiles; ++tile, ++k) {
+      const int s = k % kXStages;
+      bool ok = false;
+      if (!s_abort) {
+        ok = mbar_wait_bounded(&full[s], (k / kXStages) & 1);
+        if (!ok && lane == 0) {
+          s_abort = 1;
+          atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
+        }
+      }
+      const int t0 = tile * kXT;
+      if (!ok) {
+        bad = 1;
+      } else if ((bad |= flags[s]) == 0 && t0 <= wpos) {
+        const uint32_t kt = ring + s * C::STAGE, vt = kt + C::TILE;
+        // ---- S = Q K^T: 8 n-tiles of 8 keys ----
+        float sc[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < C::KSTEPS; ks += 2) {
+#pragma unroll
+          for (int n = 0; n < 8; ++n) {
+            // matrices: keys 8n..8n+7 x dims of chunks 2ks + mi (k-steps ks, ks + 1)
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kt + xoff<D>(8 * n + rr, 2 * ks + mi), b0, b1, b2, b3);
+            mma_bf16_16816(sc[n], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+            mma_bf16_16816(sc[n], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2,
+                           b3);
+          }
+        }
+        // ---- causal mask, online softmax per row (log2 units) ----
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int e = c >> 1;
+            const int key = t0 + 8 * n + 2 * tig + (c & 1);
+            const float v = key <= pos[e] ? sc[n][c] * qk_scale : -INFINITY;
+            sc[n][c] = v;
+            mx[e] = fmaxf(mx[e], v);
+          }
+        float al[2], mref[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 1));
+          mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 2));
+          const float mn = fmaxf(m_run[e], mx[e]);
+          mref[e] = mn == -INFINITY ? 0.f : mn;  // a row with nothing attended yet
+          al[e] = exp2f(m_run[e] - mref[e]);
+          m_run[e] = mn;
+          l_run[e] *= al[e];
+        }
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float p = exp2f(sc[n][c] - mref[c >> 1]);
+            sc[n][c] = p;
+            l_run[c >> 1] += p;
+          }
+#pragma unroll
+        for (int nd = 0; nd < C::ND; ++nd) {
+          oacc[nd][0] *= al[0];
+          oacc[nd][1] *= al[0];
+          oacc[nd][2] *= al[1];
+          oacc[nd][3] *= al[1];
+        }
+        // ---- O += P V: 4 k-steps of 16 keys, P as bf16 high + remainder ----
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t ph[4], pr[4];
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            // f: (row grp, keys lo), (row grp+8, keys lo), (row grp, keys hi), (row grp+8, keys hi)
+            const float *src = sc[2 * kk + (f >> 1)] + 2 * (f & 1);
+            ph[f] = pack_bf16x2(src[0], src[1]);
+            pr[f] = pack_bf16x2(src[0] - bf16lo(ph[f]), src[1] - bf16hi(ph[f]));
+          }
+#pragma unroll
+          for (int nd = 0; nd < C::ND; nd += 2) {
+            // matrices: keys 16kk + 8 (mi & 1) .. + 7 x dims of chunk nd + (mi >> 1)
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vt + xoff<D>(16 * kk + 8 * (mi & 1) + rr, nd + (mi >> 1)), b0, b1, b2, b3);
+            mma_bf16_16816(oacc[nd], ph[0], ph[1], ph[2], ph[3], b0, b1);
+            mma_bf16_16816(oacc[nd], pr[0], pr[1], pr[2], pr[3], b0, b1);
+            mma_bf16_16816(oacc[nd + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+            mma_bf16_16816(oacc[nd + 1], pr[0], pr[1], pr[2], pr[3], b2, b3);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // ---- normalise and write this lane's rows ----
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float l = l_run[e];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if (qrow[e] < 0) continue;
+      const float inv = (bad || !(l > 0.f)) ? 0.f : 1.f / l;
+      const long long o = (long long)qrow[e] * D + 2 * tig;
+#pragma unroll
+      for (int nd = 0; nd < C::ND; ++nd) {
+        const float v0 = oacc[nd][2 * e] * inv, v1 = oacc[nd][2 * e + 1] * inv;
+        if (a.flags & PKV_FLAG_OUT_F32) {
+          *reinterpret_cast<float2 *>(static_cast<float *>(a.out) + o + 8 * nd) =
+              make_float2(v0, v1);
+        } else {
+          *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(a.out) + o + 8 * nd) =
+              pack_bf16x2(v0, v1);
+        }
+      }
+    }
+  }
+}
+
+// Append: block (x, b) copies new tokens x, x + gridDim.x, ... of request b
+// (K and V, every KV head) to the slots of their positions.
+__global__ void __launch_bounds__(128)
+    extend_append_kernel(const __grid_constant__ pkv_workspace ws, int layer,
+                         const int *qo_indptr, int max_qo_len, const uint4 *k_new,
+                         const uint4 *v_new) {
+  const int b = blockIdx.y;
+  const int q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0, L = ws.seq_lens[b];
+  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  bool ok = n >= 0 && n <= L && n <= max_qo_len && q0 >= 0 && q0 + n <= qo_indptr[gridDim.y] &&
+            (long long)L <= cap;
+  long long base = 0;
+  if (ok && ws.index_mode == PKV_IDX_FLAT) {
+    base = ws.kv_indptr[b];
+    ok = base >= 0 && base + L <= ws.max_total_tokens;
+  } else if (ok) {
+    const int row = ws.req_pool_indices[b];
+    ok = row >= 0 && row < ws.max_reqs;
+    base = ok ? (long long)row * ws.max_pages_per_req : 0;
+  }
+  if (!ok) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(ws.err, PKV_DEVERR_LEN);
+    return;
+  }
+  const int P = ws.page_size;
+  const int V16 = ws.n_kv_heads * ws.head_dim / 8;  // 16-byte vectors per token row
+  for (int i = blockIdx.x; i < n; i += gridDim.x) {
+    const int t = L - n + i;
+    long long slot;
+    if (ws.index_mode == PKV_IDX_FLAT) {
+      const int s = ws.kv_indices[base + t];
+      if (s < 0 || s >= ws.pool_slots) {
+        if (threadIdx.x == 0) atomicOr(ws.err, PKV_DEVERR_SLOT);
+        continue;
+      }
+      slot = s;
+    } else {
+      const int page = ws.page_table[base + t / P];
+      if (page < 0 || page >= ws.pool_slots / P) {
+        if (threadIdx.x == 0) atomicOr(ws.err, PKV_DEVERR_PAGE);
+        continue;
+      }
+      slot = (long long)page * P + t % P;
+    }
+    const long long src = (long long)(q0 + i) * V16;
+    const long long dst = ((long long)layer * ws.pool_slots + slot) * V16;
+    uint4 *kp = static_cast<uint4 *>(ws.k_pool);
+    uint4 *vp = static_cast<uint4 *>(ws.v_pool);
+    for (int v = threadIdx.x; v < V16; v += blockDim.x) {
+      kp[dst + v] = k_new[src + v];
+      vp[dst + v] = v_new[src + v];
+    }
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
+  using C = XCfg<D>;
+  static int occ_cache[64] = {0};
+  static int sms_cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int di = dev & 63;
+  if (occ_cache[di] == 0) {
+    e = cudaFuncSetAttribute(extend_mma_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM);
+    if (e != cudaSuccess) return e;
+    int occ = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, extend_mma_kernel<D, G>, kXThreads,
+                                                      C::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms_cache[di] = sms;
+    occ_cache[di] = occ > 0 ? occ : 1;
+  }
+  constexpr int TQ = kXRows / G;
+  const long long units =
+      (long long)((a.max_qo_len + TQ - 1) / TQ) * a.batch * a.ws.n_kv_heads;
+  if (units <= 0) return cudaSuccess;
+  if (units > 0x7fffffffll) return cudaErrorInvalidValue;
+  const long long cap = (long long)sms_cache[di] * occ_cache[di];
+  const int grid = (int)(units < cap ? units : cap);
+  extend_mma_kernel<D, G><<<grid, kXThreads, C::SMEM, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool extend_supported(int head_dim, int group) {
+  return (head_dim == 64 || head_dim == 128) &&
+         (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+}
+
+cudaError_t launch_extend(const pkv_workspace &ws, int batch, int layer, const int *qo_indptr,
+                          int max_qo_len, const void *q, void *out, float scale, int flags,
+                          cudaStream_t st) {
+  XArgs a{ws, batch, layer, max_qo_len, flags, qo_indptr, q, out, scale};
+  const int D = ws.head_dim, G = ws.n_q_heads / ws.n_kv_heads;
+#define PKV_X_CASE(DD, GG) \
+  if (D == DD && G == GG) return launch_extend_one<DD, GG>(a, st);
+  PKV_X_CASE(128, 1) PKV_X_CASE(128, 2) PKV_X_CASE(128, 4) PKV_X_CASE(128, 8)
+  PKV_X_CASE(128, 16) PKV_X_CASE(64, 1) PKV_X_CASE(64, 2) PKV_X_CASE(64, 4)
+  PKV_X_CASE(64, 8) PKV_X_CASE(64, 16)
+#undef PKV_X_CASE
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
+                                 const int *qo_indptr, int max_qo_len, const void *k_new,
+                                 const void *v_new, cudaStream_t st) {
+  if (batch <= 0 || max_qo_len <= 0) return cudaSuccess;
+  const dim3 grid((unsigned)min(max_qo_len, 64), (unsigned)batch);
+  extend_append_kernel<<<grid, 128, 0, st>>>(ws, layer, qo_indptr, max_qo_len,
+                                             static_cast<const uint4 *>(k_new),
+                                             static_cast<const uint4 *>(v_new));
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -7,6 +7,17 @@
 
 using namespace pkv;
 
+namespace pkv {
+// extend_mma.cu
+cudaError_t launch_extend(const pkv_workspace &ws, int batch, int layer, const int *qo_indptr,
+                          int max_qo_len, const void *q, void *out, float scale, int flags,
+                          cudaStream_t st);
+cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
+                                 const int *qo_indptr, int max_qo_len, const void *k_new,
+                                 const void *v_new, cudaStream_t st);
+bool extend_supported(int head_dim, int group);
+}  // namespace pkv
+
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -238,6 +249,44 @@ pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits
   if ((flags & PKV_FLAG_WRITE_LSE) && !ws->lse) return PKV_ERR_INVALID;
   return from_cuda(launch_merge(*ws, batch, num_splits, flags,
                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Checks shared by the two extend calls.
+static pkv_status extend_common(const pkv_workspace *ws, int batch, int layer,
+                                const int32_t *qo_indptr, int max_qo_len, const void *a,
+                                const void *b) {
+  pkv_status st = check_shape(ws);
+  if (st != PKV_OK) return st;
+  if ((st = check_index(ws)) != PKV_OK) return st;
+  if (batch < 0 || layer < 0 || max_qo_len < 0) return PKV_ERR_INVALID;
+  if (batch > ws->max_batch || layer >= ws->n_layers) return PKV_ERR_CAPACITY;
+  if (!extend_supported(ws->head_dim, ws->n_q_heads / ws->n_kv_heads))
+    return PKV_ERR_UNSUPPORTED;
+  if (!qo_indptr || !a || !b || !ws->k_pool || !ws->v_pool) return PKV_ERR_INVALID;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(ws->k_pool) || !aligned16(ws->v_pool))
+    return PKV_ERR_INVALID;
+  return PKV_OK;
+}
+
+pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
+                           const int32_t *qo_indptr, int max_qo_len, const void *q, void *out,
+                           float scale, int flags, pkv_stream_t stream) {
+  pkv_status st = extend_common(ws, batch, layer, qo_indptr, max_qo_len, q, out);
+  if (st != PKV_OK) return st;
+  if (flags & ~PKV_FLAG_OUT_F32) return PKV_ERR_INVALID;
+  if (batch == 0 || max_qo_len == 0) return PKV_OK;
+  return from_cuda(launch_extend(*ws, batch, layer, qo_indptr, max_qo_len, q, out, scale, flags,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_extend_append(const pkv_workspace *ws, int batch, int layer,
+                             const int32_t *qo_indptr, int max_qo_len, const void *k_new,
+                             const void *v_new, pkv_stream_t stream) {
+  pkv_status st = extend_common(ws, batch, layer, qo_indptr, max_qo_len, k_new, v_new);
+  if (st != PKV_OK) return st;
+  if (batch == 0 || max_qo_len == 0) return PKV_OK;
+  return from_cuda(launch_extend_append(*ws, batch, layer, qo_indptr, max_qo_len, k_new, v_new,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int pkv_is_steady_increment(const int64_t *prev_ids, const int32_t *prev_lens, int n_prev,

@@ -112,6 +112,32 @@ def test_bind_and_merge_host_validation():
     assert P.pkv_decode_layer(ws, 0, 0, f, f, f, 0.1, 2, 0, 0, check=False) == P.PKV_OK
 
 
+def test_extend_host_validation():
+    # Every case fails (or no-ops) on the host: nothing is launched.
+    f = 1 << 20
+    X = P.pkv_extend_attn
+    cases = [
+        (dict(n_q_heads=24, n_kv_heads=2), 1, 0, f, 4, f, f, 0, P.PKV_ERR_UNSUPPORTED),  # G = 12
+        (dict(head_dim=96), 1, 0, f, 4, f, f, 0, P.PKV_ERR_UNSUPPORTED),
+        (dict(), 5, 0, f, 4, f, f, 0, P.PKV_ERR_CAPACITY),                           # batch
+        (dict(), 1, 2, f, 4, f, f, 0, P.PKV_ERR_CAPACITY),                           # layer
+        (dict(), 1, 0, None, 4, f, f, 0, P.PKV_ERR_INVALID),                         # qo_indptr
+        (dict(), 1, 0, f, 4, None, f, 0, P.PKV_ERR_INVALID),                         # q
+        (dict(), 1, 0, f, 4, f + 8, f, 0, P.PKV_ERR_INVALID),                        # misaligned
+        (dict(), 1, 0, f, -1, f, f, 0, P.PKV_ERR_INVALID),                           # max_qo_len
+        (dict(), 1, 0, f, 4, f, f, P.PKV_FLAG_WRITE_LSE, P.PKV_ERR_INVALID),         # flag
+        (dict(), 0, 0, f, 4, f, f, 0, P.PKV_OK),                                     # no batch
+        (dict(), 1, 0, f, 0, f, f, 0, P.PKV_OK),                                     # no tokens
+    ]
+    for kw, batch, layer, qo, mq, q, out, flags, status in cases:
+        got = X(_ws(**kw), batch, layer, qo, mq, q, out, 0.1, flags, 0, check=False)
+        assert got == status, (kw, batch, layer, mq, flags, got, status)
+    A = P.pkv_extend_append
+    assert A(_ws(), 1, 0, f, 4, f, None, 0, check=False) == P.PKV_ERR_INVALID
+    assert A(_ws(), 5, 0, f, 4, f, f, 0, check=False) == P.PKV_ERR_CAPACITY
+    assert A(_ws(), 1, 0, f, 0, f, f, 0, check=False) == P.PKV_OK
+
+
 def test_choose_splits():
     ws = _ws(max_splits=128, n_kv_heads=8, n_q_heads=32)
     # one 65536-token request: 38 splits x 8 heads = 304 units, one per

@@ -1,0 +1,163 @@
+"""GPU parity of the paged extend (prefill) path: pkv_extend_append against
+the oracle's append (bit-exact pool rows) and pkv_extend_attn against the
+oracle's causal extend attention (max |err| <= 1e-2 and normwise <= 2e-2),
+over page-table and flat indices, every group size the kernel has, ragged
+new-token counts (0, 1, a partial query block, whole-context prefill), and
+the device error paths.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle.ref as R
+import pkv_inputs as W
+from paged_kv_decode_bind_gb300 import Workspace
+from paged_kv_decode_bind_gb300 import _abi as A
+
+from parity import check_attention
+
+pytestmark = pytest.mark.gpu
+
+
+def _slots(p):
+    table, rows = p.page_table.numpy(), p.req_pool_indices.numpy()
+    return [R.token_slots(b, int(p.seq_lens[b]), page_table=table, req_pool_indices=rows,
+                          page_size=p.page_size) for b in range(p.batch)]
+
+
+def _indptr(qo, device):
+    return torch.tensor(np.concatenate([[0], np.cumsum(qo)]).astype(np.int32), device=device)
+
+
+def run_extend(cuda, *, lens, qo, Hq, Hkv, D, P, seed, NL=2, layer=1, flags=0, rows=None,
+               max_qo=None, table_edit=None, expect_err=0, check_pool=True):
+    """Append + extend attention through libpkv and the oracle; returns the
+    GPU output (float64 numpy) and the oracle's."""
+    p = W.make_problem("extend", batch=len(lens), n_layers=NL, n_q_heads=Hq, n_kv_heads=Hkv,
+                       head_dim=D, page_size=P, seq_lens=list(lens), seed=seed)
+    if table_edit:
+        table_edit(p)
+    ws = Workspace.from_problem(p)
+    B, T = p.batch, int(sum(qo))
+    q = W.normal_bf16((T, Hq, D), seed + 500)
+    kn = W.normal_bf16((T, Hkv, D), seed + 501)
+    vn = W.normal_bf16((T, Hkv, D), seed + 502)
+    if P == 1:
+        A.pkv_bind_step(ws, B, A.PKV_BIND_REBUILD)  # kv_indptr and kv_indices
+    qo_dev = _indptr(qo, cuda)
+    out_dtype = torch.float32 if flags & A.PKV_FLAG_OUT_F32 else torch.bfloat16
+    out = torch.full((T, Hq, D), 7.0, dtype=out_dtype, device=cuda)  # sentinel
+    mq = max(qo) if max_qo is None else max_qo
+    A.pkv_extend_append(ws, B, layer, qo_dev, mq, kn.to(cuda), vn.to(cuda))
+    A.pkv_extend_attn(ws, B, layer, qo_dev, mq, q.to(cuda), out, p.scale, flags)
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) == expect_err
+    slots = _slots(p)
+    ok_req = [0 <= qo[b] <= lens[b] and qo[b] <= mq for b in range(B)]
+    app_qo = [qo[b] if ok_req[b] else 0 for b in range(B)]
+    # the oracle appends only for valid requests; rows of the others are skipped
+    kb, vb = R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool)
+    kb = R.extend_append(kb, layer, slots, app_qo, _rows_of(kn, qo, ok_req))
+    vb = R.extend_append(vb, layer, slots, app_qo, _rows_of(vn, qo, ok_req))
+    if check_pool:
+        assert np.array_equal(R.tensor_bits(ws.k_pool.cpu()), kb), "K pool differs"
+        assert np.array_equal(R.tensor_bits(ws.v_pool.cpu()), vb), "V pool differs"
+    want = rows if rows is not None else [(r, h) for r in range(T) for h in range(Hq)]
+    ref, _ = R.extend_attention(R.tensor_bits(q), kb, vb, layer, slots, qo, p.scale, Hkv,
+                                rows=want)
+    got = out.to(torch.float64).cpu().numpy()
+    return got, ref, want, p
+
+
+def _rows_of(x, qo, ok_req):
+    """The new-token rows of the valid requests, in request order (bits)."""
+    bits = R.tensor_bits(x)
+    keep, r = [], 0
+    for b, n in enumerate(qo):
+        if ok_req[b]:
+            keep.extend(range(r, r + n))
+        r += n
+    return bits[keep] if keep else bits[:0]
+
+
+def _compare(got, ref, want, what):
+    g = np.stack([got[r, h] for r, h in want])
+    e = np.stack([ref[r, h] for r, h in want])
+    return check_attention(g, e, what)
+
+
+CASES = {
+    # name: (lens, qo, Hq, Hkv, D, P)
+    "paged_g4_d128": ((70, 200, 33), (5, 64, 33), 32, 8, 128, 16),
+    "paged_g1_d64_zero_and_one": ((90, 17, 40), (17, 1, 0), 4, 4, 64, 16),
+    "flat_g8_d128": ((150, 90, 1), (20, 9, 1), 16, 2, 128, 1),
+    "paged8_g16_d128": ((61, 100), (3, 5), 32, 2, 128, 8),
+    "prefill_g2_d64": ((37, 130), (37, 130), 8, 4, 64, 16),
+    "paged_g8_d64_partial_block": ((300, 129), (13, 129), 16, 2, 64, 16),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES), ids=list(CASES))
+def test_extend_parity(cuda, case):
+    lens, qo, Hq, Hkv, D, P = CASES[case]
+    got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=Hq, Hkv=Hkv, D=D, P=P, seed=4100)
+    _compare(got, ref, want, case)
+
+
+def test_extend_f32_output_one_new_token(cuda):
+    # One new token per request with fp32 output; the bf16 output is its
+    # round-to-nearest-even.
+    lens, qo = (45, 130, 8), (1, 1, 1)
+    got, ref, want, p = run_extend(cuda, lens=lens, qo=qo, Hq=32, Hkv=8, D=128, P=16, seed=4200,
+                                   flags=A.PKV_FLAG_OUT_F32)
+    _compare(got, ref, want, "f32")
+    gb, _, _, _ = run_extend(cuda, lens=lens, qo=qo, Hq=32, Hkv=8, D=128, P=16, seed=4200)
+    rb = torch.tensor(got).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(gb, rb)
+
+
+def test_extend_long_prefix_sampled(cuda):
+    # A 4096-token prefix with a 256-token chunk: many tiles per unit,
+    # compared on sampled rows.
+    rng = np.random.default_rng(3)
+    T = 256 + 64
+    rows = sorted({(int(rng.integers(T)), int(rng.integers(32))) for _ in range(40)}
+                  | {(0, 0), (T - 1, 31), (255, 5)})
+    got, ref, want, _ = run_extend(cuda, lens=(4096, 700), qo=(256, 64), Hq=32, Hkv=8, D=128,
+                                   P=16, seed=4300, NL=1, layer=0, rows=rows)
+    _compare(got, ref, want, "long prefix")
+
+
+def test_extend_invalid_request_is_skipped(cuda):
+    # Request 0 claims more new tokens than it holds: PKV_DEVERR_LEN, its rows
+    # keep the sentinel and nothing of it is appended; request 1 is exact.
+    lens, qo = (10, 40), (12, 6)
+    got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=8, Hkv=2, D=64, P=16, seed=4400,
+                                   expect_err=A.PKV_DEVERR_LEN,
+                                   rows=[(r, h) for r in range(12, 18) for h in range(8)])
+    assert np.all(got[:12] == 7.0)
+    _compare(got, ref, want, "valid request next to an invalid one")
+
+
+def test_extend_max_qo_len_too_small(cuda):
+    lens, qo = (50, 40), (9, 3)
+    got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=8, Hkv=2, D=64, P=16, seed=4500,
+                                   max_qo=4, expect_err=A.PKV_DEVERR_LEN,
+                                   rows=[(r, h) for r in range(9, 12) for h in range(8)])
+    assert np.all(got[:9] == 7.0)
+    _compare(got, ref, want, "request within max_qo_len")
+
+
+def test_extend_bad_page_zeroes_rows(cuda):
+    # Request 1's first page id is out of range: PKV_DEVERR_PAGE and its rows
+    # are zeros (every unit of it reads page 0); request 0 stays exact.
+    def edit(p):
+        row = int(p.req_pool_indices[1])
+        p.page_table[row, 0] = p.pool_slots // p.page_size  # one past the last page
+    lens, qo = (64, 80), (8, 8)
+    got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=8, Hkv=2, D=64, P=16, seed=4600,
+                                   table_edit=edit, expect_err=A.PKV_DEVERR_PAGE,
+                                   check_pool=False,
+                                   rows=[(r, h) for r in range(8) for h in range(8)])
+    assert np.all(got[8:] == 0.0)
+    _compare(got, ref, want, "request next to a bad page")
