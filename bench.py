@@ -248,6 +248,240 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- extend workloads --
+# Paged extend (prefill) attention: a step is, for every layer, the append of
+# the new tokens' K/V and the causal extend attention (two launches),
+# captured once as a CUDA graph.  Contraction-bound: reported in TFLOP/s
+# against the measured bf16 tensor peak.
+
+EXTEND_METRIC = ("paged extend attention µs/layer-step and achieved TFLOP/s "
+                 "(% of GB300 bf16 peak)")
+
+
+def extend_flops(lens, qo, p):
+    """Algorithmic FLOPs of one layer: 4 * D (scores and P V) per query head,
+    new token and attended key; new token i of a request of L tokens, n of
+    them new, attends L - n + i + 1 keys."""
+    pairs = sum(n * (L - n) + n * (n + 1) // 2 for L, n in zip(lens, qo))
+    return 4 * p.head_dim * p.n_q_heads * pairs
+
+
+def tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured (sustained)"
+    except Exception:
+        return 1700.0, "fallback (sustained)"
+
+
+def _extend_oracle_setup(name):
+    import oracle.ref as R
+    import pkv_inputs as W
+    p, qo = W.extend_workload(name, n_layers=1)
+    slots = [R.token_slots(b, int(p.seq_lens[b]), page_table=p.page_table.numpy(),
+                           req_pool_indices=p.req_pool_indices.numpy(), page_size=p.page_size)
+             for b in range(p.batch)]
+    q, _, _ = W.extend_inputs(p, qo, layers=1)
+    st = {"p": p, "qo": qo, "slots": slots, "qb": R.tensor_bits(q)[0],
+          "kb": R.tensor_bits(p.k_pool), "vb": R.tensor_bits(p.v_pool)}
+    owner = []
+    for b, n in enumerate(qo):
+        L = int(p.seq_lens[b])
+        owner += [L - n + i + 1 for i in range(n)]  # keys each query row attends
+    st["keys"] = owner
+    st["pairs"] = [(r, h) for r in range(len(owner)) for h in range(p.n_q_heads)]
+    return st
+
+
+def _extend_oracle_rows(st, rows):
+    """Oracle extend attention for the given (row, head) pairs; returns their
+    algorithmic FLOPs."""
+    import oracle.ref as R
+    p = st["p"]
+    R.extend_attention(st["qb"], st["kb"], st["vb"], 0, st["slots"], st["qo"], p.scale,
+                       p.n_kv_heads, rows=rows)
+    return sum(4 * p.head_dim * st["keys"][r] for r, _ in rows)
+
+
+def extend_cpu_worker(args):
+    st = _extend_oracle_setup(args.workload)
+    pairs = st["pairs"]
+    flops, n, i = 0.0, 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < args.cpu_seconds:
+        off = (i * 7919) % len(pairs)
+        chunk = (pairs[off:] + pairs[:off])[:8]
+        flops += _extend_oracle_rows(st, chunk)
+        n += len(chunk)
+        i += 1
+    dt = time.perf_counter() - t0
+    print(json.dumps({"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
+                      "kind": "oracle",
+                      "sample": f"{n} (new token, query head) attentions of one layer of "
+                                f"{args.workload}, {dt:.1f} s on 1 thread"}))
+
+
+def run_extend_reference(args, rank):
+    if rank != 0:
+        return
+    st = _extend_oracle_setup(args.workload)
+    pairs = st["pairs"]
+    t = time.perf_counter()
+    _extend_oracle_rows(st, pairs[:4])
+    per = max(1e-4, (time.perf_counter() - t) / 4)
+    n = int(max(1, min(len(pairs), 120.0 / max(1, args.steps + args.warmup) / per)))
+    for _ in range(args.warmup):
+        _extend_oracle_rows(st, pairs[:n])
+    done = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        off = (i * n) % len(pairs)
+        done += _extend_oracle_rows(st, (pairs[off:] + pairs[:off])[:n])
+    dt = time.perf_counter() - t0
+    v = done / dt / 1e12
+    p = st["p"]
+    line = {"impl": "reference", "metric": EXTEND_METRIC, "value": v, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": p.batch,
+                       "n_q_heads": p.n_q_heads, "n_kv_heads": p.n_kv_heads,
+                       "head_dim": p.head_dim, "page_size": p.page_size,
+                       "new_tokens": st["qo"], "seq_lens": p.seq_lens.tolist(),
+                       "timed": "one layer per step (the layers are alike)"},
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": v, "unit": "TFLOP/s",
+                             "sample": f"each step: {n} of {len(pairs)} (new token, head) "
+                                       f"attentions of one layer"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_extend_ours(args, rank, world, local_rank):
+    import itertools
+
+    import torch
+
+    import pkv_inputs as W
+    from paged_kv_decode_bind_gb300 import Workspace
+    from paged_kv_decode_bind_gb300 import _abi as A
+    from paged_kv_decode_bind_gb300 import dist as D
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    p, qo = W.extend_workload(args.workload, n_layers=args.layers,
+                              seed=D.rank_seed(20260100, rank))
+    B, NL, T = p.batch, p.n_layers, sum(qo)
+    lens = p.seq_lens.tolist()
+    ws = Workspace.from_problem(p, device=dev)
+    q, k, v = W.extend_inputs(p, qo)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty((NL, T, p.n_q_heads, p.head_dim), dtype=torch.bfloat16, device=dev)
+    qo_dev = torch.tensor([0] + list(itertools.accumulate(qo)), dtype=torch.int32, device=dev)
+    mq = max(qo)
+
+    def calls(s, attn_only):
+        for l in range(NL):
+            if not attn_only:
+                A.pkv_extend_append(ws, B, l, qo_dev, mq, kd[l], vd[l], s)
+            A.pkv_extend_attn(ws, B, l, qo_dev, mq, qd[l], out[l], p.scale, 0, s)
+
+    def capture(attn_only):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            calls(side, attn_only)  # warm launch outside the capture
+            with torch.cuda.graph(g, stream=side):
+                calls(side, attn_only)
+        torch.cuda.current_stream().wait_stream(side)
+        return g
+
+    step_g, attn_g = capture(False), capture(True)
+    torch.cuda.synchronize()
+
+    def timed(g, n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    for _ in range(args.warmup):
+        step_g.replay()
+    torch.cuda.synchronize()
+    K = args.steps
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    dt = timed(step_g, K)
+    clk = clocks.stop() if clocks else None
+    dt_attn = timed(attn_g, K)
+    flops = extend_flops(lens, qo, p)
+    # end to end through the C ABI: every step copies its inputs in from
+    # pinned host memory and the outputs back
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    s0 = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    ke = max(3, K // 8)
+    e0.record()
+    for _ in range(ke):
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        calls(s0, False)
+        outh.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    dte = e0.elapsed_time(e1) / 1e3
+    errbits = int(ws.err.item())
+    dt, total = D.reduce_time_and_work(dt, float(flops * NL * K), device=dev)
+    dte, _ = D.reduce_time_and_work(dte, 0.0, device=dev)
+    if rank != 0:
+        return
+    peak, src = tensor_peak()
+    layer_s = dt_attn / (K * NL)
+    ach = flops / layer_s / 1e12
+    line = {
+        "metric": EXTEND_METRIC, "value": total / dt / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": dt / K * 1e3,
+        "us_per_layer_step": dt / (K * NL) * 1e6, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": B, "n_layers": NL,
+                   "n_q_heads": p.n_q_heads, "n_kv_heads": p.n_kv_heads,
+                   "head_dim": p.head_dim, "page_size": p.page_size, "new_tokens": qo,
+                   "seq_lens": lens, "cuda_graph": True,
+                   "l2": "no flush: one step touches %.0f MB of KV, more than twice the 129 MB "
+                         "L2" % (sum(lens) * p.n_kv_heads * p.head_dim * 4 * NL / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                     "frac": ach / peak, "traffic": None, "peak_source": src,
+                     "kernel": "extend_mma_kernel (causal extend attention, one launch per "
+                               "layer)",
+                     "kernel_us_mean": layer_s * 1e6,
+                     "kernel_time_from": "graph of the layers' attention launches alone, CUDA "
+                                         "events over its timed replays / layers",
+                     "algorithmic_flops_per_launch": flops},
+        "gpu_launches": 2 * NL * K,
+        "clocks": clk,
+        "device_err_bits": errbits,
+        "e2e": {"value": flops * NL * ke / dte / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": (q.numel() + k.numel() + v.numel()) * 2,
+                "d2h_bytes_per_step": out.numel() * 2},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = run_cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------- GPU arm --
 
 def traffic_for(kernel_src_hash, workload, algorithmic_bytes):
@@ -504,8 +738,9 @@ def run_ours(args, rank, world, local_rank):
 
 def main(argv=None):
     args = parse_args(argv)
+    extend = args.workload.startswith("extend")
     if args.cpu_baseline_worker:
-        cpu_baseline_worker(args)
+        (extend_cpu_worker if extend else cpu_baseline_worker)(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -513,7 +748,7 @@ def main(argv=None):
     if args.impl == "reference":
         for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[v] = "1"
-        run_reference(args, rank)
+        (run_extend_reference if extend else run_reference)(args, rank)
         return
     if world > 1:
         import torch
@@ -521,7 +756,7 @@ def main(argv=None):
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        run_ours(args, rank, world, local_rank)
+        (run_extend_ours if extend else run_ours)(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

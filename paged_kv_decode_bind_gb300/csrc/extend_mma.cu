@@ -10,10 +10,11 @@
 // key tile is read once for the whole group.  Each of four consumer warps
 // owns 16 rows: S = Q K^T with warp-level bf16 mma.m16n8k16 (query rows on
 // the 16-row side, 8 keys per n-tile, fp32 accumulation), the causal mask
-// and an online softmax in fp32 (exp2), then O += P V with P entering as a
-// bf16 high part plus its bf16 remainder (~16 mantissa bits, as in the decode
-// kernel).  The accumulator fragment of S is the A fragment of P as it
-// stands, so no transpose is needed.
+// and an online softmax in fp32 (exp2), then O += P V with P rounded to bf16
+// (8 mantissa bits: each weight's rounding error is at most 2^-9 of it, far
+// inside the 1e-2 output tolerance; there are no splits to agree across).
+// The accumulator fragment of S is the A fragment of P as it stands, so no
+// transpose is needed.
 //
 // Pipeline.  One producer warp gathers each 64-key tile's K and V rows with
 // 16-byte cp.async (any page size, page-table or flat indices) into 128-byte
@@ -339,16 +340,15 @@ __global__ void __launch_bounds__(kXThreads, 2)
           oacc[nd][2] *= al[1];
           oacc[nd][3] *= al[1];
         }
-        // ---- O += P V: 4 k-steps of 16 keys, P as bf16 high + remainder ----
+        // ---- O += P V: 4 k-steps of 16 keys, P rounded to bf16 ----
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          uint32_t ph[4], pr[4];
+          uint32_t ph[4];
 #pragma unroll
           for (int f = 0; f < 4; ++f) {
             // f: (row grp, keys lo), (row grp+8, keys lo), (row grp, keys hi), (row grp+8, keys hi)
             const float *src = sc[2 * kk + (f >> 1)] + 2 * (f & 1);
             ph[f] = pack_bf16x2(src[0], src[1]);
-            pr[f] = pack_bf16x2(src[0] - bf16lo(ph[f]), src[1] - bf16hi(ph[f]));
           }
 #pragma unroll
           for (int nd = 0; nd < C::ND; nd += 2) {
@@ -356,9 +356,7 @@ __global__ void __launch_bounds__(kXThreads, 2)
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(vt + xoff<D>(16 * kk + 8 * (mi & 1) + rr, nd + (mi >> 1)), b0, b1, b2, b3);
             mma_bf16_16816(oacc[nd], ph[0], ph[1], ph[2], ph[3], b0, b1);
-            mma_bf16_16816(oacc[nd], pr[0], pr[1], pr[2], pr[3], b0, b1);
             mma_bf16_16816(oacc[nd + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
-            mma_bf16_16816(oacc[nd + 1], pr[0], pr[1], pr[2], pr[3], b2, b3);
           }
         }
       }

@@ -270,3 +270,41 @@ def workload(name: str, *, batch: int | None = None, n_layers: int | None = None
                             head_dim=128, page_size=16, seq_lens=lens, steps=steps,
                             seed=seed, fill_unused=fill_unused)
     raise KeyError(name)
+
+
+# --------------------------------------------------------------------------
+# Extend (prefill) workload: requests whose newest tokens are a chunk of new
+# positions on top of a cached prefix (the step before decode).
+# --------------------------------------------------------------------------
+
+EXTEND_WORKLOADS = ("extend_b4_chunk256",)
+
+
+def extend_workload(name: str, *, n_layers: int | None = None, shrink: int = 1,
+                    seed: int | None = None):
+    """extend_b4_chunk256: B=4, 24 layers, 32/8 heads, D=128, P=16, cached
+    prefixes ~ U{512..2048} (the paged decode workload's lengths) and 256 new
+    tokens per request; the pool holds prefix + new tokens.  Returns the
+    problem (its seq_lens count the new tokens) and the new-token counts.
+    ``shrink`` divides both lengths (and uses 2 layers)."""
+    if name != "extend_b4_chunk256":
+        raise KeyError(name)
+    seed = 20260100 if seed is None else seed
+    B, chunk = 4, max(1, 256 // shrink)
+    prefix = _uniform_lens(B, max(1, 512 // shrink), max(1, 2048 // shrink), _sub(seed, 0))
+    nl = n_layers or (24 if shrink == 1 else 2)
+    p = make_problem(name, batch=B, n_layers=nl, n_q_heads=32, n_kv_heads=8, head_dim=128,
+                     page_size=16, seq_lens=[x + chunk for x in prefix], seed=seed)
+    return p, [chunk] * B
+
+
+def extend_inputs(p: DecodeProblem, qo_lens, layers=None):
+    """Per-layer extend inputs: q [NL, T, Hq, D], k_new and v_new [NL, T, Hkv, D]
+    (bf16), T = sum of the new-token counts."""
+    NL = p.n_layers if layers is None else layers
+    T = int(sum(qo_lens))
+    s = _sub(p.seed, 40)
+    q = normal_bf16((NL, T, p.n_q_heads, p.head_dim), s)
+    k = normal_bf16((NL, T, p.n_kv_heads, p.head_dim), s + 1)
+    v = normal_bf16((NL, T, p.n_kv_heads, p.head_dim), s + 2)
+    return q, k, v
