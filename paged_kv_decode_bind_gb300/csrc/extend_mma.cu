@@ -28,6 +28,8 @@
 // n_b > max_qo_len, rows past qo_indptr[batch], L_b out of range) raise
 // PKV_DEVERR_LEN and get no output rows; a bad page id or flat slot raises its bit and writes the unit's rows
 // as zeros.
+#include <climits>
+
 #include "decode_plan.cuh"
 
 namespace pkv {
@@ -248,9 +250,13 @@ __global__ void __launch_bounds__(kXThreads, 2)
       pos[e] = valid ? x.L - x.n + i : -1;
       qrow[e] = valid ? (x.q0 + i) * Hq + x.g * G + row % G : -1;
     }
-    // the warp's last attended key: tiles past it are skipped
+    // the warp's last attended key (tiles past it are skipped) and the first
+    // valid row's position (tiles wholly before it need no mask; rows past
+    // the block's tokens, pos -1, are never written)
     int wpos = max(pos[0], pos[1]);
     wpos = __reduce_max_sync(0xffffffffu, wpos);
+    int wmin = min(pos[0] < 0 ? INT_MAX : pos[0], pos[1] < 0 ? INT_MAX : pos[1]);
+    wmin = __reduce_min_sync(0xffffffffu, wmin);
     // Q as the A operand: qa[ks] = {Q[r0][c..], Q[r1][c..], Q[r0][c+8..], Q[r1][c+8..]},
     // c = 16 ks + 2 tig
     uint32_t qa[C::KSTEPS][4];
@@ -304,16 +310,26 @@ __global__ void __launch_bounds__(kXThreads, 2)
         }
         // ---- causal mask, online softmax per row (log2 units) ----
         float mx[2] = {-INFINITY, -INFINITY};
+        if (t0 + kXT - 1 <= wmin) {  // every key of the tile is attended by every row
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+          for (int n = 0; n < 8; ++n)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int e = c >> 1;
-            const int key = t0 + 8 * n + 2 * tig + (c & 1);
-            const float v = key <= pos[e] ? sc[n][c] * qk_scale : -INFINITY;
-            sc[n][c] = v;
-            mx[e] = fmaxf(mx[e], v);
-          }
+            for (int c = 0; c < 4; ++c) {
+              sc[n][c] *= qk_scale;
+              mx[c >> 1] = fmaxf(mx[c >> 1], sc[n][c]);
+            }
+        } else {
+#pragma unroll
+          for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int e = c >> 1;
+              const int key = t0 + 8 * n + 2 * tig + (c & 1);
+              const float v = key <= pos[e] ? sc[n][c] * qk_scale : -INFINITY;
+              sc[n][c] = v;
+              mx[e] = fmaxf(mx[e], v);
+            }
+        }
         float al[2], mref[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
