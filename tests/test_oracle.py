@@ -22,6 +22,9 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 def _num(x):
     if isinstance(x, str):
+        if "/" in x:
+            a, b = x.split("/")
+            return float(a) / float(b)
         return {"ln2": math.log(2), "ln3": math.log(3), "ln4": math.log(4), "ln7": math.log(7),
                 "-inf": -math.inf}[x]
     return float(x)
@@ -301,6 +304,20 @@ def pin_bf16_decode():
     # 1.0 = 0x3F80, -2.0 = 0xC000, 0.5 = 0x3F00, smallest subnormal 0x0001 = 2^-133.
     v = R.bf16_bits_to_f64(np.array([0x3F80, 0xC000, 0x3F00, 0x0001], dtype=np.uint16))
     assert list(v) == [1.0, -2.0, 0.5, 2.0 ** -133]
+
+
+def pin_golden_extend():
+    # Hand-worked causal means (tests/golden/extend_causal_means.json).
+    g = _load("extend_causal_means.json")
+    v0, v1 = g["V_request0"], g["V_request1"]
+    V = np.array(v0 + v1, dtype=np.float64)[None, :, None, :]  # (1, slots, 1, 2)
+    vb = _bits(V)
+    kb = _bits(np.zeros_like(V))
+    qb = _bits(np.array(g["q"], dtype=np.float64)[:, None, :])
+    slots = [list(range(len(v0))), list(range(len(v0), len(v0) + len(v1)))]
+    o, lse = R.extend_attention(qb, kb, vb, 0, slots, g["new_tokens"], g["scale"], 1)
+    assert np.allclose(o[:, 0], _arr(g["o"]), rtol=0, atol=1e-13), o
+    assert np.allclose(lse[:, 0], _arr(g["lse"]), rtol=0, atol=1e-13), lse
 
 
 def _extend_case(seed=11, B=3, Hq=4, Hkv=2, D=8, P=4, lens=(6, 3, 9), qo=(2, 3, 4), NL=2):
