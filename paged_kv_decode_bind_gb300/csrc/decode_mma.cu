@@ -12,15 +12,13 @@
 // mantissa bits.  The K/V rows of a token are read from HBM once for all G
 // heads.
 //
-// Block.  4 consumer warps + 2 producer warps (one issues the TMA boxes; the
-// cp.async gathers are shared round-robin by both).  A tile is 64 tokens;
-// consumer warp w owns tokens [16w, 16w+16) of each tile with its own
-// online-softmax state; the four states merge at the end of the unit.  The
-// producers walk the block's units ahead of the consumers, across unit
-// boundaries, through a 3-stage ring (`full` mbarriers complete on the landed bytes, `empty` on the
-// four consumer warps' release), fetching index entries 8 tiles ahead (a
-// second cursor, cp.async into a shared ring) so their latency overlaps the
-// issue of earlier tiles.
+// Block.  4 consumer warps + 1 producer warp.  A tile is 64 tokens; consumer
+// warp w owns tokens [16w, 16w+16) of each tile with its own online-softmax
+// state; the four states merge at the end of the unit.  The producer walks
+// the block's units ahead of the consumers, across unit boundaries, through a
+// 3-stage ring with a `full` and an `empty` mbarrier per stage, fetching
+// index entries several tiles ahead (a second cursor, cp.async into a shared
+// ring) so their latency overlaps the issue of earlier tiles.
 //
 // Units.  With batch <= kMaxCompactBatch only the non-empty (request, split)
 // pairs are units (a per-block prefix over the requests' split counts), so a
@@ -29,12 +27,16 @@
 // Shared-memory tile layout: per K (or V) tile, D/64 column halves, each
 // [64 rows][128 B] with the 128-byte swizzle (16-byte chunk c of row r sits at
 // chunk c ^ (r & 7)), so the 8 row addresses of every ldmatrix hit distinct
-// banks.  Two producers fill it:
-//   * page mode with P % 16 == 0: one tensor-map TMA box (64 cols x 1 head x
-//     16 slots, 2 KB) per 16-token page piece and column half;
-//   * any other page size and the flat (token-level) mode: cp.async 16-byte
-//     gathers written at the swizzled positions, zero-filled where a row is
-//     past the end, completing on the same mbarriers.
+// banks.  Two ways fill it:
+//   * page mode with P % 16 == 0: the producer issues one tensor-map TMA box
+//     per 16-token page piece (both column halves) and pool; `full` completes
+//     on the landed bytes, `empty` on the four consumer warps' release;
+//   * any other page size and the flat (token-level) mode: the producer
+//     validates the tile's index entries into pool slots and publishes them
+//     on `full`; each consumer warp then copies its own 16 rows with 16-byte
+//     cp.async gathers at the swizzled positions (zero-filled past the end)
+//     two tiles ahead of the one it computes, and releases the slots on
+//     `empty`.  A single warp issuing all 64 rows' copies was the bottleneck.
 //
 // Fused append: the unit that holds a request's newest token first writes the
 // new K/V row (k_new, v_new) to pool[layer, out_loc[b]], fences the async
@@ -59,14 +61,11 @@ namespace pkv {
 namespace {
 
 constexpr int kCW = 4;                   // consumer warps
-constexpr int kMaxProducers = 2;         // producer warps (a launch has 1 or 2)
-constexpr int kMThreads = (kCW + kMaxProducers) * 32;  // largest block
-constexpr int kMMinThreads = (kCW + 1) * 32;           // smallest block
+constexpr int kMThreads = (kCW + 1) * 32;
 constexpr int kMT = 16 * kCW;            // tokens per tile
 constexpr int kMStages = 3;
 constexpr int kLA = 8;  // tiles of index lookahead (shared-memory ring of slots)
 static_assert(kLA == kPlanTiles, "the step's plan holds the first ring's worth of page ids");
-static_assert(kLA % kMaxProducers == 0, "each index ring slot belongs to one producer");
 
 template <int D, int G>
 struct MCfg {
@@ -181,60 +180,64 @@ __device__ __forceinline__ void produce_tma(const DecodeArgs &a, const Plan &pl,
     mbar_arrive_expect_tx(full, min(4, (un.t1 - tile0 + 15) / 16) * (uint32_t)(2 * C::PIECE));
 }
 
-// Producer, any page size / flat mode: cp.async 16-byte gathers.  Lane
-// validates rows lane and lane + 32 of the tile and writes their pool slots
-// (-1: none) back over the ring slot's raw entries; the copies then go two or
-// four rows per warp instruction, D / 8 consecutive lanes per row (whole
-// 128-byte lines), each row's slot read back from shared memory.  Rows past
-// the end are zero-filled.
-template <int D, int G>
-__device__ __forceinline__ void produce_cpasync(const DecodeArgs &a, const Plan &pl,
-                                                const Unit &un, int tile0,
-                                                const int (&raw)[2], int *ring, int stage,
-                                                uint32_t kv_base, uint64_t *full, int *flag4,
-                                                int lane) {
-  using C = MCfg<D, G>;
-  constexpr int CH = D / 8;     // 16-byte chunks per row
-  constexpr int RPI = 32 / CH;  // rows per warp instruction
+// Producer, any page size / flat mode: validate the tile's index entries.
+// Lane l resolves rows l and l + 32 of the tile to pool slots (-1: past the
+// unit's end or a bad entry, which raises its error bit and flags the stage)
+// and writes them, with the unit's KV head, for the consumer warps, which
+// copy their own 16 rows each (gather_rows).
+template <int D>
+__device__ __forceinline__ void validate_rows(const DecodeArgs &a, const Plan &pl, const Unit &un,
+                                              int tile0, const int (&raw)[2], int *srow,
+                                              int *sg, int *flag4, int lane) {
   const pkv_workspace &ws = a.ws;
   int kind = 0;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int tok = tile0 + lane + 32 * h;
-    ring[lane + 32 * h] = tok < un.t1 ? (int)slot_from_raw(ws, pl, raw[h], tok, kind) : -1;
+    srow[lane + 32 * h] = tok < un.t1 ? (int)slot_from_raw(ws, pl, raw[h], tok, kind) : -1;
   }
   const int bad = __reduce_or_sync(0xffffffffu, kind);
   if (lane < 4) flag4[lane] = lane == 0 ? bad : 0;
-  if (lane == 0 && bad) atomicOr(ws.err, bad);
-  __syncwarp();
-  const uint32_t kt = kv_base + stage * 2 * C::TILE;  // K then V per 16-token piece
-  const uint32_t vt = kt + C::PIECE;
+  if (lane == 0) {
+    *sg = un.g;
+    if (bad) atomicOr(ws.err, bad);
+  }
+}
+
+// Consumer warp w, gather path: 16-byte cp.async copies of its own 16 rows
+// (tokens 16w .. 16w + 15) of a tile's K and V into the stage, D / 8 lanes
+// per row (whole 128-byte lines), zero-filled where the row has no slot.
+template <int D, int G>
+__device__ __forceinline__ void gather_rows(const DecodeArgs &a, const int *srow, int g,
+                                            uint32_t kt, int warp, int lane) {
+  using C = MCfg<D, G>;
+  constexpr int CH = D / 8;     // 16-byte chunks per row
+  constexpr int RPI = 32 / CH;  // rows per warp instruction
+  const pkv_workspace &ws = a.ws;
   const int sub = lane / CH, ch = lane % CH;
-  const long long head0 = ((long long)a.layer * ws.pool_slots * ws.n_kv_heads + un.g) * D + ch * 8;
+  const long long head0 = ((long long)a.layer * ws.pool_slots * ws.n_kv_heads + g) * D + ch * 8;
   const uint16_t *kb = static_cast<const uint16_t *>(ws.k_pool) + head0;
   const uint16_t *vb = static_cast<const uint16_t *>(ws.v_pool) + head0;
   const long long slot_elems = (long long)ws.n_kv_heads * D;
-#pragma unroll 8
-  for (int i = 0; i < kMT / RPI; ++i) {
-    const int r = i * RPI + sub;
-    const int sl = ring[r];
+  const uint32_t vt = kt + C::PIECE;
+#pragma unroll
+  for (int i = 0; i < 16 / RPI; ++i) {
+    const int r = 16 * warp + i * RPI + sub;
+    const int sl = srow[r];
     const long long e = sl >= 0 ? sl * slot_elems : 0;
     const uint32_t off = kv_off<C::HALVES>(r, ch >> 3, ch & 7);
     cp_async_16(kt + off, kb + e, sl >= 0 ? 16 : 0);
     cp_async_16(vt + off, vb + e, sl >= 0 ? 16 : 0);
   }
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(full))
-               : "memory");
 }
 
-// TMA: the page-mode producer (one warp); else the cp.async gathers (two
-// warps).  The block has kCW + nprod warps.
+// TMA: the page-mode producer issues tensor-map boxes; else it validates
+// index entries and the consumer warps issue their own cp.async gathers.
 template <int D, int G, bool TMA>
-__global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
+__global__ void __launch_bounds__(kMThreads, 2)
     decode_mma_kernel(const __grid_constant__ DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
   constexpr bool use_tma = TMA;
-  constexpr int nprod = TMA ? 1 : kMaxProducers;
   using C = MCfg<D, G>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kMStages], empty[kMStages];
@@ -250,6 +253,11 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
   __shared__ __align__(16) int s_idx[kLA][64];  // index entries of tiles k .. k + kLA - 1
   __shared__ int s_tmp[32];
   __shared__ int s_max_len;
+  // gather path: the tile's KV head per stage, written by the producer with
+  // the tile's validated slots (over its index-ring entries) before the
+  // stage's full barrier; per consumer warp and stage, its tile's error bits
+  __shared__ int s_sg[TMA ? 1 : kMStages];
+  __shared__ int s_wbad[TMA ? 1 : kCW][TMA ? 1 : kMStages];
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const pkv_workspace &ws = a.ws;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -270,9 +278,10 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
   // block barrier publishes them before any use.
   if (tid == kCW * 32) {
     for (int s = 0; s < kMStages; ++s) {
-      // TMA: one expect-tx arrival; cp.async: 32 copy-completion arrivals
-      // plus one release arrival by the lane that wrote the stage flag.
-      mbar_init(&full[s], use_tma ? 1 : 33);
+      // TMA: one expect-tx arrival; gathers: the arrival that publishes the
+      // stage's slots.  empty: the four consumer warps (gathers: each once
+      // it has issued its copies of the stage's tile).
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], kCW);
     }
     *s_abort = 0;
@@ -298,8 +307,8 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
     int h[10];
 #pragma unroll
     for (int i = 0; i < 10; ++i) h[i] = __ldcg(P + i);
-    constexpr int kPer = (kMaxCompactBatch + kMMinThreads) / kMMinThreads;  // batch + 1 entries
-    const int nthr = blockDim.x;
+    constexpr int kPer = (kMaxCompactBatch + kMThreads) / kMThreads;  // batch + 1 entries
+    constexpr int nthr = kMThreads;
     int vp[kPer], vl[kPer], vb[kPer], vc[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -358,7 +367,7 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
   if (!use_tma) {
     Cursor<kMT> c;
     int at = -1;
-    for (int e = tid; e < kLA * kMT; e += blockDim.x) {
+    for (int e = tid; e < kLA * kMT; e += kMThreads) {
       const int tile = e / kMT, r = e - tile * kMT;
       if (at < 0) {
         c.start(ws, pl);
@@ -378,23 +387,17 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
     __syncthreads();
   }
 
-  if (warp >= kCW) {
-    // ------------------------------------------------------ producers ----
-    // nprod warps issue the tiles round-robin: producer pw issues the tiles
-    // k with k % nprod == pw, so the issue work of the gathers
-    // (one cp.async per 16 bytes) is split over two warps.  Each producer
-    // walks all the tiles with its cursor pc.  The index entries of the
-    // first kLA tiles are fetched at once, lane-strided, with 4-byte cp.async
-    // copies (each lane walks a copy of pc to its entry's tile); pf then runs
-    // kLA tiles ahead and fetches later entries the same way into the ring,
-    // one commit group per own tile issued at iteration k for tile k + kLA
-    // (the same producer's: kLA is a multiple of nprod), so no register ever
-    // waits on an index load: at iteration k, tile k's entries are complete
-    // once at most kLA / nprod - 1 newer groups pend.  TMA path: entries
+  if (warp == kCW) {
+    // ------------------------------------------------------- producer ----
+    // pc walks the tiles to issue.  The index entries of the first kLA tiles
+    // are fetched at once, lane-strided, with 4-byte cp.async copies (each
+    // lane walks a copy of pc to its entry's tile); pf then runs ahead and
+    // fetches later entries the same way into the ring, one commit group per
+    // tile, so no register ever waits on an index load.  TMA path: entries
     // 0..3 of a ring slot are the page ids of the tile's 16-token pieces;
-    // gather path: entries 0..63 are the slots / page ids of its rows; -1
-    // where there is none.
-    const int pw = warp - kCW;
+    // gather path: entries 0..63 are the slots / page ids of its rows,
+    // replaced by the validated slots the consumer warps copy from; -1 where
+    // there is none.
     Cursor<kMT> pc;
     pc.start(ws, pl);
     if (use_tma && !planned) {
@@ -403,7 +406,6 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
       int at = 0;
       for (int e = lane; e < kLA * per; e += 32) {
         const int tile = e / per, r = e - tile * per;
-        if ((tile & (nprod - 1)) != pw) continue;  // the other producer's tile
         c.advance_by(ws, pl, tile - at);
         at = tile;
         int *dst = &s_idx[tile][r];
@@ -424,19 +426,20 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
       }
     }
     Cursor<kMT> pf = pc;
-    pf.advance_by(ws, pl, kLA);
+    // TMA: entries are fetched kLA tiles ahead.  Gathers: the ring slot of
+    // tile k holds its validated slots until every consumer warp has issued
+    // tile k, which the producer knows at iteration k + kMStages (its empty
+    // wait), so entries are fetched kLA - kMStages tiles ahead, into the slot
+    // of tile k - kMStages.
+    constexpr int kAhead = TMA ? kLA : kLA - kMStages;
+    pf.advance_by(ws, pl, kAhead);
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
     int pf_u = -1;
     ReqIndex pf_ri{0, false};
-    // entries of the tile under pf into s_idx[slot] when it is this
-    // producer's (mine), then pf moves on
-    auto prefetch = [&](int slot, bool mine) {
+    // entries of the tile under pf into s_idx[slot], then pf moves on
+    auto prefetch = [&](int slot) {
       const Unit &fu = pf.it.un;
-      if (!mine) {
-        if (!pf.done) pf.advance(ws, pl);
-        return;
-      }
       if (!pf.done && fu.u != pf_u) {
         pf_ri = pl.pref ? req_index_cached(ws, s_base, fu.b) : req_index(ws, fu.b);
         pf_u = fu.u;
@@ -464,12 +467,6 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
     bool waited = !early;
     if (waited) pdl_trigger();
     while (!pc.done) {
-      if ((k & (nprod - 1)) != pw) {  // the other producer's tile
-        pc.advance(ws, pl);
-        prefetch(k % kLA, false);
-        ++k;
-        continue;
-      }
       const int s = k % kMStages;
       const int r = k / kMStages;
       if (r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1)) {
@@ -489,7 +486,8 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
         waited = true;
       }
       append_if_newest<D>(a, un, tile0, lane);
-      asm volatile("cp.async.wait_group %0;" ::"n"(kLA / nprod - 1) : "memory");
+      // tile k's entries: at most kAhead - 1 newer groups pend
+      asm volatile("cp.async.wait_group %0;" ::"n"(kAhead - 1) : "memory");
       const int slot = k % kLA;
       // TMA: lanes j and j + 4 both need piece j's page id
       const int cur[2] = {s_idx[slot][use_tma ? (lane & 3) : lane], s_idx[slot][lane + 32]};
@@ -499,15 +497,13 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
       } else if (use_tma) {
         produce_tma<D, G>(a, pl, un, tile0, cur[0], s, kv_base, &full[s], flags[s], &tmk, &tmv,
                           lane);
-      } else {
-        // Issued before the next index copies: the stage's copy-completion
-        // arrival covers every earlier cp.async of the lane.
-        produce_cpasync<D, G>(a, pl, un, tile0, cur, s_idx[slot], s, kv_base, &full[s], flags[s],
-                              lane);
+      } else if constexpr (!TMA) {
+        validate_rows<D>(a, pl, un, tile0, cur, s_idx[slot], &s_sg[s], flags[s], lane);
+        __syncwarp();  // every lane's slots before the arrival that publishes them
         if (lane == 0) mbar_arrive(&full[s]);
       }
       pc.advance(ws, pl);
-      prefetch(slot, true);  // tile k + kLA reuses the slot just read
+      prefetch((k + kAhead) % kLA);  // TMA: the slot just read
       ++k;
     }
     if (aborted) {
@@ -515,11 +511,9 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
         *s_abort = 1;
         atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
       }
-      // Drain: this producer's tiles among the last kMStages may still be
-      // landing.
+      // Drain: the last (up to kMStages) issued tiles may still be landing.
       for (int kk = max(0, k - kMStages); kk < k; ++kk)
-        if ((kk & (nprod - 1)) == pw)
-          mbar_wait_bounded(&full[kk % kMStages], (kk / kMStages) & 1);
+        mbar_wait_bounded(&full[kk % kMStages], (kk / kMStages) & 1);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // index copies still in flight
     return;
@@ -552,6 +546,40 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
       if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse)
         for (int h = tid; h < Hq; h += kCW * 32) ws.lse[(long long)b * Hq + h] = -INFINITY;
     }
+  }
+
+  // Gather path: each consumer warp copies its own rows of tile t two tiles
+  // ahead (at tile t - 2): it waits for the producer to publish the stage's
+  // slots, issues its copies as one cp.async group and releases the slots;
+  // before computing a tile it waits for its own group.  The stage it fills
+  // held tile t - 3, which this warp has finished.
+  int tiles_total = 0;
+  auto issue = [&](int t) {
+    const int st = t % kMStages;
+    bool ok = false;
+    if (!*s_abort) {
+      ok = mbar_wait_bounded(&full[st], (t / kMStages) & 1);
+      if (!ok && lane == 0) {
+        *s_abort = 1;
+        atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
+      }
+    }
+    if (ok) {
+      gather_rows<D, G>(a, s_idx[t % kLA], s_sg[st], kv_base + st * 2 * C::TILE, warp, lane);
+      if (lane == 0) s_wbad[warp][st] = flags[st][0] | flags[st][1] | flags[st][2] | flags[st][3];
+    } else if (lane == 0) {
+      s_wbad[warp][st] = PKV_DEVERR_TIMEOUT;
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    __syncwarp();  // every lane has read the stage's slots
+    if (lane == 0) mbar_arrive(&empty[st]);
+  };
+  if constexpr (!TMA) {
+    UnitIter u2;
+    u2.first(ws, pl);
+    for (; !u2.done; u2.next(ws, pl))
+      if (u2.un.t0 < u2.un.t1) tiles_total += (u2.un.t1 - u2.un.t0 + kMT - 1) / kMT;
+    for (int t = 0; t < 2 && t < tiles_total; ++t) issue(t);
   }
 
   int k = 0;
@@ -615,18 +643,30 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
     for (int it = 0; it < ntiles; ++it, ++k) {
       const int s = k % kMStages;
       bool ok = false;
-      if (!*s_abort) {
-        ok = mbar_wait_bounded(&full[s], (k / kMStages) & 1);
-        if (!ok && lane == 0) {
-          *s_abort = 1;
-          atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
+      if constexpr (TMA) {
+        if (!*s_abort) {
+          ok = mbar_wait_bounded(&full[s], (k / kMStages) & 1);
+          if (!ok && lane == 0) {
+            *s_abort = 1;
+            atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
+          }
         }
+      } else {
+        if (k + 2 < tiles_total) issue(k + 2);
+        // this warp's copies of tile k: the groups of tiles k+1, k+2 may pend
+        const int newer = min(2, tiles_total - 1 - k);
+        if (newer >= 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+        else if (newer == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();  // the lanes' rows visible to the whole warp
+        ok = s_wbad[warp][s] != PKV_DEVERR_TIMEOUT;
       }
       const int nv = min(16, un.t1 - (un.t0 + it * kMT) - 16 * warp);  // my valid tokens
       if (!ok) {
         bad = 1;
       } else {
-        bad |= flags[s][0] | flags[s][1] | flags[s][2] | flags[s][3];
+        if constexpr (TMA) bad |= flags[s][0] | flags[s][1] | flags[s][2] | flags[s][3];
+        else bad |= s_wbad[warp][s];
         if (nv > 0) {
           const uint32_t kt = kv_base + s * 2 * C::TILE;  // K then V per 16-token piece
           const uint32_t vt = kt + C::PIECE;
@@ -717,7 +757,7 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (TMA && lane == 0) mbar_arrive(&empty[s]);
     }
 
     // ---- merge the four warps' states ----
@@ -869,6 +909,7 @@ __global__ void __launch_bounds__(TMA ? kMMinThreads : kMThreads, 2)
     }
     named_sync(1, kCW * 32);  // s_ml, red and the ticket are reused by the next unit
   }
+  if constexpr (!TMA) asm volatile("cp.async.wait_all;" ::: "memory");  // after an abort
 }
 
 using TmapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -936,7 +977,7 @@ cudaError_t mma_shape(const DecodeArgs &a, MmaShape *sh) {
     e = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     int occ = 0, occ_g = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kt, kMMinThreads, C::SMEM);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kt, kMThreads, C::SMEM);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_g, kg, kMThreads, C::SMEM);
     if (e != cudaSuccess) return e;
@@ -977,11 +1018,9 @@ cudaError_t launch_mma_one(const DecodeArgs &a, cudaStream_t st) {
     use_tma = encode_pool_map(&tmk, ws.k_pool, ws) && encode_pool_map(&tmv, ws.v_pool, ws);
   DecodeArgs args = a;
   args.apportion = sh.apportion;
-  // The gathers issue one copy per 16 bytes: two producer warps share them.
-  static_assert(kMaxProducers == 2, "producers take tiles by the low bits of the tile index");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sh.grid);
-  cfg.blockDim = dim3(use_tma ? kMMinThreads : kMThreads);
+  cfg.blockDim = dim3(kMThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
