@@ -16,11 +16,15 @@
 // The accumulator fragment of S is the A fragment of P as it stands, so no
 // transpose is needed.
 //
-// Pipeline.  One producer warp gathers each 64-key tile's K and V rows with
-// 16-byte cp.async (any page size, page-table or flat indices) into 128-byte
-// swizzled rows of a 3-stage ring with full / empty mbarriers; the next
-// tile's index entries are loaded while the current tile's copies are
-// issued.  Every wait is bounded (~1 s) and raises PKV_DEVERR_TIMEOUT.
+// Pipeline.  One producer warp fills a 3-stage ring (full / empty
+// mbarriers) with each 64-key tile's K and V, laid out per 16-token piece as
+// [64-column half][16 rows][128 B] with the 128-byte swizzle, a piece's K
+// then its V.  Page sizes that are multiples of 16 use one tensor-map box per
+// piece and pool (the copy engine writes shared memory directly, leaving the
+// load/store pipe to the consumers' ldmatrix); other page sizes and flat
+// indices use 16-byte cp.async gathers.  The next tile's index entries load
+// while the current tile's copies are issued.  Every wait is bounded (~1 s)
+// and raises PKV_DEVERR_TIMEOUT.
 //
 // Work.  Units are (request, KV head, query block j), visited in order of
 // decreasing j so that the longest causal ranges start first; a persistent
@@ -29,6 +33,10 @@
 // PKV_DEVERR_LEN and get no output rows; a bad page id or flat slot raises its bit and writes the unit's rows
 // as zeros.
 #include <climits>
+
+#include <cuda.h>
+
+#include <cstring>
 
 #include "decode_plan.cuh"
 
@@ -52,20 +60,32 @@ constexpr int kXStages = 3;
 
 template <int D>
 struct XCfg {
-  static constexpr int HALF = kXT * 128;        // one 64-column half of a K (or V) tile
-  static constexpr int TILE = (D / 64) * HALF;  // K (or V) of a tile
-  static constexpr int STAGE = 2 * TILE;        // K then V
+  static constexpr int HALVES = D / 64;
+  static constexpr int PIECE = 16 * HALVES * 128;  // K (or V) of a 16-token piece
+  static constexpr int TILE = (kXT / 16) * PIECE;  // K (or V) of a tile
+  static constexpr int STAGE = 2 * TILE;
   static constexpr int KSTEPS = D / 16;
   static constexpr int ND = D / 8;              // 8-column output tiles
   static constexpr int SMEM = kXStages * STAGE + 1024;  // + alignment slack
   static_assert(D % 64 == 0 && KSTEPS % 2 == 0, "whole swizzled halves, paired k-steps");
 };
 
-// Byte offset of 16-byte chunk ch (0 .. D/8 - 1) of key row t inside a K or
-// V tile: [half][row][128 B], chunk c of row r at c ^ (r & 7).
+// Byte offset of 16-byte chunk ch (0 .. D/8 - 1) of key row t from the
+// stage's K base (the V base is one piece further): piece t / 16, then
+// [half][row][128 B] with chunk c of row r at c ^ (r & 7).
 template <int D>
 __device__ __forceinline__ uint32_t xoff(int t, int ch) {
-  return (uint32_t)((ch >> 3) * XCfg<D>::HALF + t * 128 + (((ch & 7) ^ (t & 7)) << 4));
+  return (uint32_t)((t >> 4) * 2 * XCfg<D>::PIECE + (((ch >> 3) * 16 + (t & 15)) * 128) +
+                    (((ch & 7) ^ (t & 7)) << 4));
+}
+
+__device__ __forceinline__ void xtma4(uint32_t dst, const CUtensorMap *tm, int c1, int c3,
+                                      uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(c1), "r"(0), "r"(c3), "r"(smem_addr(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ void xcp16(uint32_t dst, const void *src, int src_bytes) {
@@ -119,9 +139,11 @@ __device__ __forceinline__ XUnit xunit(const XArgs &a, int u, int tq, int jmax) 
   return x;
 }
 
-template <int D, int G>
+// TMA: the page-piece boxes (P % 16 == 0); else the cp.async gathers.
+template <int D, int G, bool TMA>
 __global__ void __launch_bounds__(kXThreads, 2)
-    extend_mma_kernel(const __grid_constant__ XArgs a) {
+    extend_mma_kernel(const __grid_constant__ XArgs a, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv) {
   using C = XCfg<D>;
   constexpr int TQ = kXRows / G;  // new tokens per block
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -136,8 +158,14 @@ __global__ void __launch_bounds__(kXThreads, 2)
   const int jmax = (a.max_qo_len + TQ - 1) / TQ;
   const int units = jmax * a.batch * ws.n_kv_heads;
   if (tid == kXW * 32) {
+    if (TMA) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmk) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmv) : "memory");
+    }
     for (int s = 0; s < kXStages; ++s) {
-      mbar_init(&full[s], 33);  // 32 copy-completion arrivals + the flag writer's
+      // TMA: one expect-tx arrival; gathers: 32 copy-completion arrivals +
+      // the flag writer's
+      mbar_init(&full[s], TMA ? 1 : 33);
       mbar_init(&empty[s], kXW);
     }
     s_abort = 0;
@@ -178,7 +206,8 @@ __global__ void __launch_bounds__(kXThreads, 2)
       const uint16_t *kb = static_cast<const uint16_t *>(ws.k_pool) + head0;
       const uint16_t *vb = static_cast<const uint16_t *>(ws.v_pool) + head0;
       const int ntiles = (x.kend + kXT - 1) / kXT;
-      int raw[2] = {raw_at(lane), raw_at(lane + 32)};
+      // gathers: rows lane, lane + 32; TMA: lanes j, j + 4 hold piece j's page id
+      int raw[2] = {raw_at(TMA ? 16 * (lane & 3) : lane), TMA ? -1 : raw_at(lane + 32)};
       for (int tile = 0; tile < ntiles; ++tile, ++k) {
         const int s = k % kXStages, r = k / kXStages;
         if ((r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1)) || s_abort) {
@@ -186,6 +215,30 @@ __global__ void __launch_bounds__(kXThreads, 2)
           break;
         }
         const int t0 = tile * kXT;
+        if constexpr (TMA) {
+          // one box per 16-token piece and pool; a bad page loads the
+          // in-range slot 0 and flags the stage
+          const int np = min(4, (x.kend - t0 + 15) / 16);
+          const int j = lane & 3;
+          int kind = 0, slot0 = 0;
+          if (lane < 8 && j < np) {
+            const long long s0 = slot_from_raw(ws, pl, raw[0], t0 + 16 * j, kind);
+            if (!kind) slot0 = (int)s0;
+          }
+          const int nx = raw_at(t0 + kXT + 16 * j);
+          const int bad = __reduce_or_sync(0xffffffffu, kind);
+          if (lane == 0) {
+            flags[s] = bad;
+            if (bad) atomicOr(ws.err, bad);
+          }
+          __syncwarp();
+          if (lane < 8 && j < np)
+            xtma4(ring + s * C::STAGE + j * 2 * C::PIECE + (lane >> 2) * C::PIECE,
+                  lane < 4 ? &tmk : &tmv, a.layer * ws.pool_slots + slot0, x.g, &full[s]);
+          if (lane == 0) mbar_arrive_expect_tx(&full[s], np * (uint32_t)(2 * C::PIECE));
+          raw[0] = nx;
+          continue;
+        }
         int kind = 0;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -202,7 +255,7 @@ __global__ void __launch_bounds__(kXThreads, 2)
           if (bad) atomicOr(ws.err, bad);
         }
         __syncwarp();
-        const uint32_t kt = ring + s * C::STAGE, vt = kt + C::TILE;
+        const uint32_t kt = ring + s * C::STAGE, vt = kt + C::PIECE;
 #pragma unroll 8
         for (int i = 0; i < kXT / RPI; ++i) {
           const int row = i * RPI + sub;
@@ -288,10 +341,26 @@ __global__ void __launch_bounds__(kXThreads, 2)
         }
       }
       const int t0 = tile * kXT;
+      if (TMA && t0 + kXT > x.kend) {
+        // The boxes bring whole pieces: V rows past the unit's last key hold
+        // whatever the pool (or an earlier tile) held, and P = 0 there does
+        // not cancel a NaN.  Clear them (every consumer warp reaches this
+        // for the same tile), then order the writes before the next boxes.
+        const int first = x.kend - t0;
+        const uint32_t vt0 = ring + s * C::STAGE + C::PIECE;
+        for (int i = tid; i < (kXT - first) * (D / 8); i += kXW * 32) {
+          const int r = first + i / (D / 8), c = i % (D / 8);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vt0 + xoff<D>(r, c)),
+                       "r"(0u)
+                       : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        named_sync(1, kXW * 32);
+      }
       if (!ok) {
         bad = 1;
       } else if ((bad |= flags[s]) == 0 && t0 <= wpos) {
-        const uint32_t kt = ring + s * C::STAGE, vt = kt + C::TILE;
+        const uint32_t kt = ring + s * C::STAGE, vt = kt + C::PIECE;
         // ---- S = Q K^T: 8 n-tiles of 8 keys ----
         float sc[8][4];
 #pragma unroll
@@ -386,11 +455,14 @@ __global__ void __launch_bounds__(kXThreads, 2)
       l += __shfl_xor_sync(0xffffffffu, l, 1);
       l += __shfl_xor_sync(0xffffffffu, l, 2);
       if (qrow[e] < 0) continue;
-      const float inv = (bad || !(l > 0.f)) ? 0.f : 1.f / l;
+      // a failed unit is written as zeros whatever its tiles held
+      const bool zero = bad || !(l > 0.f);
+      const float inv = zero ? 0.f : 1.f / l;
       const long long o = (long long)qrow[e] * D + 2 * tig;
 #pragma unroll
       for (int nd = 0; nd < C::ND; ++nd) {
-        const float v0 = oacc[nd][2 * e] * inv, v1 = oacc[nd][2 * e + 1] * inv;
+        const float v0 = zero ? 0.f : oacc[nd][2 * e] * inv;
+        const float v1 = zero ? 0.f : oacc[nd][2 * e + 1] * inv;
         if (a.flags & PKV_FLAG_OUT_F32) {
           *reinterpret_cast<float2 *>(static_cast<float *>(a.out) + o + 8 * nd) =
               make_float2(v0, v1);
@@ -458,6 +530,37 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+using XTmapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 4-D view of a pool [NL * pool_slots, Hkv, D] as (64 columns, slot, 64-column
+// half, KV head): a box of 64 x 16 x D/64 x 1 is one 16-token piece of one
+// head, landing 128B-swizzled as [half][token][64 columns].
+bool xencode_pool_map(CUtensorMap *m, void *base, const pkv_workspace &ws) {
+  static XTmapEncodeFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<XTmapEncodeFn>(p);
+  }
+  if (!fn) return false;
+  const cuuint64_t D = (cuuint64_t)ws.head_dim, H = (cuuint64_t)ws.n_kv_heads;
+  const cuuint64_t dims[4] = {64, (cuuint64_t)ws.n_layers * (cuuint64_t)ws.pool_slots, D / 64, H};
+  const cuuint64_t strides[3] = {H * D * 2, 128, D * 2};
+  const cuuint32_t box[4] = {64, 16, (cuuint32_t)(D / 64), 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int G>
 cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
   using C = XCfg<D>;
@@ -468,13 +571,18 @@ cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int di = dev & 63;
   if (occ_cache[di] == 0) {
-    e = cudaFuncSetAttribute(extend_mma_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM);
+    auto kt = extend_mma_kernel<D, G, true>;
+    auto kg = extend_mma_kernel<D, G, false>;
+    e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    int occ = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, extend_mma_kernel<D, G>, kXThreads,
-                                                      C::SMEM);
+    e = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    int occ = 0, occ_g = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kt, kXThreads, C::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_g, kg, kXThreads, C::SMEM);
+    if (e != cudaSuccess) return e;
+    occ = occ < occ_g ? occ : occ_g;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     sms_cache[di] = sms;
@@ -487,7 +595,15 @@ cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
   if (units > 0x7fffffffll) return cudaErrorInvalidValue;
   const long long cap = (long long)sms_cache[di] * occ_cache[di];
   const int grid = (int)(units < cap ? units : cap);
-  extend_mma_kernel<D, G><<<grid, kXThreads, C::SMEM, st>>>(a);
+  const pkv_workspace &ws = a.ws;
+  CUtensorMap tmk, tmv;
+  memset(&tmk, 0, sizeof(tmk));
+  memset(&tmv, 0, sizeof(tmv));
+  const bool tma = ws.index_mode == PKV_IDX_PAGE_TABLE && ws.page_size % 16 == 0 &&
+                   (long long)ws.n_layers * ws.pool_slots < 0x7fffffffll &&
+                   xencode_pool_map(&tmk, ws.k_pool, ws) && xencode_pool_map(&tmv, ws.v_pool, ws);
+  if (tma) extend_mma_kernel<D, G, true><<<grid, kXThreads, C::SMEM, st>>>(a, tmk, tmv);
+  else extend_mma_kernel<D, G, false><<<grid, kXThreads, C::SMEM, st>>>(a, tmk, tmv);
   return cudaGetLastError();
 }
 
