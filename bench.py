@@ -266,6 +266,24 @@ def extend_flops(lens, qo, p):
     return 4 * p.head_dim * p.n_q_heads * pairs
 
 
+def extend_splits(p, qo, sms):
+    """Splits per causal key range: as many as keep the units within one wave
+    of two blocks per SM, and no split shorter than 256 keys."""
+    tq = 64 // p.group
+    units = -(-max(qo) // tq) * p.batch * p.n_kv_heads
+    if units >= 2 * sms:
+        return 1
+    shortest = min(int(L) for L in p.seq_lens.tolist())
+    return max(1, min(2 * sms // units, shortest // 256))
+
+
+def extend_bytes(lens, qo, p):
+    """Algorithmic bytes of one layer: every context token's K and V once,
+    q and out."""
+    return (sum(lens) * p.n_kv_heads * p.head_dim * 4 +
+            sum(qo) * p.n_q_heads * p.head_dim * 4)
+
+
 def tensor_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -373,18 +391,19 @@ def run_extend_ours(args, rank, world, local_rank):
                               seed=D.rank_seed(20260100, rank))
     B, NL, T = p.batch, p.n_layers, sum(qo)
     lens = p.seq_lens.tolist()
-    ws = Workspace.from_problem(p, device=dev)
+    mq = max(qo)
+    S = extend_splits(p, qo, torch.cuda.get_device_properties(dev).multi_processor_count)
+    ws = Workspace.from_problem(p, device=dev, max_splits=mq * S if S > 1 else 1)
     q, k, v = W.extend_inputs(p, qo)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     out = torch.empty((NL, T, p.n_q_heads, p.head_dim), dtype=torch.bfloat16, device=dev)
     qo_dev = torch.tensor([0] + list(itertools.accumulate(qo)), dtype=torch.int32, device=dev)
-    mq = max(qo)
 
     def calls(s, attn_only):
         for l in range(NL):
             if not attn_only:
                 A.pkv_extend_append(ws, B, l, qo_dev, mq, kd[l], vd[l], s)
-            A.pkv_extend_attn(ws, B, l, qo_dev, mq, qd[l], out[l], p.scale, 0, s)
+            A.pkv_extend_attn(ws, B, l, qo_dev, mq, qd[l], out[l], p.scale, S, 0, s)
 
     def capture(attn_only):
         g = torch.cuda.CUDAGraph()
@@ -448,8 +467,12 @@ def run_extend_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     peak, src = tensor_peak()
+    hbm, hsrc = peaks()
     layer_s = dt_attn / (K * NL)
-    ach = flops / layer_s / 1e12
+    nbytes = extend_bytes(lens, qo, p)
+    # the bound is the roof the arithmetic intensity meets first
+    tensor_bound = flops / nbytes >= peak * 1e12 / (hbm * 1e9)
+    ach = flops / layer_s / 1e12 if tensor_bound else nbytes / layer_s / 1e9
     line = {
         "metric": EXTEND_METRIC, "value": total / dt / 1e12, "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": dt / K * 1e3,
@@ -458,19 +481,24 @@ def run_extend_ours(args, rank, world, local_rank):
         "config": {"workload": args.workload, "batch": B, "n_layers": NL,
                    "n_q_heads": p.n_q_heads, "n_kv_heads": p.n_kv_heads,
                    "head_dim": p.head_dim, "page_size": p.page_size, "new_tokens": qo,
-                   "seq_lens": lens, "cuda_graph": True,
+                   "seq_lens": lens, "num_splits": S, "cuda_graph": True,
                    "l2": "no flush: one step touches %.0f MB of KV, more than twice the 129 MB "
                          "L2" % (sum(lens) * p.n_kv_heads * p.head_dim * 4 * NL / 1e6),
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                     "frac": ach / peak, "traffic": None, "peak_source": src,
+        "roofline": {"bound": "tensor" if tensor_bound else "hbm", "achieved": ach,
+                     "peak": peak if tensor_bound else hbm,
+                     "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                     "frac": ach / (peak if tensor_bound else hbm), "traffic": None,
+                     "peak_source": src if tensor_bound else hsrc,
+                     "achieved_tflops": flops / layer_s / 1e12,
+                     "algorithmic_bytes_per_launch": nbytes, "num_splits": S,
                      "kernel": "extend_mma_kernel (causal extend attention, one launch per "
-                               "layer)",
+                               "layer" + (", + extend_merge_kernel" if S > 1 else "") + ")",
                      "kernel_us_mean": layer_s * 1e6,
                      "kernel_time_from": "graph of the layers' attention launches alone, CUDA "
                                          "events over its timed replays / layers",
                      "algorithmic_flops_per_launch": flops},
-        "gpu_launches": 2 * NL * K,
+        "gpu_launches": (3 if S > 1 else 2) * NL * K,
         "clocks": clk,
         "device_err_bits": errbits,
         "e2e": {"value": flops * NL * ke / dte / 1e12, "unit": "TFLOP/s",

@@ -335,14 +335,25 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
  *   max_qo_len  host upper bound on every n_b (sizes the grid).
  *   q           device bf16 [qo_indptr[batch], Hq, D], 16-byte aligned.
  *   out         device bf16 [qo_indptr[batch], Hq, D] (fp32 with
- *               PKV_FLAG_OUT_F32), 16-byte aligned; the only buffer written.
+ *               PKV_FLAG_OUT_F32), 16-byte aligned.
+ *   num_splits  S >= 1: every 64-row query block's causal key range
+ *               [0, kend) is cut into S splits of ceil(kend / S) keys rounded
+ *               up to 64 (later ones may be empty).  S == 1 writes `out`
+ *               directly; S > 1 writes the splits' normalised partials and
+ *               (max score, sum exp) to ws->o_part / ws->ml_part viewed as
+ *               [query row, Hq, S, D] and [query row, Hq, S, 2] (needs
+ *               batch * max_qo_len * S <= max_batch * max_splits), then a
+ *               second launch merges them into `out` by log-sum-exp.  For
+ *               long prefixes with few new tokens, where the unsplit grid has
+ *               few blocks.
  *   flags       PKV_FLAG_OUT_F32 or 0.
  * Reads seq_lens and either req_pool_indices + page_table (page mode) or
  * kv_indptr + kv_indices (flat mode: bind with PKV_BIND_REBUILD first).
  * Host errors: PKV_ERR_INVALID (null pointer, misalignment, batch < 0,
- * max_qo_len < 0, another flag), PKV_ERR_CAPACITY (batch > max_batch, layer
- * >= n_layers), PKV_ERR_UNSUPPORTED (head_dim not 64 / 128, or G not 1, 2,
- * 4, 8, 16).  Device errors: PKV_DEVERR_LEN (n_b < 0, n_b > seq_lens[b],
+ * max_qo_len < 0, num_splits < 1, another flag), PKV_ERR_CAPACITY (batch >
+ * max_batch, layer >= n_layers, the split partials do not fit),
+ * PKV_ERR_UNSUPPORTED (head_dim not 64 / 128, or G not 1, 2, 4, 8, 16).
+ * Device errors: PKV_DEVERR_LEN (n_b < 0, n_b > seq_lens[b],
  * n_b > max_qo_len or a length out of range: that request's rows are not
  * written), PKV_DEVERR_PAGE / _SLOT (a bad index entry: the affected rows are
  * written as zeros), PKV_DEVERR_TIMEOUT.  Nothing is allocated; the call is
@@ -350,7 +361,7 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
  */
 pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
                            const int32_t *qo_indptr, int max_qo_len, const void *q, void *out,
-                           float scale, int flags, pkv_stream_t stream);
+                           float scale, int num_splits, int flags, pkv_stream_t stream);
 
 /*
  * Extend append: the new tokens' K and V rows into the pool.  k_new, v_new:

@@ -91,7 +91,7 @@ def load(path: str = LIB_PATH):
     lib.pkv_plan_step.restype = i32
     lib.pkv_decode_attn_static_scratch.argtypes = [W, i32, i32, vp, f32, i32, i32, vp]
     lib.pkv_decode_attn_static_scratch.restype = i32
-    lib.pkv_extend_attn.argtypes = [W, i32, i32, vp, i32, vp, vp, f32, i32, vp]
+    lib.pkv_extend_attn.argtypes = [W, i32, i32, vp, i32, vp, vp, f32, i32, i32, vp]
     lib.pkv_extend_attn.restype = i32
     lib.pkv_extend_append.argtypes = [W, i32, i32, vp, i32, vp, vp, vp]
     lib.pkv_extend_append.restype = i32
@@ -204,13 +204,13 @@ def pkv_decode_attn_static_scratch(ws, batch, layer, q, scale, num_splits=1, fla
     return _check("pkv_decode_attn_static_scratch", s) if check else s
 
 
-def pkv_extend_attn(ws, batch, layer, qo_indptr, max_qo_len, q, out, scale, flags=0,
-                    stream=None, check=True):
+def pkv_extend_attn(ws, batch, layer, qo_indptr, max_qo_len, q, out, scale, num_splits=1,
+                    flags=0, stream=None, check=True):
     """Causal extend attention of each request's newest tokens (device
     qo_indptr int32 [batch + 1], q and out [total, Hq, D])."""
     s = load().pkv_extend_attn(_ws(ws), int(batch), int(layer), _ptr(qo_indptr),
-                               int(max_qo_len), _ptr(q), _ptr(out), float(scale), int(flags),
-                               _stream(stream))
+                               int(max_qo_len), _ptr(q), _ptr(out), float(scale),
+                               int(num_splits), int(flags), _stream(stream))
     return _check("pkv_extend_attn", s) if check else s
 
 

@@ -43,8 +43,8 @@
 namespace pkv {
 
 cudaError_t launch_extend(const pkv_workspace &ws, int batch, int layer, const int *qo_indptr,
-                          int max_qo_len, const void *q, void *out, float scale, int flags,
-                          cudaStream_t st);
+                          int max_qo_len, const void *q, void *out, float scale, int num_splits,
+                          int flags, cudaStream_t st);
 cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
                                  const int *qo_indptr, int max_qo_len, const void *k_new,
                                  const void *v_new, cudaStream_t st);
@@ -97,6 +97,7 @@ __device__ __forceinline__ void xcp16(uint32_t dst, const void *src, int src_byt
 struct XArgs {
   pkv_workspace ws;
   int batch, layer, max_qo_len, flags;
+  int S;  // splits of each unit's key range (1: rows written to out directly)
   const int *qo_indptr;
   const void *q;
   void *out;
@@ -105,21 +106,27 @@ struct XArgs {
 
 // One unit: request b's query block j for KV head g.
 struct XUnit {
-  int b, g, j;
-  int n;      // new tokens of the request
-  int L;      // its cached length (new tokens included)
-  int q0;     // qo_indptr[b]
-  int kend;   // keys 0 .. kend - 1 are read
-  bool live;  // valid request and a non-empty block
+  int b, g, j, c;
+  int n;       // new tokens of the request
+  int L;       // its cached length (new tokens included)
+  int q0;      // qo_indptr[b]
+  int kend;    // the block's rows attend keys 0 .. kend - 1 at most
+  int k0, k1;  // keys of split c: [k0, k1) (empty when k0 >= k1)
+  bool live;   // valid request and a non-empty query block
 };
 
-// Request b's new-token count and length, checked; raises PKV_DEVERR_LEN
-// (once per request, by the unit with g == 0 and j == 0).
+// Unit u = (query block j, split c, request b, KV head g), j descending.
+// Request b's new-token count and length are checked; PKV_DEVERR_LEN is
+// raised once per request (by the unit with g, j and c all 0).  Split c of a
+// block covers keys [c * chunk, (c + 1) * chunk) of its causal range,
+// chunk = ceil(kend / S) rounded up to a whole tile.
 __device__ __forceinline__ XUnit xunit(const XArgs &a, int u, int tq, int jmax) {
   const pkv_workspace &ws = a.ws;
   const int bh = a.batch * ws.n_kv_heads;
   XUnit x;
-  const int jj = u / bh, r = u - jj * bh;
+  const int jj = u / (bh * a.S), rs = u - jj * bh * a.S;
+  x.c = rs / bh;
+  const int r = rs - x.c * bh;
   x.b = r / ws.n_kv_heads;
   x.g = r - x.b * ws.n_kv_heads;
   x.j = jmax - 1 - jj;
@@ -133,9 +140,13 @@ __device__ __forceinline__ XUnit xunit(const XArgs &a, int u, int tq, int jmax) 
     const int base = ws.kv_indptr[x.b];
     ok = base >= 0 && (long long)base + x.L <= ws.max_total_tokens;
   }
-  if (!ok && x.g == 0 && x.j == 0 && (threadIdx.x & 31) == 0) atomicOr(ws.err, PKV_DEVERR_LEN);
+  if (!ok && x.g == 0 && x.j == 0 && x.c == 0 && (threadIdx.x & 31) == 0)
+    atomicOr(ws.err, PKV_DEVERR_LEN);
   x.live = ok && x.j * tq < x.n;
   x.kend = x.live ? x.L - x.n + min(x.n, (x.j + 1) * tq) : 0;
+  const int chunk = ((x.kend + a.S - 1) / a.S + kXT - 1) / kXT * kXT;
+  x.k0 = x.c * chunk;
+  x.k1 = min(x.kend, x.k0 + chunk);
   return x;
 }
 
@@ -156,7 +167,7 @@ __global__ void __launch_bounds__(kXThreads, 2)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Hq = ws.n_q_heads;
   const int jmax = (a.max_qo_len + TQ - 1) / TQ;
-  const int units = jmax * a.batch * ws.n_kv_heads;
+  const int units = jmax * a.S * a.batch * ws.n_kv_heads;
   if (tid == kXW * 32) {
     if (TMA) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmk) : "memory");
@@ -199,26 +210,27 @@ __global__ void __launch_bounds__(kXThreads, 2)
       }
       const int *idx = ws.index_mode == PKV_IDX_FLAT ? ws.kv_indices : ws.page_table;
       auto raw_at = [&](int t) {
-        if (t >= x.kend || !row_ok) return -1;
+        if (t >= x.k1 || !row_ok) return -1;
         return idx[base + (ws.index_mode == PKV_IDX_FLAT ? t : pl.page_of(t))];
       };
       const long long head0 = ((long long)a.layer * ws.pool_slots * ws.n_kv_heads + x.g) * D + ch * 8;
       const uint16_t *kb = static_cast<const uint16_t *>(ws.k_pool) + head0;
       const uint16_t *vb = static_cast<const uint16_t *>(ws.v_pool) + head0;
-      const int ntiles = (x.kend + kXT - 1) / kXT;
+      const int ntiles = x.k1 > x.k0 ? (x.k1 - x.k0 + kXT - 1) / kXT : 0;
       // gathers: rows lane, lane + 32; TMA: lanes j, j + 4 hold piece j's page id
-      int raw[2] = {raw_at(TMA ? 16 * (lane & 3) : lane), TMA ? -1 : raw_at(lane + 32)};
+      int raw[2] = {raw_at(x.k0 + (TMA ? 16 * (lane & 3) : lane)),
+                    TMA ? -1 : raw_at(x.k0 + lane + 32)};
       for (int tile = 0; tile < ntiles; ++tile, ++k) {
         const int s = k % kXStages, r = k / kXStages;
         if ((r > 0 && !mbar_wait_bounded(&empty[s], (r - 1) & 1)) || s_abort) {
           aborted = true;
           break;
         }
-        const int t0 = tile * kXT;
+        const int t0 = x.k0 + tile * kXT;
         if constexpr (TMA) {
           // one box per 16-token piece and pool; a bad page loads the
           // in-range slot 0 and flags the stage
-          const int np = min(4, (x.kend - t0 + 15) / 16);
+          const int np = min(4, (x.k1 - t0 + 15) / 16);
           const int j = lane & 3;
           int kind = 0, slot0 = 0;
           if (lane < 8 && j < np) {
@@ -244,7 +256,7 @@ __global__ void __launch_bounds__(kXThreads, 2)
         for (int h = 0; h < 2; ++h) {
           const int t = t0 + lane + 32 * h;
           // a bad table row reads as raw -1: a page error
-          const int sl = t < x.kend ? (int)slot_from_raw(ws, pl, raw[h], t, kind) : -1;
+          const int sl = t < x.k1 ? (int)slot_from_raw(ws, pl, raw[h], t, kind) : -1;
           s_slot[s][lane + 32 * h] = sl;
         }
         // the next tile's index entries load while this tile's copies issue
@@ -329,7 +341,7 @@ __global__ void __launch_bounds__(kXThreads, 2)
     for (int nd = 0; nd < C::ND; ++nd) oacc[nd][0] = oacc[nd][1] = oacc[nd][2] = oacc[nd][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     int bad = 0;
-    const int ntiles = (x.kend + kXT - 1) / kXT;
+    const int ntiles = x.k1 > x.k0 ? (x.k1 - x.k0 + kXT - 1) / kXT : 0;
     for (int tile = 0; tile < ntiles; ++tile, ++k) {
       const int s = k % kXStages;
       bool ok = false;
@@ -340,13 +352,13 @@ __global__ void __launch_bounds__(kXThreads, 2)
           atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
         }
       }
-      const int t0 = tile * kXT;
-      if (TMA && t0 + kXT > x.kend) {
+      const int t0 = x.k0 + tile * kXT;
+      if (TMA && t0 + kXT > x.k1) {
         // The boxes bring whole pieces: V rows past the unit's last key hold
         // whatever the pool (or an earlier tile) held, and P = 0 there does
         // not cancel a NaN.  Clear them (every consumer warp reaches this
         // for the same tile), then order the writes before the next boxes.
-        const int first = x.kend - t0;
+        const int first = x.k1 - t0;
         const uint32_t vt0 = ring + s * C::STAGE + C::PIECE;
         for (int i = tid; i < (kXT - first) * (D / 8); i += kXW * 32) {
           const int r = first + i / (D / 8), c = i % (D / 8);
@@ -458,6 +470,21 @@ __global__ void __launch_bounds__(kXThreads, 2)
       // a failed unit is written as zeros whatever its tiles held
       const bool zero = bad || !(l > 0.f);
       const float inv = zero ? 0.f : 1.f / l;
+      if (a.S > 1) {
+        // split partial: normalised o and (m, l) in natural-log units; a
+        // failed split is marked l = -1 so the merge writes the row as zeros
+        const long long pr = (long long)qrow[e] * a.S + x.c;
+        float *op = ws.o_part + pr * D + 2 * tig;
+#pragma unroll
+        for (int nd = 0; nd < C::ND; ++nd)
+          *reinterpret_cast<float2 *>(op + 8 * nd) =
+              make_float2(zero ? 0.f : oacc[nd][2 * e] * inv, zero ? 0.f : oacc[nd][2 * e + 1] * inv);
+        if (tig == 0) {
+          ws.ml_part[pr * 2] = zero ? -INFINITY : m_run[e] * kLn2;
+          ws.ml_part[pr * 2 + 1] = bad ? -1.f : (zero ? 0.f : l);
+        }
+        continue;
+      }
       const long long o = (long long)qrow[e] * D + 2 * tig;
 #pragma unroll
       for (int nd = 0; nd < C::ND; ++nd) {
@@ -471,6 +498,61 @@ __global__ void __launch_bounds__(kXThreads, 2)
               pack_bf16x2(v0, v1);
         }
       }
+    }
+  }
+}
+
+// Merge of the split partials: one warp per (new token, query head) of
+// request b = blockIdx.y: M = max over non-empty splits of m_s, w_s = l_s
+// exp(m_s - M), out = sum w_s o_s / sum w_s; zeros when no split has a key
+// or one failed (l = -1).
+template <int D>
+__global__ void __launch_bounds__(128)
+    extend_merge_kernel(const __grid_constant__ pkv_workspace ws, const int *qo_indptr,
+                        int max_qo_len, int S, void *out, int flags) {
+  constexpr int E = D / 32;  // elements per lane
+  const int b = blockIdx.y;
+  const int q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0, L = ws.seq_lens[b];
+  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  bool ok = n >= 0 && n <= L && n <= max_qo_len && q0 >= 0 && q0 + n <= qo_indptr[gridDim.y] &&
+            (long long)L <= cap;
+  if (ok && ws.index_mode == PKV_IDX_FLAT) {
+    const int base = ws.kv_indptr[b];
+    ok = base >= 0 && (long long)base + L <= ws.max_total_tokens;
+  }
+  if (!ok) return;  // raised by the attention kernel
+  const int Hq = ws.n_q_heads, lane = threadIdx.x & 31;
+  for (int p = blockIdx.x * 4 + (threadIdx.x >> 5); p < n * Hq; p += gridDim.x * 4) {
+    const long long row = (long long)(q0 + p / Hq) * Hq + p % Hq;
+    float M = -INFINITY;
+    bool failed = false;
+    for (int c = 0; c < S; ++c) {
+      const float m = ws.ml_part[(row * S + c) * 2], l = ws.ml_part[(row * S + c) * 2 + 1];
+      if (l < 0.f) failed = true;
+      else if (l > 0.f) M = fmaxf(M, m);
+    }
+    float acc[E], wsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) acc[i] = 0.f;
+    for (int c = 0; c < S; ++c) {
+      const float m = ws.ml_part[(row * S + c) * 2], l = ws.ml_part[(row * S + c) * 2 + 1];
+      if (!(l > 0.f)) continue;
+      const float w = l * expf(m - M);
+      wsum += w;
+      const float *op = ws.o_part + (row * S + c) * D + lane * E;
+#pragma unroll
+      for (int i = 0; i < E; ++i) acc[i] += w * op[i];
+    }
+    const bool zero = failed || !(wsum > 0.f);
+    const float inv = zero ? 0.f : 1.f / wsum;
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      const float v0 = zero ? 0.f : acc[i] * inv, v1 = zero ? 0.f : acc[i + 1] * inv;
+      const long long o = row * D + lane * E + i;
+      if (flags & PKV_FLAG_OUT_F32)
+        *reinterpret_cast<float2 *>(static_cast<float *>(out) + o) = make_float2(v0, v1);
+      else
+        *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(out) + o) = pack_bf16x2(v0, v1);
     }
   }
 }
@@ -590,7 +672,7 @@ cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
   }
   constexpr int TQ = kXRows / G;
   const long long units =
-      (long long)((a.max_qo_len + TQ - 1) / TQ) * a.batch * a.ws.n_kv_heads;
+      (long long)((a.max_qo_len + TQ - 1) / TQ) * a.S * a.batch * a.ws.n_kv_heads;
   if (units <= 0) return cudaSuccess;
   if (units > 0x7fffffffll) return cudaErrorInvalidValue;
   const long long cap = (long long)sms_cache[di] * occ_cache[di];
@@ -604,6 +686,15 @@ cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
                    xencode_pool_map(&tmk, ws.k_pool, ws) && xencode_pool_map(&tmv, ws.v_pool, ws);
   if (tma) extend_mma_kernel<D, G, true><<<grid, kXThreads, C::SMEM, st>>>(a, tmk, tmv);
   else extend_mma_kernel<D, G, false><<<grid, kXThreads, C::SMEM, st>>>(a, tmk, tmv);
+  if (a.S > 1) {
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long pairs = (long long)a.max_qo_len * ws.n_q_heads;
+    const long long mblocks = (pairs + 3) / 4;
+    const dim3 mgrid((unsigned)(mblocks < 1024 ? mblocks : 1024), (unsigned)a.batch);
+    extend_merge_kernel<D><<<mgrid, 128, 0, st>>>(ws, a.qo_indptr, a.max_qo_len, a.S, a.out,
+                                                  a.flags);
+  }
   return cudaGetLastError();
 }
 
@@ -615,9 +706,9 @@ bool extend_supported(int head_dim, int group) {
 }
 
 cudaError_t launch_extend(const pkv_workspace &ws, int batch, int layer, const int *qo_indptr,
-                          int max_qo_len, const void *q, void *out, float scale, int flags,
-                          cudaStream_t st) {
-  XArgs a{ws, batch, layer, max_qo_len, flags, qo_indptr, q, out, scale};
+                          int max_qo_len, const void *q, void *out, float scale, int num_splits,
+                          int flags, cudaStream_t st) {
+  XArgs a{ws, batch, layer, max_qo_len, flags, num_splits, qo_indptr, q, out, scale};
   const int D = ws.head_dim, G = ws.n_q_heads / ws.n_kv_heads;
 #define PKV_X_CASE(DD, GG) \
   if (D == DD && G == GG) return launch_extend_one<DD, GG>(a, st);

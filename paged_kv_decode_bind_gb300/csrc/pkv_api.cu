@@ -10,8 +10,8 @@ using namespace pkv;
 namespace pkv {
 // extend_mma.cu
 cudaError_t launch_extend(const pkv_workspace &ws, int batch, int layer, const int *qo_indptr,
-                          int max_qo_len, const void *q, void *out, float scale, int flags,
-                          cudaStream_t st);
+                          int max_qo_len, const void *q, void *out, float scale, int num_splits,
+                          int flags, cudaStream_t st);
 cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
                                  const int *qo_indptr, int max_qo_len, const void *k_new,
                                  const void *v_new, cudaStream_t st);
@@ -270,13 +270,22 @@ static pkv_status extend_common(const pkv_workspace *ws, int batch, int layer,
 
 pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
                            const int32_t *qo_indptr, int max_qo_len, const void *q, void *out,
-                           float scale, int flags, pkv_stream_t stream) {
+                           float scale, int num_splits, int flags, pkv_stream_t stream) {
   pkv_status st = extend_common(ws, batch, layer, qo_indptr, max_qo_len, q, out);
   if (st != PKV_OK) return st;
   if (flags & ~PKV_FLAG_OUT_F32) return PKV_ERR_INVALID;
+  if (num_splits < 1) return PKV_ERR_INVALID;
+  if (num_splits > 1) {
+    // partials of every (new token, query head, split) in o_part / ml_part
+    if (!ws->o_part || !ws->ml_part || !aligned16(ws->o_part)) return PKV_ERR_INVALID;
+    if ((long long)batch * max_qo_len * num_splits > (long long)ws->max_batch * ws->max_splits)
+      return PKV_ERR_CAPACITY;
+  }
+  if ((long long)max_qo_len * num_splits * batch * ws->n_kv_heads > 0x7fffffffll)
+    return PKV_ERR_CAPACITY;
   if (batch == 0 || max_qo_len == 0) return PKV_OK;
-  return from_cuda(launch_extend(*ws, batch, layer, qo_indptr, max_qo_len, q, out, scale, flags,
-                                 reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_extend(*ws, batch, layer, qo_indptr, max_qo_len, q, out, scale,
+                                 num_splits, flags, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 pkv_status pkv_extend_append(const pkv_workspace *ws, int batch, int layer,

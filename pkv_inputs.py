@@ -277,25 +277,38 @@ def workload(name: str, *, batch: int | None = None, n_layers: int | None = None
 # positions on top of a cached prefix (the step before decode).
 # --------------------------------------------------------------------------
 
-EXTEND_WORKLOADS = ("extend_b4_chunk256",)
+EXTEND_WORKLOADS = ("extend_b4_chunk256", "extend_b1_prefix32k_chunk64")
 
 
 def extend_workload(name: str, *, n_layers: int | None = None, shrink: int = 1,
                     seed: int | None = None):
-    """extend_b4_chunk256: B=4, 24 layers, 32/8 heads, D=128, P=16, cached
-    prefixes ~ U{512..2048} (the paged decode workload's lengths) and 256 new
-    tokens per request; the pool holds prefix + new tokens.  Returns the
-    problem (its seq_lens count the new tokens) and the new-token counts.
-    ``shrink`` divides both lengths (and uses 2 layers)."""
-    if name != "extend_b4_chunk256":
-        raise KeyError(name)
-    seed = 20260100 if seed is None else seed
-    B, chunk = 4, max(1, 256 // shrink)
-    prefix = _uniform_lens(B, max(1, 512 // shrink), max(1, 2048 // shrink), _sub(seed, 0))
-    nl = n_layers or (24 if shrink == 1 else 2)
-    p = make_problem(name, batch=B, n_layers=nl, n_q_heads=32, n_kv_heads=8, head_dim=128,
-                     page_size=16, seq_lens=[x + chunk for x in prefix], seed=seed)
-    return p, [chunk] * B
+    """Extend (prefill) workloads, 32/8 heads, D=128, P=16; the pool holds
+    prefix + new tokens.  Returns the problem (its seq_lens count the new
+    tokens) and the new-token counts.
+
+    extend_b4_chunk256           B=4, 24 layers, cached prefixes ~ U{512..2048}
+                                 (the paged decode workload's lengths), 256 new
+                                 tokens per request.
+    extend_b1_prefix32k_chunk64  B=1, 4 layers, a 32768-token cached prefix and
+                                 64 new tokens (a short chunk on a long
+                                 context); pool exactly the pages needed.
+
+    ``shrink`` divides the lengths (and uses 2 layers)."""
+    seed = (20260100 + EXTEND_WORKLOADS.index(name)) if seed is None else seed
+    if name == "extend_b4_chunk256":
+        B, chunk = 4, max(1, 256 // shrink)
+        prefix = _uniform_lens(B, max(1, 512 // shrink), max(1, 2048 // shrink), _sub(seed, 0))
+        nl = n_layers or (24 if shrink == 1 else 2)
+        p = make_problem(name, batch=B, n_layers=nl, n_q_heads=32, n_kv_heads=8, head_dim=128,
+                         page_size=16, seq_lens=[x + chunk for x in prefix], seed=seed)
+        return p, [chunk] * B
+    if name == "extend_b1_prefix32k_chunk64":
+        chunk, prefix = max(1, 64 // shrink), max(1, 32768 // shrink)
+        nl = n_layers or (4 if shrink == 1 else 2)
+        p = make_problem(name, batch=1, n_layers=nl, n_q_heads=32, n_kv_heads=8, head_dim=128,
+                         page_size=16, seq_lens=[prefix + chunk], pool_factor=1.0, seed=seed)
+        return p, [chunk]
+    raise KeyError(name)
 
 
 def extend_inputs(p: DecodeProblem, qo_lens, layers=None):

@@ -130,8 +130,16 @@ def test_extend_host_validation():
         (dict(), 1, 0, f, 0, f, f, 0, P.PKV_OK),                                     # no tokens
     ]
     for kw, batch, layer, qo, mq, q, out, flags, status in cases:
-        got = X(_ws(**kw), batch, layer, qo, mq, q, out, 0.1, flags, 0, check=False)
+        got = X(_ws(**kw), batch, layer, qo, mq, q, out, 0.1, num_splits=1, flags=flags,
+                stream=0, check=False)
         assert got == status, (kw, batch, layer, mq, flags, got, status)
+    # splits: partials need o_part / ml_part with room for batch * max_qo_len * S rows
+    assert X(_ws(), 1, 0, f, 4, f, f, 0.1, num_splits=0, stream=0, check=False) == \
+        P.PKV_ERR_INVALID
+    assert X(_ws(o_part=None), 1, 0, f, 4, f, f, 0.1, num_splits=2, stream=0, check=False) == \
+        P.PKV_ERR_INVALID
+    assert X(_ws(), 4, 0, f, 4, f, f, 0.1, num_splits=2, stream=0, check=False) == \
+        P.PKV_ERR_CAPACITY  # 4 * 4 * 2 rows > max_batch 4 * max_splits 4
     A = P.pkv_extend_append
     assert A(_ws(), 1, 0, f, 4, f, None, 0, check=False) == P.PKV_ERR_INVALID
     assert A(_ws(), 5, 0, f, 4, f, f, 0, check=False) == P.PKV_ERR_CAPACITY

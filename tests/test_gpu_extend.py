@@ -30,14 +30,16 @@ def _indptr(qo, device):
 
 
 def run_extend(cuda, *, lens, qo, Hq, Hkv, D, P, seed, NL=2, layer=1, flags=0, rows=None,
-               max_qo=None, table_edit=None, expect_err=0, check_pool=True):
+               max_qo=None, table_edit=None, expect_err=0, check_pool=True, S=1):
     """Append + extend attention through libpkv and the oracle; returns the
     GPU output (float64 numpy) and the oracle's."""
     p = W.make_problem("extend", batch=len(lens), n_layers=NL, n_q_heads=Hq, n_kv_heads=Hkv,
                        head_dim=D, page_size=P, seq_lens=list(lens), seed=seed)
     if table_edit:
         table_edit(p)
-    ws = Workspace.from_problem(p)
+    mq = max(qo) if max_qo is None else max_qo
+    # split partials live in o_part / ml_part: room for batch * max_qo * S rows
+    ws = Workspace.from_problem(p, max_splits=max(1, mq * S) if S > 1 else 1)
     B, T = p.batch, int(sum(qo))
     q = W.normal_bf16((T, Hq, D), seed + 500)
     kn = W.normal_bf16((T, Hkv, D), seed + 501)
@@ -47,9 +49,9 @@ def run_extend(cuda, *, lens, qo, Hq, Hkv, D, P, seed, NL=2, layer=1, flags=0, r
     qo_dev = _indptr(qo, cuda)
     out_dtype = torch.float32 if flags & A.PKV_FLAG_OUT_F32 else torch.bfloat16
     out = torch.full((T, Hq, D), 7.0, dtype=out_dtype, device=cuda)  # sentinel
-    mq = max(qo) if max_qo is None else max_qo
     A.pkv_extend_append(ws, B, layer, qo_dev, mq, kn.to(cuda), vn.to(cuda))
-    A.pkv_extend_attn(ws, B, layer, qo_dev, mq, q.to(cuda), out, p.scale, flags)
+    A.pkv_extend_attn(ws, B, layer, qo_dev, mq, q.to(cuda), out, p.scale, num_splits=S,
+                      flags=flags)
     torch.cuda.synchronize()
     assert int(ws.err.item()) == expect_err
     slots = _slots(p)
@@ -97,11 +99,29 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("S", [1, 3])
 @pytest.mark.parametrize("case", list(CASES), ids=list(CASES))
-def test_extend_parity(cuda, case):
+def test_extend_parity(cuda, case, S):
     lens, qo, Hq, Hkv, D, P = CASES[case]
-    got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=Hq, Hkv=Hkv, D=D, P=P, seed=4100)
-    _compare(got, ref, want, case)
+    got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=Hq, Hkv=Hkv, D=D, P=P, seed=4100,
+                                   S=S)
+    _compare(got, ref, want, f"{case} S={S}")
+
+
+def test_extend_splits_agree(cuda):
+    # fp32 outputs of 1, 2, 5 and 16 splits (some of them empty for early
+    # query blocks) agree with each other; P enters P V as bf16 and its
+    # rounding depends on the running maximum, so the bar is 2e-3.
+    kw = dict(lens=(1500, 700), qo=(48, 100), Hq=16, Hkv=2, D=128, P=16, seed=4700, NL=1,
+              layer=0, flags=A.PKV_FLAG_OUT_F32,
+              rows=[(r, h) for r in range(0, 148, 7) for h in range(16)])
+    outs = []
+    for S in (1, 2, 5, 16):
+        got, ref, want, _ = run_extend(cuda, S=S, **kw)
+        _compare(got, ref, want, f"S={S}")
+        outs.append(got)
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 2e-3
 
 
 def test_extend_f32_output_one_new_token(cuda):
@@ -123,9 +143,10 @@ def test_extend_long_prefix_sampled(cuda):
     T = 256 + 64
     rows = sorted({(int(rng.integers(T)), int(rng.integers(32))) for _ in range(40)}
                   | {(0, 0), (T - 1, 31), (255, 5)})
-    got, ref, want, _ = run_extend(cuda, lens=(4096, 700), qo=(256, 64), Hq=32, Hkv=8, D=128,
-                                   P=16, seed=4300, NL=1, layer=0, rows=rows)
-    _compare(got, ref, want, "long prefix")
+    for S in (1, 6):
+        got, ref, want, _ = run_extend(cuda, lens=(4096, 700), qo=(256, 64), Hq=32, Hkv=8,
+                                       D=128, P=16, seed=4300, NL=1, layer=0, rows=rows, S=S)
+        _compare(got, ref, want, f"long prefix S={S}")
 
 
 def test_extend_invalid_request_is_skipped(cuda):
@@ -155,9 +176,10 @@ def test_extend_bad_page_zeroes_rows(cuda):
         row = int(p.req_pool_indices[1])
         p.page_table[row, 0] = p.pool_slots // p.page_size  # one past the last page
     lens, qo = (64, 80), (8, 8)
-    got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=8, Hkv=2, D=64, P=16, seed=4600,
-                                   table_edit=edit, expect_err=A.PKV_DEVERR_PAGE,
-                                   check_pool=False,
-                                   rows=[(r, h) for r in range(8) for h in range(8)])
-    assert np.all(got[8:] == 0.0)
-    _compare(got, ref, want, "request next to a bad page")
+    for S in (1, 2):
+        got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=8, Hkv=2, D=64, P=16,
+                                       seed=4600, table_edit=edit, expect_err=A.PKV_DEVERR_PAGE,
+                                       check_pool=False, S=S,
+                                       rows=[(r, h) for r in range(8) for h in range(8)])
+        assert np.all(got[8:] == 0.0)
+        _compare(got, ref, want, f"request next to a bad page S={S}")
