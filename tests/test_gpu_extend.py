@@ -183,3 +183,57 @@ def test_extend_bad_page_zeroes_rows(cuda):
                                        rows=[(r, h) for r in range(8) for h in range(8)])
         assert np.all(got[8:] == 0.0)
         _compare(got, ref, want, f"request next to a bad page S={S}")
+
+
+def test_extend_graph_replay_bitexact(cuda):
+    # The extend calls allocate nothing and read no device memory on the
+    # host: a captured graph replays them with bit-identical outputs.
+    p = W.make_problem("extend_graph", batch=2, n_layers=1, n_q_heads=16, n_kv_heads=2,
+                       head_dim=128, page_size=16, seq_lens=[300, 130], seed=4800)
+    qo = [40, 130]
+    S = 3
+    ws = Workspace.from_problem(p, max_splits=max(qo) * S)
+    T = sum(qo)
+    q = W.normal_bf16((T, 16, 128), 4801).to(cuda)
+    kn = W.normal_bf16((T, 2, 128), 4802).to(cuda)
+    vn = W.normal_bf16((T, 2, 128), 4803).to(cuda)
+    qo_dev = _indptr(qo, cuda)
+    out = torch.zeros((T, 16, 128), dtype=torch.bfloat16, device=cuda)
+
+    def step(s=None):
+        A.pkv_extend_append(ws, 2, 0, qo_dev, max(qo), kn, vn, stream=s)
+        A.pkv_extend_attn(ws, 2, 0, qo_dev, max(qo), q, out, p.scale, num_splits=S, stream=s)
+
+    step()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side), torch.cuda.graph(g, stream=side):
+        step(side)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) == 0
+    assert torch.equal(out, eager)
+
+
+def test_extend_one_token_matches_decode_kernel(cuda):
+    # One new token per request: the extend kernel and the decode kernel
+    # compute the same attention; their fp32 outputs agree to the extend
+    # kernel's bf16 rounding of P.
+    lens = [700, 65, 1200]
+    p = W.make_problem("extend_vs_decode", batch=3, n_layers=1, n_q_heads=32, n_kv_heads=8,
+                       head_dim=128, page_size=16, seq_lens=lens, seed=4900)
+    ws = Workspace.from_problem(p)
+    q = W.normal_bf16((3, 32, 128), 4901).to(cuda)
+    qo_dev = _indptr([1, 1, 1], cuda)
+    out = torch.zeros((3, 32, 128), dtype=torch.float32, device=cuda)
+    A.pkv_extend_attn(ws, 3, 0, qo_dev, 1, q, out, p.scale, flags=A.PKV_FLAG_OUT_F32)
+    A.pkv_decode_attn(ws, 3, 0, q, p.scale, 1, A.PKV_FLAG_OUT_F32)
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) == 0
+    dec = ws.out_f32(3)
+    assert (out - dec).abs().max().item() <= 2e-3
