@@ -1,0 +1,50 @@
+"""bench.py's workload arithmetic (no GPU): algorithmic bytes and FLOPs
+against brute-force counts, and the extend split chooser's rules."""
+import types
+
+import bench
+
+
+def _p(batch, Hq, Hkv, D, lens):
+    return types.SimpleNamespace(batch=batch, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D,
+                                 group=Hq // Hkv,
+                                 seq_lens=types.SimpleNamespace(tolist=lambda: list(lens)))
+
+
+def test_extend_flops_brute_force():
+    lens, qo = [10, 7, 33], [3, 7, 1]
+    p = _p(3, 8, 2, 64, lens)
+    pairs = 0
+    for L, n in zip(lens, qo):
+        for i in range(n):
+            for t in range(L):
+                pairs += t <= L - n + i  # keys each new token attends
+    assert bench.extend_flops(lens, qo, p) == 4 * 64 * 8 * pairs
+
+
+def test_extend_bytes():
+    lens, qo = [10, 7], [3, 7]
+    p = _p(2, 8, 2, 64, lens)
+    kv = sum(lens) * 2 * 64 * 2 * 2  # K and V of every context token, bf16
+    qout = sum(qo) * 8 * 64 * 2 * 2  # q and out, bf16
+    assert bench.extend_bytes(lens, qo, p) == kv + qout
+
+
+def test_decode_algorithmic_bytes():
+    lens = [100, 7]
+    p = _p(2, 32, 8, 128, lens)
+    want = sum(lens) * 8 * 128 * 2 * 2 + 2 * 32 * 128 * 2 * 2
+    assert bench.algorithmic_bytes(lens, p) == want
+
+
+def test_extend_splits_one_wave():
+    # 64 new tokens at G = 4 are 4 query blocks per head; with 8 heads and one
+    # request, 32 units: 9 splits keep 288 units within 2 x 152 blocks.
+    p = _p(1, 32, 8, 128, [32832])
+    assert bench.extend_splits(p, [64], 152) == 9
+    # enough units already: no split
+    p4 = _p(4, 32, 8, 128, [1000, 2000, 1500, 900])
+    assert bench.extend_splits(p4, [256] * 4, 152) == 1
+    # no split shorter than 256 keys
+    ps = _p(1, 32, 8, 128, [600])
+    assert bench.extend_splits(ps, [64], 152) == 2
