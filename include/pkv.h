@@ -88,11 +88,14 @@ enum {
                                  ids from ws->work_plan (pkv_plan_step) when it was made
                                  for this batch size, split count and flags; else plan
                                  as without the flag */
-  PKV_FLAG_TEST_SKIP_FIRST_TILE = 256  /* test hook, tensor-core kernel: every block's
+  PKV_FLAG_TEST_SKIP_FIRST_TILE = 256, /* test hook, tensor-core kernel: every block's
                                  producer leaves its first tile unloaded, so the bounded
                                  wait for it runs out (~1 s): the launch sets
                                  PKV_DEVERR_TIMEOUT, writes those units empty and
                                  returns, and the context stays usable */
+  PKV_FLAG_EXTEND_FULL = 512  /* pkv_extend_attn: every query row of a request attends all
+                                 seq_lens[b] tokens (no causal mask), e.g. a batch's decode
+                                 queries over a prefix their requests share */
 };
 
 /* bits OR-ed into *err by device code (sticky; the caller clears the word) */
@@ -346,12 +349,16 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
  *               second launch merges them into `out` by log-sum-exp.  For
  *               long prefixes with few new tokens, where the unsplit grid has
  *               few blocks.
- *   flags       PKV_FLAG_OUT_F32 or 0.
+ *   flags       PKV_FLAG_OUT_F32; PKV_FLAG_WRITE_LSE (also lse[query row * Hq + h] =
+ *               max score + ln(sum exp) in ws->lse, which needs batch *
+ *               max_qo_len <= max_batch); PKV_FLAG_EXTEND_FULL (no causal
+ *               mask: every query row of request b attends all seq_lens[b]
+ *               tokens).
  * Reads seq_lens and either req_pool_indices + page_table (page mode) or
  * kv_indptr + kv_indices (flat mode: bind with PKV_BIND_REBUILD first).
  * Host errors: PKV_ERR_INVALID (null pointer, misalignment, batch < 0,
  * max_qo_len < 0, num_splits < 1, another flag), PKV_ERR_CAPACITY (batch >
- * max_batch, layer >= n_layers, the split partials do not fit),
+ * max_batch, layer >= n_layers, the split partials or lse rows do not fit),
  * PKV_ERR_UNSUPPORTED (head_dim not 64 / 128, or G not 1, 2, 4, 8, 16).
  * Device errors: PKV_DEVERR_LEN (n_b < 0, n_b > seq_lens[b],
  * n_b > max_qo_len or a length out of range: that request's rows are not
@@ -362,6 +369,25 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
 pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
                            const int32_t *qo_indptr, int max_qo_len, const void *q, void *out,
                            float scale, int num_splits, int flags, pkv_stream_t stream);
+
+/*
+ * Log-sum-exp merge of two attention results over disjoint key sets of the
+ * same query rows (a cascade: a prefix the requests share, attended once by
+ * pkv_extend_attn with PKV_FLAG_EXTEND_FULL, and each request's own suffix).
+ * For each of n_rows rows with normalised outputs o_a, o_b and their lse_a,
+ * lse_b (natural log; -inf: no keys):
+ *   M = max(lse_a, lse_b), w = exp(lse - M),
+ *   out = (w_a o_a + w_b o_b) / (w_a + w_b)   (zeros when both are -inf)
+ * and lse_out = M + ln(w_a + w_b) when lse_out is not NULL.
+ *   o_a, o_b   device fp32 [n_rows, head_dim], 16-byte aligned.
+ *   out        device bf16 [n_rows, head_dim] (fp32 with PKV_FLAG_OUT_F32).
+ * head_dim: a multiple of 64, at most 256.  Host errors: PKV_ERR_INVALID
+ * (null pointer, misalignment, n_rows < 0, other flags), PKV_ERR_UNSUPPORTED
+ * (head_dim).  Asynchronous on `stream`.
+ */
+pkv_status pkv_merge_lse(int n_rows, int head_dim, const float *o_a, const float *lse_a,
+                         const float *o_b, const float *lse_b, void *out, float *lse_out,
+                         int flags, pkv_stream_t stream);
 
 /*
  * Extend append: the new tokens' K and V rows into the pool.  k_new, v_new:

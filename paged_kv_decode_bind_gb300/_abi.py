@@ -19,6 +19,7 @@ PKV_FLAG_OUT_F32, PKV_FLAG_WRITE_LSE, PKV_FLAG_FORCE_SIMT, PKV_FLAG_FORCE_MMA = 
 PKV_FLAG_FORCE_GATHER, PKV_FLAG_PLAN_EARLY, PKV_FLAG_FIXED_CHUNK = 16, 32, 64
 PKV_FLAG_USE_PLAN = 128
 PKV_FLAG_TEST_SKIP_FIRST_TILE = 256
+PKV_FLAG_EXTEND_FULL = 512
 PKV_DEVERR_PAGE, PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT, PKV_DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16
 
@@ -27,7 +28,7 @@ EXPORTS = ("pkv_workspace_bytes", "pkv_bind_step", "pkv_choose_splits", "pkv_cho
            "pkv_decode_attn",
            "pkv_merge_partials", "pkv_decode_layer", "pkv_plan_step",
            "pkv_decode_attn_static_scratch",
-           "pkv_extend_attn", "pkv_extend_append",
+           "pkv_extend_attn", "pkv_extend_append", "pkv_merge_lse",
            "pkv_is_steady_increment",
            "pkv_status_string", "pkv_version")
 PKV_STATIC_SCRATCH_BYTES = 8 << 20
@@ -95,6 +96,8 @@ def load(path: str = LIB_PATH):
     lib.pkv_extend_attn.restype = i32
     lib.pkv_extend_append.argtypes = [W, i32, i32, vp, i32, vp, vp, vp]
     lib.pkv_extend_append.restype = i32
+    lib.pkv_merge_lse.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, i32, vp]
+    lib.pkv_merge_lse.restype = i32
     p64, p32 = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
     lib.pkv_is_steady_increment.argtypes = [p64, p32, i32, p64, p32, i32]
     lib.pkv_is_steady_increment.restype = i32
@@ -219,6 +222,14 @@ def pkv_extend_append(ws, batch, layer, qo_indptr, max_qo_len, k_new, v_new, str
     s = load().pkv_extend_append(_ws(ws), int(batch), int(layer), _ptr(qo_indptr),
                                  int(max_qo_len), _ptr(k_new), _ptr(v_new), _stream(stream))
     return _check("pkv_extend_append", s) if check else s
+
+
+def pkv_merge_lse(n_rows, head_dim, o_a, lse_a, o_b, lse_b, out, lse_out=None, flags=0,
+                  stream=None, check=True):
+    """Log-sum-exp merge of two results over disjoint keys of the same rows."""
+    s = load().pkv_merge_lse(int(n_rows), int(head_dim), _ptr(o_a), _ptr(lse_a), _ptr(o_b),
+                             _ptr(lse_b), _ptr(out), _ptr(lse_out), int(flags), _stream(stream))
+    return _check("pkv_merge_lse", s) if check else s
 
 
 def pkv_is_steady_increment(prev_ids, prev_lens, ids, lens) -> bool:

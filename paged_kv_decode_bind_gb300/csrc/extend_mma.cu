@@ -49,6 +49,9 @@ cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
                                  const int *qo_indptr, int max_qo_len, const void *k_new,
                                  const void *v_new, cudaStream_t st);
 bool extend_supported(int head_dim, int group);
+cudaError_t launch_merge_lse(int n_rows, int head_dim, const float *o_a, const float *lse_a,
+                             const float *o_b, const float *lse_b, void *out, float *lse_out,
+                             int flags, cudaStream_t st);
 
 namespace {
 
@@ -143,7 +146,8 @@ __device__ __forceinline__ XUnit xunit(const XArgs &a, int u, int tq, int jmax) 
   if (!ok && x.g == 0 && x.j == 0 && x.c == 0 && (threadIdx.x & 31) == 0)
     atomicOr(ws.err, PKV_DEVERR_LEN);
   x.live = ok && x.j * tq < x.n;
-  x.kend = x.live ? x.L - x.n + min(x.n, (x.j + 1) * tq) : 0;
+  x.kend = !x.live ? 0 : (a.flags & PKV_FLAG_EXTEND_FULL) ? x.L
+                                                             : x.L - x.n + min(x.n, (x.j + 1) * tq);
   const int chunk = ((x.kend + a.S - 1) / a.S + kXT - 1) / kXT * kXT;
   x.k0 = x.c * chunk;
   x.k1 = min(x.kend, x.k0 + chunk);
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(kXThreads, 2)
       const int row = 16 * warp + grp + 8 * e;
       const int i = x.j * TQ + row / G;
       const bool valid = i < x.n;
-      pos[e] = valid ? x.L - x.n + i : -1;
+      pos[e] = !valid ? -1 : (a.flags & PKV_FLAG_EXTEND_FULL) ? x.L - 1 : x.L - x.n + i;
       qrow[e] = valid ? (x.q0 + i) * Hq + x.g * G + row % G : -1;
     }
     // the warp's last attended key (tiles past it are skipped) and the first
@@ -485,6 +489,8 @@ __global__ void __launch_bounds__(kXThreads, 2)
         }
         continue;
       }
+      if ((a.flags & PKV_FLAG_WRITE_LSE) && tig == 0)
+        ws.lse[qrow[e]] = zero ? -INFINITY : m_run[e] * kLn2 + logf(l);
       const long long o = (long long)qrow[e] * D + 2 * tig;
 #pragma unroll
       for (int nd = 0; nd < C::ND; ++nd) {
@@ -545,6 +551,7 @@ __global__ void __launch_bounds__(128)
     }
     const bool zero = failed || !(wsum > 0.f);
     const float inv = zero ? 0.f : 1.f / wsum;
+    if ((flags & PKV_FLAG_WRITE_LSE) && lane == 0) ws.lse[row] = zero ? -INFINITY : M + logf(wsum);
 #pragma unroll
     for (int i = 0; i < E; i += 2) {
       const float v0 = zero ? 0.f : acc[i] * inv, v1 = zero ? 0.f : acc[i + 1] * inv;
@@ -554,6 +561,34 @@ __global__ void __launch_bounds__(128)
       else
         *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(out) + o) = pack_bf16x2(v0, v1);
     }
+  }
+}
+
+// Two-way log-sum-exp merge (a cascade's shared-prefix and own-suffix
+// results): one warp per row, two columns per lane and step.
+__global__ void __launch_bounds__(128)
+    merge_lse_kernel(int n_rows, int D, const float *o_a, const float *lse_a, const float *o_b,
+                     const float *lse_b, void *out, float *lse_out, int flags) {
+  const int lane = threadIdx.x & 31;
+  for (long long r = blockIdx.x * 4ll + (threadIdx.x >> 5); r < n_rows; r += gridDim.x * 4ll) {
+    const float la = lse_a[r], lb = lse_b[r];
+    const float M = fmaxf(la, lb);
+    const bool none = M == -INFINITY;
+    const float wa = (none || la == -INFINITY) ? 0.f : expf(la - M);
+    const float wb = (none || lb == -INFINITY) ? 0.f : expf(lb - M);
+    const float inv = none ? 0.f : 1.f / (wa + wb);
+    for (int d = 2 * lane; d < D; d += 64) {
+      const float2 x = *reinterpret_cast<const float2 *>(o_a + r * D + d);
+      const float2 y = *reinterpret_cast<const float2 *>(o_b + r * D + d);
+      const float v0 = none ? 0.f : (wa * x.x + wb * y.x) * inv;
+      const float v1 = none ? 0.f : (wa * x.y + wb * y.y) * inv;
+      if (flags & PKV_FLAG_OUT_F32)
+        *reinterpret_cast<float2 *>(static_cast<float *>(out) + r * D + d) = make_float2(v0, v1);
+      else
+        *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(out) + r * D + d) =
+            pack_bf16x2(v0, v1);
+    }
+    if (lse_out && lane == 0) lse_out[r] = none ? -INFINITY : M + logf(wa + wb);
   }
 }
 
@@ -717,6 +752,15 @@ cudaError_t launch_extend(const pkv_workspace &ws, int batch, int layer, const i
   PKV_X_CASE(64, 8) PKV_X_CASE(64, 16)
 #undef PKV_X_CASE
   return cudaErrorNotSupported;
+}
+
+cudaError_t launch_merge_lse(int n_rows, int head_dim, const float *o_a, const float *lse_a,
+                             const float *o_b, const float *lse_b, void *out, float *lse_out,
+                             int flags, cudaStream_t st) {
+  const long long blocks = ((long long)n_rows + 3) / 4;
+  merge_lse_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 128, 0, st>>>(
+      n_rows, head_dim, o_a, lse_a, o_b, lse_b, out, lse_out, flags);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,

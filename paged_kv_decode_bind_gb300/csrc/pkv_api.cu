@@ -16,6 +16,9 @@ cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
                                  const int *qo_indptr, int max_qo_len, const void *k_new,
                                  const void *v_new, cudaStream_t st);
 bool extend_supported(int head_dim, int group);
+cudaError_t launch_merge_lse(int n_rows, int head_dim, const float *o_a, const float *lse_a,
+                             const float *o_b, const float *lse_b, void *out, float *lse_out,
+                             int flags, cudaStream_t st);
 }  // namespace pkv
 
 namespace {
@@ -273,8 +276,13 @@ pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
                            float scale, int num_splits, int flags, pkv_stream_t stream) {
   pkv_status st = extend_common(ws, batch, layer, qo_indptr, max_qo_len, q, out);
   if (st != PKV_OK) return st;
-  if (flags & ~PKV_FLAG_OUT_F32) return PKV_ERR_INVALID;
+  if (flags & ~(PKV_FLAG_OUT_F32 | PKV_FLAG_WRITE_LSE | PKV_FLAG_EXTEND_FULL))
+    return PKV_ERR_INVALID;
   if (num_splits < 1) return PKV_ERR_INVALID;
+  // lse[query row, Hq] lives in ws->lse ([max_batch, Hq]): room for every row
+  if ((flags & PKV_FLAG_WRITE_LSE) &&
+      (!ws->lse || (long long)batch * max_qo_len > ws->max_batch))
+    return ws->lse ? PKV_ERR_CAPACITY : PKV_ERR_INVALID;
   if (num_splits > 1) {
     // partials of every (new token, query head, split) in o_part / ml_part
     if (!ws->o_part || !ws->ml_part || !aligned16(ws->o_part)) return PKV_ERR_INVALID;
@@ -296,6 +304,18 @@ pkv_status pkv_extend_append(const pkv_workspace *ws, int batch, int layer,
   if (batch == 0 || max_qo_len == 0) return PKV_OK;
   return from_cuda(launch_extend_append(*ws, batch, layer, qo_indptr, max_qo_len, k_new, v_new,
                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_merge_lse(int n_rows, int head_dim, const float *o_a, const float *lse_a,
+                         const float *o_b, const float *lse_b, void *out, float *lse_out,
+                         int flags, pkv_stream_t stream) {
+  if (n_rows < 0 || !o_a || !lse_a || !o_b || !lse_b || !out) return PKV_ERR_INVALID;
+  if (flags & ~PKV_FLAG_OUT_F32) return PKV_ERR_INVALID;
+  if (head_dim <= 0 || head_dim % 64 != 0 || head_dim > 256) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(o_a) || !aligned16(o_b) || !aligned16(out)) return PKV_ERR_INVALID;
+  if (n_rows == 0) return PKV_OK;
+  return from_cuda(launch_merge_lse(n_rows, head_dim, o_a, lse_a, o_b, lse_b, out, lse_out, flags,
+                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int pkv_is_steady_increment(const int64_t *prev_ids, const int32_t *prev_lens, int n_prev,

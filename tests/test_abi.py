@@ -125,7 +125,9 @@ def test_extend_host_validation():
         (dict(), 1, 0, f, 4, None, f, 0, P.PKV_ERR_INVALID),                         # q
         (dict(), 1, 0, f, 4, f + 8, f, 0, P.PKV_ERR_INVALID),                        # misaligned
         (dict(), 1, 0, f, -1, f, f, 0, P.PKV_ERR_INVALID),                           # max_qo_len
-        (dict(), 1, 0, f, 4, f, f, P.PKV_FLAG_WRITE_LSE, P.PKV_ERR_INVALID),         # flag
+        (dict(), 1, 0, f, 4, f, f, P.PKV_FLAG_FORCE_SIMT, P.PKV_ERR_INVALID),        # flag
+        (dict(lse=None), 1, 0, f, 4, f, f, P.PKV_FLAG_WRITE_LSE, P.PKV_ERR_INVALID),
+        (dict(), 2, 0, f, 4, f, f, P.PKV_FLAG_WRITE_LSE, P.PKV_ERR_CAPACITY),        # 8 rows
         (dict(), 0, 0, f, 4, f, f, 0, P.PKV_OK),                                     # no batch
         (dict(), 1, 0, f, 0, f, f, 0, P.PKV_OK),                                     # no tokens
     ]
@@ -144,6 +146,18 @@ def test_extend_host_validation():
     assert A(_ws(), 1, 0, f, 4, f, None, 0, check=False) == P.PKV_ERR_INVALID
     assert A(_ws(), 5, 0, f, 4, f, f, 0, check=False) == P.PKV_ERR_CAPACITY
     assert A(_ws(), 1, 0, f, 0, f, f, 0, check=False) == P.PKV_OK
+
+
+def test_merge_lse_host_validation():
+    f = 1 << 20
+    M = P.pkv_merge_lse
+    assert M(-1, 128, f, f, f, f, f, None, 0, 0, check=False) == P.PKV_ERR_INVALID
+    assert M(4, 96, f, f, f, f, f, None, 0, 0, check=False) == P.PKV_ERR_UNSUPPORTED
+    assert M(4, 128, None, f, f, f, f, None, 0, 0, check=False) == P.PKV_ERR_INVALID
+    assert M(4, 128, f + 8, f, f, f, f, None, 0, 0, check=False) == P.PKV_ERR_INVALID
+    assert M(4, 128, f, f, f, f, f, None, P.PKV_FLAG_WRITE_LSE, 0, check=False) == \
+        P.PKV_ERR_INVALID
+    assert M(0, 128, f, f, f, f, f, None, 0, 0, check=False) == P.PKV_OK
 
 
 def test_choose_splits():

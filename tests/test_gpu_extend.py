@@ -237,3 +237,61 @@ def test_extend_one_token_matches_decode_kernel(cuda):
     assert int(ws.err.item()) == 0
     dec = ws.out_f32(3)
     assert (out - dec).abs().max().item() <= 2e-3
+
+
+def _cascade(cuda, ws, p, B, prefix_len, q, layer, Sp, Ss):
+    """Decode attention over a shared prefix in three launches: the prefix once
+    for all B queries (extend without a causal mask over a one-request view),
+    each request's own suffix (decode over a view of the table past the
+    prefix), and their log-sum-exp merge.  Returns the fp32 output."""
+    Hq, D, P = p.n_q_heads, p.head_dim, p.page_size
+    f32 = dict(dtype=torch.float32, device=cuda)
+    i32 = dict(dtype=torch.int32, device=cuda)
+    out_a, out_b, out = (torch.zeros((B, Hq, D), **f32) for _ in range(3))
+    lse_a, lse_b = torch.zeros(B * Hq, **f32), torch.zeros(B * Hq, **f32)
+    # prefix view: one request (request 0's table row) of prefix_len tokens
+    pre_len = torch.tensor([prefix_len], **i32)
+    pre_row = ws.req_pool_indices[:1].clone()
+    qo = torch.tensor([0, B], **i32)
+    part_o = torch.zeros(B * Hq * Sp * D, **f32)
+    part_ml = torch.zeros(B * Hq * Sp * 2, **f32)
+    vp = A.PkvWorkspace.from_buffer_copy(ws.struct)
+    vp.seq_lens, vp.req_pool_indices = pre_len.data_ptr(), pre_row.data_ptr()
+    vp.max_batch, vp.max_splits = B, Sp
+    vp.lse, vp.o_part, vp.ml_part = lse_a.data_ptr(), part_o.data_ptr(), part_ml.data_ptr()
+    A.pkv_extend_attn(vp, 1, layer, qo, B, q, out_a, p.scale, num_splits=Sp,
+                      flags=A.PKV_FLAG_EXTEND_FULL | A.PKV_FLAG_OUT_F32 | A.PKV_FLAG_WRITE_LSE)
+    # suffix view: the table past the prefix's pages, the own lengths
+    suf_len = (ws.seq_lens[:B] - prefix_len).contiguous()
+    vs = A.PkvWorkspace.from_buffer_copy(ws.struct)
+    vs.page_table = ws.page_table.data_ptr() + (prefix_len // P) * 4
+    vs.seq_lens = suf_len.data_ptr()
+    vs.out, vs.lse = out_b.data_ptr(), lse_b.data_ptr()
+    A.pkv_decode_attn(vs, B, layer, q, p.scale, Ss, A.PKV_FLAG_OUT_F32 | A.PKV_FLAG_WRITE_LSE)
+    if Ss > 1:
+        A.pkv_merge_partials(vs, B, Ss, A.PKV_FLAG_OUT_F32 | A.PKV_FLAG_WRITE_LSE)
+    A.pkv_merge_lse(B * Hq, D, out_a, lse_a, out_b, lse_b, out, None, A.PKV_FLAG_OUT_F32)
+    torch.cuda.synchronize()
+    return out.to(torch.float64).cpu().numpy()
+
+
+@pytest.mark.parametrize("Sp,Ss", [(1, 1), (4, 2)])
+def test_cascade_shared_prefix(cuda, Sp, Ss):
+    # Requests whose first 512 tokens alias the same pages: the cascade
+    # (shared prefix once + own suffix + merge) equals decode attention over
+    # each request's whole context.
+    B, prefix_len = 8, 512
+    lens = [prefix_len + x for x in (40, 1, 130, 77, 200, 16, 95, 3)]
+    p = W.make_problem("cascade", batch=B, n_layers=2, n_q_heads=32, n_kv_heads=8,
+                       head_dim=128, page_size=16, seq_lens=lens, seed=5100)
+    rows = p.req_pool_indices.tolist()
+    shared = p.page_table[rows[0], :prefix_len // 16].clone()
+    for b in range(1, B):
+        p.page_table[rows[b], :prefix_len // 16] = shared
+    ws = Workspace.from_problem(p, max_splits=max(2, Ss))
+    q = W.normal_bf16((B, 32, 128), 5101)
+    got = _cascade(cuda, ws, p, B, prefix_len, q.to(cuda), 1, Sp, Ss)
+    assert int(ws.err.item()) == 0
+    ref, _ = R.decode_attention(R.tensor_bits(q), R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool),
+                                1, _slots(p), p.scale, 8)
+    check_attention(got, ref, f"cascade Sp={Sp} Ss={Ss}")
