@@ -1,0 +1,100 @@
+"""Decode attention for a batch whose requests share prefix pages.
+
+When every request of a batch starts with the same ``prefix_len`` tokens
+stored in the same physical pages (the engine's prefix-shared pages: many
+requests aliasing one prompt's pages), attending each request's whole
+context reads the shared prefix once per request.  ``CascadeDecoder`` reads
+it once for the batch, in three calls of the C ABI per layer:
+
+1. ``pkv_extend_attn`` with ``PKV_FLAG_EXTEND_FULL`` over a one-request view
+   of the workspace whose context is the prefix: every (request, query head)
+   row attends all ``prefix_len`` tokens, writing its normalised output and
+   log-sum-exp;
+2. ``pkv_decode_attn`` over a view whose page table starts past the prefix's
+   pages and whose lengths are the requests' own suffix lengths;
+3. ``pkv_merge_lse``, which combines the two by log-sum-exp into ``out``.
+
+Every buffer is allocated here once, at fixed addresses, so a step (and its
+capture into a CUDA graph) allocates nothing.  The suffix lengths live in
+``suffix_lens``; ``bind`` advances them with the library's metadata bind on
+the suffix view (and appends the new K/V rows), like ``pkv_bind_step`` does
+for a plain batch; the view has its own ``kv_indptr``, ``position_ids`` and
+``out_loc`` (positions relative to the end of the prefix), so the main
+workspace's metadata is left as it is.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _abi
+
+
+class CascadeDecoder:
+    def __init__(self, ws, batch: int, prefix_len: int, *, scale: float, prefix_splits: int = 1,
+                 suffix_splits: int = 1):
+        sh = ws.shape
+        P, Hq, D = sh["page_size"], sh["n_q_heads"], sh["head_dim"]
+        if sh["index_mode"] != _abi.PKV_IDX_PAGE_TABLE or prefix_len % P:
+            raise ValueError("the shared prefix must be whole pages of a page-table workspace")
+        if suffix_splits > sh["max_splits"]:
+            raise ValueError("suffix_splits exceeds the workspace's max_splits")
+        dev = ws.device
+        f32 = dict(dtype=torch.float32, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.ws, self.batch, self.prefix_len, self.scale = ws, batch, prefix_len, scale
+        self.prefix_splits, self.suffix_splits = prefix_splits, suffix_splits
+        self.out_prefix = torch.zeros((batch, Hq, D), **f32)
+        self.out_suffix = torch.zeros((batch, Hq, D), **f32)
+        self.lse_prefix = torch.zeros(batch * Hq, **f32)
+        self.lse_suffix = torch.zeros(batch * Hq, **f32)
+        self.qo_indptr = torch.tensor([0, batch], **i32)
+        self.prefix_lens = torch.tensor([prefix_len], **i32)
+        self.prefix_row = ws.req_pool_indices[:1].clone()
+        self.part_o = torch.zeros(batch * Hq * max(1, prefix_splits) * D, **f32)
+        self.part_ml = torch.zeros(batch * Hq * max(1, prefix_splits) * 2, **f32)
+        self.suffix_lens = (ws.seq_lens[:batch] - prefix_len).contiguous()
+        self.suffix_indptr = torch.zeros(batch + 1, **i32)
+        self.suffix_positions = torch.zeros(batch, **i32)
+        self.suffix_out_loc = torch.zeros(batch, **i32)
+        # prefix view: one request (request 0's table row) of prefix_len tokens
+        # whose batch's queries are the extend rows
+        vp = _abi.PkvWorkspace.from_buffer_copy(ws.struct)
+        vp.seq_lens, vp.req_pool_indices = self.prefix_lens.data_ptr(), self.prefix_row.data_ptr()
+        vp.max_batch, vp.max_splits = batch, max(1, prefix_splits)
+        vp.lse, vp.o_part, vp.ml_part = (self.lse_prefix.data_ptr(), self.part_o.data_ptr(),
+                                         self.part_ml.data_ptr())
+        self.prefix_view = vp
+        # suffix view: the table past the prefix's pages, the own lengths
+        vs = _abi.PkvWorkspace.from_buffer_copy(ws.struct)
+        vs.page_table = ws.page_table.data_ptr() + (prefix_len // P) * 4
+        vs.seq_lens = self.suffix_lens.data_ptr()
+        vs.kv_indptr, vs.position_ids = (self.suffix_indptr.data_ptr(),
+                                         self.suffix_positions.data_ptr())
+        vs.out_loc = self.suffix_out_loc.data_ptr()
+        vs.max_batch = batch
+        vs.out, vs.lse = self.out_suffix.data_ptr(), self.lse_suffix.data_ptr()
+        self.suffix_view = vs
+
+    def bind(self, mode=_abi.PKV_BIND_STEADY, layer_begin=0, layer_count=0, k_new=None,
+             v_new=None, stream=None):
+        """Metadata bind (and appends) on the suffix view: its lengths, and
+        out_loc of the new tokens past the shared prefix."""
+        _abi.pkv_bind_step(self.suffix_view, self.batch, mode, layer_begin, layer_count, k_new,
+                           v_new, stream)
+
+    def layer(self, layer, q, out, flags=0, stream=None):
+        """Attention of the batch's queries q [batch, Hq, D] over each request's
+        shared prefix and own suffix into out (bf16, fp32 with
+        PKV_FLAG_OUT_F32)."""
+        lse = _abi.PKV_FLAG_OUT_F32 | _abi.PKV_FLAG_WRITE_LSE
+        _abi.pkv_extend_attn(self.prefix_view, 1, layer, self.qo_indptr, self.batch, q,
+                             self.out_prefix, self.scale, num_splits=self.prefix_splits,
+                             flags=_abi.PKV_FLAG_EXTEND_FULL | lse, stream=stream)
+        _abi.pkv_decode_attn(self.suffix_view, self.batch, layer, q, self.scale,
+                             self.suffix_splits, lse, stream)
+        if self.suffix_splits > 1:
+            _abi.pkv_merge_partials(self.suffix_view, self.batch, self.suffix_splits, lse, stream)
+        sh = self.ws.shape
+        _abi.pkv_merge_lse(self.batch * sh["n_q_heads"], sh["head_dim"], self.out_prefix,
+                           self.lse_prefix, self.out_suffix, self.lse_suffix, out, None,
+                           flags & _abi.PKV_FLAG_OUT_F32, stream)

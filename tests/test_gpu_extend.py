@@ -11,7 +11,7 @@ import torch
 
 import oracle.ref as R
 import pkv_inputs as W
-from paged_kv_decode_bind_gb300 import Workspace
+from paged_kv_decode_bind_gb300 import CascadeDecoder, Workspace
 from paged_kv_decode_bind_gb300 import _abi as A
 
 from parity import check_attention
@@ -239,42 +239,6 @@ def test_extend_one_token_matches_decode_kernel(cuda):
     assert (out - dec).abs().max().item() <= 2e-3
 
 
-def _cascade(cuda, ws, p, B, prefix_len, q, layer, Sp, Ss):
-    """Decode attention over a shared prefix in three launches: the prefix once
-    for all B queries (extend without a causal mask over a one-request view),
-    each request's own suffix (decode over a view of the table past the
-    prefix), and their log-sum-exp merge.  Returns the fp32 output."""
-    Hq, D, P = p.n_q_heads, p.head_dim, p.page_size
-    f32 = dict(dtype=torch.float32, device=cuda)
-    i32 = dict(dtype=torch.int32, device=cuda)
-    out_a, out_b, out = (torch.zeros((B, Hq, D), **f32) for _ in range(3))
-    lse_a, lse_b = torch.zeros(B * Hq, **f32), torch.zeros(B * Hq, **f32)
-    # prefix view: one request (request 0's table row) of prefix_len tokens
-    pre_len = torch.tensor([prefix_len], **i32)
-    pre_row = ws.req_pool_indices[:1].clone()
-    qo = torch.tensor([0, B], **i32)
-    part_o = torch.zeros(B * Hq * Sp * D, **f32)
-    part_ml = torch.zeros(B * Hq * Sp * 2, **f32)
-    vp = A.PkvWorkspace.from_buffer_copy(ws.struct)
-    vp.seq_lens, vp.req_pool_indices = pre_len.data_ptr(), pre_row.data_ptr()
-    vp.max_batch, vp.max_splits = B, Sp
-    vp.lse, vp.o_part, vp.ml_part = lse_a.data_ptr(), part_o.data_ptr(), part_ml.data_ptr()
-    A.pkv_extend_attn(vp, 1, layer, qo, B, q, out_a, p.scale, num_splits=Sp,
-                      flags=A.PKV_FLAG_EXTEND_FULL | A.PKV_FLAG_OUT_F32 | A.PKV_FLAG_WRITE_LSE)
-    # suffix view: the table past the prefix's pages, the own lengths
-    suf_len = (ws.seq_lens[:B] - prefix_len).contiguous()
-    vs = A.PkvWorkspace.from_buffer_copy(ws.struct)
-    vs.page_table = ws.page_table.data_ptr() + (prefix_len // P) * 4
-    vs.seq_lens = suf_len.data_ptr()
-    vs.out, vs.lse = out_b.data_ptr(), lse_b.data_ptr()
-    A.pkv_decode_attn(vs, B, layer, q, p.scale, Ss, A.PKV_FLAG_OUT_F32 | A.PKV_FLAG_WRITE_LSE)
-    if Ss > 1:
-        A.pkv_merge_partials(vs, B, Ss, A.PKV_FLAG_OUT_F32 | A.PKV_FLAG_WRITE_LSE)
-    A.pkv_merge_lse(B * Hq, D, out_a, lse_a, out_b, lse_b, out, None, A.PKV_FLAG_OUT_F32)
-    torch.cuda.synchronize()
-    return out.to(torch.float64).cpu().numpy()
-
-
 @pytest.mark.parametrize("Sp,Ss", [(1, 1), (4, 2)])
 def test_cascade_shared_prefix(cuda, Sp, Ss):
     # Requests whose first 512 tokens alias the same pages: the cascade
@@ -290,8 +254,46 @@ def test_cascade_shared_prefix(cuda, Sp, Ss):
         p.page_table[rows[b], :prefix_len // 16] = shared
     ws = Workspace.from_problem(p, max_splits=max(2, Ss))
     q = W.normal_bf16((B, 32, 128), 5101)
-    got = _cascade(cuda, ws, p, B, prefix_len, q.to(cuda), 1, Sp, Ss)
+    cas = CascadeDecoder(ws, B, prefix_len, scale=p.scale, prefix_splits=Sp, suffix_splits=Ss)
+    out = torch.zeros((B, 32, 128), dtype=torch.float32, device=cuda)
+    cas.layer(1, q.to(cuda), out, flags=A.PKV_FLAG_OUT_F32)
+    torch.cuda.synchronize()
     assert int(ws.err.item()) == 0
     ref, _ = R.decode_attention(R.tensor_bits(q), R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool),
                                 1, _slots(p), p.scale, 8)
-    check_attention(got, ref, f"cascade Sp={Sp} Ss={Ss}")
+    check_attention(out.to(torch.float64).cpu().numpy(), ref, f"cascade Sp={Sp} Ss={Ss}")
+
+
+def test_cascade_steady_step(cuda):
+    # A steady decode step through the cascade: its bind advances the suffix
+    # lengths and appends the new rows past the prefix; the attention then
+    # equals decode over the whole grown contexts.
+    B, prefix_len = 6, 256
+    lens = [prefix_len + x for x in (30, 1, 100, 64, 7, 150)]
+    p = W.make_problem("cascade_step", batch=B, n_layers=2, n_q_heads=16, n_kv_heads=2,
+                       head_dim=128, page_size=16, seq_lens=lens, steps=1, seed=5200)
+    rows = p.req_pool_indices.tolist()
+    shared = p.page_table[rows[0], :prefix_len // 16].clone()
+    for b in range(1, B):
+        p.page_table[rows[b], :prefix_len // 16] = shared
+    ws = Workspace.from_problem(p, max_splits=2)
+    q, k, v = W.step_inputs(p, 0)
+    cas = CascadeDecoder(ws, B, prefix_len, scale=p.scale, prefix_splits=2)
+    cas.bind(A.PKV_BIND_STEADY, 0, 2, k.to(cuda), v.to(cuda))
+    out = torch.zeros((B, 16, 128), dtype=torch.bfloat16, device=cuda)
+    cas.layer(1, q[1].to(cuda), out)
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) == 0
+    assert cas.suffix_lens.tolist() == [x - prefix_len + 1 for x in lens]
+    meta = R.bind(lens, req_pool_indices=p.req_pool_indices.numpy(),
+                  page_table=p.page_table.numpy(), page_size=16, mode=R.STEADY)
+    kb, vb = R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool)
+    for layer in range(2):
+        kb = R.append_rows(kb, layer, meta["out_loc"], R.tensor_bits(k)[layer])
+        vb = R.append_rows(vb, layer, meta["out_loc"], R.tensor_bits(v)[layer])
+    assert np.array_equal(R.tensor_bits(ws.k_pool.cpu()), kb)
+    slots = [R.token_slots(b, meta["seq_lens"][b], page_table=p.page_table.numpy(),
+                           req_pool_indices=p.req_pool_indices.numpy(), page_size=16)
+             for b in range(B)]
+    ref, _ = R.decode_attention(R.tensor_bits(q)[1], kb, vb, 1, slots, p.scale, 2)
+    check_attention(out.to(torch.float64).cpu().numpy(), ref, "cascade steady step")
