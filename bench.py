@@ -47,6 +47,8 @@ def parse_args(argv=None):
                     help="0 = pkv_choose_pieces (fused) / pkv_choose_splits (fixed chunks)")
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--unfused", action="store_true", help="separate append/attention/merge")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared_prefix_b32: the shared prefix once per batch (CascadeDecoder)")
     ap.add_argument("--no-kernel-events", action="store_true",
                     help="skip the graphs with per-kernel event nodes")
     ap.add_argument("--layers", type=int, default=None,
@@ -130,7 +132,7 @@ class ClockSampler:
 
 # layers of each workload (the oracle arm times one; the layers are alike)
 WORKLOAD_LAYERS = {"single_d64": 1, "gqa4_b4_paged": 24, "gqa4_b16_flat_skewed": 24,
-                   "gqa4_long_65536": 1, "gqa8_graph_sweep": 24}
+                   "gqa4_long_65536": 1, "gqa8_graph_sweep": 24, "shared_prefix_b32": 24}
 
 
 def _oracle_problem(name, batch):
@@ -510,6 +512,119 @@ def run_extend_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- cascade decode --
+
+def run_cascade_ours(args, rank, world, local_rank):
+    """shared_prefix_b32 through CascadeDecoder: a step is its bind (suffix
+    lengths, appends past the prefix) and, per layer, the shared prefix once
+    for the batch, the own suffixes and their log-sum-exp merge, captured as
+    one CUDA graph per position in a round of steady steps."""
+    import torch
+
+    import pkv_inputs as W
+    from paged_kv_decode_bind_gb300 import CascadeDecoder, Workspace
+    from paged_kv_decode_bind_gb300 import _abi as A
+    from paged_kv_decode_bind_gb300 import dist as D
+
+    if args.workload != "shared_prefix_b32":
+        raise SystemExit("--cascade applies to shared_prefix_b32")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    p = W.workload(args.workload, batch=args.batch, steps=ROUND, n_layers=args.layers,
+                   seed=D.rank_seed(20260000 + W.WORKLOADS.index(args.workload) + 1, rank))
+    B, NL = p.batch, p.n_layers
+    prefix = p.shared_prefix_pages * p.page_size
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    tq = 64 // p.group
+    Sp = max(1, min(2 * sms // (-(-B // tq) * p.n_kv_heads), prefix // 256))
+    ws = Workspace.from_problem(p, device=dev)
+    cas = CascadeDecoder(ws, B, prefix, scale=p.scale, prefix_splits=Sp)
+    q, k, v = W.step_inputs(p, 0)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty((NL, B, p.n_q_heads, p.head_dim), dtype=torch.bfloat16, device=dev)
+    suf0 = cas.suffix_lens.clone()
+    L0 = p.seq_lens.tolist()
+
+    def calls(s):
+        cas.bind(A.PKV_BIND_STEADY, 0, NL, kd, vd, s)
+        for l in range(NL):
+            cas.layer(l, qd[l], out[l], stream=s)
+
+    graphs = []
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(ROUND):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                calls(side)
+            graphs.append(g)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    cas.suffix_lens.copy_(suf0)
+
+    def step(i):
+        if i % ROUND == 0:
+            cas.suffix_lens.copy_(suf0)
+        graphs[i % ROUND].replay()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    dt = e0.elapsed_time(e1) / 1e3
+    errbits = int(ws.err.item())
+
+    def lens_at(i):
+        return [x + i % ROUND + 1 for x in L0]
+    total = sum(NL * algorithmic_bytes(lens_at(i), p) for i in range(K))
+    # the bytes a reader of each distinct page needs: the prefix once
+    uniq = sum(NL * (algorithmic_bytes(lens_at(i), p) -
+                     (B - 1) * prefix * p.n_kv_heads * p.head_dim * 4) for i in range(K))
+    dt, total = D.reduce_time_and_work(dt, float(total), device=dev)
+    if rank != 0:
+        return
+    peak, src = peaks()
+    layer_s = dt / (K * NL)
+    ach = uniq / K / NL / layer_s / 1e9
+    line = {
+        "metric": METRIC, "value": total / dt / 1e9, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": dt / K * 1e3, "us_per_layer_step": layer_s * 1e6,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": B, "n_layers": NL,
+                   "n_q_heads": p.n_q_heads, "n_kv_heads": p.n_kv_heads, "head_dim": p.head_dim,
+                   "page_size": p.page_size, "shared_prefix": prefix,
+                   "seq_lens_start": [min(L0), max(L0), sum(L0)], "prefix_splits": Sp,
+                   "steady_steps_per_round": ROUND, "cuda_graph": True, "cascade": True,
+                   "l2": "no flush: the prefix is read once per layer by design",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                     "frac": ach / peak, "traffic": None, "peak_source": src,
+                     "kernel": "CascadeDecoder: extend_mma_kernel (prefix, no causal mask) + "
+                               "extend_merge_kernel + decode_mma_kernel (suffixes) + "
+                               "merge_lse_kernel, per layer",
+                     "kernel_us_mean": layer_s * 1e6,
+                     "kernel_time_from": "whole steady step (bind + layers) / layers",
+                     "bytes_counted": "each distinct page once (the shared prefix once per layer)"},
+        "gpu_launches": (1 + NL * (4 if Sp > 1 else 3)) * K,
+        "clocks": clk,
+        "device_err_bits": errbits,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------------- GPU arm --
 
 def traffic_for(kernel_src_hash, workload, algorithmic_bytes):
@@ -784,7 +899,8 @@ def main(argv=None):
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        (run_extend_ours if extend else run_ours)(args, rank, world, local_rank)
+        fn = run_extend_ours if extend else (run_cascade_ours if args.cascade else run_ours)
+        fn(args, rank, world, local_rank)
     finally:
         if world > 1:
             import torch.distributed as dist

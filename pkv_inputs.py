@@ -60,6 +60,7 @@ class DecodeProblem:
     v_pool: torch.Tensor            # bf16 [NL, pool_slots, Hkv, D]
     scale: float                    # softmax scale, an fp32-representable value
     seed: int
+    shared_prefix_pages: int = 0    # leading table entries every request shares
 
     @property
     def group(self) -> int:
@@ -118,12 +119,15 @@ def make_problem(
     scale: float | None = None,
     seed: int = 20260000,
     fill_unused: bool = True,
+    shared_prefix_pages: int = 0,
 ) -> DecodeProblem:
     """Build one decode problem.
 
     ``seq_lens`` is a list of cached lengths.  Flat mode (token-level
     ``kv_indices``) is used when ``page_size == 1`` unless ``index_mode`` says
     otherwise; then ``page_table`` is the request-to-token table.
+    ``shared_prefix_pages`` > 0: every request's first that many table
+    entries are the same physical pages (request 0's), stored once.
     """
     seq = [int(x) for x in seq_lens]
     assert len(seq) == batch
@@ -131,7 +135,9 @@ def make_problem(
     if index_mode is None:
         index_mode = INDEX_FLAT if P == 1 else INDEX_PAGE_TABLE
     pages_per_req = [max(1, math.ceil((L + steps) / P)) for L in seq]
-    need = sum(pages_per_req)
+    sp = shared_prefix_pages
+    assert all(n > sp for n in pages_per_req) or sp == 0, "a request must own a page past the prefix"
+    need = sum(pages_per_req) - sp * (batch - 1)
     n_pages = pool_pages if pool_pages is not None else max(need, int(math.ceil(need * pool_factor)))
     assert n_pages >= need, "pool too small"
     pool_slots = n_pages * P
@@ -145,8 +151,13 @@ def make_problem(
     off = 0
     for b in range(batch):
         n = pages_per_req[b]
-        table[rows[b], :n] = perm[off:off + n]
-        off += n
+        if b > 0 and sp:
+            table[rows[b], :sp] = table[rows[0], :sp]
+            table[rows[b], sp:n] = perm[off:off + n - sp]
+            off += n - sp
+        else:
+            table[rows[b], :n] = perm[off:off + n]
+            off += n
 
     shape = (n_layers, pool_slots, n_kv_heads, head_dim)
     if fill_unused:
@@ -180,7 +191,7 @@ def make_problem(
         pool_slots=pool_slots, max_reqs=max_reqs, max_pages_per_req=max_pages,
         steps=steps, seq_lens=torch.tensor(seq, dtype=torch.int32),
         req_pool_indices=rows, page_table=table, k_pool=k_pool, v_pool=v_pool,
-        scale=scale, seed=seed,
+        scale=scale, seed=seed, shared_prefix_pages=shared_prefix_pages,
     )
 
 
@@ -200,7 +211,7 @@ def step_inputs(p: DecodeProblem, step: int, layers=None):
 # --------------------------------------------------------------------------
 
 WORKLOADS = ("single_d64", "gqa4_b4_paged", "gqa4_b16_flat_skewed",
-             "gqa4_long_65536", "gqa8_graph_sweep")
+             "gqa4_long_65536", "gqa8_graph_sweep", "shared_prefix_b32")
 
 
 def _uniform_lens(n, lo, hi, seed):
@@ -229,6 +240,9 @@ def workload(name: str, *, batch: int | None = None, n_layers: int | None = None
                         1% of key rows scaled x8.
     gqa8_graph_sweep    B in {1,4,8,16,32,64}, 24 layers, 16/2, D=128, P=16,
                         L ~ U{1024..4096}.
+    shared_prefix_b32   B=32, 24 layers, 32/8, D=128, P=16: every request's
+                        first 4096 tokens are the same 256 pages (stored
+                        once), then 64..192 tokens of its own.
 
     ``shrink`` > 1 divides lengths (and layers, to at most 2) for the
     oracle-sized variants of the same recipe.
@@ -262,6 +276,15 @@ def workload(name: str, *, batch: int | None = None, n_layers: int | None = None
                             head_dim=128, page_size=16, seq_lens=[L] * B, steps=steps,
                             pool_factor=1.0, outlier_frac=0.01, seed=seed,
                             fill_unused=fill_unused)
+    if name == "shared_prefix_b32":
+        B = batch or 32
+        prefix = max(16, 4096 // shrink) // 16 * 16
+        own = _uniform_lens(B, max(1, 64 // shrink), max(1, 192 // shrink), _sub(seed, 0))
+        nl = n_layers or (24 if shrink == 1 else 2)
+        return make_problem(name, batch=B, n_layers=nl, n_q_heads=32, n_kv_heads=8,
+                            head_dim=128, page_size=16, seq_lens=[prefix + x for x in own],
+                            steps=steps, pool_factor=1.0, seed=seed, fill_unused=fill_unused,
+                            shared_prefix_pages=prefix // 16)
     if name == "gqa8_graph_sweep":
         B = batch or 16
         lens = _uniform_lens(B, max(1, 1024 // shrink), max(1, 4096 // shrink), _sub(seed, 0))

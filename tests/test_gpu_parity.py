@@ -357,3 +357,10 @@ def test_shared_prefix_pages(cuda):
     for kern in ("fused", "mma", "fused_gather"):
         run_steps(p, S=3, check_pool=True, check_partials=kern == "mma",
                   flags=PATHS[kern][0], fused=PATHS[kern][1])
+
+
+def test_shared_prefix_workload_small(cuda):
+    # The benchmark's prefix-shared workload (every request's first pages are
+    # one set stored once), oracle-sized: fused decode through the aliased pages.
+    p = W.workload("shared_prefix_b32", shrink=16, steps=1)
+    run_steps(p, S=4, check_pool=True)
