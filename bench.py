@@ -545,10 +545,12 @@ def run_cascade_ours(args, rank, world, local_rank):
     suf0 = cas.suffix_lens.clone()
     L0 = p.seq_lens.tolist()
 
+    branch = torch.cuda.Stream()  # the suffix attention's parallel graph branch
+
     def calls(s):
         cas.bind(A.PKV_BIND_STEADY, 0, NL, kd, vd, s)
         for l in range(NL):
-            cas.layer(l, qd[l], out[l], stream=s)
+            cas.layer(l, qd[l], out[l], stream=s, suffix_stream=branch)
 
     graphs = []
     side = torch.cuda.Stream()

@@ -74,6 +74,9 @@ class CascadeDecoder:
         vs.max_batch = batch
         vs.out, vs.lse = self.out_suffix.data_ptr(), self.lse_suffix.data_ptr()
         self.suffix_view = vs
+        # fork / join of the optional second stream (a parallel graph branch)
+        self.fork = torch.cuda.Event()
+        self.join = torch.cuda.Event()
 
     def bind(self, mode=_abi.PKV_BIND_STEADY, layer_begin=0, layer_count=0, k_new=None,
              v_new=None, stream=None):
@@ -82,19 +85,29 @@ class CascadeDecoder:
         _abi.pkv_bind_step(self.suffix_view, self.batch, mode, layer_begin, layer_count, k_new,
                            v_new, stream)
 
-    def layer(self, layer, q, out, flags=0, stream=None):
+    def layer(self, layer, q, out, flags=0, stream=None, suffix_stream=None):
         """Attention of the batch's queries q [batch, Hq, D] over each request's
         shared prefix and own suffix into out (bf16, fp32 with
-        PKV_FLAG_OUT_F32)."""
+        PKV_FLAG_OUT_F32).  With suffix_stream the suffix attention runs there,
+        concurrently with the prefix's (fork and join by events, which a CUDA
+        graph capture turns into a parallel branch)."""
         lse = _abi.PKV_FLAG_OUT_F32 | _abi.PKV_FLAG_WRITE_LSE
+        main = stream if stream is not None else torch.cuda.current_stream()
+        side = suffix_stream if suffix_stream is not None else main
+        if side is not main:
+            self.fork.record(main)
+            side.wait_event(self.fork)
+        _abi.pkv_decode_attn(self.suffix_view, self.batch, layer, q, self.scale,
+                             self.suffix_splits, lse, side)
+        if self.suffix_splits > 1:
+            _abi.pkv_merge_partials(self.suffix_view, self.batch, self.suffix_splits, lse, side)
         _abi.pkv_extend_attn(self.prefix_view, 1, layer, self.qo_indptr, self.batch, q,
                              self.out_prefix, self.scale, num_splits=self.prefix_splits,
-                             flags=_abi.PKV_FLAG_EXTEND_FULL | lse, stream=stream)
-        _abi.pkv_decode_attn(self.suffix_view, self.batch, layer, q, self.scale,
-                             self.suffix_splits, lse, stream)
-        if self.suffix_splits > 1:
-            _abi.pkv_merge_partials(self.suffix_view, self.batch, self.suffix_splits, lse, stream)
+                             flags=_abi.PKV_FLAG_EXTEND_FULL | lse, stream=main)
+        if side is not main:
+            self.join.record(side)
+            main.wait_event(self.join)
         sh = self.ws.shape
         _abi.pkv_merge_lse(self.batch * sh["n_q_heads"], sh["head_dim"], self.out_prefix,
                            self.lse_prefix, self.out_suffix, self.lse_suffix, out, None,
-                           flags & _abi.PKV_FLAG_OUT_F32, stream)
+                           flags & _abi.PKV_FLAG_OUT_F32, main)

@@ -256,7 +256,9 @@ def test_cascade_shared_prefix(cuda, Sp, Ss):
     q = W.normal_bf16((B, 32, 128), 5101)
     cas = CascadeDecoder(ws, B, prefix_len, scale=p.scale, prefix_splits=Sp, suffix_splits=Ss)
     out = torch.zeros((B, 32, 128), dtype=torch.float32, device=cuda)
-    cas.layer(1, q.to(cuda), out, flags=A.PKV_FLAG_OUT_F32)
+    # the suffix attention on a second stream when the prefix is split
+    cas.layer(1, q.to(cuda), out, flags=A.PKV_FLAG_OUT_F32,
+              suffix_stream=torch.cuda.Stream() if Sp > 1 else None)
     torch.cuda.synchronize()
     assert int(ws.err.item()) == 0
     ref, _ = R.decode_attention(R.tensor_bits(q), R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool),
