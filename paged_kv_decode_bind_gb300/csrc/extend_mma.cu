@@ -3,7 +3,9 @@
 // engine keeps in its workspace for the prefill step (workspace.py page,
 // bullet 19).  Request b holds L_b tokens in the pool, the last n_b of them
 // new (qo_indptr[b + 1] - qo_indptr[b]); new token i sits at position
-// L_b - n_b + i and attends causally to tokens 0 .. L_b - n_b + i.
+// L_b - n_b + i and attends causally to tokens 0 .. L_b - n_b + i
+// (PKV_FLAG_EXTEND_FULL: every row attends all L_b tokens, as a batch's
+// decode queries over a prefix their requests share).
 //
 // Math.  A block computes 64 query rows of one (request, KV head): rows are
 // (new token, query head of the group) pairs, 64 / G tokens x G heads, so a
@@ -12,7 +14,7 @@
 // the 16-row side, 8 keys per n-tile, fp32 accumulation), the causal mask
 // and an online softmax in fp32 (exp2), then O += P V with P rounded to bf16
 // (8 mantissa bits: each weight's rounding error is at most 2^-9 of it, far
-// inside the 1e-2 output tolerance; there are no splits to agree across).
+// inside the 1e-2 output tolerance; splits agree within 2e-3).
 // The accumulator fragment of S is the A fragment of P as it stands, so no
 // transpose is needed.
 //
@@ -26,12 +28,16 @@
 // while the current tile's copies are issued.  Every wait is bounded (~1 s)
 // and raises PKV_DEVERR_TIMEOUT.
 //
-// Work.  Units are (request, KV head, query block j), visited in order of
-// decreasing j so that the longest causal ranges start first; a persistent
-// grid strides over them.  Invalid requests (n_b < 0, n_b > L_b,
-// n_b > max_qo_len, rows past qo_indptr[batch], L_b out of range) raise
-// PKV_DEVERR_LEN and get no output rows; a bad page id or flat slot raises its bit and writes the unit's rows
-// as zeros.
+// Work.  Units are (query block j, split c, request, KV head), visited in
+// order of decreasing j so that the longest causal ranges start first; a
+// persistent grid strides over them.  With S > 1 splits each split writes
+// its rows' normalised partials and (m, l) to the workspace's o_part /
+// ml_part and extend_merge_kernel combines them.  Invalid requests (n_b < 0,
+// n_b > L_b, n_b > max_qo_len, rows past qo_indptr[batch], L_b out of range)
+// raise PKV_DEVERR_LEN and get no output rows; a bad page id or flat slot
+// raises its bit and writes the unit's rows as zeros.  merge_lse_kernel
+// combines two results over disjoint keys of the same rows (a shared
+// prefix's and each request's own suffix's).
 #include <climits>
 
 #include <cuda.h>
