@@ -43,6 +43,7 @@
 #include <cuda.h>
 
 #include <cstring>
+#include <utility>
 
 #include "decode_plan.cuh"
 
@@ -165,6 +166,11 @@ template <int D, int G, bool TMA>
 __global__ void __launch_bounds__(kXThreads, 2)
     extend_mma_kernel(const __grid_constant__ XArgs a, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
+  // With programmatic dependent launch everything read here may come from
+  // the previous kernel on the stream: wait for it (a no-op for a plain
+  // launch), then let the next kernel be scheduled.
+  pdl_wait();
+  pdl_trigger();
   using C = XCfg<D>;
   constexpr int TQ = kXRows / G;  // new tokens per block
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -522,6 +528,8 @@ template <int D>
 __global__ void __launch_bounds__(128)
     extend_merge_kernel(const __grid_constant__ pkv_workspace ws, const int *qo_indptr,
                         int max_qo_len, int S, void *out, int flags) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int E = D / 32;  // elements per lane
   const int b = blockIdx.y;
   const int q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0, L = ws.seq_lens[b];
@@ -575,6 +583,8 @@ __global__ void __launch_bounds__(128)
 __global__ void __launch_bounds__(128)
     merge_lse_kernel(int n_rows, int D, const float *o_a, const float *lse_a, const float *o_b,
                      const float *lse_b, void *out, float *lse_out, int flags) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   for (long long r = blockIdx.x * 4ll + (threadIdx.x >> 5); r < n_rows; r += gridDim.x * 4ll) {
     const float la = lse_a[r], lb = lse_b[r];
@@ -604,6 +614,8 @@ __global__ void __launch_bounds__(128)
     extend_append_kernel(const __grid_constant__ pkv_workspace ws, int layer,
                          const int *qo_indptr, int max_qo_len, const uint4 *k_new,
                          const uint4 *v_new) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.y;
   const int q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0, L = ws.seq_lens[b];
   const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
@@ -684,6 +696,24 @@ bool xencode_pool_map(CUtensorMap *m, void *base, const pkv_workspace &ws) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch with programmatic dependent launch allowed (the kernels wait for
+// the previous kernel on the stream at entry).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int D, int G>
 cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
   using C = XCfg<D>;
@@ -725,18 +755,29 @@ cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
   const bool tma = ws.index_mode == PKV_IDX_PAGE_TABLE && ws.page_size % 16 == 0 &&
                    (long long)ws.n_layers * ws.pool_slots < 0x7fffffffll &&
                    xencode_pool_map(&tmk, ws.k_pool, ws) && xencode_pool_map(&tmv, ws.v_pool, ws);
-  if (tma) extend_mma_kernel<D, G, true><<<grid, kXThreads, C::SMEM, st>>>(a, tmk, tmv);
-  else extend_mma_kernel<D, G, false><<<grid, kXThreads, C::SMEM, st>>>(a, tmk, tmv);
-  if (a.S > 1) {
+  // Programmatic dependent launch when the grid leaves block slots free (its
+  // start then overlaps the previous kernel's end: the cascade's prefix
+  // attention, 36.4 -> 31.6 us per layer); a grid that fills every slot
+  // launches plainly (early, its blocks only park: 3 % slower measured).
+  if (grid < cap) {
+    e = tma ? launch_pdl(extend_mma_kernel<D, G, true>, dim3(grid), dim3(kXThreads), C::SMEM,
+                         st, a, tmk, tmv)
+            : launch_pdl(extend_mma_kernel<D, G, false>, dim3(grid), dim3(kXThreads), C::SMEM,
+                         st, a, tmk, tmv);
+  } else {
+    if (tma) extend_mma_kernel<D, G, true><<<grid, kXThreads, C::SMEM, st>>>(a, tmk, tmv);
+    else extend_mma_kernel<D, G, false><<<grid, kXThreads, C::SMEM, st>>>(a, tmk, tmv);
     e = cudaGetLastError();
+  }
+  if (a.S > 1) {
     if (e != cudaSuccess) return e;
     const long long pairs = (long long)a.max_qo_len * ws.n_q_heads;
     const long long mblocks = (pairs + 3) / 4;
     const dim3 mgrid((unsigned)(mblocks < 1024 ? mblocks : 1024), (unsigned)a.batch);
-    extend_merge_kernel<D><<<mgrid, 128, 0, st>>>(ws, a.qo_indptr, a.max_qo_len, a.S, a.out,
-                                                  a.flags);
+    e = launch_pdl(extend_merge_kernel<D>, mgrid, dim3(128), 0, st, ws, a.qo_indptr, a.max_qo_len,
+                   a.S, a.out, a.flags);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -764,9 +805,8 @@ cudaError_t launch_merge_lse(int n_rows, int head_dim, const float *o_a, const f
                              const float *o_b, const float *lse_b, void *out, float *lse_out,
                              int flags, cudaStream_t st) {
   const long long blocks = ((long long)n_rows + 3) / 4;
-  merge_lse_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 128, 0, st>>>(
-      n_rows, head_dim, o_a, lse_a, o_b, lse_b, out, lse_out, flags);
-  return cudaGetLastError();
+  return launch_pdl(merge_lse_kernel, dim3((unsigned)(blocks < 4096 ? blocks : 4096)), dim3(128),
+                    0, st, n_rows, head_dim, o_a, lse_a, o_b, lse_b, out, lse_out, flags);
 }
 
 cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
@@ -774,10 +814,9 @@ cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
                                  const void *v_new, cudaStream_t st) {
   if (batch <= 0 || max_qo_len <= 0) return cudaSuccess;
   const dim3 grid((unsigned)min(max_qo_len, 64), (unsigned)batch);
-  extend_append_kernel<<<grid, 128, 0, st>>>(ws, layer, qo_indptr, max_qo_len,
-                                             static_cast<const uint4 *>(k_new),
-                                             static_cast<const uint4 *>(v_new));
-  return cudaGetLastError();
+  return launch_pdl(extend_append_kernel, grid, dim3(128), 0, st, ws, layer, qo_indptr,
+                    max_qo_len, static_cast<const uint4 *>(k_new),
+                    static_cast<const uint4 *>(v_new));
 }
 
 }  // namespace pkv
