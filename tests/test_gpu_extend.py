@@ -299,3 +299,35 @@ def test_cascade_steady_step(cuda):
              for b in range(B)]
     ref, _ = R.decode_attention(R.tensor_bits(q)[1], kb, vb, 1, slots, p.scale, 2)
     check_attention(out.to(torch.float64).cpu().numpy(), ref, "cascade steady step")
+
+
+def test_cascade_graph_branch_bitexact(cuda):
+    # The cascade captured in a CUDA graph with its suffix attention on a
+    # parallel branch replays to the eager result bit for bit.
+    B, prefix_len = 8, 256
+    lens = [prefix_len + x for x in (9, 70, 33, 1, 120, 64, 5, 200)]
+    p = W.make_problem("cascade_graph", batch=B, n_layers=1, n_q_heads=32, n_kv_heads=8,
+                       head_dim=128, page_size=16, seq_lens=lens, seed=5300,
+                       shared_prefix_pages=prefix_len // 16)
+    ws = Workspace.from_problem(p, max_splits=2)
+    q = W.normal_bf16((B, 32, 128), 5301).to(cuda)
+    cas = CascadeDecoder(ws, B, prefix_len, scale=p.scale, prefix_splits=4)
+    out = torch.zeros((B, 32, 128), dtype=torch.bfloat16, device=cuda)
+    branch = torch.cuda.Stream()
+    cas.layer(0, q, out, suffix_stream=branch)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side), torch.cuda.graph(g, stream=side):
+        cas.layer(0, q, out, stream=side, suffix_stream=branch)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) == 0
+    assert torch.equal(out, eager)
+    ref, _ = R.decode_attention(R.tensor_bits(q.cpu()), R.tensor_bits(p.k_pool),
+                                R.tensor_bits(p.v_pool), 0, _slots(p), p.scale, 8)
+    check_attention(out.to(torch.float64).cpu().numpy(), ref, "cascade graph")
