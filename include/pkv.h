@@ -353,7 +353,9 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
  *               max score + ln(sum exp) in ws->lse, which needs batch *
  *               max_qo_len <= max_batch); PKV_FLAG_EXTEND_FULL (no causal
  *               mask: every query row of request b attends all seq_lens[b]
- *               tokens).
+ *               tokens; the rows are then not tokens of the context, so n_b
+ *               may exceed seq_lens[b], and seq_lens[b] = 0 gives zero rows
+ *               with lse -inf).
  * Reads seq_lens and either req_pool_indices + page_table (page mode) or
  * kv_indptr + kv_indices (flat mode: bind with PKV_BIND_REBUILD first).
  * Host errors: PKV_ERR_INVALID (null pointer, misalignment, batch < 0,

@@ -144,7 +144,9 @@ __device__ __forceinline__ XUnit xunit(const XArgs &a, int u, int tq, int jmax) 
   x.n = a.qo_indptr[x.b + 1] - x.q0;
   x.L = ws.seq_lens[x.b];
   const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
-  bool ok = x.n >= 0 && x.n <= x.L && x.n <= a.max_qo_len && x.q0 >= 0 &&
+  // full mode: the query rows are not tokens of the context, so n_b may exceed L_b
+  const bool fits = (a.flags & PKV_FLAG_EXTEND_FULL) || x.n <= x.L;
+  bool ok = x.n >= 0 && fits && x.n <= a.max_qo_len && x.q0 >= 0 &&
             x.q0 + x.n <= a.qo_indptr[a.batch] && (long long)x.L <= cap;
   if (ok && ws.index_mode == PKV_IDX_FLAT) {
     const int base = ws.kv_indptr[x.b];
@@ -534,7 +536,8 @@ __global__ void __launch_bounds__(128)
   const int b = blockIdx.y;
   const int q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0, L = ws.seq_lens[b];
   const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
-  bool ok = n >= 0 && n <= L && n <= max_qo_len && q0 >= 0 && q0 + n <= qo_indptr[gridDim.y] &&
+  const bool fits = (flags & PKV_FLAG_EXTEND_FULL) || n <= L;  // as the attention kernel
+  bool ok = n >= 0 && fits && n <= max_qo_len && q0 >= 0 && q0 + n <= qo_indptr[gridDim.y] &&
             (long long)L <= cap;
   if (ok && ws.index_mode == PKV_IDX_FLAT) {
     const int base = ws.kv_indptr[b];

@@ -331,3 +331,35 @@ def test_cascade_graph_branch_bitexact(cuda):
     ref, _ = R.decode_attention(R.tensor_bits(q.cpu()), R.tensor_bits(p.k_pool),
                                 R.tensor_bits(p.v_pool), 0, _slots(p), p.scale, 8)
     check_attention(out.to(torch.float64).cpu().numpy(), ref, "cascade graph")
+
+
+def test_extend_full_mode_more_rows_than_keys(cuda):
+    # Full mode: 40 query rows over a 16-token context (rows are not context
+    # tokens), and an empty context (zero rows, lse -inf), without error bits.
+    p = W.make_problem("full", batch=2, n_layers=1, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                       page_size=16, seq_lens=[16, 32], seed=5400)
+    ws = Workspace.from_problem(p)
+    ws.seq_lens[1] = 0  # request 1: no context at all
+    qo = [40, 3]
+    T = sum(qo)
+    lse = torch.zeros(T * 8, dtype=torch.float32, device=cuda)
+    view = A.PkvWorkspace.from_buffer_copy(ws.struct)
+    view.lse, view.max_batch = lse.data_ptr(), 2 * max(qo)
+    q = W.normal_bf16((T, 8, 64), 5401)
+    out = torch.full((T, 8, 64), 7.0, dtype=torch.float32, device=cuda)
+    A.pkv_extend_attn(view, 2, 0, _indptr(qo, cuda), max(qo), q.to(cuda), out, p.scale,
+                      flags=A.PKV_FLAG_EXTEND_FULL | A.PKV_FLAG_OUT_F32 | A.PKV_FLAG_WRITE_LSE)
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) == 0
+    slots = _slots(p)
+    qb = R.tensor_bits(q)
+    kb, vb = R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool)
+    # every row of request 0 attends its whole 16-token context: decode
+    # attention of each row as its own one-token query
+    ref, ref_lse = R.decode_attention(qb[:40], kb, vb, 0, [slots[0]] * 40, p.scale, 2)
+    got = out.to(torch.float64).cpu().numpy()
+    check_attention(got[:40], ref, "full mode")
+    lse_got = lse.cpu().numpy().reshape(T, 8)
+    assert np.abs(lse_got[:40] - ref_lse).max() < 1e-3
+    assert np.all(got[40:] == 0.0)
+    assert np.all(np.isneginf(lse_got[40:]))
