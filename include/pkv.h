@@ -362,9 +362,11 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
  * max_qo_len < 0, num_splits < 1, another flag), PKV_ERR_CAPACITY (batch >
  * max_batch, layer >= n_layers, the split partials or lse rows do not fit),
  * PKV_ERR_UNSUPPORTED (head_dim not 64 / 128, or G not 1, 2, 4, 8, 16).
- * Device errors: PKV_DEVERR_LEN (n_b < 0, n_b > seq_lens[b],
- * n_b > max_qo_len or a length out of range: that request's rows are not
- * written), PKV_DEVERR_PAGE / _SLOT (a bad index entry: the affected rows are
+ * Device errors: PKV_DEVERR_LEN (n_b < 0, n_b > seq_lens[b] in the causal
+ * mode, n_b > max_qo_len, a length out of range, or, with num_splits > 1 or
+ * PKV_FLAG_WRITE_LSE, rows past the batch * max_qo_len new tokens the
+ * workspace holds (qo_indptr[b + 1] > batch * max_qo_len): that request's
+ * rows are not written), PKV_DEVERR_PAGE / _SLOT (a bad index entry: the affected rows are
  * written as zeros), PKV_DEVERR_TIMEOUT.  Nothing is allocated; the call is
  * asynchronous on `stream` and graph-capturable.
  */

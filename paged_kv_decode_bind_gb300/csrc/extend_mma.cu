@@ -46,6 +46,7 @@
 #include <utility>
 
 #include "decode_plan.cuh"
+#include "merge.cuh"
 
 namespace pkv {
 
@@ -152,6 +153,11 @@ __device__ __forceinline__ XUnit xunit(const XArgs &a, int u, int tq, int jmax) 
     const int base = ws.kv_indptr[x.b];
     ok = base >= 0 && (long long)base + x.L <= ws.max_total_tokens;
   }
+  // split partials and lse rows live in the workspace, sized for batch *
+  // max_qo_len new tokens: a request whose rows lie past that (qo_indptr
+  // running on past an invalid request) is rejected, not written
+  if (ok && (a.S > 1 || (a.flags & PKV_FLAG_WRITE_LSE)))
+    ok = (long long)x.q0 + x.n <= (long long)a.batch * a.max_qo_len;
   if (!ok && x.g == 0 && x.j == 0 && x.c == 0 && (threadIdx.x & 31) == 0)
     atomicOr(ws.err, PKV_DEVERR_LEN);
   x.live = ok && x.j * tq < x.n;
@@ -525,20 +531,22 @@ __global__ void __launch_bounds__(kXThreads, 2)
 // Merge of the split partials: one warp per (new token, query head) of
 // request b = blockIdx.y: M = max over non-empty splits of m_s, w_s = l_s
 // exp(m_s - M), out = sum w_s o_s / sum w_s; zeros when no split has a key
-// or one failed (l = -1).
+// or one failed (l = -1).  The splits' (m, l) are read one per lane and the
+// partial rows with independent loads (merge_row), so a row costs a few
+// memory round trips, not two per split.
 template <int D>
 __global__ void __launch_bounds__(128)
     extend_merge_kernel(const __grid_constant__ pkv_workspace ws, const int *qo_indptr,
                         int max_qo_len, int S, void *out, int flags) {
   pdl_wait();
   pdl_trigger();
-  constexpr int E = D / 32;  // elements per lane
+  constexpr int NV = D / 4;  // float4 vectors per row
   const int b = blockIdx.y;
   const int q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0, L = ws.seq_lens[b];
   const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
   const bool fits = (flags & PKV_FLAG_EXTEND_FULL) || n <= L;  // as the attention kernel
   bool ok = n >= 0 && fits && n <= max_qo_len && q0 >= 0 && q0 + n <= qo_indptr[gridDim.y] &&
-            (long long)L <= cap;
+            (long long)L <= cap && (long long)q0 + n <= (long long)gridDim.y * max_qo_len;
   if (ok && ws.index_mode == PKV_IDX_FLAT) {
     const int base = ws.kv_indptr[b];
     ok = base >= 0 && (long long)base + L <= ws.max_total_tokens;
@@ -547,36 +555,25 @@ __global__ void __launch_bounds__(128)
   const int Hq = ws.n_q_heads, lane = threadIdx.x & 31;
   for (int p = blockIdx.x * 4 + (threadIdx.x >> 5); p < n * Hq; p += gridDim.x * 4) {
     const long long row = (long long)(q0 + p / Hq) * Hq + p % Hq;
-    float M = -INFINITY;
+    const float *ml = ws.ml_part + row * S * 2;
     bool failed = false;
-    for (int c = 0; c < S; ++c) {
-      const float m = ws.ml_part[(row * S + c) * 2], l = ws.ml_part[(row * S + c) * 2 + 1];
-      if (l < 0.f) failed = true;
-      else if (l > 0.f) M = fmaxf(M, m);
-    }
-    float acc[E], wsum = 0.f;
-#pragma unroll
-    for (int i = 0; i < E; ++i) acc[i] = 0.f;
-    for (int c = 0; c < S; ++c) {
-      const float m = ws.ml_part[(row * S + c) * 2], l = ws.ml_part[(row * S + c) * 2 + 1];
-      if (!(l > 0.f)) continue;
-      const float w = l * expf(m - M);
-      wsum += w;
-      const float *op = ws.o_part + (row * S + c) * D + lane * E;
-#pragma unroll
-      for (int i = 0; i < E; ++i) acc[i] += w * op[i];
-    }
-    const bool zero = failed || !(wsum > 0.f);
-    const float inv = zero ? 0.f : 1.f / wsum;
-    if ((flags & PKV_FLAG_WRITE_LSE) && lane == 0) ws.lse[row] = zero ? -INFINITY : M + logf(wsum);
-#pragma unroll
-    for (int i = 0; i < E; i += 2) {
-      const float v0 = zero ? 0.f : acc[i] * inv, v1 = zero ? 0.f : acc[i + 1] * inv;
-      const long long o = row * D + lane * E + i;
-      if (flags & PKV_FLAG_OUT_F32)
-        *reinterpret_cast<float2 *>(static_cast<float *>(out) + o) = make_float2(v0, v1);
-      else
-        *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(out) + o) = pack_bf16x2(v0, v1);
+    for (int c = lane; c < S; c += 32) failed |= __ldcg(ml + 2 * c + 1) < 0.f;
+    float M, den;
+    float4 acc;
+    merge_row<D>(ml, ws.o_part + row * S * D, S, lane, M, den, acc);
+    const bool zero = __any_sync(0xffffffffu, failed) || !(den > 0.f);
+    const float inv = zero ? 0.f : 1.f / den;
+    if ((flags & PKV_FLAG_WRITE_LSE) && lane == 0) ws.lse[row] = zero ? -INFINITY : M + logf(den);
+    if (lane < NV) {
+      const float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (flags & PKV_FLAG_OUT_F32) {
+        reinterpret_cast<float4 *>(static_cast<float *>(out) + row * D)[lane] = r;
+      } else {
+        uint2 pk;
+        pk.x = pack_bf16x2(r.x, r.y);
+        pk.y = pack_bf16x2(r.z, r.w);
+        reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + row * D)[lane] = pk;
+      }
     }
   }
 }

@@ -363,3 +363,13 @@ def test_extend_full_mode_more_rows_than_keys(cuda):
     assert np.abs(lse_got[:40] - ref_lse).max() < 1e-3
     assert np.all(got[40:] == 0.0)
     assert np.all(np.isneginf(lse_got[40:]))
+
+
+def test_extend_rows_past_workspace_rejected(cuda):
+    # With splits the partials live in the workspace, sized for batch *
+    # max_qo_len new tokens.  Request 0 (9 tokens, max_qo_len 4) is invalid and
+    # pushes request 1's rows to 9..11, past the 8 rows held: request 1 is
+    # rejected too, and neither request's rows are written.
+    got, _, _, _ = run_extend(cuda, lens=(50, 40), qo=(9, 3), Hq=8, Hkv=2, D=64, P=16,
+                              seed=4500, max_qo=4, expect_err=A.PKV_DEVERR_LEN, rows=[], S=3)
+    assert np.all(got == 7.0)
