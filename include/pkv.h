@@ -135,10 +135,11 @@ typedef struct pkv_workspace {
   int32_t *kv_indptr;        /* [max_batch+1] exclusive prefix sum of seq_lens       */
   int32_t *out_loc;          /* [max_batch]   slot receiving the newest token        */
   int32_t *kv_indices;       /* [max_total_tokens] flat slots (flat mode only)       */
-  float *o_part;             /* >= max_batch*Hq*max_splits*D floats; a call with S
-                                splits uses it as dense [batch, Hq, S, D]            */
-  float *ml_part;            /* >= max_batch*Hq*max_splits*2 floats; used as dense
-                                [batch, Hq, S, 2] = (max score, sum exp), ln units   */
+  float *o_part;             /* >= max_batch*Hq*max_splits*D floats, 16-byte aligned;
+                                a call with S splits uses it as dense [batch, Hq, S, D] */
+  float *ml_part;            /* >= max_batch*Hq*max_splits*2 floats, 8-byte aligned;
+                                used as dense [batch, Hq, S, 2] = (max score, sum exp),
+                                ln units                                             */
   void *out;                 /* [max_batch, Hq, D] bf16 (fp32 with PKV_FLAG_OUT_F32) */
   float *lse;                /* [max_batch, Hq] or NULL                               */
   int32_t *err;              /* one sticky int32 of PKV_DEVERR_* bits                */

@@ -24,6 +24,8 @@ cudaError_t launch_merge_lse(int n_rows, int head_dim, const float *o_a, const f
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// ml_part is read as (m, l) float pairs
+bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 
 // Shape checks shared by every entry point.
 pkv_status check_shape(const pkv_workspace *ws) {
@@ -189,7 +191,8 @@ static pkv_status decode_common(const pkv_workspace *ws, int batch, int layer, c
   if (!q || !ws->k_pool || !ws->v_pool || !ws->out) return PKV_ERR_INVALID;
   if (!aligned16(q) || !aligned16(ws->k_pool) || !aligned16(ws->v_pool) || !aligned16(ws->out))
     return PKV_ERR_INVALID;
-  if (num_splits > 1 && (!ws->o_part || !ws->ml_part || !aligned16(ws->o_part)))
+  if (num_splits > 1 &&
+      (!ws->o_part || !ws->ml_part || !aligned16(ws->o_part) || !aligned8(ws->ml_part)))
     return PKV_ERR_INVALID;
   if ((flags & PKV_FLAG_WRITE_LSE) && !ws->lse) return PKV_ERR_INVALID;
   if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
@@ -248,7 +251,8 @@ pkv_status pkv_merge_partials(const pkv_workspace *ws, int batch, int num_splits
   if (num_splits == 1 || batch == 0) return PKV_OK;
   if (ws->head_dim != 64 && ws->head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (!ws->o_part || !ws->ml_part || !ws->out) return PKV_ERR_INVALID;
-  if (!aligned16(ws->o_part) || !aligned16(ws->out)) return PKV_ERR_INVALID;
+  if (!aligned16(ws->o_part) || !aligned8(ws->ml_part) || !aligned16(ws->out))
+    return PKV_ERR_INVALID;
   if ((flags & PKV_FLAG_WRITE_LSE) && !ws->lse) return PKV_ERR_INVALID;
   return from_cuda(launch_merge(*ws, batch, num_splits, flags,
                                 reinterpret_cast<cudaStream_t>(stream)));
@@ -285,7 +289,8 @@ pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
     return ws->lse ? PKV_ERR_CAPACITY : PKV_ERR_INVALID;
   if (num_splits > 1) {
     // partials of every (new token, query head, split) in o_part / ml_part
-    if (!ws->o_part || !ws->ml_part || !aligned16(ws->o_part)) return PKV_ERR_INVALID;
+    if (!ws->o_part || !ws->ml_part || !aligned16(ws->o_part) || !aligned8(ws->ml_part))
+      return PKV_ERR_INVALID;
     if ((long long)batch * max_qo_len * num_splits > (long long)ws->max_batch * ws->max_splits)
       return PKV_ERR_CAPACITY;
   }

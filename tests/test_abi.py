@@ -71,6 +71,8 @@ def test_workspace_bytes():
     (dict(err=None), 1, 0, 1, 0, P.PKV_ERR_INVALID),
     (dict(k_pool=(1 << 20) + 8), 1, 0, 1, 0, P.PKV_ERR_INVALID),             # misaligned
     (dict(o_part=None), 1, 0, 2, 0, P.PKV_ERR_INVALID),
+    (dict(o_part=(1 << 20) + 8), 1, 0, 2, 0, P.PKV_ERR_INVALID),            # misaligned
+    (dict(ml_part=(1 << 20) + 4), 1, 0, 2, 0, P.PKV_ERR_INVALID),           # (m, l) pairs
     (dict(lse=None), 1, 0, 1, P.PKV_FLAG_WRITE_LSE, P.PKV_ERR_INVALID),
     (dict(index_mode=1), 1, 0, 1, 0, P.PKV_ERR_INVALID),                     # flat needs P == 1
     (dict(pool_slots=60), 1, 0, 1, 0, P.PKV_ERR_INVALID),                    # slots % P
@@ -101,6 +103,8 @@ def test_bind_and_merge_host_validation():
     assert P.pkv_merge_partials(ws, 2, 9, 0, 0, check=False) == P.PKV_ERR_CAPACITY
     assert P.pkv_decode_attn(ws, 0, 0, 1 << 20, 0.1, 1, 0, 0, check=False) == P.PKV_OK
     assert P.pkv_merge_partials(None, 1, 2, 0, 0, check=False) == P.PKV_ERR_INVALID
+    assert P.pkv_merge_partials(_ws(ml_part=(1 << 20) + 4), 1, 2, 0, 0, check=False) == \
+        P.PKV_ERR_INVALID
     # fused layer: k/v rows both or neither; split counters needed when S > 1
     f = 1 << 20
     assert P.pkv_decode_layer(ws, 1, 0, f, f, None, 0.1, 1, 0, 0, check=False) == \
@@ -139,6 +143,8 @@ def test_extend_host_validation():
     assert X(_ws(), 1, 0, f, 4, f, f, 0.1, num_splits=0, stream=0, check=False) == \
         P.PKV_ERR_INVALID
     assert X(_ws(o_part=None), 1, 0, f, 4, f, f, 0.1, num_splits=2, stream=0, check=False) == \
+        P.PKV_ERR_INVALID
+    assert X(_ws(ml_part=f + 4), 1, 0, f, 4, f, f, 0.1, num_splits=2, stream=0, check=False) == \
         P.PKV_ERR_INVALID
     assert X(_ws(), 4, 0, f, 4, f, f, 0.1, num_splits=2, stream=0, check=False) == \
         P.PKV_ERR_CAPACITY  # 4 * 4 * 2 rows > max_batch 4 * max_splits 4
