@@ -33,8 +33,10 @@
 // persistent grid strides over them.  With S > 1 splits each split writes
 // its rows' normalised partials and (m, l) to the workspace's o_part /
 // ml_part and extend_merge_kernel combines them.  Invalid requests (n_b < 0,
-// n_b > L_b, n_b > max_qo_len, rows past qo_indptr[batch], L_b out of range)
-// raise PKV_DEVERR_LEN and get no output rows; a bad page id or flat slot
+// n_b > L_b in the causal mode, n_b > max_qo_len, rows past qo_indptr[batch],
+// L_b out of range, or, when the workspace's partials or lse are written,
+// rows past the batch * max_qo_len it holds) raise PKV_DEVERR_LEN and get no
+// output rows; a bad page id or flat slot
 // raises its bit and writes the unit's rows as zeros.  merge_lse_kernel
 // combines two results over disjoint keys of the same rows (a shared
 // prefix's and each request's own suffix's).
