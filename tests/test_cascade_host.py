@@ -1,0 +1,63 @@
+"""Host logic of CascadeDecoder on a CPU workspace (nothing is launched): its
+argument checks and the two views it builds over the workspace."""
+import pytest
+import torch
+
+from paged_kv_decode_bind_gb300 import CascadeDecoder, Workspace
+from paged_kv_decode_bind_gb300 import _abi as A
+
+
+def _ws(page_size=16, max_splits=4):
+    ws = Workspace(n_layers=2, pool_slots=64 * page_size, n_q_heads=8, n_kv_heads=2,
+                   head_dim=64, page_size=page_size, max_batch=4, max_reqs=4,
+                   max_pages_per_req=16, max_splits=max_splits, max_total_tokens=1024,
+                   device="cpu")
+    ws.seq_lens[:3] = torch.tensor([70, 90, 64], dtype=torch.int32)
+    ws.req_pool_indices[:3] = torch.tensor([2, 0, 1], dtype=torch.int32)
+    return ws
+
+
+def test_rejects_a_prefix_that_is_not_whole_pages():
+    with pytest.raises(ValueError):
+        CascadeDecoder(_ws(), 3, 40, scale=0.125)
+
+
+def test_rejects_flat_indices():
+    with pytest.raises(ValueError):
+        CascadeDecoder(_ws(page_size=1), 3, 32, scale=0.125)
+
+
+def test_rejects_more_suffix_splits_than_the_workspace_holds():
+    with pytest.raises(ValueError):
+        CascadeDecoder(_ws(max_splits=2), 3, 32, scale=0.125, suffix_splits=3)
+
+
+def test_views():
+    ws = _ws()
+    cas = CascadeDecoder(ws, 3, 48, scale=0.125, prefix_splits=2)
+    vp, vs = cas.prefix_view, cas.suffix_view
+    # prefix: one request, request 0's page-table row, prefix_len tokens; its
+    # batch * Hq query rows get lse rows and, with splits, partials of their own
+    assert vp.seq_lens == cas.prefix_lens.data_ptr() and cas.prefix_lens.tolist() == [48]
+    assert cas.prefix_row.tolist() == [2]
+    assert vp.max_batch == 3 and vp.max_splits == 2
+    assert vp.lse == cas.lse_prefix.data_ptr() and cas.lse_prefix.numel() == 3 * 8
+    assert cas.part_o.numel() == 3 * 8 * 2 * 64 and cas.part_ml.numel() == 3 * 8 * 2 * 2
+    assert cas.qo_indptr.tolist() == [0, 3]
+    # suffix: the table from the first page past the prefix, the own lengths,
+    # private bind outputs; the main workspace's pointers are untouched
+    assert vs.page_table == ws.page_table.data_ptr() + 3 * 4
+    assert vs.seq_lens == cas.suffix_lens.data_ptr()
+    assert cas.suffix_lens.tolist() == [22, 42, 16]
+    assert vs.kv_indptr == cas.suffix_indptr.data_ptr()
+    assert vs.position_ids == cas.suffix_positions.data_ptr()
+    assert vs.out_loc == cas.suffix_out_loc.data_ptr()
+    assert vs.out == cas.out_suffix.data_ptr() and vs.lse == cas.lse_suffix.data_ptr()
+    assert vs.req_pool_indices == ws.struct.req_pool_indices
+    assert ws.struct.page_table == ws.page_table.data_ptr()
+    assert ws.struct.seq_lens == ws.seq_lens.data_ptr()
+    # both views keep the pools and the model shape
+    for v in (vp, vs):
+        assert v.k_pool == ws.struct.k_pool and v.v_pool == ws.struct.v_pool
+        assert (v.n_q_heads, v.n_kv_heads, v.head_dim, v.page_size) == (8, 2, 64, 16)
+        assert v.index_mode == A.PKV_IDX_PAGE_TABLE
