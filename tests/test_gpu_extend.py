@@ -373,3 +373,52 @@ def test_extend_rows_past_workspace_rejected(cuda):
     got, _, _, _ = run_extend(cuda, lens=(50, 40), qo=(9, 3), Hq=8, Hkv=2, D=64, P=16,
                               seed=4500, max_qo=4, expect_err=A.PKV_DEVERR_LEN, rows=[], S=3)
     assert np.all(got == 7.0)
+
+
+def _merge_lse_inputs(n, D, seed):
+    """Two parts' outputs and lse over n rows: finite on both sides, one side
+    empty (-inf), both empty, equal lse, and one side larger by 40."""
+    rng = np.random.default_rng(seed)
+    oa = rng.standard_normal((n, D)).astype(np.float32)
+    ob = rng.standard_normal((n, D)).astype(np.float32)
+    la = rng.uniform(-6.0, 6.0, n).astype(np.float32)
+    lb = rng.uniform(-6.0, 6.0, n).astype(np.float32)
+    la[3] = -np.inf
+    lb[5] = -np.inf
+    la[7] = lb[7] = -np.inf
+    la[11] = lb[11] = 2.5
+    lb[13] = la[13] + 40.0
+    return oa, la, ob, lb
+
+
+def _merge_lse_check(oa, la, ob, lb, got, got_lse, out_f32):
+    """Compare with the oracle's log-sum-exp merge of the two parts (each
+    part's lse as its max, with a unit sum; an empty part has sum 0)."""
+    n, D = oa.shape
+    ref, ref_lse = np.zeros((n, D)), np.zeros(n)
+    for r in range(n):
+        ms = [float(la[r]), float(lb[r])]
+        ls = [0.0 if np.isneginf(m) else 1.0 for m in ms]
+        ref[r], ref_lse[r] = R.merge(ms, ls, [oa[r].astype(np.float64), ob[r].astype(np.float64)])
+    # fp32 arithmetic on O(1) values; bf16 output adds its rounding (2^-9 relative)
+    tol = 2e-5 + (0.0 if out_f32 else 2.0 ** -8) * np.abs(ref)
+    assert np.all(np.abs(got - ref) <= tol), float(np.abs(got - ref).max())
+    both_empty = np.isneginf(la) & np.isneginf(lb)
+    assert np.all(np.isneginf(got_lse[both_empty])) and np.all(got[both_empty] == 0.0)
+    fin = ~both_empty
+    assert np.all(np.abs(got_lse[fin] - ref_lse[fin]) <= 2e-5)
+
+
+@pytest.mark.parametrize("D,out_f32", [(64, True), (128, False), (256, True)])
+def test_merge_lse_two_way(cuda, D, out_f32):
+    # 37 rows: a ragged last block of four rows
+    oa, la, ob, lb = _merge_lse_inputs(37, D, 5500 + D)
+    dt = torch.float32 if out_f32 else torch.bfloat16
+    out = torch.full(oa.shape, 7.0, dtype=dt, device=cuda)
+    lse = torch.full((oa.shape[0],), 7.0, dtype=torch.float32, device=cuda)
+    dev = [torch.from_numpy(x).to(cuda) for x in (oa, la, ob, lb)]
+    A.pkv_merge_lse(oa.shape[0], D, dev[0], dev[1], dev[2], dev[3], out, lse,
+                    A.PKV_FLAG_OUT_F32 if out_f32 else 0)
+    torch.cuda.synchronize()
+    _merge_lse_check(oa, la, ob, lb, out.to(torch.float64).cpu().numpy(),
+                     lse.to(torch.float64).cpu().numpy(), out_f32)
