@@ -522,7 +522,7 @@ def run_cascade_ours(args, rank, world, local_rank):
     import torch
 
     import pkv_inputs as W
-    from paged_kv_decode_bind_gb300 import CascadeDecoder, Workspace
+    from paged_kv_decode_bind_gb300 import CascadeDecoder, Workspace, choose_prefix_splits
     from paged_kv_decode_bind_gb300 import _abi as A
     from paged_kv_decode_bind_gb300 import dist as D
 
@@ -535,8 +535,7 @@ def run_cascade_ours(args, rank, world, local_rank):
     B, NL = p.batch, p.n_layers
     prefix = p.shared_prefix_pages * p.page_size
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    tq = 64 // p.group
-    Sp = max(1, min(2 * sms // (-(-B // tq) * p.n_kv_heads), prefix // 256))
+    Sp = choose_prefix_splits(B, p.group, p.n_kv_heads, prefix, sms)
     ws = Workspace.from_problem(p, device=dev)
     cas = CascadeDecoder(ws, B, prefix, scale=p.scale, prefix_splits=Sp)
     q, k, v = W.step_inputs(p, 0)

@@ -29,6 +29,17 @@ import torch
 from . import _abi
 
 
+def choose_prefix_splits(batch: int, group: int, n_kv_heads: int, prefix_len: int,
+                         num_sms: int) -> int:
+    """Splits of the shared prefix for the extend kernel's pass over it: as
+    many as keep its blocks within one wave of two per SM, and no split
+    shorter than four 64-key tiles.  A block holds 64 query rows, 64 / group
+    requests of one KV head."""
+    per_block = max(1, 64 // group)
+    blocks = -(-batch // per_block) * n_kv_heads
+    return max(1, min(2 * num_sms // max(1, blocks), prefix_len // 256))
+
+
 class CascadeDecoder:
     def __init__(self, ws, batch: int, prefix_len: int, *, scale: float, prefix_splits: int = 1,
                  suffix_splits: int = 1):
@@ -38,6 +49,8 @@ class CascadeDecoder:
             raise ValueError("the shared prefix must be whole pages of a page-table workspace")
         if suffix_splits > sh["max_splits"]:
             raise ValueError("suffix_splits exceeds the workspace's max_splits")
+        if prefix_splits < 1 or suffix_splits < 1:
+            raise ValueError("split counts start at 1")
         dev = ws.device
         f32 = dict(dtype=torch.float32, device=dev)
         i32 = dict(dtype=torch.int32, device=dev)

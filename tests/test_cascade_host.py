@@ -3,7 +3,7 @@ argument checks and the two views it builds over the workspace."""
 import pytest
 import torch
 
-from paged_kv_decode_bind_gb300 import CascadeDecoder, Workspace
+from paged_kv_decode_bind_gb300 import CascadeDecoder, Workspace, choose_prefix_splits
 from paged_kv_decode_bind_gb300 import _abi as A
 
 
@@ -61,3 +61,22 @@ def test_views():
         assert v.k_pool == ws.struct.k_pool and v.v_pool == ws.struct.v_pool
         assert (v.n_q_heads, v.n_kv_heads, v.head_dim, v.page_size) == (8, 2, 64, 16)
         assert v.index_mode == A.PKV_IDX_PAGE_TABLE
+
+
+def test_rejects_zero_splits():
+    with pytest.raises(ValueError):
+        CascadeDecoder(_ws(), 3, 32, scale=0.125, prefix_splits=0)
+
+
+def test_choose_prefix_splits():
+    # 32 requests, G = 4: 16 per block, 2 blocks per KV head, 16 blocks; two
+    # per SM on 152 SMs leave room for 19 splits, and a 4096-token prefix
+    # allows 16 of at least 256 keys
+    assert choose_prefix_splits(32, 4, 8, 4096, 152) == 16
+    assert choose_prefix_splits(32, 4, 8, 4096 * 4, 152) == 19
+    # short prefixes are not split; G = 16 packs 4 requests in a block: 8
+    # blocks per KV head, 16 blocks over 2 KV heads
+    assert choose_prefix_splits(32, 4, 8, 255, 152) == 1
+    assert choose_prefix_splits(32, 16, 2, 65536, 152) == 19
+    # more blocks than two per SM: one split
+    assert choose_prefix_splits(4096, 1, 8, 65536, 152) == 1
