@@ -215,3 +215,20 @@ def test_status_strings():
     for s in range(5):
         assert P.pkv_status_string(s)
     assert "sm_103a" in P.pkv_version()
+
+
+def test_bind_tracker_sequence():
+    # The host record of the last bind: the first step and any step whose task
+    # set or lengths did not just grow by one token rebuild; the record moves
+    # to every step it was asked about, steady or not.
+    t = P.BindTracker()
+    S, RB = P.PKV_BIND_STEADY, P.PKV_BIND_REBUILD
+    assert t.mode([7, 3], [10, 4]) == RB          # nothing bound yet
+    assert t.mode([7, 3], [11, 5]) == S
+    assert t.mode([7, 3], [12, 6]) == S
+    assert t.mode([7, 3], [14, 7]) == RB          # one request grew by two
+    assert t.mode([7, 3], [15, 8]) == S           # ... against the rebuilt record
+    assert t.mode([3, 7], [9, 16]) == RB          # same tasks, other order
+    assert t.mode([3, 7, 5], [10, 17, 1]) == RB   # a task joined
+    assert t.mode([3, 7, 5], [11, 18, 2]) == S
+    assert t.mode([], []) == RB                   # an empty batch is never steady
