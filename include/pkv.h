@@ -367,8 +367,8 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
  * mode, n_b > max_qo_len, a length out of range, or, with num_splits > 1 or
  * PKV_FLAG_WRITE_LSE, rows past the batch * max_qo_len new tokens the
  * workspace holds (qo_indptr[b + 1] > batch * max_qo_len): that request's
- * rows are not written), PKV_DEVERR_PAGE / _SLOT (a bad index entry: the affected rows are
- * written as zeros), PKV_DEVERR_TIMEOUT.  Nothing is allocated; the call is
+ * rows are not written), PKV_DEVERR_PAGE / _SLOT (a bad index entry: the
+ * affected rows are written as zeros), PKV_DEVERR_TIMEOUT.  Nothing is allocated; the call is
  * asynchronous on `stream` and graph-capturable.
  */
 pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
