@@ -48,3 +48,39 @@ def test_extend_splits_one_wave():
     # no split shorter than 256 keys
     ps = _p(1, 32, 8, 128, [600])
     assert bench.extend_splits(ps, [64], 152) == 2
+
+
+def test_traffic_record_applies_only_to_its_kernel_source(tmp_path, monkeypatch):
+    # The committed DRAM traffic per launch is reported only while the decode
+    # kernel's sources hash to the recorded value, scaled by the algorithmic
+    # bytes of the two launches; another source, another workload or a
+    # missing record gives None.
+    import json
+    import os
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    rec = {"w": {"kernel_src_sha1": "abc", "dram_bytes_per_launch": 1100.0,
+                 "algorithmic_bytes_per_launch": 1000.0}}
+    (prof / "decode_attn_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_for("abc", "w", 2000.0) == 2200.0
+    assert bench.traffic_for("abd", "w", 2000.0) is None
+    assert bench.traffic_for("abc", "other", 2000.0) is None
+    os.remove(prof / "decode_attn_traffic.json")
+    assert bench.traffic_for("abc", "w", 2000.0) is None
+
+
+def test_kernel_source_hash_covers_the_decode_sources(tmp_path, monkeypatch):
+    # The hash changes with decode*.cu and the shared headers, not with the
+    # extend kernel or the host entry points.
+    csrc = tmp_path / "paged_kv_decode_bind_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in ("decode_mma.cu", "merge.cuh", "extend_mma.cu", "pkv_api.cu"):
+        (csrc / name).write_text(name)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_src_hash()
+    for name, moves in (("extend_mma.cu", False), ("pkv_api.cu", False),
+                        ("decode_mma.cu", True), ("merge.cuh", True)):
+        (csrc / name).write_text(name + " changed")
+        assert (bench.kernel_src_hash() != h0) == moves, name
+        (csrc / name).write_text(name)
