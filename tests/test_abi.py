@@ -15,7 +15,8 @@ HEADER = os.path.join(ROOT, "include", "pkv.h")
 
 
 def _declared():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
 

@@ -405,14 +405,16 @@ def pin_extend_causality():
     b = 2  # L = 9, new tokens at positions 5..8 -> query rows 5..8
     r_first = sum(qo[:b])
     k2, v2 = kb.copy(), vb.copy()
+    # sign flips: the rows change and stay finite (an exponent-bit flip would
+    # make Inf / NaN rows, which differ from anything)
     for t in range(6, 9):  # after the first new token's position (5)
-        k2[layer, slots[b][t]] ^= np.uint16(0x4000)
-        v2[layer, slots[b][t]] ^= np.uint16(0x4000)
+        k2[layer, slots[b][t]] ^= np.uint16(0x8000)
+        v2[layer, slots[b][t]] ^= np.uint16(0x8000)
     o1, _ = R.extend_attention(qb, k2, v2, layer, slots, qo, p.scale, p.n_kv_heads)
     assert np.array_equal(o0[r_first], o1[r_first])
     assert not np.allclose(o0[r_first + 1], o1[r_first + 1])
     k3 = kb.copy()
-    k3[layer, slots[b][5]] ^= np.uint16(0x4000)
+    k3[layer, slots[b][5]] ^= np.uint16(0x8000)
     o2, _ = R.extend_attention(qb, k3, vb, layer, slots, qo, p.scale, p.n_kv_heads)
     assert not np.allclose(o0[r_first], o2[r_first])
 
