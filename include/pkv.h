@@ -216,6 +216,22 @@ int pkv_choose_pieces(const pkv_workspace *ws, int batch, int max_seq_len_hint,
                       long long total_tokens_hint, int num_sms);
 
 /*
+ * Split count for pkv_extend_attn, host only.  A block takes 64 query rows
+ * (64 / G new tokens of one request and KV head), so a batch has units =
+ * ceil(max_qo_len / (64 / G)) * batch * Hkv blocks' worth of work; splits of
+ * the causal key ranges fill the two resident blocks per SM when units fall
+ * short of them:
+ *   S = 1                                         if units >= 2 * num_sms,
+ *   S = min(2 * num_sms / units, min_seq_len_hint / 256)   otherwise,
+ * so no split is shorter than four 64-key tiles, then at most what the
+ * workspace's partials hold (batch * max_qo_len * S <= max_batch * max_splits)
+ * and at least 1.  Returns 1 for a null workspace, non-positive batch,
+ * max_qo_len or SM count, or a head count G does not divide.
+ */
+int pkv_choose_extend_splits(const pkv_workspace *ws, int batch, int max_qo_len,
+                             int min_seq_len_hint, int num_sms);
+
+/*
  * Split-KV GQA decode attention for one layer (workspace.py page, bullets 1,
  * 14-16).  For every live b and query head h (KV head g = h / G):
  *   s_t = scale * q[b,h,:] . K[layer, slot(b,t), g, :]   for t < seq_lens[b]

@@ -25,6 +25,7 @@ PKV_DEVERR_PAGE, PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT, PKV_DEVERR_T
 
 # Every symbol include/pkv.h declares (checked by the ABI test).
 EXPORTS = ("pkv_workspace_bytes", "pkv_bind_step", "pkv_choose_splits", "pkv_choose_pieces",
+           "pkv_choose_extend_splits",
            "pkv_decode_attn",
            "pkv_merge_partials", "pkv_decode_layer", "pkv_plan_step",
            "pkv_decode_attn_static_scratch",
@@ -82,6 +83,8 @@ def load(path: str = LIB_PATH):
     lib.pkv_choose_splits.restype = i32
     lib.pkv_choose_pieces.argtypes = [W, i32, i32, ctypes.c_longlong, i32]
     lib.pkv_choose_pieces.restype = i32
+    lib.pkv_choose_extend_splits.argtypes = [W, i32, i32, i32, i32]
+    lib.pkv_choose_extend_splits.restype = i32
     lib.pkv_decode_attn.argtypes = [W, i32, i32, vp, f32, i32, i32, vp]
     lib.pkv_decode_attn.restype = i32
     lib.pkv_merge_partials.argtypes = [W, i32, i32, i32, vp]
@@ -170,6 +173,11 @@ def pkv_choose_splits(ws, batch, max_seq_len_hint, total_tokens_hint, num_sms) -
 def pkv_choose_pieces(ws, batch, max_seq_len_hint, total_tokens_hint, num_sms) -> int:
     return int(load().pkv_choose_pieces(_ws(ws), int(batch), int(max_seq_len_hint),
                                         int(total_tokens_hint), int(num_sms)))
+
+
+def pkv_choose_extend_splits(ws, batch, max_qo_len, min_seq_len_hint, num_sms) -> int:
+    return int(load().pkv_choose_extend_splits(_ws(ws), int(batch), int(max_qo_len),
+                                               int(min_seq_len_hint), int(num_sms)))
 
 
 def pkv_decode_attn(ws, batch, layer, q, scale, num_splits=1, flags=0, stream=None, check=True):

@@ -172,6 +172,24 @@ int pkv_choose_pieces(const pkv_workspace *ws, int batch, int max_seq_len_hint,
   return (int)(S < ws->max_splits ? S : ws->max_splits);
 }
 
+int pkv_choose_extend_splits(const pkv_workspace *ws, int batch, int max_qo_len,
+                             int min_seq_len_hint, int num_sms) {
+  if (!ws || batch <= 0 || max_qo_len <= 0 || num_sms <= 0 || ws->n_kv_heads <= 0 ||
+      ws->n_q_heads <= 0 || ws->n_q_heads % ws->n_kv_heads)
+    return 1;
+  const int G = ws->n_q_heads / ws->n_kv_heads;
+  const int tq = G <= 64 ? 64 / G : 1;  // new tokens per block
+  const long long units = (long long)((max_qo_len + tq - 1) / tq) * batch * ws->n_kv_heads;
+  const long long blocks = 2ll * num_sms;
+  if (units >= blocks) return 1;
+  long long S = blocks / units;
+  const long long by_len = min_seq_len_hint > 0 ? min_seq_len_hint / 256 : 1;
+  if (by_len < S) S = by_len;
+  const long long room = (long long)ws->max_batch * ws->max_splits / ((long long)batch * max_qo_len);
+  if (room < S) S = room;
+  return (int)(S < 1 ? 1 : S);
+}
+
 static pkv_status decode_common(const pkv_workspace *ws, int batch, int layer, const void *q,
                                 const void *k_new, const void *v_new, float scale,
                                 int num_splits, int flags, int fused, pkv_stream_t stream) {

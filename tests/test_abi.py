@@ -233,3 +233,29 @@ def test_bind_tracker_sequence():
     assert t.mode([3, 7, 5], [10, 17, 1]) == RB   # a task joined
     assert t.mode([3, 7, 5], [11, 18, 2]) == S
     assert t.mode([], []) == RB                   # an empty batch is never steady
+
+
+def test_choose_extend_splits():
+    # Fill two blocks per SM, no split under 256 keys, within the partials'
+    # room; the bench's own rule gives the same where the room does not bind.
+    import types
+
+    import bench
+    big = _ws(n_q_heads=32, n_kv_heads=8, max_batch=64, max_splits=4096)
+    C = P.pkv_choose_extend_splits
+    # 64 new tokens at G = 4: 4 blocks per head, 8 heads, one request: 32 units
+    assert C(big, 1, 64, 32832, 152) == 9
+    assert C(big, 4, 256, 900, 152) == 1           # 512 units already fill the SMs
+    assert C(big, 1, 64, 600, 152) == 2            # 600 keys: two splits of >= 256
+    assert C(big, 1, 64, 100, 152) == 1
+    # the partials' room: max_batch * max_splits rows over batch * max_qo_len
+    assert C(_ws(n_q_heads=32, n_kv_heads=8, max_batch=4, max_splits=4), 1, 4, 32832, 152) == 4
+    assert C(None, 1, 64, 32832, 152) == 1
+    assert C(big, 0, 64, 32832, 152) == 1
+    assert C(big, 1, 64, 32832, 0) == 1
+    for B, Hq, Hkv, qo, lens in ((1, 32, 8, 64, 32832), (2, 16, 2, 40, 3000), (3, 8, 8, 17, 700),
+                                 (1, 32, 2, 1, 70000)):
+        p = types.SimpleNamespace(batch=B, n_q_heads=Hq, n_kv_heads=Hkv, group=Hq // Hkv,
+                                  seq_lens=types.SimpleNamespace(tolist=lambda: [lens] * B))
+        ws = _ws(n_q_heads=Hq, n_kv_heads=Hkv, max_batch=64, max_splits=4096)
+        assert C(ws, B, qo, lens, 152) == bench.extend_splits(p, [qo] * B, 152), (B, Hq, Hkv)
