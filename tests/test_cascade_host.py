@@ -1,5 +1,6 @@
-"""Host logic of CascadeDecoder on a CPU workspace (nothing is launched): its
-argument checks and the two views it builds over the workspace."""
+"""Host logic of CascadeDecoder and DecodeRunner on a CPU workspace (nothing
+is launched): the cascade's argument checks, its two views over the
+workspace and its split rule, and the runner's kernel count per step."""
 import pytest
 import torch
 
@@ -80,3 +81,19 @@ def test_choose_prefix_splits():
     assert choose_prefix_splits(32, 16, 2, 65536, 152) == 19
     # more blocks than two per SM: one split
     assert choose_prefix_splits(4096, 1, 8, 65536, 152) == 1
+
+
+def test_decode_runner_launch_count():
+    # kernels per step, as the bench reports them: the bind (+ the flat index
+    # build), then per layer one fused kernel, or append + attention (+ merge
+    # when split); the step's plan adds one launch when used
+    from paged_kv_decode_bind_gb300 import DecodeRunner
+    ws = _ws()  # 2 layers, G = 4, D = 64, page table
+    assert DecodeRunner(ws, 3, num_splits=4).launches_per_step == 1 + 2
+    assert DecodeRunner(ws, 3, num_splits=4, fused=False).launches_per_step == 1 + 2 * 3
+    assert DecodeRunner(ws, 3, num_splits=1, fused=False).launches_per_step == 1 + 2 * 2
+    simt = DecodeRunner(ws, 3, num_splits=4, flags=A.PKV_FLAG_FORCE_SIMT)
+    assert simt.launches_per_step == 1 + 2 * 3  # no fused CUDA-core kernel
+    assert DecodeRunner(ws, 3, num_splits=4, plan=True).launches_per_step == 1 + 1 + 2
+    flat = _ws(page_size=1)
+    assert DecodeRunner(flat, 3, num_splits=4).launches_per_step == 2 + 2
