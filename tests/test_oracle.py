@@ -435,6 +435,33 @@ def pin_extend_append():
     assert {(int(a), int(c)) for a, c in diff} <= changed
 
 
+def pin_token_slots_flat_golden():
+    # Flat mode: token t of entry b is kv_indices[kv_indptr[b] + t], read here
+    # from the hand-worked index of the flat bind fixture (not from bind).
+    g = _load("bind_rebuild_flat.json")
+    e = g["expect"]
+    for b, want in enumerate(g["slots"]):
+        got = R.token_slots(b, g["seq_lens"][b], index_mode=R.FLAT, kv_indptr=e["kv_indptr"],
+                            kv_indices=e["kv_indices"])
+        assert got == want, (b, got, want)
+
+
+def pin_token_slots_flat_equals_table_walk():
+    # With token-level pages (P = 1) the flat index built by the bind and the
+    # request-to-token table walk name the same slots for every token.
+    p = W.make_problem("flat", batch=4, n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=8,
+                       page_size=1, seq_lens=[3, 1, 7, 5], seed=31)
+    tbl, rows = p.page_table.numpy(), p.req_pool_indices.numpy()
+    meta = R.bind(p.seq_lens.tolist(), req_pool_indices=rows, page_table=tbl, page_size=1,
+                  mode=R.REBUILD, index_mode=R.FLAT)
+    for b in range(p.batch):
+        L = int(p.seq_lens[b])
+        flat = R.token_slots(b, L, index_mode=R.FLAT, kv_indptr=meta["kv_indptr"],
+                             kv_indices=meta["kv_indices"])
+        walk = R.token_slots(b, L, page_table=tbl, req_pool_indices=rows, page_size=1)
+        assert flat == walk, (b, flat, walk)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
@@ -476,6 +503,15 @@ def _mut_merge_unweighted(ms, ls, os_):
     return out, max(ms[s] for s in live) + math.log(sum(ls[s] for s in live))
 
 
+def _mut_token_slots_flat_next(b, seq_len, *, index_mode=R.PAGE_TABLE, kv_indptr=None,
+                               kv_indices=None, **kw):
+    if index_mode == R.FLAT:  # the next entry's base: kv_indptr[b + 1]
+        base = int(kv_indptr[b + 1])
+        return [int(kv_indices[(base + t) % len(kv_indices)]) for t in range(seq_len)]
+    return _orig["token_slots"](b, seq_len, index_mode=index_mode, kv_indptr=kv_indptr,
+                                kv_indices=kv_indices, **kw)
+
+
 def _mut_bind_inclusive(seq_lens, **kw):
     res = _orig["bind"](seq_lens, **kw)
     res["kv_indptr"] = res["kv_indptr"][1:] + [res["kv_indptr"][-1]]
@@ -495,7 +531,7 @@ def _mut_positions_all(seq_len, n_new):
     return [seq_len - 1] * n_new
 
 
-_orig = {"attend": R.attend, "bind": R.bind}
+_orig = {"attend": R.attend, "bind": R.bind, "token_slots": R.token_slots}
 
 MUTATIONS = {
     "gqa_modulo": ("kv_head_of", _mut_gqa),
@@ -505,6 +541,7 @@ MUTATIONS = {
     "slot_without_page_size": ("slot_of_token", _mut_slot),
     "merge_without_max_shift": ("merge", _mut_merge_unweighted),
     "indptr_inclusive": ("bind", _mut_bind_inclusive),
+    "flat_slots_next_base": ("token_slots", _mut_token_slots_flat_next),
     "bf16_shift": ("bf16_bits_to_f64", _mut_bf16),
     "extend_position_shifted": ("extend_positions", _mut_positions_late),
     "extend_not_causal": ("extend_positions", _mut_positions_all),
