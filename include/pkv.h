@@ -101,7 +101,8 @@ enum {
 /* bits OR-ed into *err by device code (sticky; the caller clears the word) */
 enum {
   PKV_DEVERR_PAGE = 1,     /* page id < 0 or >= pool_slots / page_size          */
-  PKV_DEVERR_LEN = 2,      /* seq_len < 0 or > max_pages_per_req * page_size    */
+  PKV_DEVERR_LEN = 2,      /* seq_len < 0 or > max_pages_per_req * page_size (or
+                              max_seq_len when set)                            */
   PKV_DEVERR_TOTAL = 4,    /* flat mode: kv_indptr[b] + seq_len > max_total_tokens */
   PKV_DEVERR_SLOT = 8,     /* a flat slot or out_loc outside [0, pool_slots)    */
   PKV_DEVERR_TIMEOUT = 16  /* a bounded wait on an async copy ran out (~1 s)    */
@@ -150,6 +151,13 @@ typedef struct pkv_workspace {
                                 split plan written by pkv_plan_step and read by
                                 pkv_decode_layer with PKV_FLAG_USE_PLAN; may be
                                 NULL if those are not used                          */
+  int32_t max_seq_len;       /* 0: a request may hold max_pages_per_req * page_size
+                                tokens; else at most this many (<= that product), for
+                                views whose page_table points part-way into a row of a
+                                larger table (the rows keep the stride
+                                max_pages_per_req but hold fewer columns).  Longer
+                                lengths raise PKV_DEVERR_LEN like any other.  Negative
+                                values are PKV_ERR_INVALID                          */
 } pkv_workspace;
 
 /*

@@ -53,6 +53,7 @@ class PkvWorkspace(ctypes.Structure):
         ("ml_part", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("lse", ctypes.c_void_p), ("err", ctypes.c_void_p),
         ("split_counters", ctypes.c_void_p), ("work_plan", ctypes.c_void_p),
+        ("max_seq_len", ctypes.c_int32),
     ]
 
 

@@ -51,6 +51,13 @@ class CascadeDecoder:
             raise ValueError("suffix_splits exceeds the workspace's max_splits")
         if prefix_splits < 1 or suffix_splits < 1:
             raise ValueError("split counts start at 1")
+        if not 0 < batch <= sh["max_batch"]:
+            raise ValueError("batch must be in 1 .. the workspace's max_batch")
+        # the suffix view's rows start prefix_len / P entries into the table's
+        # rows: they keep the table's stride but hold only the rest of a row
+        suffix_cap = (sh["max_pages_per_req"] - prefix_len // P) * P
+        if suffix_cap <= 0:
+            raise ValueError("the shared prefix fills the whole page-table row")
         dev = ws.device
         f32 = dict(dtype=torch.float32, device=dev)
         i32 = dict(dtype=torch.int32, device=dev)
@@ -84,7 +91,10 @@ class CascadeDecoder:
         vs.kv_indptr, vs.position_ids = (self.suffix_indptr.data_ptr(),
                                          self.suffix_positions.data_ptr())
         vs.out_loc = self.suffix_out_loc.data_ptr()
-        vs.max_batch = batch
+        vs.max_batch = batch  # <= the workspace's: o_part / ml_part hold its rows
+        # a suffix length past the rest of the row raises PKV_DEVERR_LEN on the
+        # device (the bind and the kernels) instead of reading the next row
+        vs.max_seq_len = suffix_cap
         vs.out, vs.lse = self.out_suffix.data_ptr(), self.lse_suffix.data_ptr()
         self.suffix_view = vs
         # fork / join of the optional second stream (a parallel graph branch)

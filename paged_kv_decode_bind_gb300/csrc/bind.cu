@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(kMetaThreads) bind_meta_kernel(pkv_workspace w
   const int tid = threadIdx.x;
   const int per = (batch + kMetaThreads - 1) / kMetaThreads;
   const int lo = tid * per;
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  const long long cap = len_cap(ws);
 
   int old_len[kMetaPer];
   int new_len[kMetaPer];
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kFlatThreads) flat_index_kernel(pkv_workspace 
   const int base = ws.kv_indptr[b];
   const bool lead = blockIdx.x == 0 && threadIdx.x == 0;
   if (L <= 0) return;
-  if ((long long)L > ws.max_pages_per_req) {
+  if ((long long)L > len_cap(ws)) {
     if (lead) atomicOr(ws.err, PKV_DEVERR_LEN);
     return;
   }

@@ -186,11 +186,19 @@ __host__ __device__ __forceinline__ int split_chunk(int max_len, int num_splits,
   return (c + gran - 1) / gran * gran;
 }
 
+// Most tokens a request may hold: its table row's capacity, or less where
+// the workspace sets max_seq_len (a view whose rows start part-way into the
+// table keeps the table's row stride but not its whole row).
+__host__ __device__ __forceinline__ long long len_cap(const pkv_workspace &ws) {
+  const long long row = (long long)ws.max_pages_per_req * ws.page_size;
+  return ws.max_seq_len > 0 && (long long)ws.max_seq_len < row ? ws.max_seq_len : row;
+}
+
 // Length of request b as the kernels see it: out-of-range lengths raise
 // PKV_DEVERR_LEN / PKV_DEVERR_TOTAL and count as empty.
 __device__ __forceinline__ int checked_len(const pkv_workspace &ws, int b, int *err) {
   int L = ws.seq_lens[b];
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  const long long cap = len_cap(ws);
   if (L < 0 || (long long)L > cap) {
     atomicOr(err, PKV_DEVERR_LEN);
     return 0;

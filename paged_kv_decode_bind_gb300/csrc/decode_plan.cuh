@@ -74,7 +74,7 @@ struct Unit {
 // Length of request b as the kernels use it (0 if out of range).
 __device__ __forceinline__ int usable_len(const pkv_workspace &ws, int b) {
   int L = ws.seq_lens[b];
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  const long long cap = len_cap(ws);
   if (L < 0 || (long long)L > cap) return 0;
   if (ws.index_mode == PKV_IDX_FLAT && L > 0) {
     const int base = ws.kv_indptr[b];
@@ -195,7 +195,7 @@ __device__ __forceinline__ int batch_max_len(const pkv_workspace &ws, int batch,
   if (threadIdx.x == 0) *s_max = 0;
   __syncthreads();
   int mx = 0;
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  const long long cap = len_cap(ws);
   for (int b = threadIdx.x; b < batch; b += blockDim.x) {
     const int L = ws.seq_lens[b];
     if (L >= 0 && (long long)L <= cap) mx = max(mx, L);
@@ -256,7 +256,7 @@ __device__ __forceinline__ int batch_plan_compact(const pkv_workspace &ws, int b
                                                   int *s_max, int *chunk_out) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int hkv = ws.n_kv_heads;
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  const long long cap = len_cap(ws);
   // request b's usable length (and its index base into s_base[b])
   auto read_req = [&](int b) {
     const int raw = ws.seq_lens[b];

@@ -108,7 +108,7 @@ __device__ __forceinline__ Unit unit_at(const pkv_workspace &ws, const Plan &pl,
   x.b = r / pl.hkv;
   x.g = r - x.b * pl.hkv;
   int L = ws.seq_lens[x.b];
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  const long long cap = len_cap(ws);
   if (L < 0 || (long long)L > cap) L = 0;  // flagged once per request by the c == 0 unit
   if (ws.index_mode == PKV_IDX_FLAT && L > 0) {
     const int base = ws.kv_indptr[x.b];
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
   __syncthreads();
   {
     int mx = 0;
-    const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+    const long long cap = len_cap(ws);
     for (int b = tid; b < a.batch; b += kThreads) {
       const int L = ws.seq_lens[b];
       if (L >= 0 && (long long)L <= cap) mx = max(mx, L);

@@ -146,7 +146,7 @@ __device__ __forceinline__ XUnit xunit(const XArgs &a, int u, int tq, int jmax) 
   x.q0 = a.qo_indptr[x.b];
   x.n = a.qo_indptr[x.b + 1] - x.q0;
   x.L = ws.seq_lens[x.b];
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  const long long cap = len_cap(ws);
   // full mode: the query rows are not tokens of the context, so n_b may exceed L_b
   const bool fits = (a.flags & PKV_FLAG_EXTEND_FULL) || x.n <= x.L;
   bool ok = x.n >= 0 && fits && x.n <= a.max_qo_len && x.q0 >= 0 &&
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(128)
   constexpr int NV = D / 4;  // float4 vectors per row
   const int b = blockIdx.y;
   const int q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0, L = ws.seq_lens[b];
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  const long long cap = len_cap(ws);
   const bool fits = (flags & PKV_FLAG_EXTEND_FULL) || n <= L;  // as the attention kernel
   bool ok = n >= 0 && fits && n <= max_qo_len && q0 >= 0 && q0 + n <= qo_indptr[gridDim.y] &&
             (long long)L <= cap && (long long)q0 + n <= (long long)gridDim.y * max_qo_len;
@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(128)
   pdl_trigger();
   const int b = blockIdx.y;
   const int q0 = qo_indptr[b], n = qo_indptr[b + 1] - q0, L = ws.seq_lens[b];
-  const long long cap = (long long)ws.max_pages_per_req * ws.page_size;
+  const long long cap = len_cap(ws);
   bool ok = n >= 0 && n <= L && n <= max_qo_len && q0 >= 0 && q0 + n <= qo_indptr[gridDim.y] &&
             (long long)L <= cap;
   long long base = 0;

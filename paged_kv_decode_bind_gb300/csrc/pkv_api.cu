@@ -32,7 +32,7 @@ pkv_status check_shape(const pkv_workspace *ws) {
   if (!ws) return PKV_ERR_INVALID;
   if (ws->n_layers <= 0 || ws->pool_slots <= 0 || ws->n_q_heads <= 0 || ws->n_kv_heads <= 0 ||
       ws->head_dim <= 0 || ws->page_size <= 0 || ws->max_batch < 0 || ws->max_reqs <= 0 ||
-      ws->max_pages_per_req <= 0 || ws->max_splits <= 0)
+      ws->max_pages_per_req <= 0 || ws->max_splits <= 0 || ws->max_seq_len < 0)
     return PKV_ERR_INVALID;
   if (ws->n_q_heads % ws->n_kv_heads != 0) return PKV_ERR_INVALID;
   if (ws->pool_slots % ws->page_size != 0) return PKV_ERR_INVALID;

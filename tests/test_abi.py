@@ -31,15 +31,17 @@ def test_exports_match_header():
 
 
 def test_struct_layout():
-    # 12 int32 shape fields then 16 pointers, no padding on LP64.
-    assert ctypes.sizeof(_abi.PkvWorkspace) == 12 * 4 + 16 * 8
+    # 12 int32 shape fields, 16 pointers, then max_seq_len (and 4 bytes of
+    # tail padding to the pointers' 8-byte alignment) on LP64.
+    assert ctypes.sizeof(_abi.PkvWorkspace) == 12 * 4 + 16 * 8 + 8
     assert _abi.PkvWorkspace.k_pool.offset == 48
+    assert _abi.PkvWorkspace.max_seq_len.offset == 12 * 4 + 16 * 8
 
 
 def _ws(**kw):
     shape = dict(n_layers=2, pool_slots=64, n_q_heads=8, n_kv_heads=2, head_dim=128,
                  page_size=16, index_mode=0, max_batch=4, max_reqs=8, max_pages_per_req=4,
-                 max_splits=4, max_total_tokens=0)
+                 max_splits=4, max_total_tokens=0, max_seq_len=0)
     fake = 1 << 20  # non-null, 16-byte aligned; never dereferenced (validation fails first)
     ptrs = dict(k_pool=fake, v_pool=fake, req_pool_indices=fake, page_table=fake,
                 seq_lens=fake, position_ids=fake, kv_indptr=fake, out_loc=fake,
@@ -77,6 +79,7 @@ def test_workspace_bytes():
     (dict(lse=None), 1, 0, 1, P.PKV_FLAG_WRITE_LSE, P.PKV_ERR_INVALID),
     (dict(index_mode=1), 1, 0, 1, 0, P.PKV_ERR_INVALID),                     # flat needs P == 1
     (dict(pool_slots=60), 1, 0, 1, 0, P.PKV_ERR_INVALID),                    # slots % P
+    (dict(max_seq_len=-1), 1, 0, 1, 0, P.PKV_ERR_INVALID),
     (dict(n_q_heads=32, n_kv_heads=2), 1, 0, 1, P.PKV_FLAG_FORCE_SIMT, P.PKV_ERR_UNSUPPORTED),
     (dict(), 1, 0, 1, P.PKV_FLAG_FORCE_SIMT | P.PKV_FLAG_FORCE_MMA, P.PKV_ERR_INVALID),
     (dict(), 1, 0, 1, P.PKV_FLAG_FORCE_SIMT | P.PKV_FLAG_FORCE_GATHER, P.PKV_ERR_INVALID),

@@ -97,3 +97,28 @@ def test_decode_runner_launch_count():
     assert DecodeRunner(ws, 3, num_splits=4, plan=True).launches_per_step == 1 + 1 + 2
     flat = _ws(page_size=1)
     assert DecodeRunner(flat, 3, num_splits=4).launches_per_step == 2 + 2
+
+
+def test_rejects_batch_beyond_the_workspace():
+    # the suffix pass writes batch * Hq * S partial rows into the workspace's
+    # o_part / ml_part and reads batch entries of its request rows
+    with pytest.raises(ValueError):
+        CascadeDecoder(_ws(), 5, 32, scale=0.125)  # max_batch is 4
+    with pytest.raises(ValueError):
+        CascadeDecoder(_ws(), 0, 32, scale=0.125)
+    assert CascadeDecoder(_ws(), 4, 32, scale=0.125).suffix_view.max_batch == 4
+
+
+def test_suffix_length_limit():
+    # rows of 16 pages of 16 tokens; a 48-token prefix leaves 13 pages for
+    # the suffix: the view keeps the table's row stride (16 entries) and
+    # limits the suffix length to 13 * 16, which the device checks
+    ws = _ws()
+    vs = CascadeDecoder(ws, 3, 48, scale=0.125).suffix_view
+    assert vs.max_pages_per_req == 16
+    assert vs.max_seq_len == 13 * 16
+    assert ws.struct.max_seq_len == 0  # the main workspace: the whole row
+    # the boundary: a prefix of 15 pages leaves one page, 16 pages none
+    assert CascadeDecoder(ws, 3, 15 * 16, scale=0.125).suffix_view.max_seq_len == 16
+    with pytest.raises(ValueError):
+        CascadeDecoder(ws, 3, 16 * 16, scale=0.125)

@@ -422,3 +422,29 @@ def test_merge_lse_two_way(cuda, D, out_f32):
     torch.cuda.synchronize()
     _merge_lse_check(oa, la, ob, lb, out.to(torch.float64).cpu().numpy(),
                      lse.to(torch.float64).cpu().numpy(), out_f32)
+
+
+def test_cascade_suffix_past_its_row_is_rejected(cuda):
+    # The suffix view's table rows start past the prefix's pages, so a
+    # suffix may hold only the rest of a row.  Request 1 fills its whole row
+    # (16 pages); the steady bind's +1 takes its suffix past the 12 pages left
+    # after the 4-page prefix: the bind raises PKV_DEVERR_LEN and gives it no
+    # slot, instead of reading the next row's first page id.
+    B, prefix_len = 3, 64
+    lens = [prefix_len + 40, 16 * 16, prefix_len + 100]
+    p = W.make_problem("cascade_cap", batch=B, n_layers=1, n_q_heads=8, n_kv_heads=2,
+                       head_dim=128, page_size=16, seq_lens=lens, seed=5400,
+                       shared_prefix_pages=prefix_len // 16)
+    assert p.max_pages_per_req == 16
+    ws = Workspace.from_problem(p)
+    cas = CascadeDecoder(ws, B, prefix_len, scale=p.scale)
+    assert cas.suffix_view.max_seq_len == 12 * 16
+    cas.bind(A.PKV_BIND_STEADY)
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) & A.PKV_DEVERR_LEN
+    assert cas.suffix_out_loc[1].item() == -1
+    meta = R.bind([x - prefix_len for x in lens], req_pool_indices=p.req_pool_indices.numpy(),
+                  page_table=p.page_table[:, prefix_len // 16:].contiguous().numpy(),
+                  page_size=16, mode=R.STEADY)
+    got = cas.suffix_out_loc.tolist()
+    assert [got[0], got[2]] == [meta["out_loc"][0], meta["out_loc"][2]]
