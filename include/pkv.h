@@ -337,6 +337,7 @@ pkv_status pkv_plan_step(const pkv_workspace *ws, int batch, int num_splits, int
  *   ws->ml_part are ignored and may be NULL.
  *   Limit: batch * Hq * num_splits * (D + 2) * 4 bytes must fit in
  *   PKV_STATIC_SCRATCH_BYTES, else PKV_ERR_CAPACITY and nothing is launched.
+ *   That limit, not ws->max_splits, bounds num_splits here.
  *   The array exists once per GPU that loads the library, for the life of the
  *   process.  The first call on each device looks up its device address
  *   (cudaGetSymbolAddress, with that device current); make that first call

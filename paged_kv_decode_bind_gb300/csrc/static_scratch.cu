@@ -65,6 +65,9 @@ extern "C" pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, in
                                                      int num_splits, int flags,
                                                      pkv_stream_t stream) {
   if (!ws || batch < 0 || num_splits < 1) return PKV_ERR_INVALID;
+  // The size check below multiplies these: reject what the shape check of
+  // pkv_decode_attn would, before they can make `need` small or negative.
+  if (ws->head_dim <= 0 || ws->n_q_heads <= 0) return PKV_ERR_INVALID;
   const long long per_split = (long long)ws->head_dim + 2;  // o row + (m, l)
   const long long need = (long long)batch * ws->n_q_heads * num_splits * per_split * 4;
   if (num_splits > 1 && need > (long long)kStaticScratchBytes) return PKV_ERR_CAPACITY;
@@ -75,7 +78,9 @@ extern "C" pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, in
     const long long n_o = (long long)batch * ws->n_q_heads * num_splits * ws->head_dim;
     w.o_part = base;
     w.ml_part = base + n_o;  // n_o * 4 bytes is a multiple of 32: ml stays aligned
-    // The partial buffers only have to hold this call's [batch, Hq, S, *] block.
+    // The partial buffers only have to hold this call's [batch, Hq, S, *]
+    // block: the array's size, checked above, bounds num_splits here, not
+    // the caller's max_splits.
     w.max_splits = num_splits;
     if (w.max_batch < batch) return PKV_ERR_CAPACITY;
   }

@@ -262,3 +262,16 @@ def test_choose_extend_splits():
                                   seq_lens=types.SimpleNamespace(tolist=lambda: [lens] * B))
         ws = _ws(n_q_heads=Hq, n_kv_heads=Hkv, max_batch=64, max_splits=4096)
         assert C(ws, B, qo, lens, 152) == bench.extend_splits(p, [qo] * B, 152), (B, Hq, Hkv)
+
+
+def test_static_scratch_host_validation():
+    # Rejected before any CUDA call: a shape that would make the scratch size
+    # product non-positive, and a size beyond the static array.
+    q = 1 << 20
+    assert P.pkv_decode_attn_static_scratch(_ws(head_dim=-128), 1, 0, q, 0.1, 4, 0,
+                                            check=False) == P.PKV_ERR_INVALID
+    assert P.pkv_decode_attn_static_scratch(_ws(n_q_heads=0), 1, 0, q, 0.1, 4, 0,
+                                            check=False) == P.PKV_ERR_INVALID
+    big = _ws(max_batch=4096)
+    assert P.pkv_decode_attn_static_scratch(big, 4096, 0, q, 0.1, 64, 0,
+                                            check=False) == P.PKV_ERR_CAPACITY
