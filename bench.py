@@ -4,9 +4,14 @@
 One step = one steady decode step of the whole hot path: the metadata bind,
 then for every layer the KV append, split-KV decode attention and the partial
 merge, captured once as a CUDA graph at fixed workspace addresses and
-replayed.  Default workload: B=4, 24 layers, 32/8 heads, D=128, P=16,
-seq_lens ~ U{512..2048}, run as rounds of 64 consecutive steady steps (the
-lengths are rewound to their start values between rounds).
+replayed.  Default workload: the graph-captured sweep's largest batch, B=64,
+24 layers, 16/2 heads, D=128, P=16, seq_lens ~ U{1024..4096} (the largest
+decode step that fits one GPU), run as rounds of 64 consecutive steady steps
+(the lengths are rewound to their start values between rounds).  Every layer
+writes its own output rows.  The default run then times every other decode
+configuration the same way (the ``sweep`` list: the single-request D=64 case,
+the paged B=4 case, the token-level B=16 case, the 65536-token requests and
+the sweep's other batches) and times the oracle beside them.
 
 Prints one JSON line.  ``value`` = algorithmic bytes (K+V of every cached
 token, q and out, per layer) of all timed steps on all ranks / max-over-ranks
@@ -29,7 +34,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention µs/layer-step and achieved HBM GB/s (% of GB300 peak)"
-DEFAULT_WORKLOAD = "gqa4_b4_paged"
+DEFAULT_WORKLOAD = "gqa8_graph_sweep"
+DEFAULT_BATCH = 64  # the sweep's largest batch: the largest decode step that fits one GPU
 ROUND = 64  # consecutive steady steps before the lengths are rewound
 L2_BYTES = 129 * 10**6          # GB300 L2
 L2_FLUSH_BYTES = 256 << 20      # written between steps to flush it
@@ -54,6 +60,10 @@ def parse_args(argv=None):
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (small profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", dest="sweep", action="store_true", default=None,
+                    help="also time every other decode configuration (default: on for the "
+                         "default workload)")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
@@ -191,19 +201,41 @@ def cpu_baseline_worker(args):
                                 f"{args.workload} (B={p.batch}), {dt:.1f} s on 1 thread"}))
 
 
-def run_cpu_baseline(args):
+def run_cpu_baselines(configs, seconds):
+    """The oracle timed on one host core per configuration, the
+    configurations side by side (one process each); returns their records."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker", "--workload",
-           args.workload, "--cpu-seconds", str(args.cpu_seconds)]
-    if args.batch:
-        cmd += ["--batch", str(args.batch)]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
-    for line in r.stdout.splitlines()[::-1]:
-        if line.startswith("{"):
-            return json.loads(line)
-    return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "failed: " + r.stderr[-200:]}
+    procs = []
+    for wl, b in configs:
+        cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-worker", "--workload",
+               wl, "--cpu-seconds", str(seconds)]
+        if b:
+            cmd += ["--batch", str(b)]
+        procs.append(subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                      text=True, env=env))
+    out = []
+    for (wl, b), pr in zip(configs, procs):
+        try:
+            so, se = pr.communicate(timeout=600)
+        except subprocess.TimeoutExpired:
+            pr.kill()
+            so, se = "", "timeout"
+        rec = None
+        for line in so.splitlines()[::-1]:
+            if line.startswith("{"):
+                rec = json.loads(line)
+                break
+        if rec is None:
+            rec = {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": "failed: " + (se or "")[-200:]}
+        rec["workload"] = wl if b is None else f"{wl} B={b}"
+        out.append(rec)
+    return out
+
+
+def run_cpu_baseline(args):
+    return run_cpu_baselines([(args.workload, args.batch)], args.cpu_seconds)[0]
 
 
 def run_reference(args, rank):
@@ -211,7 +243,7 @@ def run_reference(args, rank):
     of (request, head) attentions of one layer of the same workload."""
     if rank != 0:
         return
-    p = _oracle_problem(args.workload, args.batch)
+    p = _oracle_problem(args.workload, _batch_of(args.workload, args.batch))
     st = _oracle_state(p)
     pairs_all = [(b, h) for b in range(p.batch) for h in range(p.n_q_heads)]
     t = time.perf_counter()
@@ -656,35 +688,50 @@ def kernel_src_hash():
     return h.hexdigest()
 
 
-def run_ours(args, rank, world, local_rank):
+def _decode_setup(workload, batch, layers, splits, flags, unfused, rank, dev):
+    """Problem, workspace and runner of one decode workload on `dev`."""
     import torch
-    import torch.distributed as dist
 
     import pkv_inputs as W
     from paged_kv_decode_bind_gb300 import DecodeRunner, Workspace
     from paged_kv_decode_bind_gb300 import _abi as A
-
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
     from paged_kv_decode_bind_gb300 import dist as D
-    p = W.workload(args.workload, batch=args.batch, steps=ROUND, n_layers=args.layers,
-                   seed=D.rank_seed(20260000 + W.WORKLOADS.index(args.workload) + 1, rank))
-    B, NL = p.batch, p.n_layers
+
+    p = W.workload(workload, batch=batch, steps=ROUND, n_layers=layers,
+                   seed=D.rank_seed(20260000 + W.WORKLOADS.index(workload) + 1, rank))
+    B = p.batch
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     shape_only = A.PkvWorkspace(n_kv_heads=p.n_kv_heads, max_splits=1 << 20)
     # the fused layer kernel cuts apportioned splits (S caps them per request and
     # head); the separate calls and PKV_FLAG_FIXED_CHUNK cut fixed chunks
-    apportioned = not args.unfused and not (args.flags & A.PKV_FLAG_FIXED_CHUNK)
+    apportioned = not unfused and not (flags & A.PKV_FLAG_FIXED_CHUNK)
     choose = A.pkv_choose_pieces if apportioned else A.pkv_choose_splits
-    S = args.splits or choose(shape_only, B, int(p.seq_lens.max()) + ROUND,
-                              int(p.seq_lens.sum()) + B * ROUND // 2, sms)
+    S = splits or choose(shape_only, B, int(p.seq_lens.max()) + ROUND,
+                         int(p.seq_lens.sum()) + B * ROUND // 2, sms)
     ws = Workspace.from_problem(p, max_splits=S, device=dev)
-    run = DecodeRunner(ws, B, num_splits=S, flags=args.flags, scale=p.scale,
-                       fused=not args.unfused)
+    # every layer writes its own output rows: a step's result is all of them
+    run = DecodeRunner(ws, B, num_splits=S, flags=flags, scale=p.scale, fused=not unfused,
+                       out_per_layer=True)
     q, k, v = W.step_inputs(p, 0)
     run.q_in.copy_(q)
     run.k_in.copy_(k)
     run.v_in.copy_(v)
+    return p, ws, run, S, (q, k, v)
+
+
+def measure_decode(args, workload, batch, steps, warmup, rank, world, dev, *, e2e=False,
+                   kernel_events=False, layers=None, splits=0, flags=0, unfused=False):
+    """Time whole steady steps of one decode workload (CUDA-graph replays);
+    returns its numbers.  The layer time is (step - metadata bind) / layers."""
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_decode_bind_gb300 import _abi as A
+
+    p, ws, run, S, (q, k, v) = _decode_setup(workload, batch, layers, splits, flags, unfused,
+                                             rank, dev)
+    p.k_pool = p.v_pool = None  # uploaded: the host copies are not needed again
+    B, NL = p.batch, p.n_layers
     lens0 = ws.seq_lens[:B].clone()
     L0 = p.seq_lens.tolist()
 
@@ -693,11 +740,13 @@ def run_ours(args, rank, world, local_rank):
     # graphs with event nodes around every layer's attention kernel give the
     # event-bracketed per-kernel times (the nodes themselves cost time, so
     # those are an upper bound); a bind-only graph gives the bind time.
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        ext = not args.no_kernel_events
-    except TypeError:
-        ext = False
+    ext = False
+    if kernel_events:
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+            ext = True
+        except TypeError:
+            ext = False
     plain = [run.capture(A.PKV_BIND_STEADY) for _ in range(ROUND)]
     graphs, events = [], []
     if ext:
@@ -726,7 +775,7 @@ def run_ours(args, rank, world, local_rank):
         lens = [x + j + 1 for x in L0]
         return NL * algorithmic_bytes(lens, p)
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
 
@@ -762,8 +811,8 @@ def run_ours(args, rank, world, local_rank):
         return sum(a.elapsed_time(b) for a, b in evs) / 1e3
 
     # ---- device-timed region: inputs resident in HBM ----
-    K = args.steps
-    clocks = ClockSampler(local_rank) if rank == 0 else None
+    K = steps
+    clocks = ClockSampler(dev.index or 0) if rank == 0 else None
     barrier()
     torch.cuda.synchronize()
     if clocks:
@@ -792,14 +841,15 @@ def run_ours(args, rank, world, local_rank):
                 attn_ms.append(a.elapsed_time(b))
     mean_layer_bytes = statistics.fmean(step_bytes(i) / NL for i in range(K))
 
-    # ---- end to end: pinned host inputs in, result out, every step ----
-    e2e = None
-    if not args.no_e2e:
+    # ---- end to end: pinned host inputs in, every layer's result out ----
+    e2e_rec = None
+    if e2e:
         qh = q.pin_memory()
         kh = k.pin_memory()
         vh = v.pin_memory()
-        outh = torch.empty((B, p.n_q_heads, p.head_dim), dtype=torch.bfloat16).pin_memory()
-        for i in range(args.warmup):
+        out_dev = run.outs  # [NL, B, Hq, D]: every layer's output rows
+        outh = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+        for i in range(warmup):
             step(i)
         barrier()
         torch.cuda.synchronize()
@@ -811,73 +861,157 @@ def run_ours(args, rank, world, local_rank):
             run.k_in.copy_(kh, non_blocking=True)
             run.v_in.copy_(vh, non_blocking=True)
             step(i)
-            outh.copy_(ws.out_bf16(B), non_blocking=True)
+            outh.copy_(out_dev, non_blocking=True)
         e1.record()
         torch.cuda.synchronize()
         barrier()
         dte = e0.elapsed_time(e1) / 1e3
-        e2e = {"dt": dte, "h2d": q.numel() * 2 + k.numel() * 2 + v.numel() * 2,
-               "d2h": outh.numel() * 2}
+        e2e_rec = {"dt": dte, "h2d": q.numel() * 2 + k.numel() * 2 + v.numel() * 2,
+                   "d2h": outh.numel() * 2}
 
     errbits = int(ws.err.item())
-    # max over ranks of the times, sum of the work
+    res = {"p": p, "S": S, "dt": dt, "dt_bind": dt_bind, "layer_s": layer_s, "K": K,
+           "total_bytes": total_bytes, "mean_layer_bytes": mean_layer_bytes,
+           "attn_ms": attn_ms, "clk": clk, "errbits": errbits, "e2e": e2e_rec,
+           "launches_per_step": run.launches_per_step, "fused": run.fused,
+           "flush": flush_buf is not None, "step_bytes0": step_bytes(0), "L0": L0}
+    del run, ws, plain, graphs, bind_graph, flush_buf
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+# Configurations with the >= 70 % of HBM peak target (B >= 16 and the
+# long-context split-KV requests), and the small ones, measured after the
+# headline in the same run: (workload, batch).
+SWEEP = [("single_d64", None), ("gqa4_b4_paged", None), ("gqa4_b16_flat_skewed", None),
+         ("gqa4_long_65536", 1), ("gqa4_long_65536", 4), ("gqa8_graph_sweep", 1),
+         ("gqa8_graph_sweep", 4), ("gqa8_graph_sweep", 8), ("gqa8_graph_sweep", 16),
+         ("gqa8_graph_sweep", 32)]
+TARGET_70 = {("gqa4_b16_flat_skewed", None), ("gqa4_long_65536", 1), ("gqa4_long_65536", 4),
+             ("gqa8_graph_sweep", 16), ("gqa8_graph_sweep", 32), ("gqa8_graph_sweep", 64)}
+# oracle timings reported beside the sweep (one host core each, run side by side)
+ORACLE_SWEEP = [("single_d64", None), ("gqa4_b4_paged", None), ("gqa4_b16_flat_skewed", None),
+                ("gqa4_long_65536", 1), ("gqa4_long_65536", 4)]
+
+
+def _batch_of(workload, batch):
+    if batch is not None:
+        return batch
+    return DEFAULT_BATCH if workload == DEFAULT_WORKLOAD else None
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from paged_kv_decode_bind_gb300 import _abi as A
     from paged_kv_decode_bind_gb300 import dist as D
-    dt, total_all = D.reduce_time_and_work(dt, float(total_bytes), device=dev)
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    batch = _batch_of(args.workload, args.batch)
+    r = measure_decode(args, args.workload, batch, args.steps, args.warmup, rank, world, dev,
+                       e2e=not args.no_e2e, kernel_events=not args.no_kernel_events,
+                       layers=args.layers, splits=args.splits, flags=args.flags,
+                       unfused=args.unfused)
+    p, S, K, NL = r["p"], r["S"], r["K"], r["p"].n_layers
+    # max over ranks of the times, sum of the work
+    dt, total_all = D.reduce_time_and_work(r["dt"], float(r["total_bytes"]), device=dev)
+    e2e = r["e2e"]
     if e2e:
         e2e["dt"], _ = D.reduce_time_and_work(e2e["dt"], 0.0, device=dev)
+    sweep_on = (args.sweep if args.sweep is not None else
+                args.workload == DEFAULT_WORKLOAD and args.batch is None and not args.layers
+                and not args.splits and not args.flags and not args.unfused)
+    sweep = []
+    if sweep_on and world == 1:
+        for wl, b in SWEEP:
+            s = measure_decode(args, wl, b, min(args.steps, 256), args.warmup, rank, world, dev)
+            sweep.append(_sweep_entry(wl, b, s))
     if rank != 0:
         return
 
     peak, peak_src = peaks()
     simt = bool(args.flags & A.PKV_FLAG_FORCE_SIMT)
     value = total_all / dt / 1e9
-    layer_steps = K * NL
+    layer_s = r["layer_s"]
     layer_kernel = ("decode_mma_kernel (append+attention+merge, one launch per layer)"
-                    if run.fused and not simt else
+                    if r["fused"] and not simt else
                     "append_kernel + " + ("decode_simt_kernel" if simt else "decode_mma_kernel") +
                     (" + merge_kernel" if S > 1 else ""))
-    ach = mean_layer_bytes / layer_s / 1e9
+    mlb = r["mean_layer_bytes"]
+    ach = mlb / layer_s / 1e9
     roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "traffic": (traffic_for(kernel_src_hash(), args.workload, mean_layer_bytes)
-                        if run.fused and not args.flags and not args.splits else None),
+            "traffic": (traffic_for(kernel_src_hash(), _traffic_key(args.workload, p.batch), mlb)
+                        if r["fused"] and not args.flags and not args.splits else None),
             "peak_source": peak_src,
             "kernel": layer_kernel, "kernel_us_mean": layer_s * 1e6,
             "kernel_time_from": "(step - metadata bind) / layers (the step's split plan counts "
                                 "in the layers), both timed with CUDA events over "
                                 "their own timed regions of graph replays",
-            "kernel_launches_timed": K * NL, "algorithmic_bytes_per_launch": mean_layer_bytes}
-    if attn_ms:
-        roof["attention_us_event_bracketed"] = statistics.fmean(attn_ms) * 1e3
-    roof["bind_us"] = dt_bind / K * 1e6
+            "kernel_launches_timed": K * NL, "algorithmic_bytes_per_launch": mlb}
+    if r["attn_ms"]:
+        roof["attention_us_event_bracketed"] = statistics.fmean(r["attn_ms"]) * 1e3
+    roof["bind_us"] = r["dt_bind"] / K * 1e6
+    L0 = r["L0"]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": dt / K * 1e3,
-        "us_per_layer_step": dt / layer_steps * 1e6,
+        "us_per_layer_step": dt / (K * NL) * 1e6,
         "frac_of_peak": value / peak,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "batch": B, "n_layers": NL,
+        "config": {"workload": args.workload, "batch": p.batch, "n_layers": NL,
                    "n_q_heads": p.n_q_heads, "n_kv_heads": p.n_kv_heads,
                    "head_dim": p.head_dim, "page_size": p.page_size,
                    "seq_lens_start": [min(L0), max(L0), sum(L0)],
                    "steady_steps_per_round": ROUND, "num_splits": S, "cuda_graph": True,
                    "l2": ("no flush: one step touches %.0f MB of KV, more than twice the "
-                          "129 MB L2" if flush_buf is None else
+                          "129 MB L2" if not r["flush"] else
                           "L2 flushed between steps (256 MB written), each step timed alone: "
-                          "one step touches %.0f MB of KV") %
-                         (step_bytes(0) / 1e6),
+                          "one step touches %.0f MB of KV") % (r["step_bytes0"] / 1e6),
+                   "outputs": "every layer writes its own [B, Hq, D] rows",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof,
-        "gpu_launches": run.launches_per_step * K,
-        "clocks": clk,
-        "device_err_bits": errbits,
+        "gpu_launches": r["launches_per_step"] * K,
+        "clocks": r["clk"],
+        "device_err_bits": r["errbits"],
     }
     if e2e:
         line["e2e"] = {"value": total_all / e2e["dt"] / 1e9, "unit": "GB/s",
-                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
+                       "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                       "result": "every layer's bf16 output rows, copied back each step"}
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = run_cpu_baseline(args)
+        wanted = [(args.workload, batch)] + (ORACLE_SWEEP if sweep else [])
+        base = run_cpu_baselines(wanted, args.cpu_seconds)
+        line["cpu_baseline"] = base[0]
+        for e in sweep:
+            for (wl, b), cb in zip(wanted[1:], base[1:]):
+                if (e["workload"], e["batch_arg"]) == (wl, b):
+                    e["cpu_baseline"] = cb
+    if sweep:
+        line["sweep"] = [{k: v for k, v in e.items() if k != "batch_arg"} for e in sweep]
+        line["target_70"] = {
+            "configs": [f"{wl} B={b or 'default'}" for wl, b in sorted(TARGET_70, key=str)],
+            "met": all(e["frac"] >= 0.70 for e in sweep if e["target_70"]) and
+            roof["frac"] >= 0.70}
     print(json.dumps(line), flush=True)
+
+
+def _traffic_key(workload, batch):
+    return f"{workload}@B{batch}"
+
+
+def _sweep_entry(wl, b, s):
+    peak, src = peaks()
+    ach = s["mean_layer_bytes"] / s["layer_s"] / 1e9
+    return {"workload": wl, "batch": s["p"].batch, "batch_arg": b, "n_layers": s["p"].n_layers,
+            "num_splits": s["S"], "steps": s["K"],
+            "us_per_layer_step": s["layer_s"] * 1e6, "achieved_gbs": ach, "frac": ach / peak,
+            "peak_source": src, "bind_us": s["dt_bind"] / s["K"] * 1e6,
+            "algorithmic_bytes_per_layer": s["mean_layer_bytes"],
+            "l2_flushed_between_steps": s["flush"], "target_70": (wl, b) in TARGET_70,
+            "clocks": s["clk"], "device_err_bits": s["errbits"]}
 
 
 def main(argv=None):

@@ -34,7 +34,7 @@ class DecodeRunner:
 
     def __init__(self, ws: Workspace, batch: int, *, num_splits: int = 1, flags: int = 0,
                  scale: float | None = None, stream: torch.cuda.Stream | None = None,
-                 fused: bool = True, plan: bool = False):
+                 fused: bool = True, plan: bool = False, out_per_layer: bool = False):
         self.ws = ws
         self.batch = batch
         sh = ws.shape
@@ -49,6 +49,21 @@ class DecodeRunner:
         self.k_in = torch.zeros((NL, B, sh["n_kv_heads"], sh["head_dim"]), dtype=torch.bfloat16,
                                 device=dev)
         self.v_in = torch.zeros_like(self.k_in)
+        # out_per_layer: every layer writes its own output rows (layer l's into
+        # outs[l], through a copy of the workspace struct whose `out` points
+        # there), so a step leaves all its layers' results behind instead of
+        # the last one's in ws.out.  bf16, or fp32 with PKV_FLAG_OUT_F32.
+        self.outs = None
+        self.views = None
+        if out_per_layer:
+            odt = torch.float32 if flags & _abi.PKV_FLAG_OUT_F32 else torch.bfloat16
+            self.outs = torch.zeros((NL, B, sh["n_q_heads"], sh["head_dim"]), dtype=odt,
+                                    device=dev)
+            self.views = []
+            for l in range(NL):
+                v = _abi.PkvWorkspace.from_buffer_copy(ws.struct)
+                v.out = self.outs[l].data_ptr()
+                self.views.append(v)
         self.graph = None
         self.fused = fused
         flat = sh["index_mode"] == _abi.PKV_IDX_FLAT
@@ -65,6 +80,9 @@ class DecodeRunner:
         per_layer = 1 if fused and mma else 2 + int(split)
         self.launches_per_step = (1 + int(flat) + int(self.use_plan and 0 < batch <= 256) +
                                   NL * per_layer)
+
+    def _wsl(self, l):
+        return self.views[l] if self.views is not None else self.ws
 
     # --- pieces -------------------------------------------------------------
     def bind(self, mode=_abi.PKV_BIND_STEADY):
@@ -83,7 +101,7 @@ class DecodeRunner:
             # more launches earlier, so they may start before layer l-1 ends.
             early = _abi.PKV_FLAG_PLAN_EARLY if (l > 0 and events is None) else 0
             use = _abi.PKV_FLAG_USE_PLAN if self.use_plan else 0
-            _abi.pkv_decode_layer(self.ws, self.batch, l, self.q_in[l], self.k_in[l],
+            _abi.pkv_decode_layer(self._wsl(l), self.batch, l, self.q_in[l], self.k_in[l],
                                   self.v_in[l], self.scale, self.num_splits,
                                   self.flags | early | use, s)
             if events is not None:
@@ -93,12 +111,12 @@ class DecodeRunner:
                            self.v_in[l], s)
         if events is not None:
             events[0].record(s)
-        _abi.pkv_decode_attn(self.ws, self.batch, l, self.q_in[l], self.scale, self.num_splits,
-                             self.flags, s)
+        _abi.pkv_decode_attn(self._wsl(l), self.batch, l, self.q_in[l], self.scale,
+                             self.num_splits, self.flags, s)
         if events is not None:
             events[1].record(s)
         if self.num_splits > 1:
-            _abi.pkv_merge_partials(self.ws, self.batch, self.num_splits, self.flags, s)
+            _abi.pkv_merge_partials(self._wsl(l), self.batch, self.num_splits, self.flags, s)
 
     def step(self, mode=_abi.PKV_BIND_STEADY, layer_events=None):
         """Bind, then every layer.  ``layer_events[l]`` = (start, end) CUDA

@@ -92,11 +92,15 @@ def check_meta(ws, st: OracleState, B):
 
 
 def run_steps(p: W.DecodeProblem, *, S=1, steps=1, check_layers=None, heads=None,
-              check_partials=False, check_pool=False, flags=0, device="cuda", fused=False):
+              check_partials=False, check_pool=False, flags=0, device="cuda", fused=False,
+              plan=False):
     """Run `steps` steady steps; on the last one compare every checked layer.
+    plan=True: the fused layers take the step's split plan (pkv_plan_step).
     Returns dict of max errors."""
     ws = Workspace.from_problem(p, max_splits=S, device=device)
-    run = DecodeRunner(ws, p.batch, num_splits=S, flags=flags, scale=p.scale, fused=fused)
+    run = DecodeRunner(ws, p.batch, num_splits=S, flags=flags, scale=p.scale, fused=fused,
+                       plan=plan)
+    assert run.use_plan == (plan and fused and not flags & A.PKV_FLAG_FORCE_SIMT)
     st = OracleState(p)
     B = p.batch
     check_layers = list(range(p.n_layers)) if check_layers is None else check_layers

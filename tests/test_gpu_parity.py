@@ -11,10 +11,10 @@ import torch
 
 import oracle.ref as R
 import pkv_inputs as W
-from paged_kv_decode_bind_gb300 import DecodeRunner, Workspace
+from paged_kv_decode_bind_gb300 import BindTracker, DecodeRunner, Workspace
 from paged_kv_decode_bind_gb300 import _abi as A
 
-from parity import bf16_to_f64, check_attention, run_steps
+from parity import OracleState, bf16_to_f64, check_attention, check_meta, run_steps
 
 pytestmark = pytest.mark.gpu
 
@@ -237,7 +237,8 @@ def _bench_splits(p, chooser=A.pkv_choose_splits):
 
 @pytest.mark.parametrize("name,batch", [("gqa4_b4_paged", None), ("gqa4_b16_flat_skewed", None),
                                         ("gqa4_long_65536", 1), ("gqa4_long_65536", 4),
-                                        ("gqa8_graph_sweep", 16)])
+                                        ("gqa8_graph_sweep", 16), ("gqa8_graph_sweep", 32),
+                                        ("gqa8_graph_sweep", 64)])
 def test_full_size_sampled(cuda, name, batch):
     p = W.workload(name, batch=batch, steps=1)
     layers = sorted({0, p.n_layers - 1})
@@ -364,3 +365,97 @@ def test_shared_prefix_workload_small(cuda):
     # one set stored once), oracle-sized: fused decode through the aliased pages.
     p = W.workload("shared_prefix_b32", shrink=16, steps=1)
     run_steps(p, S=4, check_pool=True)
+
+
+# ------------------------------------------- the block-wide batch plan ----
+
+_PLAN_PROBLEMS = {}
+
+
+@pytest.mark.parametrize("plan", [False, True], ids=["self_planned", "step_plan"])
+@pytest.mark.parametrize("producer", ["tma", "gather"])
+@pytest.mark.parametrize("B", [33, 64, 200])
+def test_block_wide_plan_batches(cuda, B, producer, plan):
+    # 33..256 requests: the fused layer's compact plan runs its block-wide
+    # scan (one warp plans up to 32 requests), with the step's plan and
+    # without, for both producers; every output element is compared.
+    if B not in _PLAN_PROBLEMS:
+        _PLAN_PROBLEMS[B] = W.workload("gqa8_graph_sweep", batch=B, shrink=16, steps=1)
+    p = _PLAN_PROBLEMS[B]
+    assert 32 < p.batch <= 256
+    run_steps(p, S=4, check_pool=True, flags=GATHER if producer == "gather" else 0, fused=True,
+              plan=plan)
+
+
+# --------------------------------------------- REBUILD at large batch ----
+
+@pytest.mark.parametrize("B", [64, 256, 2000])
+def test_rebuild_changed_task_set_large_batch(cuda, B):
+    # A steady step, then the task set changes (a quarter of the requests
+    # leave, the rest come back in another order, each one token longer): the
+    # host sees a non-steady step, writes the lengths and request rows, and
+    # the REBUILD bind and a fused layer follow.  Metadata bit-exact, the
+    # appended pool bit-exact, attention against the oracle (sampled heads
+    # for the largest batch).  2000 requests take the bind kernel's
+    # several-requests-per-thread scan and the fused layer's enumeration
+    # without the compact plan.
+    rng = np.random.default_rng(B)
+    lens = [int(x) for x in rng.integers(1, 97, size=B)]
+    p = W.make_problem("rebuild", batch=B, n_layers=1, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                       page_size=16, seq_lens=lens, steps=2, seed=40 + B)
+    S = 3
+    ws = Workspace.from_problem(p, max_splits=S)
+    tracker = BindTracker()
+    ids = list(range(B))
+    assert tracker.mode(ids, lens) == A.PKV_BIND_REBUILD  # the first bind
+    heads = _sample_heads(p, 64) if B > 256 else None
+    # step 0: steady (every length + 1)
+    assert tracker.mode(ids, [x + 1 for x in lens]) == A.PKV_BIND_STEADY
+    run = DecodeRunner(ws, B, num_splits=S, scale=p.scale)
+    q, k, v = W.step_inputs(p, 0)
+    run.q_in.copy_(q), run.k_in.copy_(k), run.v_in.copy_(v)
+    run.step()
+    st = OracleState(p)
+    st.bind()
+    st.append(0, R.tensor_bits(k)[0], R.tensor_bits(v)[0])
+    torch.cuda.synchronize()
+    check_meta(ws, st, B)
+    # step 1: a changed task set
+    keep = rng.permutation(B)[: B - B // 4]
+    B2 = len(keep)
+    new_ids = [ids[i] for i in keep]
+    new_lens = [st.lens[i] + 1 for i in keep]
+    new_rows = p.req_pool_indices.numpy()[keep]
+    assert tracker.mode(new_ids, new_lens) == A.PKV_BIND_REBUILD
+    ws.seq_lens[:B2].copy_(torch.tensor(new_lens, dtype=torch.int32))
+    ws.req_pool_indices[:B2].copy_(torch.from_numpy(new_rows.astype(np.int32)))
+    run2 = DecodeRunner(ws, B2, num_splits=S, scale=p.scale)
+    q2 = W.normal_bf16((1, B2, 8, 64), 7000 + B)
+    k2 = W.normal_bf16((1, B2, 2, 64), 7001 + B)
+    v2 = W.normal_bf16((1, B2, 2, 64), 7002 + B)
+    run2.q_in.copy_(q2), run2.k_in.copy_(k2), run2.v_in.copy_(v2)
+    run2.step(A.PKV_BIND_REBUILD)
+    torch.cuda.synchronize()
+    assert int(ws.err.item()) == 0
+    assert int(ws.split_counters.abs().sum().item()) == 0
+    table = p.page_table.numpy()
+    meta = R.bind(new_lens, req_pool_indices=new_rows, page_table=table, page_size=16,
+                  mode=R.REBUILD)
+    assert ws.seq_lens[:B2].tolist() == meta["seq_lens"]
+    assert ws.position_ids[:B2].tolist() == meta["position_ids"]
+    assert ws.kv_indptr[:B2 + 1].tolist() == meta["kv_indptr"]
+    assert ws.out_loc[:B2].tolist() == meta["out_loc"]
+    kb = R.append_rows(st.kb, 0, meta["out_loc"], R.tensor_bits(k2)[0])
+    vb = R.append_rows(st.vb, 0, meta["out_loc"], R.tensor_bits(v2)[0])
+    assert np.array_equal(R.tensor_bits(ws.k_pool.cpu()), kb)
+    assert np.array_equal(R.tensor_bits(ws.v_pool.cpu()), vb)
+    slots = [R.token_slots(b, meta["seq_lens"][b], page_table=table, req_pool_indices=new_rows,
+                           page_size=16) for b in range(B2)]
+    heads2 = None if heads is None else [(b, h) for b, h in heads if b < B2]
+    ref, _ = R.decode_attention(R.tensor_bits(q2)[0], kb, vb, 0, slots, p.scale, 2,
+                                heads=heads2)
+    got = bf16_to_f64(ws.out_bf16(B2))
+    if heads2 is not None:
+        idx = tuple(np.array(heads2).T)
+        got, ref = got[idx], ref[idx]
+    check_attention(got, ref, f"REBUILD B={B} -> {B2}")
