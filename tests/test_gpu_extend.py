@@ -443,8 +443,10 @@ def test_cascade_suffix_past_its_row_is_rejected(cuda):
     torch.cuda.synchronize()
     assert int(ws.err.item()) & A.PKV_DEVERR_LEN
     assert cas.suffix_out_loc[1].item() == -1
-    meta = R.bind([x - prefix_len for x in lens], req_pool_indices=p.req_pool_indices.numpy(),
+    # the other two requests' slots, from the oracle over the suffix table
+    meta = R.bind([lens[0] - prefix_len, lens[2] - prefix_len],
+                  req_pool_indices=p.req_pool_indices.numpy()[[0, 2]],
                   page_table=p.page_table[:, prefix_len // 16:].contiguous().numpy(),
                   page_size=16, mode=R.STEADY)
     got = cas.suffix_out_loc.tolist()
-    assert [got[0], got[2]] == [meta["out_loc"][0], meta["out_loc"][2]]
+    assert [got[0], got[2]] == meta["out_loc"]
