@@ -300,17 +300,6 @@ def extend_flops(lens, qo, p):
     return 4 * p.head_dim * p.n_q_heads * pairs
 
 
-def extend_splits(p, qo, sms):
-    """Splits per causal key range: as many as keep the units within one wave
-    of two blocks per SM, and no split shorter than 256 keys."""
-    tq = 64 // p.group
-    units = -(-max(qo) // tq) * p.batch * p.n_kv_heads
-    if units >= 2 * sms:
-        return 1
-    shortest = min(int(L) for L in p.seq_lens.tolist())
-    return max(1, min(2 * sms // units, shortest // 256))
-
-
 def extend_bytes(lens, qo, p):
     """Algorithmic bytes of one layer: every context token's K and V once,
     q and out."""
@@ -426,7 +415,12 @@ def run_extend_ours(args, rank, world, local_rank):
     B, NL, T = p.batch, p.n_layers, sum(qo)
     lens = p.seq_lens.tolist()
     mq = max(qo)
-    S = extend_splits(p, qo, torch.cuda.get_device_properties(dev).multi_processor_count)
+    # splits as the library's chooser gives them for the kernel it picks
+    shape = A.PkvWorkspace(n_layers=NL, pool_slots=p.pool_slots, n_q_heads=p.n_q_heads,
+                           n_kv_heads=p.n_kv_heads, head_dim=p.head_dim, page_size=p.page_size,
+                           index_mode=p.index_mode, max_batch=B, max_splits=1 << 20)
+    S = A.pkv_choose_extend_splits(shape, B, mq, min(lens),
+                                   torch.cuda.get_device_properties(dev).multi_processor_count)
     ws = Workspace.from_problem(p, device=dev, max_splits=mq * S if S > 1 else 1)
     q, k, v = W.extend_inputs(p, qo)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)

@@ -93,9 +93,11 @@ enum {
                                  wait for it runs out (~1 s): the launch sets
                                  PKV_DEVERR_TIMEOUT, writes those units empty and
                                  returns, and the context stays usable */
-  PKV_FLAG_EXTEND_FULL = 512  /* pkv_extend_attn: every query row of a request attends all
+  PKV_FLAG_EXTEND_FULL = 512,  /* pkv_extend_attn: every query row of a request attends all
                                  seq_lens[b] tokens (no causal mask), e.g. a batch's decode
                                  queries over a prefix their requests share */
+  PKV_FLAG_EXTEND_WARP_MMA = 1024 /* pkv_extend_attn: the warp-level mma.sync kernel even
+                                 where the tcgen05 kernel applies (comparisons) */
 };
 
 /* bits OR-ed into *err by device code (sticky; the caller clears the word) */
@@ -224,13 +226,16 @@ int pkv_choose_pieces(const pkv_workspace *ws, int batch, int max_seq_len_hint,
                       long long total_tokens_hint, int num_sms);
 
 /*
- * Split count for pkv_extend_attn, host only.  A block takes 64 query rows
- * (64 / G new tokens of one request and KV head), so a batch has units =
- * ceil(max_qo_len / (64 / G)) * batch * Hkv blocks' worth of work; splits of
- * the causal key ranges fill the two resident blocks per SM when units fall
+ * Split count for pkv_extend_attn, host only.  A block takes R query rows
+ * (R / G new tokens of one request and KV head), so a batch has units =
+ * ceil(max_qo_len / (R / G)) * batch * Hkv blocks' worth of work; splits of
+ * the causal key ranges fill the resident blocks (c per SM) when units fall
  * short of them:
- *   S = 1                                         if units >= 2 * num_sms,
- *   S = min(2 * num_sms / units, min_seq_len_hint / 256)   otherwise,
+ *   S = 1                                         if units >= c * num_sms,
+ *   S = min(c * num_sms / units, min_seq_len_hint / 256)   otherwise,
+ * with the geometry of the kernel pkv_extend_attn picks for the workspace:
+ * the tcgen05 kernel (page sizes that are a multiple of 16) R = 128, c = 1;
+ * the warp-level kernel R = 64, c = 2;
  * so no split is shorter than four 64-key tiles, then at most what the
  * workspace's partials hold (batch * max_qo_len * S <= max_batch * max_splits)
  * and at least 1.  Returns 1 for a null workspace, non-positive batch,
@@ -375,6 +380,12 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
  *               second launch merges them into `out` by log-sum-exp.  For
  *               long prefixes with few new tokens, where the unsplit grid has
  *               few blocks.
+ *   kernels     page sizes that are a multiple of 16: the tcgen05 kernel (128
+ *               query rows per CTA, S = Q K^T and O = P V accumulated in tensor
+ *               memory, P applied as bf16 high and low parts); flat indices,
+ *               other page sizes or PKV_FLAG_EXTEND_WARP_MMA: the warp-level
+ *               mma.sync kernel (64 rows per block).  Both give the same
+ *               results up to rounding.
  *   flags       PKV_FLAG_OUT_F32; PKV_FLAG_WRITE_LSE (also lse[query row * Hq + h] =
  *               max score + ln(sum exp) in ws->lse, which needs batch *
  *               max_qo_len <= max_batch); PKV_FLAG_EXTEND_FULL (no causal

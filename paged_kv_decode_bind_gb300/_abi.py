@@ -20,6 +20,7 @@ PKV_FLAG_FORCE_GATHER, PKV_FLAG_PLAN_EARLY, PKV_FLAG_FIXED_CHUNK = 16, 32, 64
 PKV_FLAG_USE_PLAN = 128
 PKV_FLAG_TEST_SKIP_FIRST_TILE = 256
 PKV_FLAG_EXTEND_FULL = 512
+PKV_FLAG_EXTEND_WARP_MMA = 1024
 PKV_DEVERR_PAGE, PKV_DEVERR_LEN, PKV_DEVERR_TOTAL, PKV_DEVERR_SLOT, PKV_DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16
 

@@ -47,7 +47,7 @@
 #include <cstring>
 #include <utility>
 
-#include "decode_plan.cuh"
+#include "extend_common.cuh"
 #include "merge.cuh"
 
 namespace pkv {
@@ -67,7 +67,6 @@ namespace {
 
 constexpr int kXW = 4;                  // consumer warps
 constexpr int kXThreads = (kXW + 1) * 32;
-constexpr int kXT = 64;                 // keys per tile
 constexpr int kXRows = 16 * kXW;        // query rows per block
 constexpr int kXStages = 3;
 
@@ -105,70 +104,6 @@ __device__ __forceinline__ void xcp16(uint32_t dst, const void *src, int src_byt
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(src_bytes)
                : "memory");
-}
-
-struct XArgs {
-  pkv_workspace ws;
-  int batch, layer, max_qo_len, flags;
-  int S;  // splits of each unit's key range (1: rows written to out directly)
-  const int *qo_indptr;
-  const void *q;
-  void *out;
-  float scale;
-};
-
-// One unit: request b's query block j for KV head g.
-struct XUnit {
-  int b, g, j, c;
-  int n;       // new tokens of the request
-  int L;       // its cached length (new tokens included)
-  int q0;      // qo_indptr[b]
-  int kend;    // the block's rows attend keys 0 .. kend - 1 at most
-  int k0, k1;  // keys of split c: [k0, k1) (empty when k0 >= k1)
-  bool live;   // valid request and a non-empty query block
-};
-
-// Unit u = (query block j, split c, request b, KV head g), j descending.
-// Request b's new-token count and length are checked; PKV_DEVERR_LEN is
-// raised once per request (by the unit with g, j and c all 0).  Split c of a
-// block covers keys [c * chunk, (c + 1) * chunk) of its causal range,
-// chunk = ceil(kend / S) rounded up to a whole tile.
-__device__ __forceinline__ XUnit xunit(const XArgs &a, int u, int tq, int jmax) {
-  const pkv_workspace &ws = a.ws;
-  const int bh = a.batch * ws.n_kv_heads;
-  XUnit x;
-  const int jj = u / (bh * a.S), rs = u - jj * bh * a.S;
-  x.c = rs / bh;
-  const int r = rs - x.c * bh;
-  x.b = r / ws.n_kv_heads;
-  x.g = r - x.b * ws.n_kv_heads;
-  x.j = jmax - 1 - jj;
-  x.q0 = a.qo_indptr[x.b];
-  x.n = a.qo_indptr[x.b + 1] - x.q0;
-  x.L = ws.seq_lens[x.b];
-  const long long cap = len_cap(ws);
-  // full mode: the query rows are not tokens of the context, so n_b may exceed L_b
-  const bool fits = (a.flags & PKV_FLAG_EXTEND_FULL) || x.n <= x.L;
-  bool ok = x.n >= 0 && fits && x.n <= a.max_qo_len && x.q0 >= 0 &&
-            x.q0 + x.n <= a.qo_indptr[a.batch] && (long long)x.L <= cap;
-  if (ok && ws.index_mode == PKV_IDX_FLAT) {
-    const int base = ws.kv_indptr[x.b];
-    ok = base >= 0 && (long long)base + x.L <= ws.max_total_tokens;
-  }
-  // split partials and lse rows live in the workspace, sized for batch *
-  // max_qo_len new tokens: a request whose rows lie past that (qo_indptr
-  // running on past an invalid request) is rejected, not written
-  if (ok && (a.S > 1 || (a.flags & PKV_FLAG_WRITE_LSE)))
-    ok = (long long)x.q0 + x.n <= (long long)a.batch * a.max_qo_len;
-  if (!ok && x.g == 0 && x.j == 0 && x.c == 0 && (threadIdx.x & 31) == 0)
-    atomicOr(ws.err, PKV_DEVERR_LEN);
-  x.live = ok && x.j * tq < x.n;
-  x.kend = !x.live ? 0 : (a.flags & PKV_FLAG_EXTEND_FULL) ? x.L
-                                                             : x.L - x.n + min(x.n, (x.j + 1) * tq);
-  const int chunk = ((x.kend + a.S - 1) / a.S + kXT - 1) / kXT * kXT;
-  x.k0 = x.c * chunk;
-  x.k1 = min(x.kend, x.k0 + chunk);
-  return x;
 }
 
 // TMA: the page-piece boxes (P % 16 == 0); else the cp.async gathers.
@@ -667,55 +602,6 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-using XTmapEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// 4-D view of a pool [NL * pool_slots, Hkv, D] as (64 columns, slot, 64-column
-// half, KV head): a box of 64 x 16 x D/64 x 1 is one 16-token piece of one
-// head, landing 128B-swizzled as [half][token][64 columns].
-bool xencode_pool_map(CUtensorMap *m, void *base, const pkv_workspace &ws) {
-  static XTmapEncodeFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<XTmapEncodeFn>(p);
-  }
-  if (!fn) return false;
-  const cuuint64_t D = (cuuint64_t)ws.head_dim, H = (cuuint64_t)ws.n_kv_heads;
-  const cuuint64_t dims[4] = {64, (cuuint64_t)ws.n_layers * (cuuint64_t)ws.pool_slots, D / 64, H};
-  const cuuint64_t strides[3] = {H * D * 2, 128, D * 2};
-  const cuuint32_t box[4] = {64, 16, (cuuint32_t)(D / 64), 1};
-  const cuuint32_t elem[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, elem,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Launch with programmatic dependent launch allowed (the kernels wait for
-// the previous kernel on the stream at entry).
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t st, Args &&...args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
 template <int D, int G>
 cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
   using C = XCfg<D>;
@@ -756,7 +642,8 @@ cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
   memset(&tmv, 0, sizeof(tmv));
   const bool tma = ws.index_mode == PKV_IDX_PAGE_TABLE && ws.page_size % 16 == 0 &&
                    (long long)ws.n_layers * ws.pool_slots < 0x7fffffffll &&
-                   xencode_pool_map(&tmk, ws.k_pool, ws) && xencode_pool_map(&tmv, ws.v_pool, ws);
+                   xencode_pool_map(&tmk, ws.k_pool, ws, D / 64) &&
+                   xencode_pool_map(&tmv, ws.v_pool, ws, D / 64);
   // Programmatic dependent launch when the grid leaves block slots free (its
   // start then overlaps the previous kernel's end: the cascade's prefix
   // attention, 36.4 -> 31.6 us per layer); a grid that fills every slot
@@ -771,18 +658,25 @@ cudaError_t launch_extend_one(const XArgs &a, cudaStream_t st) {
     else extend_mma_kernel<D, G, false><<<grid, kXThreads, C::SMEM, st>>>(a, tmk, tmv);
     e = cudaGetLastError();
   }
-  if (a.S > 1) {
-    if (e != cudaSuccess) return e;
-    const long long pairs = (long long)a.max_qo_len * ws.n_q_heads;
-    const long long mblocks = (pairs + 3) / 4;
-    const dim3 mgrid((unsigned)(mblocks < 1024 ? mblocks : 1024), (unsigned)a.batch);
-    e = launch_pdl(extend_merge_kernel<D>, mgrid, dim3(128), 0, st, ws, a.qo_indptr, a.max_qo_len,
-                   a.S, a.out, a.flags);
-  }
+  if (a.S > 1 && e == cudaSuccess) e = launch_extend_merge(a, D, st);
   return e;
 }
 
 }  // namespace
+
+cudaError_t launch_extend_merge(const XArgs &a, int D, cudaStream_t st) {
+  const pkv_workspace &ws = a.ws;
+  const long long pairs = (long long)a.max_qo_len * ws.n_q_heads;
+  const long long mblocks = (pairs + 3) / 4;
+  const dim3 mgrid((unsigned)(mblocks < 1024 ? mblocks : 1024), (unsigned)a.batch);
+  if (D == 128)
+    return launch_pdl(extend_merge_kernel<128>, mgrid, dim3(128), 0, st, ws, a.qo_indptr,
+                      a.max_qo_len, a.S, a.out, a.flags);
+  if (D == 64)
+    return launch_pdl(extend_merge_kernel<64>, mgrid, dim3(128), 0, st, ws, a.qo_indptr,
+                      a.max_qo_len, a.S, a.out, a.flags);
+  return cudaErrorNotSupported;
+}
 
 bool extend_supported(int head_dim, int group) {
   return (head_dim == 64 || head_dim == 128) &&
@@ -792,7 +686,14 @@ bool extend_supported(int head_dim, int group) {
 cudaError_t launch_extend(const pkv_workspace &ws, int batch, int layer, const int *qo_indptr,
                           int max_qo_len, const void *q, void *out, float scale, int num_splits,
                           int flags, cudaStream_t st) {
-  XArgs a{ws, batch, layer, max_qo_len, flags, num_splits, qo_indptr, q, out, scale};
+  XArgs a{ws, batch, layer, max_qo_len, flags & ~PKV_FLAG_EXTEND_WARP_MMA, num_splits, qo_indptr,
+          q, out, scale};
+  // the tcgen05 kernel where tensor-map boxes carry the pages; this file's
+  // warp-level kernel for the rest (and by request)
+  if (!(flags & PKV_FLAG_EXTEND_WARP_MMA) && extend_umma_supported(ws)) {
+    const cudaError_t e = launch_extend_umma(a, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
   const int D = ws.head_dim, G = ws.n_q_heads / ws.n_kv_heads;
 #define PKV_X_CASE(DD, GG) \
   if (D == DD && G == GG) return launch_extend_one<DD, GG>(a, st);

@@ -1,0 +1,648 @@
+// Paged extend (prefill) attention on the fifth-generation tensor cores:
+// tcgen05.mma with both contractions' accumulators in tensor memory (TMEM).
+// Same arguments, units, outputs and error rules as the warp-level kernel in
+// extend_mma.cu (the engine keeps the prefill step's qo_indptr in its
+// workspace: workspace.py page, bullet 19), which still serves the layouts
+// this one does not carry: flat token indices and page sizes that are not a
+// multiple of 16.
+//
+// A CTA owns 128 query rows of one (request, KV head): 128 / G new tokens x
+// the G query heads of the group, row r = (token r / G, head r % G), so a key
+// tile is read once for the whole group.  Per 128-key tile:
+//   S = Q K^T   tcgen05.mma M = 128, N = 128, K = D in steps of 16.  Q and the
+//               tile's K sit K-major in shared memory with the 128-byte
+//               swizzle ([64-column half][rows][128 B]); S lands in one of
+//               three 128-column TMEM buffers, so later tiles' products run
+//               while this tile's softmax reads its own.  (N = 128: measured,
+//               an N = 64 MMA runs at about half the tensor rate.)
+//   softmax     one thread per row: it loads its row of S from TMEM
+//               (tcgen05.ld, no shuffles), applies the causal mask, keeps the
+//               running max and sum in fp32 (exp2) and writes the weights P
+//               back into the same TMEM buffer as bf16 high and low parts,
+//               P = P_hi + P_lo to ~2^-17 (pairs of keys per 32-bit column).
+//   O += P V    tcgen05.mma M = 128, N = D, K = 128 keys in steps of 16 with
+//               P_hi and P_lo each as the A operand from TMEM and V read from
+//               shared memory as an MN-major operand (the tile's V rows,
+//               [half][key][128 B], are rows of 64 dims).  O stays in TMEM
+//               for the unit's whole key range.
+// A row's reference maximum is raised, and its O row rescaled through
+// tcgen05.ld / st, only when a tile's maximum exceeds it by more than 2^8;
+// the weights exp2(s - m) then stay below 256 and the sum and O use the same
+// reference, so the result is unchanged.
+//
+// Warps: 0 issues the tensor-map boxes of each tile's K and V into a 3-stage
+// ring (per 16-token page piece four boxes: K and V, each 64-column half);
+// 1 allocates the TMEM and issues every MMA from one thread (descriptors made
+// once, advanced by constant offsets), tracking their completion with
+// tcgen05.commit on mbarriers; 2-5 load Q, run the softmax and write the
+// outputs (warp w reads TMEM lanes 32 (w % 4) .. + 31, its rows).  Every wait
+// is bounded (~1 s) and raises PKV_DEVERR_TIMEOUT; the MMAs in flight are
+// drained before the TMEM is freed.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "extend_common.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kUM = 128;          // query rows per CTA (TMEM lanes)
+constexpr int kUN = 128;          // keys per tile (N of Q K^T: the MMA's full rate)
+constexpr int kUStages = 3;
+constexpr int kUSBufs = 3;        // S / P buffers in TMEM
+constexpr int kUThreads = 192;
+constexpr int kUTmemCols = 512;   // three S buffers of 128 columns, O of D <= 128
+constexpr int kUOCol = kUSBufs * kUN;  // O's first column
+constexpr float kURescale = 8.f;  // raise a row's reference max only past this (log2)
+
+template <int D>
+struct UCfg {
+  static constexpr int HALVES = D / 64;
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int QHALF = kUM * 128;   // one 64-column half of Q
+  static constexpr int KVHALF = kUN * 128;  // one half of a tile's K (or V)
+  static constexpr int KBYTES = HALVES * KVHALF;
+  static constexpr int STAGE = 2 * KBYTES;  // K then V
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + HALVES * QHALF;
+  static constexpr int SMEM = OFF_KV + kUStages * STAGE + 1024;  // + alignment slack
+  static constexpr uint32_t PIECE_TX = 2 * HALVES * 16 * 128;  // K and V of 16 tokens
+  static_assert(D == 64 || D == 128, "one or two 64-column halves");
+  static_assert(D <= kUTmemCols - kUOCol, "O fits the allocation");
+  static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+};
+
+// Shared-memory matrix descriptor of tcgen05.mma: start address, leading and
+// stride byte offsets (16-byte units), the descriptor version bit (46) and
+// the 128-byte swizzle (2 at bit 61).  K-major operands: rows 128 B apart,
+// 8-row groups SBO apart, LBO unused; MN-major: LBO between 64-element
+// blocks of the MN dimension, SBO between groups of 8 K rows.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5), bf16 A
+// (7-9) and B (10-12), A K-major, B K-major or MN-major (bit 16), N / 8
+// (17-22), M / 16 (24-28).
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                     int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// As umma, with the A operand (M x 16, bf16 pairs per 32-bit column) in TMEM.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                        uint32_t idesc, int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once) on the mbarrier when every MMA this thread issued so far is done.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane (warp-collective).
+__device__ __forceinline__ void tmem_ld32(uint32_t (&r)[32], uint32_t taddr) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2^x with the SFU's ex2.approx (relative error ~2^-22, far below the
+// weights' bf16 high + low rounding); 2^-inf = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
+               "r"(w)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *tm, int c1, int c2,
+                                        int c3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ int unit_tiles(const XUnit &x) {
+  return x.k1 > x.k0 ? (x.k1 - x.k0 + kUN - 1) / kUN : 0;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kUThreads, 1)
+    extend_umma_kernel(const __grid_constant__ XArgs a, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv) {
+  // Everything read here may come from the previous kernel on the stream
+  // (programmatic dependent launch): wait for it, then let the next start.
+  pdl_wait();
+  pdl_trigger();
+  using C = UCfg<D>;
+  constexpr int TQ = kUM / G;  // new tokens per CTA
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kUStages], empty[kUStages];
+  __shared__ __align__(8) uint64_t s_full[kUSBufs], buf_free[kUSBufs];
+  __shared__ __align__(8) uint64_t q_full, p_full, pv_done, drain;
+  __shared__ int flags[kUStages];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(smem);
+  const pkv_workspace &ws = a.ws;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Hq = ws.n_q_heads;
+  const int jmax = (a.max_qo_len + TQ - 1) / TQ;
+  const int units = jmax * a.S * a.batch * ws.n_kv_heads;
+  if (tid == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmk) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmv) : "memory");
+    for (int s = 0; s < kUStages; ++s) {
+      mbar_init(&full[s], 1);   // the producer's expect-tx arrival
+      mbar_init(&empty[s], 1);  // commit after the tile's P V
+    }
+    for (int i = 0; i < kUSBufs; ++i) {
+      mbar_init(&s_full[i], 1);    // commit after the tile's Q K^T
+      mbar_init(&buf_free[i], 1);  // commit after the tile's P V (P read from the buffer)
+    }
+    mbar_init(&q_full, 4);   // the four softmax warps have written Q
+    mbar_init(&p_full, 4);   // ... and P (and rescaled O)
+    mbar_init(&pv_done, 1);  // commit after a tile's P V
+    mbar_init(&drain, 1);
+    s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&s_tmem)),
+                 "r"(kUTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  // A bounded wait; one that runs out stops the whole CTA.
+  auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+    if (s_abort) return false;
+    if (mbar_wait_bounded(bar, parity)) return true;
+    s_abort = 1;
+    atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
+    return false;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------- producer ----
+    // Lane (box, piece): piece j = lane & 7 of the tile's eight 16-token
+    // pieces, box = lane >> 3: K's halves, then V's.  A bad page id loads the
+    // in-range slot 0 instead and flags the stage (its unit is written empty).
+    Plan pl;
+    pl.set_pages(ws);
+    const int j = lane & 7, box = lane >> 3;
+    int k = 0;
+    bool aborted = false;
+    for (int u = blockIdx.x; u < units && !aborted; u += gridDim.x) {
+      const XUnit x = xunit(a, u, TQ, jmax);
+      if (!x.live) continue;
+      const int rrow = ws.req_pool_indices[x.b];
+      const bool row_ok = rrow >= 0 && rrow < ws.max_reqs;
+      const long long base = row_ok ? (long long)rrow * ws.max_pages_per_req : 0;
+      auto raw_at = [&](int t) {
+        return (t >= x.k1 || !row_ok) ? -1 : ws.page_table[base + pl.page_of(t)];
+      };
+      const int ntiles = unit_tiles(x);
+      int raw = raw_at(x.k0 + 16 * j);
+      for (int tile = 0; tile < ntiles; ++tile, ++k) {
+        const int s = k % kUStages, r = k / kUStages;
+        if ((r > 0 && !wait(&empty[s], (r - 1) & 1)) || s_abort) {
+          aborted = true;
+          break;
+        }
+        const int t0 = x.k0 + tile * kUN;
+        const int np = min(kUN / 16, (x.k1 - t0 + 15) / 16);
+        int kind = 0, slot0 = 0;
+        if (j < np) {
+          const long long s0 = slot_from_raw(ws, pl, raw, t0 + 16 * j, kind);
+          if (!kind) slot0 = (int)s0;
+        }
+        const int nx = raw_at(t0 + kUN + 16 * j);  // the next tile's, while these issue
+        const int bad = __reduce_or_sync(0xffffffffu, kind);
+        if (lane == 0) {
+          flags[s] = bad;
+          if (bad) atomicOr(ws.err, bad);
+        }
+        __syncwarp();
+        if (box < 2 * C::HALVES && j < np) {
+          const int isv = box >= C::HALVES, h = box - isv * C::HALVES;
+          tma_box(sbase + C::OFF_KV + s * C::STAGE + isv * C::KBYTES + h * C::KVHALF + j * 2048,
+                  isv ? &tmv : &tmk, a.layer * ws.pool_slots + slot0, h, x.g, &full[s]);
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], np * C::PIECE_TX);
+        raw = nx;
+      }
+    }
+    if (aborted) {
+      // the last (up to kUStages) tiles issued may still be landing
+      for (int kk = max(0, k - kUStages); kk < k; ++kk)
+        mbar_wait_bounded(&full[kk % kUStages], (kk / kUStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA ----
+    if (lane == 0) {
+      constexpr uint32_t kIdS = umma_idesc(kUM, kUN, 0);  // S = Q K^T: both K-major
+      constexpr uint32_t kIdO = umma_idesc(kUM, D, 1);    // O += P V: V MN-major
+      // descriptors of Q and of stage 0's K and V; every other operand is one
+      // of these plus a byte offset (in 16-byte units, inside the start field)
+      const uint64_t dq = umma_desc(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dk = umma_desc(sbase + C::OFF_KV, 16, 1024);
+      const uint64_t dv = umma_desc(sbase + C::OFF_KV + C::KBYTES, C::KVHALF, 1024);
+      int k = 0, ul = 0;
+      bool dead = false;
+      for (int u = blockIdx.x; u < units && !dead; u += gridDim.x) {
+        const XUnit x = xunit(a, u, TQ, jmax);
+        if (!x.live) continue;
+        const int T = unit_tiles(x);
+        if (T == 0) continue;
+        if (!wait(&q_full, ul & 1)) break;
+        tc_fence_after();
+        // Q K^T of tile t, then P V of tile t - 1 (whose softmax ran meanwhile)
+        for (int t = 0; t <= T && !dead; ++t) {
+          if (t < T) {
+            const int kk = k + t, s = kk % kUStages, b = kk % kUSBufs;
+            if (!wait(&full[s], (kk / kUStages) & 1) ||
+                (kk >= kUSBufs && !wait(&buf_free[b], ((kk / kUSBufs) - 1) & 1))) {
+              dead = true;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ks0 = (uint64_t)((s * C::STAGE) >> 4);
+#pragma unroll
+            for (int ks = 0; ks < C::KSTEPS; ++ks) {
+              // k-step ks: half ks / 4, 32 bytes further per step inside the row
+              constexpr int kQH = C::QHALF, kKH = C::KVHALF;
+              const uint64_t qo = (uint64_t)(((ks >> 2) * kQH + (ks & 3) * 32) >> 4);
+              const uint64_t ko = (uint64_t)(((ks >> 2) * kKH + (ks & 3) * 32) >> 4);
+              umma(tmem + b * kUN, dq + qo, dk + ks0 + ko, kIdS, ks > 0);
+            }
+            umma_commit(&s_full[b]);
+          }
+          if (t >= 1) {
+            const int kk = k + t - 1, s = kk % kUStages, b = kk % kUSBufs;
+            if (!wait(&p_full, kk & 1)) {
+              dead = true;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t vs0 = (uint64_t)((s * C::STAGE) >> 4);
+            const uint32_t pb = tmem + b * kUN;  // P_hi in the buffer's first 64 columns
+#pragma unroll
+            for (int ks = 0; ks < kUN / 16; ++ks) {
+              // 16 keys per step: 16 V rows (2048 B) further, 8 P columns
+              const uint64_t bd = dv + vs0 + (uint64_t)((ks * 2048) >> 4);
+              umma_ts(tmem + kUOCol, pb + ks * 8, bd, kIdO, t > 1 || ks > 0);
+              umma_ts(tmem + kUOCol, pb + kUN / 2 + ks * 8, bd, kIdO, 1);
+            }
+            umma_commit(&pv_done);
+            umma_commit(&buf_free[b]);
+            umma_commit(&empty[s]);
+          }
+        }
+        k += T;
+        ++ul;
+      }
+      // every MMA issued is done before the TMEM is freed
+      umma_commit(&drain);
+      mbar_wait_bounded(&drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------- softmax ----
+    const int wq = warp & 3;
+    const int row = 32 * wq + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * wq) << 16);
+    const float qk_scale = a.scale * kLog2e;
+    const bool full_mode = (a.flags & PKV_FLAG_EXTEND_FULL) != 0;
+    const bool out_f32 = (a.flags & PKV_FLAG_OUT_F32) != 0;
+    const int tw = tid - 64;  // 0 .. 127 over the four warps
+    int k = 0;
+    for (int u = blockIdx.x; u < units && !s_abort; u += gridDim.x) {
+      const XUnit x = xunit(a, u, TQ, jmax);
+      if (!x.live) continue;
+      const int T = unit_tiles(x);
+      const int i = x.j * TQ + row / G;
+      const bool valid = i < x.n;
+      const int pos = !valid ? -1 : full_mode ? x.L - 1 : x.L - x.n + i;
+      const long long qrow = valid ? (long long)(x.q0 + i) * Hq + x.g * G + row % G : 0;
+      float m_used = -INFINITY, l = 0.f;
+      int bad = 0;
+      bool ok = true;
+      if (T > 0) {
+        // this row of Q, swizzled into the K-major Q tile (zeros past the tokens)
+        const uint4 *src =
+            reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + qrow * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+          st_shared_v4(sbase + C::OFF_Q + (c >> 3) * C::QHALF + row * 128 +
+                           (((c & 7) ^ (row & 7)) << 4),
+                       v.x, v.y, v.z, v.w);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full);
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const int kk = k + t, s = kk % kUStages, b = kk % kUSBufs;
+        const int t0 = x.k0 + t * kUN;
+        if (!wait(&s_full[b], (kk / kUSBufs) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[kUN / 32][32];
+#pragma unroll
+        for (int c = 0; c < kUN / 32; ++c) tmem_ld32(sv[c], trow + b * kUN + 32 * c);
+        tmem_wait_ld();
+        // the stage's boxes have landed (S was computed from them): its flags
+        if (!wait(&full[s], (kk / kUStages) & 1)) {
+          ok = false;
+          break;
+        }
+        bad |= flags[s];
+        // scores in log2 units; keys past the row's position or the split's
+        // end count as -inf.  Eight partial maxima and sums keep the
+        // dependent chains short (one warp per sub-partition runs this).
+        const int lim = min(pos, x.k1 - 1) - t0;
+        float mxp[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kUN; ++c) {
+          float v = __uint_as_float(sv[c >> 5][c & 31]) * qk_scale;
+          if (c > lim) v = -INFINITY;
+          sv[c >> 5][c & 31] = __float_as_uint(v);
+          mxp[c & 7] = fmaxf(mxp[c & 7], v);
+        }
+        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_used + kURescale || (m_used == -INFINITY && mx != -INFINITY)) {
+          if (m_used != -INFINITY) {
+            alpha = exp2f(m_used - mx);
+            rescale = true;
+          }
+          m_used = mx;
+        }
+        // no key of this row attended yet: every weight is 0
+        const float mref = m_used == -INFINITY ? INFINITY : m_used;
+        float sp[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sp[e] = 0.f;
+        // P into the tile's S buffer, bf16 pairs (even key in the low half):
+        // P_hi in its first 64 columns, P_lo in the next 64
+#pragma unroll
+        for (int c0 = 0; c0 < kUN; c0 += 32) {
+          uint32_t ph[16], pl[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float e0 = ex2_approx(__uint_as_float(sv[c0 >> 5][c]) - mref);
+            const float e1 = ex2_approx(__uint_as_float(sv[c0 >> 5][c + 1]) - mref);
+            sp[(c >> 1) & 7] += e0 + e1;
+            const uint32_t hi = pack_bf16x2(e0, e1);
+            ph[c >> 1] = hi;
+            pl[c >> 1] = pack_bf16x2(e0 - bf16lo(hi), e1 - bf16hi(hi));
+          }
+          tmem_st16(trow + b * kUN + c0 / 2, ph);
+          tmem_st16(trow + b * kUN + kUN / 2 + c0 / 2, pl);
+        }
+        const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        l = l * alpha + sum;
+        if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
+          // O holds every earlier tile once the previous tile's P V is done
+          if (!wait(&pv_done, (kk - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(o, trow + kUOCol + c);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(trow + kUOCol + c, o);
+          }
+        }
+        if (t0 + kUN > x.k1) {
+          // The last tile: V rows past the split's end hold what the pool or
+          // the stage's previous tile held, and P = 0 does not cancel a NaN.
+          const int first = x.k1 - t0;
+          const uint32_t vb = sbase + C::OFF_KV + s * C::STAGE + C::KBYTES;
+          for (int e = tw; e < (kUN - first) * C::HALVES * 8; e += 128) {
+            const int r = first + e / (C::HALVES * 8), rem = e % (C::HALVES * 8);
+            st_shared_v4(vb + (rem >> 3) * C::KVHALF + r * 128 + (((rem & 7) ^ (r & 7)) << 4),
+                         0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full);
+      }
+      if (!ok) break;
+      // ---- the unit's rows: O / l, or the split's partial ----
+      const bool zero = bad || !(l > 0.f);
+      const float inv = zero ? 0.f : 1.f / l;
+      if (T > 0) {
+        if (!wait(&pv_done, (k + T - 1) & 1)) break;
+        tc_fence_after();
+      }
+      const long long pr = qrow * a.S + x.c;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        if (T > 0) {
+          tmem_ld32(o, trow + kUOCol + c);
+          tmem_wait_ld();
+        }
+        if (!valid) continue;
+        float f[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = (zero || T == 0) ? 0.f : __uint_as_float(o[e]) * inv;
+        if (a.S > 1 || out_f32) {
+          float *dst = a.S > 1 ? ws.o_part + pr * D + c : static_cast<float *>(a.out) + qrow * D + c;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4 *>(dst + e) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + qrow * D + c);
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+            dst[e / 8] = make_uint4(pack_bf16x2(f[e], f[e + 1]), pack_bf16x2(f[e + 2], f[e + 3]),
+                                    pack_bf16x2(f[e + 4], f[e + 5]), pack_bf16x2(f[e + 6], f[e + 7]));
+        }
+      }
+      if (valid) {
+        if (a.S > 1) {
+          // a failed split is marked l = -1: the merge writes the row as zeros
+          ws.ml_part[pr * 2] = zero ? -INFINITY : m_used * kLn2;
+          ws.ml_part[pr * 2 + 1] = bad ? -1.f : (zero ? 0.f : l);
+        } else if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse) {
+          ws.lse[qrow] = zero ? -INFINITY : m_used * kLn2 + logf(l);
+        }
+      }
+      // O's loads are done before the next unit's Q is published (its first
+      // P V overwrites O)
+      tc_fence_before();
+      k += T;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kUTmemCols)
+                 : "memory");
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_umma_one(const XArgs &a, cudaStream_t st) {
+  using C = UCfg<D>;
+  static int occ_cache[64] = {0};
+  static int sms_cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int di = dev & 63;
+  auto kern = extend_umma_kernel<D, G>;
+  if (occ_cache[di] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    int occ = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kUThreads, C::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms_cache[di] = sms;
+    // every resident CTA holds kUTmemCols of the SM's 512 TMEM columns
+    const int tmem_cap = 512 / kUTmemCols;
+    occ_cache[di] = occ < 1 ? 1 : (occ > tmem_cap ? tmem_cap : occ);
+  }
+  constexpr int TQ = kUM / G;
+  const long long units =
+      (long long)((a.max_qo_len + TQ - 1) / TQ) * a.S * a.batch * a.ws.n_kv_heads;
+  if (units <= 0) return cudaSuccess;
+  if (units > 0x7fffffffll) return cudaErrorInvalidValue;
+  const long long cap = (long long)sms_cache[di] * occ_cache[di];
+  const int grid = (int)(units < cap ? units : cap);
+  CUtensorMap tmk, tmv;
+  memset(&tmk, 0, sizeof(tmk));
+  memset(&tmv, 0, sizeof(tmv));
+  if (!xencode_pool_map(&tmk, a.ws.k_pool, a.ws, 1) || !xencode_pool_map(&tmv, a.ws.v_pool, a.ws, 1))
+    return cudaErrorNotSupported;
+  // Programmatic dependent launch when the grid leaves CTA slots free (its
+  // start then overlaps the previous kernel's end); a grid that fills every
+  // slot launches plainly.
+  if (grid < cap) {
+    e = launch_pdl(kern, dim3(grid), dim3(kUThreads), C::SMEM, st, a, tmk, tmv);
+  } else {
+    kern<<<grid, kUThreads, C::SMEM, st>>>(a, tmk, tmv);
+    e = cudaGetLastError();
+  }
+  if (a.S > 1 && e == cudaSuccess) e = launch_extend_merge(a, D, st);
+  return e;
+}
+
+}  // namespace
+
+bool extend_umma_supported(const pkv_workspace &ws) {
+  if (ws.n_kv_heads <= 0 || ws.n_q_heads % ws.n_kv_heads) return false;
+  const int G = ws.n_q_heads / ws.n_kv_heads;
+  return (ws.head_dim == 64 || ws.head_dim == 128) &&
+         (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) && xtma_pages(ws);
+}
+
+cudaError_t launch_extend_umma(const XArgs &a, cudaStream_t st) {
+  const int D = a.ws.head_dim, G = a.ws.n_q_heads / a.ws.n_kv_heads;
+#define PKV_U_CASE(DD, GG) \
+  if (D == DD && G == GG) return launch_umma_one<DD, GG>(a, st);
+  PKV_U_CASE(128, 1) PKV_U_CASE(128, 2) PKV_U_CASE(128, 4) PKV_U_CASE(128, 8)
+  PKV_U_CASE(128, 16) PKV_U_CASE(64, 1) PKV_U_CASE(64, 2) PKV_U_CASE(64, 4)
+  PKV_U_CASE(64, 8) PKV_U_CASE(64, 16)
+#undef PKV_U_CASE
+  return cudaErrorNotSupported;
+}
+
+}  // namespace pkv

@@ -16,6 +16,7 @@ cudaError_t launch_extend_append(const pkv_workspace &ws, int batch, int layer,
                                  const int *qo_indptr, int max_qo_len, const void *k_new,
                                  const void *v_new, cudaStream_t st);
 bool extend_supported(int head_dim, int group);
+bool extend_umma_supported(const pkv_workspace &ws);  // extend_umma.cu
 cudaError_t launch_merge_lse(int n_rows, int head_dim, const float *o_a, const float *lse_a,
                              const float *o_b, const float *lse_b, void *out, float *lse_out,
                              int flags, cudaStream_t st);
@@ -178,9 +179,13 @@ int pkv_choose_extend_splits(const pkv_workspace *ws, int batch, int max_qo_len,
       ws->n_q_heads <= 0 || ws->n_q_heads % ws->n_kv_heads)
     return 1;
   const int G = ws->n_q_heads / ws->n_kv_heads;
-  const int tq = G <= 64 ? 64 / G : 1;  // new tokens per block
+  // the tcgen05 kernel: 128 query rows per CTA, one CTA per SM; the
+  // warp-level kernel: 64 rows, two blocks per SM
+  const bool umma = extend_umma_supported(*ws);
+  const int rows = umma ? 128 : 64;
+  const int tq = G <= rows ? rows / G : 1;  // new tokens per block
   const long long units = (long long)((max_qo_len + tq - 1) / tq) * batch * ws->n_kv_heads;
-  const long long blocks = 2ll * num_sms;
+  const long long blocks = (umma ? 1ll : 2ll) * num_sms;
   if (units >= blocks) return 1;
   long long S = blocks / units;
   const long long by_len = min_seq_len_hint > 0 ? min_seq_len_hint / 256 : 1;
@@ -298,7 +303,8 @@ pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
                            float scale, int num_splits, int flags, pkv_stream_t stream) {
   pkv_status st = extend_common(ws, batch, layer, qo_indptr, max_qo_len, q, out);
   if (st != PKV_OK) return st;
-  if (flags & ~(PKV_FLAG_OUT_F32 | PKV_FLAG_WRITE_LSE | PKV_FLAG_EXTEND_FULL))
+  if (flags & ~(PKV_FLAG_OUT_F32 | PKV_FLAG_WRITE_LSE | PKV_FLAG_EXTEND_FULL |
+                PKV_FLAG_EXTEND_WARP_MMA))
     return PKV_ERR_INVALID;
   if (num_splits < 1) return PKV_ERR_INVALID;
   // lse[query row, Hq] lives in ws->lse ([max_batch, Hq]): room for every row

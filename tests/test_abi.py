@@ -239,16 +239,14 @@ def test_bind_tracker_sequence():
 
 
 def test_choose_extend_splits():
-    # Fill two blocks per SM, no split under 256 keys, within the partials'
-    # room; the bench's own rule gives the same where the room does not bind.
-    import types
-
-    import bench
+    # Fill the resident blocks, no split under 256 keys, within the partials'
+    # room.  Page sizes that are a multiple of 16 take the tcgen05 kernel:
+    # 128 query rows per CTA, one CTA per SM at D = 128.
     big = _ws(n_q_heads=32, n_kv_heads=8, max_batch=64, max_splits=4096)
     C = P.pkv_choose_extend_splits
-    # 64 new tokens at G = 4: 4 blocks per head, 8 heads, one request: 32 units
+    # 64 new tokens at G = 4: 2 blocks per head, 8 heads, one request: 16 units
     assert C(big, 1, 64, 32832, 152) == 9
-    assert C(big, 4, 256, 900, 152) == 1           # 512 units already fill the SMs
+    assert C(big, 4, 256, 900, 152) == 1           # 256 units already fill the SMs
     assert C(big, 1, 64, 600, 152) == 2            # 600 keys: two splits of >= 256
     assert C(big, 1, 64, 100, 152) == 1
     # the partials' room: max_batch * max_splits rows over batch * max_qo_len
@@ -256,12 +254,20 @@ def test_choose_extend_splits():
     assert C(None, 1, 64, 32832, 152) == 1
     assert C(big, 0, 64, 32832, 152) == 1
     assert C(big, 1, 64, 32832, 0) == 1
-    for B, Hq, Hkv, qo, lens in ((1, 32, 8, 64, 32832), (2, 16, 2, 40, 3000), (3, 8, 8, 17, 700),
-                                 (1, 32, 2, 1, 70000)):
-        p = types.SimpleNamespace(batch=B, n_q_heads=Hq, n_kv_heads=Hkv, group=Hq // Hkv,
-                                  seq_lens=types.SimpleNamespace(tolist=lambda: [lens] * B))
-        ws = _ws(n_q_heads=Hq, n_kv_heads=Hkv, max_batch=64, max_splits=4096)
-        assert C(ws, B, qo, lens, 152) == bench.extend_splits(p, [qo] * B, 152), (B, Hq, Hkv)
+    ws = lambda Hq, Hkv, **kw: _ws(n_q_heads=Hq, n_kv_heads=Hkv, max_batch=64, max_splits=4096,
+                                   **kw)
+    # G = 8: 16 tokens per CTA, 3 x 2 x 2 = 12 units, 152 / 12 = 12, 3000 keys allow 11
+    assert C(ws(16, 2), 2, 40, 3000, 152) == 11
+    # G = 1: 128 tokens per CTA, 24 units, 6 by the SMs, 700 keys allow 2
+    assert C(ws(8, 8), 3, 17, 700, 152) == 2
+    # G = 16: 8 tokens per CTA, 2 units: 76 splits
+    assert C(ws(32, 2), 1, 1, 70000, 152) == 76
+    # head_dim 64: the same geometry
+    assert C(ws(32, 2, head_dim=64), 1, 1, 70000, 152) == 76
+    # page size 8: the warp-level kernel, 64 rows per block (4 tokens at
+    # G = 16), two blocks per SM
+    assert C(ws(32, 2, page_size=8), 1, 1, 70000, 152) == 152
+
 
 
 def test_static_scratch_host_validation():

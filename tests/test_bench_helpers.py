@@ -37,19 +37,6 @@ def test_decode_algorithmic_bytes():
     assert bench.algorithmic_bytes(lens, p) == want
 
 
-def test_extend_splits_one_wave():
-    # 64 new tokens at G = 4 are 4 query blocks per head; with 8 heads and one
-    # request, 32 units: 9 splits keep 288 units within 2 x 152 blocks.
-    p = _p(1, 32, 8, 128, [32832])
-    assert bench.extend_splits(p, [64], 152) == 9
-    # enough units already: no split
-    p4 = _p(4, 32, 8, 128, [1000, 2000, 1500, 900])
-    assert bench.extend_splits(p4, [256] * 4, 152) == 1
-    # no split shorter than 256 keys
-    ps = _p(1, 32, 8, 128, [600])
-    assert bench.extend_splits(ps, [64], 152) == 2
-
-
 def test_traffic_record_applies_only_to_its_kernel_source(tmp_path, monkeypatch):
     # The committed DRAM traffic per launch is reported only while the decode
     # kernel's sources hash to the recorded value, scaled by the algorithmic

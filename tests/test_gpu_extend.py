@@ -99,21 +99,29 @@ CASES = {
 }
 
 
+# the kernel pkv_extend_attn picks (tcgen05 where page sizes are a multiple
+# of 16, else the warp-level one), and the warp-level one by request
+KERNS = {"auto": 0, "warp": A.PKV_FLAG_EXTEND_WARP_MMA}
+
+
+@pytest.mark.parametrize("kern", list(KERNS))
 @pytest.mark.parametrize("S", [1, 3])
 @pytest.mark.parametrize("case", list(CASES), ids=list(CASES))
-def test_extend_parity(cuda, case, S):
+def test_extend_parity(cuda, case, S, kern):
     lens, qo, Hq, Hkv, D, P = CASES[case]
     got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=Hq, Hkv=Hkv, D=D, P=P, seed=4100,
-                                   S=S)
-    _compare(got, ref, want, f"{case} S={S}")
+                                   S=S, flags=KERNS[kern])
+    _compare(got, ref, want, f"{case} S={S} {kern}")
 
 
-def test_extend_splits_agree(cuda):
+@pytest.mark.parametrize("kern,bar", [("auto", 1e-3), ("warp", 2e-3)])
+def test_extend_splits_agree(cuda, kern, bar):
     # fp32 outputs of 1, 2, 5 and 16 splits (some of them empty for early
-    # query blocks) agree with each other; P enters P V as bf16 and its
-    # rounding depends on the running maximum, so the bar is 2e-3.
+    # query blocks) agree with each other.  The tcgen05 kernel applies P as
+    # bf16 high and low parts (~2^-17 of each weight): 1e-3.  The warp-level
+    # kernel rounds P to one bf16, which depends on the running maximum: 2e-3.
     kw = dict(lens=(1500, 700), qo=(48, 100), Hq=16, Hkv=2, D=128, P=16, seed=4700, NL=1,
-              layer=0, flags=A.PKV_FLAG_OUT_F32,
+              layer=0, flags=A.PKV_FLAG_OUT_F32 | KERNS[kern],
               rows=[(r, h) for r in range(0, 148, 7) for h in range(16)])
     outs = []
     for S in (1, 2, 5, 16):
@@ -121,7 +129,53 @@ def test_extend_splits_agree(cuda):
         _compare(got, ref, want, f"S={S}")
         outs.append(got)
     for o in outs[1:]:
-        assert np.abs(o - outs[0]).max() <= 2e-3
+        assert np.abs(o - outs[0]).max() <= bar
+
+
+def test_extend_kernels_agree(cuda):
+    # fp32 outputs of the tcgen05 and the warp-level kernel, same inputs.  The
+    # tcgen05 kernel's P = P_hi + P_lo keeps it within 1e-3 of the fp64
+    # oracle; the warp-level kernel's single bf16 P moves it by up to a few
+    # 1e-3, so the two agree within 5e-3.
+    kw = dict(lens=(900, 333, 64), qo=(200, 33, 64), Hq=32, Hkv=8, D=128, P=16, seed=5000,
+              NL=1, layer=0)
+    a, ref, _, _ = run_extend(cuda, flags=A.PKV_FLAG_OUT_F32, **kw)
+    b, _, _, _ = run_extend(cuda, flags=A.PKV_FLAG_OUT_F32 | A.PKV_FLAG_EXTEND_WARP_MMA, **kw)
+    assert np.abs(a - ref).max() <= 1e-3
+    assert np.abs(a - b).max() <= 5e-3
+
+
+def test_extend_many_units_per_cta(cuda):
+    # More (query block, request, KV head) units than CTAs: every CTA runs
+    # several units back to back through the same barriers and tensor memory.
+    lens, qo = (700, 420, 900, 512, 300, 640), (256, 256, 200, 256, 256, 100)
+    rng = np.random.default_rng(5)
+    T = sum(qo)
+    rows = sorted({(int(rng.integers(T)), int(rng.integers(32))) for _ in range(300)}
+                  | {(0, 0), (T - 1, 31)})
+    for S in (1, 2):
+        got, ref, want, _ = run_extend(cuda, lens=lens, qo=qo, Hq=32, Hkv=8, D=128, P=16,
+                                       seed=5100, NL=1, layer=0, rows=rows, S=S)
+        _compare(got, ref, want, f"many units S={S}")
+
+
+def test_extend_running_max_jumps(cuda):
+    # Key rows scaled x40 part-way through each context lift the scores by
+    # far more than 2^8: the tcgen05 kernel raises its reference maximum and
+    # rescales O in tensor memory.  Outputs against the oracle, both kernels.
+    def edit(p):
+        table, rows = p.page_table, p.req_pool_indices
+        for b in range(p.batch):
+            L = int(p.seq_lens[b])
+            for t in (L // 3, L // 2 + 5, L - 70):
+                page = int(table[int(rows[b]), t // p.page_size])
+                slot = page * p.page_size + t % p.page_size
+                p.k_pool[:, slot] = (p.k_pool[:, slot].float() * 40).to(torch.bfloat16)
+    for kern in KERNS.values():
+        got, ref, want, _ = run_extend(cuda, lens=(600, 1000), qo=(100, 300), Hq=16, Hkv=2,
+                                       D=128, P=16, seed=5200, NL=1, layer=0, table_edit=edit,
+                                       flags=A.PKV_FLAG_OUT_F32 | kern)
+        _compare(got, ref, want, f"outlier keys {kern}")
 
 
 def test_extend_f32_output_one_new_token(cuda):
