@@ -50,12 +50,16 @@ namespace {
 
 constexpr int kUM = 128;          // query rows per CTA (TMEM lanes)
 constexpr int kUN = 128;          // keys per tile (N of Q K^T: the MMA's full rate)
-constexpr int kUStages = 3;
+constexpr int kUKStages = 3;      // K ring: a tile's K is free once its Q K^T is done
+constexpr int kUVStages = 2;      // V ring: free once the tile's P V is done
 constexpr int kUSBufs = 3;        // S / P buffers in TMEM
-constexpr int kUThreads = 192;
+constexpr int kUSoftWarps = 8;    // two per TMEM lane quarter, 64 keys of a tile each
+constexpr int kUThreads = (3 + kUSoftWarps) * 32;  // K loader, MMA, softmax, V loader
+constexpr int kUVWarp = 2 + kUSoftWarps;
 constexpr int kUTmemCols = 512;   // three S buffers of 128 columns, O of D <= 128
 constexpr int kUOCol = kUSBufs * kUN;  // O's first column
 constexpr float kURescale = 8.f;  // raise a row's reference max only past this (log2)
+constexpr int kUSortMax = 256;    // (query block, split, request) triples ordered by cost
 
 template <int D>
 struct UCfg {
@@ -63,15 +67,15 @@ struct UCfg {
   static constexpr int KSTEPS = D / 16;
   static constexpr int QHALF = kUM * 128;   // one 64-column half of Q
   static constexpr int KVHALF = kUN * 128;  // one half of a tile's K (or V)
-  static constexpr int KBYTES = HALVES * KVHALF;
-  static constexpr int STAGE = 2 * KBYTES;  // K then V
+  static constexpr int KBYTES = HALVES * KVHALF;  // a tile's K (or V)
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + HALVES * QHALF;
-  static constexpr int SMEM = OFF_KV + kUStages * STAGE + 1024;  // + alignment slack
-  static constexpr uint32_t PIECE_TX = 2 * HALVES * 16 * 128;  // K and V of 16 tokens
+  static constexpr int OFF_K = OFF_Q + HALVES * QHALF;
+  static constexpr int OFF_V = OFF_K + kUKStages * KBYTES;
+  static constexpr int SMEM = OFF_V + kUVStages * KBYTES + 1024;  // + alignment slack
+  static constexpr uint32_t PIECE_TX = HALVES * 16 * 128;  // K (or V) of 16 tokens
   static_assert(D == 64 || D == 128, "one or two 64-column halves");
   static_assert(D <= kUTmemCols - kUOCol, "O fits the allocation");
-  static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+  static_assert(SMEM + 8192 <= 227 * 1024, "shared memory of one CTA");
 };
 
 // Shared-memory matrix descriptor of tcgen05.mma: start address, leading and
@@ -174,6 +178,30 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Blackwell's paired fp32 arithmetic: two lanes of a 64-bit register pair
+// per instruction (x in the low word).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three (one instruction on this architecture)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
                                              uint32_t w) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
@@ -205,10 +233,22 @@ __global__ void __launch_bounds__(kUThreads, 1)
   using C = UCfg<D>;
   constexpr int TQ = kUM / G;  // new tokens per CTA
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[kUStages], empty[kUStages];
+  __shared__ __align__(8) uint64_t k_full[kUKStages], k_empty[kUKStages];
+  __shared__ __align__(8) uint64_t v_full[kUVStages], v_empty[kUVStages];
   __shared__ __align__(8) uint64_t s_full[kUSBufs], buf_free[kUSBufs];
-  __shared__ __align__(8) uint64_t q_full, p_full, pv_done, drain;
-  __shared__ int flags[kUStages];
+  // p_full alternates by tile: the softmax may finish tile kk + 1 before the
+  // MMA thread looks for tile kk's phase, which one barrier would then have
+  // passed twice
+  __shared__ __align__(8) uint64_t q_full, p_full[2], pv_done, drain;
+  __shared__ __align__(8) uint64_t xbar[4];  // per lane quarter: its two softmax warps
+  // per V stage: the tile's bad page bits.  The softmax reads them after the
+  // stage's V has landed; the stage is refilled only after the tile's P V,
+  // which waits for that softmax.  (A K stage is refilled as soon as its
+  // Q K^T is done, possibly before the softmax of its tile has started.)
+  __shared__ int flags[kUVStages];
+  __shared__ float s_xmax[2][2][kUM];  // [tile parity][key half][row]: partial row maxima
+  __shared__ float s_xsum[2][kUM];     // [key half][row]: partial row sums, at the end
+  __shared__ int s_cost[kUSortMax], s_order[kUSortMax];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -221,18 +261,24 @@ __global__ void __launch_bounds__(kUThreads, 1)
   if (tid == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmk) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmv) : "memory");
-    for (int s = 0; s < kUStages; ++s) {
-      mbar_init(&full[s], 1);   // the producer's expect-tx arrival
-      mbar_init(&empty[s], 1);  // commit after the tile's P V
+    for (int s = 0; s < kUKStages; ++s) {
+      mbar_init(&k_full[s], 1);   // the K loader's expect-tx arrival
+      mbar_init(&k_empty[s], 1);  // commit after the tile's Q K^T
+    }
+    for (int s = 0; s < kUVStages; ++s) {
+      mbar_init(&v_full[s], 1);   // the V loader's expect-tx arrival
+      mbar_init(&v_empty[s], 1);  // commit after the tile's P V
     }
     for (int i = 0; i < kUSBufs; ++i) {
       mbar_init(&s_full[i], 1);    // commit after the tile's Q K^T
       mbar_init(&buf_free[i], 1);  // commit after the tile's P V (P read from the buffer)
     }
-    mbar_init(&q_full, 4);   // the four softmax warps have written Q
-    mbar_init(&p_full, 4);   // ... and P (and rescaled O)
+    mbar_init(&q_full, kUSoftWarps);  // the softmax warps have written Q
+    mbar_init(&p_full[0], kUSoftWarps);  // ... and P (and rescaled O)
+    mbar_init(&p_full[1], kUSoftWarps);
     mbar_init(&pv_done, 1);  // commit after a tile's P V
     mbar_init(&drain, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 2);
     s_abort = 0;
     fence_barrier_init();
   }
@@ -243,10 +289,44 @@ __global__ void __launch_bounds__(kUThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // Work order.  Units are (query block j, split c, request b, KV head g);
+  // the heads of a (j, c, b) triple cost the same.  With at most kUSortMax
+  // triples every CTA ranks them by tile count (descending, ties by index),
+  // then takes positions in snake order over that list: i-th round position
+  // i * grid + blockIdx.x, every other round reversed, so the CTA with the
+  // costliest unit takes the cheapest of the next round.
+  const int n3 = jmax * a.S * a.batch, hkv = ws.n_kv_heads;
+  const bool ranked = n3 <= kUSortMax;
+  if (ranked) {
+    for (int t = tid; t < n3; t += kUThreads) {
+      const XUnit x = xunit(a, t * hkv, TQ, jmax);
+      s_cost[t] = x.live ? unit_tiles(x) : 0;
+    }
+  }
   tc_fence_before();
+  __syncthreads();
+  if (ranked) {
+    for (int t = tid; t < n3; t += kUThreads) {
+      const int ct = s_cost[t];
+      int rank = 0;
+      for (int o = 0; o < n3; ++o) {
+        const int co = s_cost[o];
+        rank += (co > ct) || (co == ct && o < t);
+      }
+      s_order[rank] = t;
+    }
+  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  // the CTA's i-th unit, or -1 past the last
+  auto unit_of = [&](int i) -> int {
+    const long long pos = (i & 1) ? (long long)(i + 1) * gridDim.x - 1 - blockIdx.x
+                                  : (long long)i * gridDim.x + blockIdx.x;
+    if (pos >= units) return -1;
+    const int t3 = ranked ? s_order[pos / hkv] : (int)(pos / hkv);
+    return t3 * hkv + (int)(pos % hkv);
+  };
 
   // A bounded wait; one that runs out stops the whole CTA.
   auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -257,17 +337,25 @@ __global__ void __launch_bounds__(kUThreads, 1)
     return false;
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------- producer ----
-    // Lane (box, piece): piece j = lane & 7 of the tile's eight 16-token
-    // pieces, box = lane >> 3: K's halves, then V's.  A bad page id loads the
-    // in-range slot 0 instead and flags the stage (its unit is written empty).
+  if (warp == 0 || warp == kUVWarp) {
+    // ------------------------------------------------------- loaders ----
+    // Warp 0 loads each tile's K into the K ring, the last warp its V into
+    // the V ring.  Lane (box, piece): piece j = lane & 7 of the tile's eight
+    // 16-token pieces, box = lane >> 3: the 64-column half.  A bad page id
+    // loads the in-range slot 0 instead (both loaders raise its error bit)
+    // and flags the V stage (its unit is written empty).
+    const bool isv = warp == kUVWarp;
+    const int nst = isv ? kUVStages : kUKStages;
+    uint64_t *fullb = isv ? v_full : k_full;
+    uint64_t *emptyb = isv ? v_empty : k_empty;
+    const CUtensorMap *tm = isv ? &tmv : &tmk;
+    const uint32_t ring = sbase + (isv ? C::OFF_V : C::OFF_K);
     Plan pl;
     pl.set_pages(ws);
-    const int j = lane & 7, box = lane >> 3;
+    const int j = lane & 7, h = lane >> 3;
     int k = 0;
     bool aborted = false;
-    for (int u = blockIdx.x; u < units && !aborted; u += gridDim.x) {
+    for (int ui = 0, u; !aborted && (u = unit_of(ui)) >= 0; ++ui) {
       const XUnit x = xunit(a, u, TQ, jmax);
       if (!x.live) continue;
       const int rrow = ws.req_pool_indices[x.b];
@@ -279,8 +367,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
       const int ntiles = unit_tiles(x);
       int raw = raw_at(x.k0 + 16 * j);
       for (int tile = 0; tile < ntiles; ++tile, ++k) {
-        const int s = k % kUStages, r = k / kUStages;
-        if ((r > 0 && !wait(&empty[s], (r - 1) & 1)) || s_abort) {
+        const int s = k % nst, r = k / nst;
+        if ((r > 0 && !wait(&emptyb[s], (r - 1) & 1)) || s_abort) {
           aborted = true;
           break;
         }
@@ -294,23 +382,20 @@ __global__ void __launch_bounds__(kUThreads, 1)
         const int nx = raw_at(t0 + kUN + 16 * j);  // the next tile's, while these issue
         const int bad = __reduce_or_sync(0xffffffffu, kind);
         if (lane == 0) {
-          flags[s] = bad;
+          if (isv) flags[s] = bad;
           if (bad) atomicOr(ws.err, bad);
         }
         __syncwarp();
-        if (box < 2 * C::HALVES && j < np) {
-          const int isv = box >= C::HALVES, h = box - isv * C::HALVES;
-          tma_box(sbase + C::OFF_KV + s * C::STAGE + isv * C::KBYTES + h * C::KVHALF + j * 2048,
-                  isv ? &tmv : &tmk, a.layer * ws.pool_slots + slot0, h, x.g, &full[s]);
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], np * C::PIECE_TX);
+        if (h < C::HALVES && j < np)
+          tma_box(ring + s * C::KBYTES + h * C::KVHALF + j * 2048, tm,
+                  a.layer * ws.pool_slots + slot0, h, x.g, &fullb[s]);
+        if (lane == 0) mbar_arrive_expect_tx(&fullb[s], np * C::PIECE_TX);
         raw = nx;
       }
     }
     if (aborted) {
-      // the last (up to kUStages) tiles issued may still be landing
-      for (int kk = max(0, k - kUStages); kk < k; ++kk)
-        mbar_wait_bounded(&full[kk % kUStages], (kk / kUStages) & 1);
+      // the last (up to nst) tiles issued may still be landing
+      for (int kk = max(0, k - nst); kk < k; ++kk) mbar_wait_bounded(&fullb[kk % nst], (kk / nst) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA ----
@@ -320,11 +405,11 @@ __global__ void __launch_bounds__(kUThreads, 1)
       // descriptors of Q and of stage 0's K and V; every other operand is one
       // of these plus a byte offset (in 16-byte units, inside the start field)
       const uint64_t dq = umma_desc(sbase + C::OFF_Q, 16, 1024);
-      const uint64_t dk = umma_desc(sbase + C::OFF_KV, 16, 1024);
-      const uint64_t dv = umma_desc(sbase + C::OFF_KV + C::KBYTES, C::KVHALF, 1024);
+      const uint64_t dk = umma_desc(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dv = umma_desc(sbase + C::OFF_V, C::KVHALF, 1024);
       int k = 0, ul = 0;
       bool dead = false;
-      for (int u = blockIdx.x; u < units && !dead; u += gridDim.x) {
+      for (int ui = 0, u; !dead && (u = unit_of(ui)) >= 0; ++ui) {
         const XUnit x = xunit(a, u, TQ, jmax);
         if (!x.live) continue;
         const int T = unit_tiles(x);
@@ -334,14 +419,14 @@ __global__ void __launch_bounds__(kUThreads, 1)
         // Q K^T of tile t, then P V of tile t - 1 (whose softmax ran meanwhile)
         for (int t = 0; t <= T && !dead; ++t) {
           if (t < T) {
-            const int kk = k + t, s = kk % kUStages, b = kk % kUSBufs;
-            if (!wait(&full[s], (kk / kUStages) & 1) ||
+            const int kk = k + t, s = kk % kUKStages, b = kk % kUSBufs;
+            if (!wait(&k_full[s], (kk / kUKStages) & 1) ||
                 (kk >= kUSBufs && !wait(&buf_free[b], ((kk / kUSBufs) - 1) & 1))) {
               dead = true;
               break;
             }
             tc_fence_after();
-            const uint64_t ks0 = (uint64_t)((s * C::STAGE) >> 4);
+            const uint64_t ks0 = (uint64_t)((s * C::KBYTES) >> 4);
 #pragma unroll
             for (int ks = 0; ks < C::KSTEPS; ++ks) {
               // k-step ks: half ks / 4, 32 bytes further per step inside the row
@@ -351,15 +436,16 @@ __global__ void __launch_bounds__(kUThreads, 1)
               umma(tmem + b * kUN, dq + qo, dk + ks0 + ko, kIdS, ks > 0);
             }
             umma_commit(&s_full[b]);
+            umma_commit(&k_empty[s]);
           }
           if (t >= 1) {
-            const int kk = k + t - 1, s = kk % kUStages, b = kk % kUSBufs;
-            if (!wait(&p_full, kk & 1)) {
+            const int kk = k + t - 1, s = kk % kUVStages, b = kk % kUSBufs;
+            if (!wait(&p_full[kk & 1], (kk >> 1) & 1) || !wait(&v_full[s], (kk / kUVStages) & 1)) {
               dead = true;
               break;
             }
             tc_fence_after();
-            const uint64_t vs0 = (uint64_t)((s * C::STAGE) >> 4);
+            const uint64_t vs0 = (uint64_t)((s * C::KBYTES) >> 4);
             const uint32_t pb = tmem + b * kUN;  // P_hi in the buffer's first 64 columns
 #pragma unroll
             for (int ks = 0; ks < kUN / 16; ++ks) {
@@ -370,7 +456,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
             }
             umma_commit(&pv_done);
             umma_commit(&buf_free[b]);
-            umma_commit(&empty[s]);
+            umma_commit(&v_empty[s]);
           }
         }
         k += T;
@@ -383,15 +469,29 @@ __global__ void __launch_bounds__(kUThreads, 1)
     __syncwarp();
   } else {
     // -------------------------------------------------------- softmax ----
-    const int wq = warp & 3;
+    // Warp w owns TMEM lane quarter w % 4 (rows 32 (w % 4) .. + 31) and key
+    // half hf of every tile (columns 64 hf .. + 63 of S, 32 hf .. of P_hi and
+    // P_lo) and half hf of O's columns; the two threads of a row swap their
+    // partial maxima (and, at the end, sums) through shared memory, meeting
+    // on the quarter's mbarrier (a bounded wait, like every other).
+    const int wq = warp & 3, hf = (warp - 2) >> 2;
     const int row = 32 * wq + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * wq) << 16);
     const float qk_scale = a.scale * kLog2e;
+    const bool pos_scale = qk_scale > 0.f;
     const bool full_mode = (a.flags & PKV_FLAG_EXTEND_FULL) != 0;
     const bool out_f32 = (a.flags & PKV_FLAG_OUT_F32) != 0;
-    const int tw = tid - 64;  // 0 .. 127 over the four warps
+    const int tw = tid - 64;  // 0 .. 255 over the softmax warps
+    constexpr int KH = kUN / 2;  // keys of a tile per thread
+    constexpr int DH = D / 2;    // O columns per thread
+    int xphase = 0;
+    auto quarter_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xbar[wq]);
+      return wait(&xbar[wq], (xphase++) & 1);
+    };
     int k = 0;
-    for (int u = blockIdx.x; u < units && !s_abort; u += gridDim.x) {
+    for (int ui = 0, u; !s_abort && (u = unit_of(ui)) >= 0; ++ui) {
       const XUnit x = xunit(a, u, TQ, jmax);
       if (!x.live) continue;
       const int T = unit_tiles(x);
@@ -403,11 +503,12 @@ __global__ void __launch_bounds__(kUThreads, 1)
       int bad = 0;
       bool ok = true;
       if (T > 0) {
-        // this row of Q, swizzled into the K-major Q tile (zeros past the tokens)
+        // half hf of this row of Q, swizzled into the K-major Q tile (zeros
+        // past the tokens)
         const uint4 *src =
             reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + qrow * D);
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
+        for (int c = hf * (D / 16); c < (hf + 1) * (D / 16); ++c) {
           const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
           st_shared_v4(sbase + C::OFF_Q + (c >> 3) * C::QHALF + row * 128 +
                            (((c & 7) ^ (row & 7)) << 4),
@@ -418,39 +519,57 @@ __global__ void __launch_bounds__(kUThreads, 1)
         if (lane == 0) mbar_arrive(&q_full);
       }
       for (int t = 0; t < T && ok; ++t) {
-        const int kk = k + t, s = kk % kUStages, b = kk % kUSBufs;
-        const int t0 = x.k0 + t * kUN;
+        const int kk = k + t, b = kk % kUSBufs;
+        const int t0 = x.k0 + t * kUN + hf * KH;  // this thread's first key
         if (!wait(&s_full[b], (kk / kUSBufs) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t sv[kUN / 32][32];
+        uint32_t sv[KH / 32][32];
 #pragma unroll
-        for (int c = 0; c < kUN / 32; ++c) tmem_ld32(sv[c], trow + b * kUN + 32 * c);
+        for (int c = 0; c < KH / 32; ++c) tmem_ld32(sv[c], trow + b * kUN + hf * KH + 32 * c);
         tmem_wait_ld();
-        // the stage's boxes have landed (S was computed from them): its flags
-        if (!wait(&full[s], (kk / kUStages) & 1)) {
+        // the V stage's flags, once its boxes have landed
+        const int vs = kk % kUVStages;
+        if (!wait(&v_full[vs], (kk / kUVStages) & 1)) {
           ok = false;
           break;
         }
-        bad |= flags[s];
-        // scores in log2 units; keys past the row's position or the split's
-        // end count as -inf.  Eight partial maxima and sums keep the
-        // dependent chains short (one warp per sub-partition runs this).
+        bad |= flags[vs];
+        // keys past the row's position or the split's end count as -inf
         const int lim = min(pos, x.k1 - 1) - t0;
-        float mxp[8];
+        const bool whole = lim >= KH - 1;  // every key of this half attended
+        // partial row maximum in log2 units (four partial maxima, two scores
+        // per 3-input max); with a positive scale the raw scores' maximum is
+        // scaled once and each pair of weights is one paired FMA and two ex2
+        if (!pos_scale) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kUN; ++c) {
-          float v = __uint_as_float(sv[c >> 5][c & 31]) * qk_scale;
-          if (c > lim) v = -INFINITY;
-          sv[c >> 5][c & 31] = __float_as_uint(v);
-          mxp[c & 7] = fmaxf(mxp[c & 7], v);
+          for (int c = 0; c < KH; ++c)
+            sv[c >> 5][c & 31] = __float_as_uint(__uint_as_float(sv[c >> 5][c & 31]) * qk_scale);
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        float mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (whole) {
+#pragma unroll
+          for (int c = 0; c < KH; c += 2)
+            mxp[(c >> 1) & 3] = fmax3(mxp[(c >> 1) & 3], __uint_as_float(sv[c >> 5][c & 31]),
+                                      __uint_as_float(sv[c >> 5][(c & 31) + 1]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < KH; c += 2)
+            mxp[(c >> 1) & 3] = fmax3(mxp[(c >> 1) & 3],
+                                      c <= lim ? __uint_as_float(sv[c >> 5][c & 31]) : -INFINITY,
+                                      c + 1 <= lim ? __uint_as_float(sv[c >> 5][(c & 31) + 1])
+                                                   : -INFINITY);
+        }
+        float mpart = fmaxf(fmax3(mxp[0], mxp[1], mxp[2]), mxp[3]);
+        if (pos_scale) mpart *= qk_scale;
+        s_xmax[kk & 1][hf][row] = mpart;
+        if (!quarter_sync()) {  // both halves' maxima, and both have loaded their S
+          ok = false;
+          break;
+        }
+        const float mx = fmaxf(mpart, s_xmax[kk & 1][hf ^ 1][row]);
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_used + kURescale || (m_used == -INFINITY && mx != -INFINITY)) {
@@ -462,27 +581,36 @@ __global__ void __launch_bounds__(kUThreads, 1)
         }
         // no key of this row attended yet: every weight is 0
         const float mref = m_used == -INFINITY ? INFINITY : m_used;
-        float sp[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sp[e] = 0.f;
+        const float fs = pos_scale ? qk_scale : 1.f;
+        const uint64_t fs2 = f2(fs, fs), nm2 = f2(-mref, -mref), neg1 = f2(-1.f, -1.f);
+        uint64_t sp2[4] = {0ull, 0ull, 0ull, 0ull};
         // P into the tile's S buffer, bf16 pairs (even key in the low half):
-        // P_hi in its first 64 columns, P_lo in the next 64
+        // P_hi in its first 64 columns, P_lo (the residual e - P_hi) in the next 64
 #pragma unroll
-        for (int c0 = 0; c0 < kUN; c0 += 32) {
+        for (int c0 = 0; c0 < KH; c0 += 32) {
           uint32_t ph[16], pl[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float e0 = ex2_approx(__uint_as_float(sv[c0 >> 5][c]) - mref);
-            const float e1 = ex2_approx(__uint_as_float(sv[c0 >> 5][c + 1]) - mref);
-            sp[(c >> 1) & 7] += e0 + e1;
+            const uint64_t x2 = f2_fma(f2(__uint_as_float(sv[c0 >> 5][c]),
+                                          __uint_as_float(sv[c0 >> 5][c + 1])),
+                                       fs2, nm2);
+            float e0 = ex2_approx(f2_lo(x2)), e1 = ex2_approx(f2_hi(x2));
+            if (!whole) {
+              e0 = c0 + c <= lim ? e0 : 0.f;
+              e1 = c0 + c + 1 <= lim ? e1 : 0.f;
+            }
+            const uint64_t e2 = f2(e0, e1);
+            sp2[(c >> 1) & 3] = f2_add(sp2[(c >> 1) & 3], e2);
             const uint32_t hi = pack_bf16x2(e0, e1);
+            const uint64_t r2 = f2_fma(f2(bf16lo(hi), bf16hi(hi)), neg1, e2);
             ph[c >> 1] = hi;
-            pl[c >> 1] = pack_bf16x2(e0 - bf16lo(hi), e1 - bf16hi(hi));
+            pl[c >> 1] = pack_bf16x2(f2_lo(r2), f2_hi(r2));
           }
-          tmem_st16(trow + b * kUN + c0 / 2, ph);
-          tmem_st16(trow + b * kUN + kUN / 2 + c0 / 2, pl);
+          tmem_st16(trow + b * kUN + hf * (KH / 2) + c0 / 2, ph);
+          tmem_st16(trow + b * kUN + kUN / 2 + hf * (KH / 2) + c0 / 2, pl);
         }
-        const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+        const uint64_t s2 = f2_add(f2_add(sp2[0], sp2[1]), f2_add(sp2[2], sp2[3]));
+        const float sum = f2_lo(s2) + f2_hi(s2);
         l = l * alpha + sum;
         if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
           // O holds every earlier tile once the previous tile's P V is done
@@ -492,21 +620,23 @@ __global__ void __launch_bounds__(kUThreads, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < D; c += 32) {
+          for (int c = 0; c < DH; c += 32) {
             uint32_t o[32];
-            tmem_ld32(o, trow + kUOCol + c);
+            tmem_ld32(o, trow + kUOCol + hf * DH + c);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(trow + kUOCol + c, o);
+            tmem_st32(trow + kUOCol + hf * DH + c, o);
           }
         }
-        if (t0 + kUN > x.k1) {
+        if (x.k0 + (t + 1) * kUN > x.k1) {
           // The last tile: V rows past the split's end hold what the pool or
           // the stage's previous tile held, and P = 0 does not cancel a NaN.
-          const int first = x.k1 - t0;
-          const uint32_t vb = sbase + C::OFF_KV + s * C::STAGE + C::KBYTES;
-          for (int e = tw; e < (kUN - first) * C::HALVES * 8; e += 128) {
+          // Cleared after the tile's V has landed (above); its P V waits for
+          // this warp's arrival.
+          const int first = x.k1 - (x.k0 + t * kUN);
+          const uint32_t vb = sbase + C::OFF_V + vs * C::KBYTES;
+          for (int e = tw; e < (kUN - first) * C::HALVES * 8; e += 32 * kUSoftWarps) {
             const int r = first + e / (C::HALVES * 8), rem = e % (C::HALVES * 8);
             st_shared_v4(vb + (rem >> 3) * C::KVHALF + r * 128 + (((rem & 7) ^ (r & 7)) << 4),
                          0u, 0u, 0u, 0u);
@@ -516,19 +646,22 @@ __global__ void __launch_bounds__(kUThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full);
+        if (lane == 0) mbar_arrive(&p_full[kk & 1]);
       }
       if (!ok) break;
       // ---- the unit's rows: O / l, or the split's partial ----
-      const bool zero = bad || !(l > 0.f);
-      const float inv = zero ? 0.f : 1.f / l;
+      s_xsum[hf][row] = l;
+      if (!quarter_sync()) break;
+      const float lt = l + s_xsum[hf ^ 1][row];
+      const bool zero = bad || !(lt > 0.f);
+      const float inv = zero ? 0.f : 1.f / lt;
       if (T > 0) {
         if (!wait(&pv_done, (k + T - 1) & 1)) break;
         tc_fence_after();
       }
       const long long pr = qrow * a.S + x.c;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
+      for (int c = hf * DH; c < (hf + 1) * DH; c += 32) {
         uint32_t o[32];
         if (T > 0) {
           tmem_ld32(o, trow + kUOCol + c);
@@ -551,18 +684,19 @@ __global__ void __launch_bounds__(kUThreads, 1)
                                     pack_bf16x2(f[e + 4], f[e + 5]), pack_bf16x2(f[e + 6], f[e + 7]));
         }
       }
-      if (valid) {
+      if (valid && hf == 0) {
         if (a.S > 1) {
           // a failed split is marked l = -1: the merge writes the row as zeros
           ws.ml_part[pr * 2] = zero ? -INFINITY : m_used * kLn2;
-          ws.ml_part[pr * 2 + 1] = bad ? -1.f : (zero ? 0.f : l);
+          ws.ml_part[pr * 2 + 1] = bad ? -1.f : (zero ? 0.f : lt);
         } else if ((a.flags & PKV_FLAG_WRITE_LSE) && ws.lse) {
-          ws.lse[qrow] = zero ? -INFINITY : m_used * kLn2 + logf(l);
+          ws.lse[qrow] = zero ? -INFINITY : m_used * kLn2 + logf(lt);
         }
       }
       // O's loads are done before the next unit's Q is published (its first
-      // P V overwrites O)
+      // P V overwrites O); the row sums are read before they are rewritten
       tc_fence_before();
+      if (!quarter_sync()) break;
       k += T;
     }
   }
