@@ -50,8 +50,8 @@ namespace {
 
 constexpr int kUM = 128;          // query rows per CTA (TMEM lanes)
 constexpr int kUN = 128;          // keys per tile (N of Q K^T: the MMA's full rate)
-constexpr int kUKStages = 3;      // K ring: a tile's K is free once its Q K^T is done
-constexpr int kUVStages = 2;      // V ring: free once the tile's P V is done
+constexpr int kUKStages = 2;      // K ring: a tile's K is free once its Q K^T is done
+constexpr int kUVStages = 3;      // V ring: free once the tile's P V is done
 constexpr int kUSBufs = 3;        // S / P buffers in TMEM
 constexpr int kUSoftWarps = 8;    // two per TMEM lane quarter, 64 keys of a tile each
 constexpr int kUThreads = (3 + kUSoftWarps) * 32;  // K loader, MMA, softmax, V loader
@@ -178,6 +178,28 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// mbarrier phase wait that suspends the thread in hardware (up to the hint)
+// instead of spinning, bounded like mbar_wait_bounded: false after ~1 s.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // Blackwell's paired fp32 arithmetic: two lanes of a 64-bit register pair
 // per instruction (x in the low word).
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
@@ -236,16 +258,20 @@ __global__ void __launch_bounds__(kUThreads, 1)
   __shared__ __align__(8) uint64_t k_full[kUKStages], k_empty[kUKStages];
   __shared__ __align__(8) uint64_t v_full[kUVStages], v_empty[kUVStages];
   __shared__ __align__(8) uint64_t s_full[kUSBufs], buf_free[kUSBufs];
-  // p_full alternates by tile: the softmax may finish tile kk + 1 before the
-  // MMA thread looks for tile kk's phase, which one barrier would then have
-  // passed twice
-  __shared__ __align__(8) uint64_t q_full, p_full[2], pv_done, drain;
+  // p_full rotates over the S buffers: the Q K^T of tiles kk + 1 and kk + 2
+  // may already be done when the MMA thread looks for tile kk's P, so the
+  // softmax could publish those too; one barrier would then have passed the
+  // phase looked for
+  __shared__ __align__(8) uint64_t q_full, p_full[kUSBufs], drain;
   __shared__ __align__(8) uint64_t xbar[4];  // per lane quarter: its two softmax warps
-  // per V stage: the tile's bad page bits.  The softmax reads them after the
-  // stage's V has landed; the stage is refilled only after the tile's P V,
-  // which waits for that softmax.  (A K stage is refilled as soon as its
-  // Q K^T is done, possibly before the softmax of its tile has started.)
-  __shared__ int flags[kUVStages];
+  // Bad page bits of the CTA's i-th unit in s_ubad[i % 4], written by the V
+  // loader before it publishes each of the unit's tiles (set by the first,
+  // OR-ed by the rest); the softmax reads them once the unit's last V tile
+  // has landed, and the loader is then at most three tiles, so three units,
+  // ahead of it.  (A K
+  // stage is refilled as soon as its Q K^T is done, possibly before the
+  // softmax of its tile has started, so the K side carries no flags.)
+  __shared__ int s_ubad[4];
   __shared__ float s_xmax[2][2][kUM];  // [tile parity][key half][row]: partial row maxima
   __shared__ float s_xsum[2][kUM];     // [key half][row]: partial row sums, at the end
   __shared__ int s_cost[kUSortMax], s_order[kUSortMax];
@@ -271,14 +297,20 @@ __global__ void __launch_bounds__(kUThreads, 1)
     }
     for (int i = 0; i < kUSBufs; ++i) {
       mbar_init(&s_full[i], 1);    // commit after the tile's Q K^T
-      mbar_init(&buf_free[i], 1);  // commit after the tile's P V (P read from the buffer)
+      // commit after the tile's P V (P read from the buffer, O holds the tile);
+      // the softmax waits here for O too.  One barrier per buffer: waiting
+      // on the P V of tile kk, the barrier's previous phase (tile kk - 3) is
+      // always complete, so a parity wait cannot pass early, as it could on a
+      // single barrier two phases behind once Q K^T runs ahead.
+      mbar_init(&buf_free[i], 1);
     }
     mbar_init(&q_full, kUSoftWarps);  // the softmax warps have written Q
-    mbar_init(&p_full[0], kUSoftWarps);  // ... and P (and rescaled O)
-    mbar_init(&p_full[1], kUSoftWarps);
-    mbar_init(&pv_done, 1);  // commit after a tile's P V
+    for (int i = 0; i < kUSBufs; ++i) mbar_init(&p_full[i], kUSoftWarps);  // ... and P
     mbar_init(&drain, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 2);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&xbar[i], 2);
+      s_ubad[i] = 0;
+    }
     s_abort = 0;
     fence_barrier_init();
   }
@@ -331,7 +363,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
   // A bounded wait; one that runs out stops the whole CTA.
   auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
     if (s_abort) return false;
-    if (mbar_wait_bounded(bar, parity)) return true;
+    if (mbar_wait_sleep(bar, parity)) return true;
     s_abort = 1;
     atomicOr(ws.err, PKV_DEVERR_TIMEOUT);
     return false;
@@ -382,7 +414,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
         const int nx = raw_at(t0 + kUN + 16 * j);  // the next tile's, while these issue
         const int bad = __reduce_or_sync(0xffffffffu, kind);
         if (lane == 0) {
-          if (isv) flags[s] = bad;
+          // the unit's first tile sets the bits, later tiles add to them
+          if (isv && tile == 0) s_ubad[ui & 3] = bad;
+          else if (isv && bad) atomicOr(&s_ubad[ui & 3], bad);
           if (bad) atomicOr(ws.err, bad);
         }
         __syncwarp();
@@ -416,48 +450,52 @@ __global__ void __launch_bounds__(kUThreads, 1)
         if (T == 0) continue;
         if (!wait(&q_full, ul & 1)) break;
         tc_fence_after();
-        // Q K^T of tile t, then P V of tile t - 1 (whose softmax ran meanwhile)
-        for (int t = 0; t <= T && !dead; ++t) {
-          if (t < T) {
-            const int kk = k + t, s = kk % kUKStages, b = kk % kUSBufs;
-            if (!wait(&k_full[s], (kk / kUKStages) & 1) ||
-                (kk >= kUSBufs && !wait(&buf_free[b], ((kk / kUSBufs) - 1) & 1))) {
-              dead = true;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t ks0 = (uint64_t)((s * C::KBYTES) >> 4);
+        // Q K^T runs two tiles ahead of P V: the S of tile t + 1 is ready when
+        // the softmax finishes tile t, instead of queueing behind the P V of
+        // tile t - 1 (which waits for that softmax).  The Q K^T of tile t + 2
+        // takes the buffer of tile t - 1, free once its P V is done.
+        auto issue_qk = [&](int t) -> bool {
+          const int kk = k + t, s = kk % kUKStages, b = kk % kUSBufs;
+          if (!wait(&k_full[s], (kk / kUKStages) & 1) ||
+              (kk >= kUSBufs && !wait(&buf_free[b], ((kk / kUSBufs) - 1) & 1)))
+            return false;
+          tc_fence_after();
+          const uint64_t ks0 = (uint64_t)((s * C::KBYTES) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < C::KSTEPS; ++ks) {
-              // k-step ks: half ks / 4, 32 bytes further per step inside the row
-              constexpr int kQH = C::QHALF, kKH = C::KVHALF;
-              const uint64_t qo = (uint64_t)(((ks >> 2) * kQH + (ks & 3) * 32) >> 4);
-              const uint64_t ko = (uint64_t)(((ks >> 2) * kKH + (ks & 3) * 32) >> 4);
-              umma(tmem + b * kUN, dq + qo, dk + ks0 + ko, kIdS, ks > 0);
-            }
-            umma_commit(&s_full[b]);
-            umma_commit(&k_empty[s]);
+          for (int ks = 0; ks < C::KSTEPS; ++ks) {
+            // k-step ks: half ks / 4, 32 bytes further per step inside the row
+            constexpr int kQH = C::QHALF, kKH = C::KVHALF;
+            const uint64_t qo = (uint64_t)(((ks >> 2) * kQH + (ks & 3) * 32) >> 4);
+            const uint64_t ko = (uint64_t)(((ks >> 2) * kKH + (ks & 3) * 32) >> 4);
+            umma(tmem + b * kUN, dq + qo, dk + ks0 + ko, kIdS, ks > 0);
           }
-          if (t >= 1) {
-            const int kk = k + t - 1, s = kk % kUVStages, b = kk % kUSBufs;
-            if (!wait(&p_full[kk & 1], (kk >> 1) & 1) || !wait(&v_full[s], (kk / kUVStages) & 1)) {
-              dead = true;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t vs0 = (uint64_t)((s * C::KBYTES) >> 4);
-            const uint32_t pb = tmem + b * kUN;  // P_hi in the buffer's first 64 columns
+          umma_commit(&s_full[b]);
+          umma_commit(&k_empty[s]);
+          return true;
+        };
+        dead = !issue_qk(0) || (T > 1 && !issue_qk(1));
+        for (int t = 0; t < T && !dead; ++t) {
+          if (t + 2 < T && !issue_qk(t + 2)) {
+            dead = true;
+            break;
+          }
+          const int kk = k + t, s = kk % kUVStages, b = kk % kUSBufs;
+          if (!wait(&p_full[b], (kk / kUSBufs) & 1) || !wait(&v_full[s], (kk / kUVStages) & 1)) {
+            dead = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t vs0 = (uint64_t)((s * C::KBYTES) >> 4);
+          const uint32_t pb = tmem + b * kUN;  // P_hi in the buffer's first 64 columns
 #pragma unroll
-            for (int ks = 0; ks < kUN / 16; ++ks) {
-              // 16 keys per step: 16 V rows (2048 B) further, 8 P columns
-              const uint64_t bd = dv + vs0 + (uint64_t)((ks * 2048) >> 4);
-              umma_ts(tmem + kUOCol, pb + ks * 8, bd, kIdO, t > 1 || ks > 0);
-              umma_ts(tmem + kUOCol, pb + kUN / 2 + ks * 8, bd, kIdO, 1);
-            }
-            umma_commit(&pv_done);
-            umma_commit(&buf_free[b]);
-            umma_commit(&v_empty[s]);
+          for (int ks = 0; ks < kUN / 16; ++ks) {
+            // 16 keys per step: 16 V rows (2048 B) further, 8 P columns
+            const uint64_t bd = dv + vs0 + (uint64_t)((ks * 2048) >> 4);
+            umma_ts(tmem + kUOCol, pb + ks * 8, bd, kIdO, t > 0 || ks > 0);
+            umma_ts(tmem + kUOCol, pb + kUN / 2 + ks * 8, bd, kIdO, 1);
           }
+          umma_commit(&buf_free[b]);
+          umma_commit(&v_empty[s]);
         }
         k += T;
         ++ul;
@@ -530,13 +568,6 @@ __global__ void __launch_bounds__(kUThreads, 1)
 #pragma unroll
         for (int c = 0; c < KH / 32; ++c) tmem_ld32(sv[c], trow + b * kUN + hf * KH + 32 * c);
         tmem_wait_ld();
-        // the V stage's flags, once its boxes have landed
-        const int vs = kk % kUVStages;
-        if (!wait(&v_full[vs], (kk / kUVStages) & 1)) {
-          ok = false;
-          break;
-        }
-        bad |= flags[vs];
         // keys past the row's position or the split's end count as -inf
         const int lim = min(pos, x.k1 - 1) - t0;
         const bool whole = lim >= KH - 1;  // every key of this half attended
@@ -614,7 +645,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
         l = l * alpha + sum;
         if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
           // O holds every earlier tile once the previous tile's P V is done
-          if (!wait(&pv_done, (kk - 1) & 1)) {
+          if (!wait(&buf_free[(kk - 1) % kUSBufs], ((kk - 1) / kUSBufs) & 1)) {
             ok = false;
             break;
           }
@@ -629,11 +660,17 @@ __global__ void __launch_bounds__(kUThreads, 1)
             tmem_st32(trow + kUOCol + hf * DH + c, o);
           }
         }
-        if (x.k0 + (t + 1) * kUN > x.k1) {
-          // The last tile: V rows past the split's end hold what the pool or
-          // the stage's previous tile held, and P = 0 does not cancel a NaN.
-          // Cleared after the tile's V has landed (above); its P V waits for
-          // this warp's arrival.
+        if (t == T - 1) {
+          // The last tile: once its V has landed, the unit's bad page bits;
+          // V rows past the split's end hold what the pool or the stage's
+          // previous tile held, and P = 0 does not cancel a NaN, so they are
+          // cleared (its P V waits for this warp's arrival).
+          const int vs = kk % kUVStages;
+          if (!wait(&v_full[vs], (kk / kUVStages) & 1)) {
+            ok = false;
+            break;
+          }
+          bad |= s_ubad[ui & 3];
           const int first = x.k1 - (x.k0 + t * kUN);
           const uint32_t vb = sbase + C::OFF_V + vs * C::KBYTES;
           for (int e = tw; e < (kUN - first) * C::HALVES * 8; e += 32 * kUSoftWarps) {
@@ -646,7 +683,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[kk & 1]);
+        if (lane == 0) mbar_arrive(&p_full[b]);
       }
       if (!ok) break;
       // ---- the unit's rows: O / l, or the split's partial ----
@@ -656,7 +693,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
       const bool zero = bad || !(lt > 0.f);
       const float inv = zero ? 0.f : 1.f / lt;
       if (T > 0) {
-        if (!wait(&pv_done, (k + T - 1) & 1)) break;
+        const int kl = k + T - 1;  // the unit's last tile
+        if (!wait(&buf_free[kl % kUSBufs], (kl / kUSBufs) & 1)) break;
         tc_fence_after();
       }
       const long long pr = qrow * a.S + x.c;
