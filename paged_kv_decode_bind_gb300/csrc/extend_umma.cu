@@ -15,11 +15,13 @@
 //               three 128-column TMEM buffers, so later tiles' products run
 //               while this tile's softmax reads its own.  (N = 128: measured,
 //               an N = 64 MMA runs at about half the tensor rate.)
-//   softmax     one thread per row: it loads its row of S from TMEM
-//               (tcgen05.ld, no shuffles), applies the causal mask, keeps the
-//               running max and sum in fp32 (exp2) and writes the weights P
-//               back into the same TMEM buffer as bf16 high and low parts,
-//               P = P_hi + P_lo to ~2^-17 (pairs of keys per 32-bit column).
+//   softmax     two threads per row, 64 keys each: a thread loads its half
+//               row of S from TMEM (tcgen05.ld), applies the causal mask,
+//               swaps its partial maximum with the other half's thread
+//               through shared memory, keeps the running max and sum in fp32
+//               (exp2) and writes the weights P back into the same TMEM
+//               buffer as bf16 high and low parts, P = P_hi + P_lo to ~2^-17
+//               (pairs of keys per 32-bit column).
 //   O += P V    tcgen05.mma M = 128, N = D, K = 128 keys in steps of 16 with
 //               P_hi and P_lo each as the A operand from TMEM and V read from
 //               shared memory as an MN-major operand (the tile's V rows,
@@ -30,14 +32,14 @@
 // the weights exp2(s - m) then stay below 256 and the sum and O use the same
 // reference, so the result is unchanged.
 //
-// Warps: 0 issues the tensor-map boxes of each tile's K and V into a 3-stage
-// ring (per 16-token page piece four boxes: K and V, each 64-column half);
-// 1 allocates the TMEM and issues every MMA from one thread (descriptors made
-// once, advanced by constant offsets), tracking their completion with
-// tcgen05.commit on mbarriers; 2-5 load Q, run the softmax and write the
-// outputs (warp w reads TMEM lanes 32 (w % 4) .. + 31, its rows).  Every wait
-// is bounded (~1 s) and raises PKV_DEVERR_TIMEOUT; the MMAs in flight are
-// drained before the TMEM is freed.
+// Warps: 0 and 10 issue the tensor-map boxes of each tile's K and V (per
+// 16-token page piece one box per 64-column half) into a 2-stage K ring and a
+// 3-stage V ring; 1 issues every tile's Q K^T and 11 every P V (each from one
+// lane chosen by elect.sync while the whole warp runs the loop), tracking
+// their completion with tcgen05.commit on mbarriers; 2-9 load Q, run the
+// softmax (two warps per TMEM lane quarter, 64 keys of a tile each) and write
+// the outputs.  Every wait is bounded (~1 s) and raises PKV_DEVERR_TIMEOUT;
+// the MMAs in flight are drained before the TMEM is freed.
 #include <cuda.h>
 
 #include <cstring>
@@ -54,8 +56,10 @@ constexpr int kUKStages = 2;      // K ring: a tile's K is free once its Q K^T i
 constexpr int kUVStages = 3;      // V ring: free once the tile's P V is done
 constexpr int kUSBufs = 3;        // S / P buffers in TMEM
 constexpr int kUSoftWarps = 8;    // two per TMEM lane quarter, 64 keys of a tile each
-constexpr int kUThreads = (3 + kUSoftWarps) * 32;  // K loader, MMA, softmax, V loader
+// warps: K loader, Q K^T issuer, softmax, V loader, P V issuer
+constexpr int kUThreads = (4 + kUSoftWarps) * 32;
 constexpr int kUVWarp = 2 + kUSoftWarps;
+constexpr int kUPVWarp = 3 + kUSoftWarps;
 constexpr int kUTmemCols = 512;   // three S buffers of 128 columns, O of D <= 128
 constexpr int kUOCol = kUSBufs * kUN;  // O's first column
 constexpr float kURescale = 8.f;  // raise a row's reference max only past this (log2)
@@ -96,11 +100,16 @@ __host__ __device__ constexpr uint32_t umma_idesc(int M, int N, int b_mn_major) 
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The MMA warp runs its loop with all 32 lanes (so its operands stay
+// warp-uniform) and one lane, chosen by elect.sync, issues each instruction.
+// Measured: an MMA stream issued from a lone divergent lane ran 3x slower
+// while other warps of its SM sub-partition kept the issue slots busy (the
+// softmax warps here); issued this way it ran within 2 % of its rate alone.
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                      int accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -109,16 +118,19 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                         uint32_t idesc, int accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive (once) on the mbarrier when every MMA this thread issued so far is done.
+// Arrive (once) on the mbarrier when every MMA issued so far is done.  The
+// elected lane is the one that issued them (the warp is converged: the
+// lowest lane every time), as the commit tracks its own thread's MMAs.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_addr(bar))
       : "memory");
 }
@@ -231,11 +243,17 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t
                : "memory");
 }
 
+// One tensor-map box, issued by one lane chosen by elect.sync; the whole
+// warp executes it with the same (warp-uniform) operands.  Measured: boxes
+// issued this way cost about a third of the per-lane issue (each lane its own
+// box), whose issue also slowed 3x while other warps of the sub-partition
+// were busy.
 __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *tm, int c1, int c2,
                                         int c3, uint64_t *bar) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
-      "[%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4, %5}], [%6];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
       : "memory");
 }
@@ -262,7 +280,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
   // may already be done when the MMA thread looks for tile kk's P, so the
   // softmax could publish those too; one barrier would then have passed the
   // phase looked for
-  __shared__ __align__(8) uint64_t q_full, p_full[kUSBufs], drain;
+  __shared__ __align__(8) uint64_t q_full, p_full[kUSBufs], drain[2];
   __shared__ __align__(8) uint64_t xbar[4];  // per lane quarter: its two softmax warps
   // Bad page bits of the CTA's i-th unit in s_ubad[i % 4], written by the V
   // loader before it publishes each of the unit's tiles (set by the first,
@@ -306,7 +324,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
     }
     mbar_init(&q_full, kUSoftWarps);  // the softmax warps have written Q
     for (int i = 0; i < kUSBufs; ++i) mbar_init(&p_full[i], kUSoftWarps);  // ... and P
-    mbar_init(&drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&xbar[i], 2);
       s_ubad[i] = 0;
@@ -362,6 +381,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
 
   // A bounded wait; one that runs out stops the whole CTA.
   auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
     if (s_abort) return false;
     if (mbar_wait_sleep(bar, parity)) return true;
     s_abort = 1;
@@ -372,10 +392,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
   if (warp == 0 || warp == kUVWarp) {
     // ------------------------------------------------------- loaders ----
     // Warp 0 loads each tile's K into the K ring, the last warp its V into
-    // the V ring.  Lane (box, piece): piece j = lane & 7 of the tile's eight
-    // 16-token pieces, box = lane >> 3: the 64-column half.  A bad page id
-    // loads the in-range slot 0 instead (both loaders raise its error bit)
-    // and flags the V stage (its unit is written empty).
+    // the V ring.  Lane j & 7 looks up the slot of piece j of the tile's
+    // eight 16-token pieces; the warp then issues the boxes (piece x 64-column
+    // half).  A bad page id loads the in-range slot 0 instead (both loaders
+    // raise its error bit) and flags the V stage (its unit is written empty).
     const bool isv = warp == kUVWarp;
     const int nst = isv ? kUVStages : kUKStages;
     uint64_t *fullb = isv ? v_full : k_full;
@@ -384,7 +404,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
     const uint32_t ring = sbase + (isv ? C::OFF_V : C::OFF_K);
     Plan pl;
     pl.set_pages(ws);
-    const int j = lane & 7, h = lane >> 3;
+    const int j = lane & 7;
     int k = 0;
     bool aborted = false;
     for (int ui = 0, u; !aborted && (u = unit_of(ui)) >= 0; ++ui) {
@@ -400,7 +420,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
       int raw = raw_at(x.k0 + 16 * j);
       for (int tile = 0; tile < ntiles; ++tile, ++k) {
         const int s = k % nst, r = k / nst;
-        if ((r > 0 && !wait(&emptyb[s], (r - 1) & 1)) || s_abort) {
+        // the decision is the warp's (the boxes below are issued by all lanes)
+        if (!__all_sync(0xffffffffu, !((r > 0 && !wait(&emptyb[s], (r - 1) & 1)) || s_abort))) {
           aborted = true;
           break;
         }
@@ -420,9 +441,15 @@ __global__ void __launch_bounds__(kUThreads, 1)
           if (bad) atomicOr(ws.err, bad);
         }
         __syncwarp();
-        if (h < C::HALVES && j < np)
-          tma_box(ring + s * C::KBYTES + h * C::KVHALF + j * 2048, tm,
-                  a.layer * ws.pool_slots + slot0, h, x.g, &fullb[s]);
+        // the boxes, one after another from the whole warp: piece pj's slot
+        // comes from lane pj
+        for (int pj = 0; pj < np; ++pj) {
+          const int sl = __shfl_sync(0xffffffffu, slot0, pj);
+#pragma unroll
+          for (int hh = 0; hh < C::HALVES; ++hh)
+            tma_box(ring + s * C::KBYTES + hh * C::KVHALF + pj * 2048, tm,
+                    a.layer * ws.pool_slots + sl, hh, x.g, &fullb[s]);
+        }
         if (lane == 0) mbar_arrive_expect_tx(&fullb[s], np * C::PIECE_TX);
         raw = nx;
       }
@@ -431,34 +458,46 @@ __global__ void __launch_bounds__(kUThreads, 1)
       // the last (up to nst) tiles issued may still be landing
       for (int kk = max(0, k - nst); kk < k; ++kk) mbar_wait_bounded(&fullb[kk % nst], (kk / nst) & 1);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == kUPVWarp) {
     // ------------------------------------------------------------ MMA ----
-    if (lane == 0) {
-      constexpr uint32_t kIdS = umma_idesc(kUM, kUN, 0);  // S = Q K^T: both K-major
-      constexpr uint32_t kIdO = umma_idesc(kUM, D, 1);    // O += P V: V MN-major
-      // descriptors of Q and of stage 0's K and V; every other operand is one
-      // of these plus a byte offset (in 16-byte units, inside the start field)
-      const uint64_t dq = umma_desc(sbase + C::OFF_Q, 16, 1024);
-      const uint64_t dk = umma_desc(sbase + C::OFF_K, 16, 1024);
-      const uint64_t dv = umma_desc(sbase + C::OFF_V, C::KVHALF, 1024);
-      int k = 0, ul = 0;
-      bool dead = false;
-      for (int ui = 0, u; !dead && (u = unit_of(ui)) >= 0; ++ui) {
-        const XUnit x = xunit(a, u, TQ, jmax);
-        if (!x.live) continue;
-        const int T = unit_tiles(x);
-        if (T == 0) continue;
-        if (!wait(&q_full, ul & 1)) break;
+    // Two issuing warps, so that neither kind of product waits behind the
+    // other's barriers: warp 1 issues every tile's S = Q K^T as soon as its K
+    // has landed and its S / P buffer is free (the P V of the tile three
+    // before is done); the P V warp issues O += P V as soon as the softmax
+    // has written the tile's P and its V has landed.  The tensor pipe takes
+    // both streams; each warp's commits track its own products.
+    const bool pv = warp == kUPVWarp;
+    // a wait that fails for any lane stops the warp
+    auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, wait(bar, parity));
+    };
+    constexpr uint32_t kIdS = umma_idesc(kUM, kUN, 0);  // S = Q K^T: both K-major
+    constexpr uint32_t kIdO = umma_idesc(kUM, D, 1);    // O += P V: V MN-major
+    // descriptors of Q and of stage 0's K and V; every other operand is one
+    // of these plus a byte offset (in 16-byte units, inside the start field)
+    const uint64_t dq = umma_desc(sbase + C::OFF_Q, 16, 1024);
+    const uint64_t dk = umma_desc(sbase + C::OFF_K, 16, 1024);
+    const uint64_t dv = umma_desc(sbase + C::OFF_V, C::KVHALF, 1024);
+    int k = 0, ul = 0;
+    bool dead = false;
+    for (int ui = 0, u; !dead && (u = unit_of(ui)) >= 0; ++ui) {
+      const XUnit x = xunit(a, u, TQ, jmax);
+      if (!x.live) continue;
+      const int T = unit_tiles(x);
+      if (T == 0) continue;
+      if (!pv) {
+        if (!wwait(&q_full, ul & 1)) break;
         tc_fence_after();
-        // Q K^T runs two tiles ahead of P V: the S of tile t + 1 is ready when
-        // the softmax finishes tile t, instead of queueing behind the P V of
-        // tile t - 1 (which waits for that softmax).  The Q K^T of tile t + 2
-        // takes the buffer of tile t - 1, free once its P V is done.
-        auto issue_qk = [&](int t) -> bool {
-          const int kk = k + t, s = kk % kUKStages, b = kk % kUSBufs;
-          if (!wait(&k_full[s], (kk / kUKStages) & 1) ||
-              (kk >= kUSBufs && !wait(&buf_free[b], ((kk / kUSBufs) - 1) & 1)))
-            return false;
+      }
+      for (int t = 0; t < T && !dead; ++t) {
+        const int kk = k + t, b = kk % kUSBufs;
+        if (!pv) {
+          const int s = kk % kUKStages;
+          if (!wwait(&k_full[s], (kk / kUKStages) & 1) ||
+              (kk >= kUSBufs && !wwait(&buf_free[b], ((kk / kUSBufs) - 1) & 1))) {
+            dead = true;
+            break;
+          }
           tc_fence_after();
           const uint64_t ks0 = (uint64_t)((s * C::KBYTES) >> 4);
 #pragma unroll
@@ -471,16 +510,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
           }
           umma_commit(&s_full[b]);
           umma_commit(&k_empty[s]);
-          return true;
-        };
-        dead = !issue_qk(0) || (T > 1 && !issue_qk(1));
-        for (int t = 0; t < T && !dead; ++t) {
-          if (t + 2 < T && !issue_qk(t + 2)) {
-            dead = true;
-            break;
-          }
-          const int kk = k + t, s = kk % kUVStages, b = kk % kUSBufs;
-          if (!wait(&p_full[b], (kk / kUSBufs) & 1) || !wait(&v_full[s], (kk / kUVStages) & 1)) {
+        } else {
+          const int s = kk % kUVStages;
+          if (!wwait(&p_full[b], (kk / kUSBufs) & 1) || !wwait(&v_full[s], (kk / kUVStages) & 1)) {
             dead = true;
             break;
           }
@@ -497,13 +529,13 @@ __global__ void __launch_bounds__(kUThreads, 1)
           umma_commit(&buf_free[b]);
           umma_commit(&v_empty[s]);
         }
-        k += T;
-        ++ul;
       }
-      // every MMA issued is done before the TMEM is freed
-      umma_commit(&drain);
-      mbar_wait_bounded(&drain, 0);
+      k += T;
+      ++ul;
     }
+    // every MMA this warp issued is done before the TMEM is freed
+    umma_commit(&drain[pv]);
+    mbar_wait_bounded(&drain[pv], 0);
     __syncwarp();
   } else {
     // -------------------------------------------------------- softmax ----
