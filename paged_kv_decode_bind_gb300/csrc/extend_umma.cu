@@ -560,6 +560,30 @@ __global__ void __launch_bounds__(kUThreads, 1)
       if (lane == 0) mbar_arrive(&xbar[wq]);
       return wait(&xbar[wq], (xphase++) & 1);
     };
+    // half hf of this thread's row of a unit's Q into the K-major Q tile
+    // (swizzled; zeros past the unit's tokens), by 16-byte cp.async
+    auto q_copy = [&](const XUnit &y) {
+      const int iy = y.j * TQ + row / G;
+      const bool vy = iy < y.n;
+      const long long qy = vy ? (long long)(y.q0 + iy) * Hq + y.g * G + row % G : 0;
+      const uint16_t *src = static_cast<const uint16_t *>(a.q) + qy * D;
+#pragma unroll
+      for (int c = hf * (D / 16); c < (hf + 1) * (D / 16); ++c)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                         sbase + C::OFF_Q + (c >> 3) * C::QHALF + row * 128 +
+                         (((c & 7) ^ (row & 7)) << 4)),
+                     "l"(src + c * 8), "r"(vy ? 16 : 0)
+                     : "memory");
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    // the copies landed, visible to the tensor cores: arrive on q_full
+    auto q_publish = [&]() {
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full);
+    };
+    bool q_pre = false;  // the current unit's Q was published with the previous unit's last P
     int k = 0;
     for (int ui = 0, u; !s_abort && (u = unit_of(ui)) >= 0; ++ui) {
       const XUnit x = xunit(a, u, TQ, jmax);
@@ -572,22 +596,12 @@ __global__ void __launch_bounds__(kUThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       int bad = 0;
       bool ok = true;
-      if (T > 0) {
-        // half hf of this row of Q, swizzled into the K-major Q tile (zeros
-        // past the tokens)
-        const uint4 *src =
-            reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + qrow * D);
-#pragma unroll
-        for (int c = hf * (D / 16); c < (hf + 1) * (D / 16); ++c) {
-          const uint4 v = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-          st_shared_v4(sbase + C::OFF_Q + (c >> 3) * C::QHALF + row * 128 +
-                           (((c & 7) ^ (row & 7)) << 4),
-                       v.x, v.y, v.z, v.w);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&q_full);
+      if (T > 0 && !q_pre) {
+        q_copy(x);
+        q_publish();
       }
+      q_pre = false;
+      bool pre = false;  // the next unit's Q is being copied
       for (int t = 0; t < T && ok; ++t) {
         const int kk = k + t, b = kk % kUSBufs;
         const int t0 = x.k0 + t * kUN + hf * KH;  // this thread's first key
@@ -596,6 +610,19 @@ __global__ void __launch_bounds__(kUThreads, 1)
           break;
         }
         tc_fence_after();
+        if (t == T - 1) {
+          // Every Q K^T of the unit is done: the next unit's Q goes into the Q
+          // tile now, behind this tile's softmax, and is published with its
+          // P, so the next unit's Q K^T overlaps this unit's epilogue.
+          XUnit y;
+          for (int uj = ui + 1, u2; !pre && (u2 = unit_of(uj)) >= 0; ++uj) {
+            y = xunit(a, u2, TQ, jmax);
+            if (y.live && unit_tiles(y) > 0) {
+              q_copy(y);
+              pre = true;
+            }
+          }
+        }
         uint32_t sv[KH / 32][32];
 #pragma unroll
         for (int c = 0; c < KH / 32; ++c) tmem_ld32(sv[c], trow + b * kUN + hf * KH + 32 * c);
@@ -716,6 +743,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[b]);
+        if (pre) {
+          q_publish();
+          q_pre = true;
+        }
       }
       if (!ok) break;
       // ---- the unit's rows: O / l, or the split's partial ----
@@ -763,12 +794,14 @@ __global__ void __launch_bounds__(kUThreads, 1)
           ws.lse[qrow] = zero ? -INFINITY : m_used * kLn2 + logf(lt);
         }
       }
-      // O's loads are done before the next unit's Q is published (its first
-      // P V overwrites O); the row sums are read before they are rewritten
+      // O's loads are done before the next unit's first P is published (its
+      // first P V overwrites O); the row sums are read before they are
+      // rewritten
       tc_fence_before();
       if (!quarter_sync()) break;
       k += T;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // a Q copy an abort left in flight
   }
 
   tc_fence_before();
