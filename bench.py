@@ -520,8 +520,10 @@ def run_extend_ours(args, rank, world, local_rank):
                      "peak_source": src if tensor_bound else hsrc,
                      "achieved_tflops": flops / layer_s / 1e12,
                      "algorithmic_bytes_per_launch": nbytes, "num_splits": S,
-                     "kernel": "extend_mma_kernel (causal extend attention, one launch per "
-                               "layer" + (", + extend_merge_kernel" if S > 1 else "") + ")",
+                     "kernel": ("extend_umma_kernel (tcgen05" if p.page_size % 16 == 0
+                                else "extend_mma_kernel (warp-level mma.sync") +
+                               ", causal extend attention, one launch per layer" +
+                               (", + extend_merge_kernel" if S > 1 else "") + ")",
                      "kernel_us_mean": layer_s * 1e6,
                      "kernel_time_from": "graph of the layers' attention launches alone, CUDA "
                                          "events over its timed replays / layers",
@@ -639,9 +641,10 @@ def run_cascade_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "traffic": None, "peak_source": src,
-                     "kernel": "CascadeDecoder: extend_mma_kernel (prefix, no causal mask) + "
-                               "extend_merge_kernel + decode_mma_kernel (suffixes) + "
-                               "merge_lse_kernel, per layer",
+                     "kernel": "CascadeDecoder: " +
+                               ("extend_mma_kernel" if cas.prefix_kernel else "extend_umma_kernel") +
+                               " (prefix, no causal mask) + extend_merge_kernel + "
+                               "decode_mma_kernel (suffixes) + merge_lse_kernel, per layer",
                      "kernel_us_mean": layer_s * 1e6,
                      "kernel_time_from": "whole steady step (bind + layers) / layers",
                      "bytes_counted": "each distinct page once (the shared prefix once per layer)"},
