@@ -380,10 +380,17 @@ __global__ void __launch_bounds__(kMThreads, 2)
         const Unit &u = c.it.un;
         const int tok = u.t0 + c.i * kMT + r;
         const ReqIndex ri = pl.pref ? req_index_cached(ws, s_base, u.b) : req_index(ws, u.b);
-        if (tok < u.t1 && ri.ok) v = *index_src(ws, pl, ri, tok);
+        if (tok < u.t1 && ri.ok) {
+          // a 4-byte asynchronous copy: every thread's entries in flight at once
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&s_idx[tile][r])),
+                       "l"(index_src(ws, pl, ri, tok))
+                       : "memory");
+          continue;
+        }
       }
       s_idx[tile][r] = v;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
   }
 
