@@ -2,8 +2,11 @@
 // warp (workspace.py page, bullet 14: decode_o_part / decode_ml_part):
 //   M = max over non-empty splits of m_s,  w_s = l_s * exp(m_s - M),
 //   out = sum_s w_s o_s / sum_s w_s,  lse = M + ln(sum_s w_s).
-// Lane s holds split s's (m, l); the partial rows are then read four at a
-// time with independent L2 loads (they may come from other CTAs).
+// Splits come in chunks of 32, lane s holding split s's (m, l); the chunk's
+// first eight partial rows are loaded together with the (m, l) pairs and the
+// rest eight at a time, every load of a group in flight at once (they may
+// come from other CTAs, so L2 loads).  A row of more than 32 splits rebases
+// the earlier chunks' sums onto the running maximum.
 #pragma once
 
 #include "common.cuh"
@@ -14,45 +17,51 @@ template <int D>
 __device__ __forceinline__ void merge_row(const float *ml, const float *op, int n, int lane,
                                           float &M_out, float &den_out, float4 &acc_out) {
   constexpr int NV = D / 4;  // float4 vectors per row
+  constexpr int GS = 8;      // partial rows per group of loads
   static_assert(NV <= 32, "one float4 per lane");
   const float2 *ml2 = reinterpret_cast<const float2 *>(ml);
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) {
-    const float2 v = __ldcg(ml2 + s);
-    if (v.y > 0.f) M = fmaxf(M, v.x);
-  }
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, d));
+  float M = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < n; s0 += 32) {
-      float w = 0.f;
-      if (s0 + lane < n) {
-        const float2 v = __ldcg(ml2 + s0 + lane);
-        w = v.y > 0.f ? v.y * expf(v.x - M) : 0.f;
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    const int m = min(32, n - s0);
+    float2 v = make_float2(-INFINITY, 0.f);
+    if (lane < m) v = __ldcg(ml2 + s0 + lane);
+    float4 oj[GS];
+#pragma unroll
+    for (int t = 0; t < GS; ++t)
+      oj[t] = (t < m && lane < NV)
+                  ? __ldcg(reinterpret_cast<const float4 *>(op + (long long)(s0 + t) * D) + lane)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mc = v.y > 0.f ? v.x : -INFINITY;
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, d));
+    const float Mn = fmaxf(M, mc);
+    if (Mn == -INFINITY) continue;  // no non-empty split yet
+    if (M != -INFINITY && Mn != M) {
+      const float sc = expf(M - Mn);
+      den *= sc;
+      acc = make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+    }
+    M = Mn;
+    const float w = v.y > 0.f ? v.y * expf(v.x - M) : 0.f;
+    den += w;
+    for (int j = 0; j < m; j += GS) {
+      if (j > 0) {
+#pragma unroll
+        for (int t = 0; t < GS; ++t)
+          oj[t] = (j + t < m && lane < NV)
+                      ? __ldcg(reinterpret_cast<const float4 *>(op + (long long)(s0 + j + t) * D) +
+                               lane)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      den += w;
-      const int m = min(32, n - s0);
-      for (int j = 0; j < m; j += 4) {
-        float wj[4];
-        float4 oj[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) wj[t] = __shfl_sync(0xffffffffu, w, (j + t) & 31);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          oj[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j + t < m && lane < NV)
-            oj[t] = __ldcg(reinterpret_cast<const float4 *>(op + (long long)(s0 + j + t) * D) + lane);
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (j + t < m && wj[t] > 0.f) {
-            acc.x = fmaf(wj[t], oj[t].x, acc.x);
-            acc.y = fmaf(wj[t], oj[t].y, acc.y);
-            acc.z = fmaf(wj[t], oj[t].z, acc.z);
-            acc.w = fmaf(wj[t], oj[t].w, acc.w);
-          }
+      for (int t = 0; t < GS; ++t) {
+        const float wj = __shfl_sync(0xffffffffu, w, (j + t) & 31);
+        if (j + t < m && wj > 0.f) {
+          acc.x = fmaf(wj, oj[t].x, acc.x);
+          acc.y = fmaf(wj, oj[t].y, acc.y);
+          acc.z = fmaf(wj, oj[t].z, acc.z);
+          acc.w = fmaf(wj, oj[t].w, acc.w);
         }
       }
     }
