@@ -276,10 +276,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
   __shared__ __align__(8) uint64_t k_full[kUKStages], k_empty[kUKStages];
   __shared__ __align__(8) uint64_t v_full[kUVStages], v_empty[kUVStages];
   __shared__ __align__(8) uint64_t s_full[kUSBufs], buf_free[kUSBufs];
-  // p_full rotates over the S buffers: the Q K^T of tiles kk + 1 and kk + 2
-  // may already be done when the MMA thread looks for tile kk's P, so the
-  // softmax could publish those too; one barrier would then have passed the
-  // phase looked for
+  // p_full rotates over the S buffers: the Q K^T of the next tiles may
+  // already be done when the P V warp looks for tile kk's P, so the softmax
+  // could publish theirs too; one barrier would then have passed the phase
+  // looked for
   __shared__ __align__(8) uint64_t q_full, p_full[kUSBufs], drain[2];
   __shared__ __align__(8) uint64_t xbar[4];  // per lane quarter: its two softmax warps
   // Bad page bits of the CTA's i-th unit in s_ubad[i % 4], written by the V
