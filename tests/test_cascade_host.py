@@ -122,3 +122,18 @@ def test_suffix_length_limit():
     assert CascadeDecoder(ws, 3, 15 * 16, scale=0.125).suffix_view.max_seq_len == 16
     with pytest.raises(ValueError):
         CascadeDecoder(ws, 3, 16 * 16, scale=0.125)
+
+
+def test_prefix_kernel_choice():
+    # The prefix pass takes the tcgen05 extend kernel from 512 prefix tokens a
+    # split, the warp-level one below (its units too short for the 128-row
+    # CTAs' setup)
+    ws = Workspace(n_layers=1, pool_slots=512 * 16, n_q_heads=8, n_kv_heads=2, head_dim=64,
+                   page_size=16, max_batch=4, max_reqs=4, max_pages_per_req=512,
+                   max_splits=16, max_total_tokens=8192, device="cpu")
+    ws.req_pool_indices[:2] = torch.tensor([0, 1], dtype=torch.int32)
+    ws.seq_lens[:2] = torch.tensor([4200, 4300], dtype=torch.int32)
+    for splits, kernel in [(1, 0), (8, 0), (9, A.PKV_FLAG_EXTEND_WARP_MMA),
+                           (16, A.PKV_FLAG_EXTEND_WARP_MMA)]:
+        cas = CascadeDecoder(ws, 2, 4096, scale=0.125, prefix_splits=splits)
+        assert cas.prefix_kernel == kernel, splits
