@@ -596,11 +596,15 @@ __global__ void __launch_bounds__(kUThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       int bad = 0;
       bool ok = true;
-      if (T > 0 && !q_pre) {
-        q_copy(x);
-        q_publish();
+      if (T > 0) {
+        if (!q_pre) {
+          q_copy(x);
+          q_publish();
+        }
+        // consumed here: a unit without tiles in between keeps it for the
+        // next unit that has some
+        q_pre = false;
       }
-      q_pre = false;
       bool pre = false;  // the next unit's Q is being copied
       for (int t = 0; t < T && ok; ++t) {
         const int kk = k + t, b = kk % kUSBufs;

@@ -192,12 +192,14 @@ def test_extend_f32_output_one_new_token(cuda):
 
 def test_extend_long_prefix_sampled(cuda):
     # A 4096-token prefix with a 256-token chunk: many tiles per unit,
-    # compared on sampled rows.
+    # compared on sampled rows.  40 splits: rows of more than 32 partials,
+    # merged in two chunks, and (the 700-token request's splits past its
+    # end) units without tiles between units with tiles in a CTA's list.
     rng = np.random.default_rng(3)
     T = 256 + 64
     rows = sorted({(int(rng.integers(T)), int(rng.integers(32))) for _ in range(40)}
                   | {(0, 0), (T - 1, 31), (255, 5)})
-    for S in (1, 6):
+    for S in (1, 6, 40):
         got, ref, want, _ = run_extend(cuda, lens=(4096, 700), qo=(256, 64), Hq=32, Hkv=8,
                                        D=128, P=16, seed=4300, NL=1, layer=0, rows=rows, S=S)
         _compare(got, ref, want, f"long prefix S={S}")

@@ -117,8 +117,10 @@ def test_cross_split_agreement(cuda):
     # fp32 outputs from different split counts agree within 1e-3.
     p = W.workload("gqa4_long_65536", batch=2, shrink=32, steps=1)
     outs = []
+    # (64 splits: rows of more than 32 partials, merged in two chunks)
     for S, fused, fl in ((1, False, 0), (2, False, 0), (9, False, 0), (32, False, 0),
-                         (2, True, 0), (9, True, 0), (32, True, 0), (9, True, FIXED)):
+                         (64, False, 0), (2, True, 0), (9, True, 0), (32, True, 0),
+                         (64, True, 0), (9, True, FIXED)):
         ws = Workspace.from_problem(p, max_splits=S)
         run = DecodeRunner(ws, p.batch, num_splits=S, flags=A.PKV_FLAG_OUT_F32 | fl,
                            scale=p.scale, fused=fused)
