@@ -431,7 +431,7 @@ def run_extend_ours(args, rank, world, local_rank):
         for l in range(NL):
             if not attn_only:
                 A.pkv_extend_append(ws, B, l, qo_dev, mq, kd[l], vd[l], s)
-            A.pkv_extend_attn(ws, B, l, qo_dev, mq, qd[l], out[l], p.scale, S, 0, s)
+            A.pkv_extend_attn(ws, B, l, qo_dev, mq, qd[l], out[l], p.scale, S, args.flags, s)
 
     def capture(attn_only):
         g = torch.cuda.CUDAGraph()
@@ -520,7 +520,9 @@ def run_extend_ours(args, rank, world, local_rank):
                      "peak_source": src if tensor_bound else hsrc,
                      "achieved_tflops": flops / layer_s / 1e12,
                      "algorithmic_bytes_per_launch": nbytes, "num_splits": S,
-                     "kernel": ("extend_umma_kernel (tcgen05" if p.page_size % 16 == 0
+                     "kernel": ("extend_umma_kernel (tcgen05"
+                                if p.page_size % 16 == 0
+                                and not args.flags & A.PKV_FLAG_EXTEND_WARP_MMA
                                 else "extend_mma_kernel (warp-level mma.sync") +
                                ", causal extend attention, one launch per layer" +
                                (", + extend_merge_kernel" if S > 1 else "") + ")",
