@@ -431,7 +431,11 @@ def run_extend_ours(args, rank, world, local_rank):
         for l in range(NL):
             if not attn_only:
                 A.pkv_extend_append(ws, B, l, qo_dev, mq, kd[l], vd[l], s)
-            A.pkv_extend_attn(ws, B, l, qo_dev, mq, qd[l], out[l], p.scale, S, args.flags, s)
+            # layers after the first may start before the previous launch ends:
+            # the lengths, tables and cached K/V rows are older than it
+            early = A.PKV_FLAG_PLAN_EARLY if l > 0 else 0
+            A.pkv_extend_attn(ws, B, l, qo_dev, mq, qd[l], out[l], p.scale, S,
+                              args.flags | early, s)
 
     def capture(attn_only):
         g = torch.cuda.CUDAGraph()

@@ -80,7 +80,17 @@ enum {
                                 on this stream (or by the host), so the kernel may read
                                 them and start loading K/V before the previous kernel
                                 finishes (programmatic dependent launch); q, k_new and
-                                all outputs are still touched only after it finishes  */
+                                all outputs are still touched only after it finishes.
+                                pkv_extend_attn (tcgen05 kernel): the same for seq_lens,
+                                qo_indptr, req_pool_indices, page_table and the pool
+                                rows of each request's cached tokens (those before its
+                                new tokens; all of its context with
+                                PKV_FLAG_EXTEND_FULL): the CTAs order their units and
+                                load those rows early; tiles holding new tokens, q and
+                                the outputs wait for the previous kernel.  Either way
+                                device error bits may be OR-ed into ws->err before the
+                                previous kernel ends, so the operation just before must
+                                not be the one that clears it                          */
   PKV_FLAG_FIXED_CHUNK = 64,  /* pkv_decode_layer, tensor-core kernel: cut the KV axis
                                  into pkv_decode_attn's fixed chunks instead of
                                  apportioned splits */
@@ -386,7 +396,8 @@ pkv_status pkv_decode_attn_static_scratch(const pkv_workspace *ws, int batch, in
  *               other page sizes or PKV_FLAG_EXTEND_WARP_MMA: the warp-level
  *               mma.sync kernel (64 rows per block).  Both give the same
  *               results up to rounding.
- *   flags       PKV_FLAG_OUT_F32; PKV_FLAG_WRITE_LSE (also lse[query row * Hq + h] =
+ *   flags       PKV_FLAG_OUT_F32; PKV_FLAG_PLAN_EARLY (see its definition);
+ *               PKV_FLAG_WRITE_LSE (also lse[query row * Hq + h] =
  *               max score + ln(sum exp) in ws->lse, which needs batch *
  *               max_qo_len <= max_batch); PKV_FLAG_EXTEND_FULL (no causal
  *               mask: every query row of request b attends all seq_lens[b]

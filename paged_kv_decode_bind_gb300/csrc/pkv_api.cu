@@ -304,7 +304,7 @@ pkv_status pkv_extend_attn(const pkv_workspace *ws, int batch, int layer,
   pkv_status st = extend_common(ws, batch, layer, qo_indptr, max_qo_len, q, out);
   if (st != PKV_OK) return st;
   if (flags & ~(PKV_FLAG_OUT_F32 | PKV_FLAG_WRITE_LSE | PKV_FLAG_EXTEND_FULL |
-                PKV_FLAG_EXTEND_WARP_MMA))
+                PKV_FLAG_EXTEND_WARP_MMA | PKV_FLAG_PLAN_EARLY))
     return PKV_ERR_INVALID;
   if (num_splits < 1) return PKV_ERR_INVALID;
   // lse[query row, Hq] lives in ws->lse ([max_batch, Hq]): room for every row

@@ -138,6 +138,7 @@ def test_extend_host_validation():
         (dict(), 2, 0, f, 4, f, f, P.PKV_FLAG_WRITE_LSE, P.PKV_ERR_CAPACITY),        # 8 rows
         (dict(), 0, 0, f, 4, f, f, 0, P.PKV_OK),                                     # no batch
         (dict(), 1, 0, f, 0, f, f, 0, P.PKV_OK),                                     # no tokens
+        (dict(), 0, 0, f, 4, f, f, P.PKV_FLAG_PLAN_EARLY, P.PKV_OK),                 # accepted
     ]
     for kw, batch, layer, qo, mq, q, out, flags, status in cases:
         got = X(_ws(**kw), batch, layer, qo, mq, q, out, 0.1, num_splits=1, flags=flags,

@@ -276,6 +276,78 @@ def test_extend_graph_replay_bitexact(cuda):
     assert torch.equal(out, eager)
 
 
+@pytest.mark.parametrize("S,full", [(1, False), (3, False), (1, True)])
+def test_extend_plan_early_layers(cuda, S, full):
+    # Layers after the first with PKV_FLAG_PLAN_EARLY: the tcgen05 kernel
+    # orders its units and loads the cached tokens' K/V before the previous
+    # launch (this layer's append) ends, so its CTAs start on the SMs the
+    # previous kernel frees.  Outputs equal those of plain launches bit for
+    # bit, eagerly and replayed from a graph, with several units per CTA.
+    NL, lens, qo = 3, [900, 1500, 700, 1200], [200, 96, 160, 64]
+    if full:
+        lens, qo = [1500, 900, 700, 1200], [32, 32, 32, 32]
+    p = W.make_problem("extend_early", batch=4, n_layers=NL, n_q_heads=32, n_kv_heads=8,
+                       head_dim=128, page_size=16, seq_lens=lens, seed=6100 + S)
+    T, mq = sum(qo), max(qo)
+    q = [W.normal_bf16((T, 32, 128), 6200 + l).to(cuda) for l in range(NL)]
+    kn = [W.normal_bf16((T, 8, 128), 6300 + l).to(cuda) for l in range(NL)]
+    vn = [W.normal_bf16((T, 8, 128), 6400 + l).to(cuda) for l in range(NL)]
+    qo_dev = _indptr(qo, cuda)
+    base = A.PKV_FLAG_EXTEND_FULL if full else 0
+
+    def run(early, graph):
+        ws = Workspace.from_problem(p, max_splits=mq * S if S > 1 else 1)
+        out = torch.zeros((NL, T, 32, 128), dtype=torch.bfloat16, device=cuda)
+
+        def step(s=None):
+            for l in range(NL):
+                if not full:  # the cascade's prefix pass has no new tokens in the pool
+                    A.pkv_extend_append(ws, 4, l, qo_dev, mq, kn[l], vn[l], stream=s)
+                fl = base | (A.PKV_FLAG_PLAN_EARLY if early and l > 0 else 0)
+                A.pkv_extend_attn(ws, 4, l, qo_dev, mq, q[l], out[l], p.scale, num_splits=S,
+                                  flags=fl, stream=s)
+
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side), torch.cuda.graph(g, stream=side):
+                step(side)
+            torch.cuda.current_stream().wait_stream(side)
+            for _ in range(2):
+                g.replay()
+        else:
+            step()
+        torch.cuda.synchronize()
+        assert int(ws.err.item()) == 0
+        return out
+
+    ref = run(False, False)
+    assert torch.equal(run(True, False), ref)
+    assert torch.equal(run(True, True), ref)
+    # the plain launches against the oracle on a sample of layer 2's rows
+    slots = _slots(p)
+    kb, vb = R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool)
+    rng = np.random.default_rng(6500 + S)
+    rows = sorted({(int(rng.integers(T)), int(rng.integers(32))) for _ in range(40)})
+    if full:
+        qb = R.tensor_bits(q[2].cpu())
+        r0, parts = 0, []
+        for b in range(4):
+            o, _ = R.decode_attention(qb[r0:r0 + qo[b]], kb, vb, 2, [slots[b][:lens[b]]] * qo[b],
+                                      p.scale, 8)
+            parts.append(o)
+            r0 += qo[b]
+        _compare(ref[2].to(torch.float64).cpu().numpy(), np.concatenate(parts), rows,
+                 "early full")
+    else:
+        kb = R.extend_append(kb, 2, slots, qo, R.tensor_bits(kn[2].cpu()))
+        vb = R.extend_append(vb, 2, slots, qo, R.tensor_bits(vn[2].cpu()))
+        oracle_out, _ = R.extend_attention(R.tensor_bits(q[2].cpu()), kb, vb, 2, slots, qo,
+                                           p.scale, 8, rows=rows)
+        _compare(ref[2].to(torch.float64).cpu().numpy(), oracle_out, rows, f"early S={S}")
+
+
 def test_extend_one_token_matches_decode_kernel(cuda):
     # One new token per request: the extend kernel and the decode kernel
     # compute the same attention; their fp32 outputs agree to the extend
