@@ -874,7 +874,9 @@ cudaError_t launch_umma_one(const XArgs &a, cudaStream_t st) {
   if (grid < cap) {
     e = launch_pdl(kern, dim3(grid), dim3(kUThreads), C::SMEM, st, a, tmk, tmv);
   } else {
-    kern<<<grid, kUThreads, C::SMEM, st>>>(a, tmk, tmv);
+    XArgs b = a;  // nothing to overlap: the plain kernel
+    b.flags &= ~PKV_FLAG_PLAN_EARLY;
+    kern<<<grid, kUThreads, C::SMEM, st>>>(b, tmk, tmv);
     e = cudaGetLastError();
   }
   if (a.S > 1 && e == cudaSuccess) e = launch_extend_merge(a, D, st);

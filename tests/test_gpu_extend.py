@@ -276,16 +276,19 @@ def test_extend_graph_replay_bitexact(cuda):
     assert torch.equal(out, eager)
 
 
-@pytest.mark.parametrize("S,full", [(1, False), (3, False), (1, True)])
-def test_extend_plan_early_layers(cuda, S, full):
-    # Layers after the first with PKV_FLAG_PLAN_EARLY: the tcgen05 kernel
-    # orders its units and loads the cached tokens' K/V before the previous
-    # launch (this layer's append) ends, so its CTAs start on the SMs the
-    # previous kernel frees.  Outputs equal those of plain launches bit for
-    # bit, eagerly and replayed from a graph, with several units per CTA.
-    NL, lens, qo = 3, [900, 1500, 700, 1200], [200, 96, 160, 64]
+@pytest.mark.parametrize("S,full,big", [(1, False, False), (2, False, False), (1, True, False),
+                                        (3, False, True)])
+def test_extend_plan_early_layers(cuda, S, full, big):
+    # Layers after the first with PKV_FLAG_PLAN_EARLY: with CTA slots to
+    # spare the tcgen05 kernel orders its units and loads the cached tokens'
+    # K/V before the previous launch (this layer's append) ends; a grid that
+    # fills every slot launches plainly and ignores the flag.  Outputs equal
+    # those of plain launches bit for bit, eagerly and replayed from a graph.
+    NL, lens, qo = 3, [900, 1500, 700, 1200], [64, 40, 64, 17]
     if full:
         lens, qo = [1500, 900, 700, 1200], [32, 32, 32, 32]
+    if big:  # 672 units: several per CTA
+        qo = [200, 96, 160, 64]
     p = W.make_problem("extend_early", batch=4, n_layers=NL, n_q_heads=32, n_kv_heads=8,
                        head_dim=128, page_size=16, seq_lens=lens, seed=6100 + S)
     T, mq = sum(qo), max(qo)
@@ -328,7 +331,7 @@ def test_extend_plan_early_layers(cuda, S, full):
     # the plain launches against the oracle on a sample of layer 2's rows
     slots = _slots(p)
     kb, vb = R.tensor_bits(p.k_pool), R.tensor_bits(p.v_pool)
-    rng = np.random.default_rng(6500 + S)
+    rng = np.random.default_rng(6500 + S + 2 * big)
     rows = sorted({(int(rng.integers(T)), int(rng.integers(32))) for _ in range(40)})
     if full:
         qb = R.tensor_bits(q[2].cpu())
