@@ -1014,6 +1014,11 @@ def _sweep_entry(wl, b, s):
             "peak_source": src, "bind_us": s["dt_bind"] / s["K"] * 1e6,
             "algorithmic_bytes_per_layer": s["mean_layer_bytes"],
             "l2_flushed_between_steps": s["flush"], "target_70": (wl, b) in TARGET_70,
+            # ncu DRAM bytes per attention launch (committed one-pass capture of
+            # this workload on the current kernel source), scaled to this run's
+            # algorithmic bytes; None when there is none
+            "traffic": traffic_for(kernel_src_hash(), _traffic_key(wl, s["p"].batch),
+                                   s["mean_layer_bytes"]),
             "clocks": s["clk"], "device_err_bits": s["errbits"]}
 
 
