@@ -1,7 +1,10 @@
 """Seeded random sweeps of the GPU paths against the oracle: shapes, page
 sizes, lengths, new-token counts and split counts drawn from a fixed seed, so
 that combinations the hand-written cases do not name still get compared
-(every case is reproducible from its index)."""
+(every case is reproducible from its index).  PKV_RANDOM_CASES=n runs cases
+0 .. n-1 of each sweep instead of the default counts."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -14,6 +17,11 @@ from parity import check_attention, run_steps
 from test_gpu_extend import KERNS, _indptr, _slots, _compare, run_extend
 
 pytestmark = pytest.mark.gpu
+_N = int(os.environ.get("PKV_RANDOM_CASES", "0"))
+
+
+def _cases(default):
+    return range(_N or default)
 
 
 def _shape(rng, g16_hkv=(1, 2), hkv=(1, 2, 4)):
@@ -22,7 +30,7 @@ def _shape(rng, g16_hkv=(1, 2), hkv=(1, 2, 4)):
     return G, Hkv, int(rng.choice([64, 128]))
 
 
-@pytest.mark.parametrize("case", range(24))
+@pytest.mark.parametrize("case", _cases(24))
 def test_random_causal_extend(cuda, case):
     # Causal extend, both kernels, 1 / 2 / 7 / 33 splits, page sizes 16 and 32.
     rng = np.random.default_rng(7100 + case)
@@ -44,7 +52,7 @@ def test_random_causal_extend(cuda, case):
         _compare(got, ref, want, f"case {case} {kern} S={S}")
 
 
-@pytest.mark.parametrize("case", range(16))
+@pytest.mark.parametrize("case", _cases(16))
 def test_random_full_extend(cuda, case):
     # No causal mask (a cascade's prefix pass): every query row of request b
     # attends keys [0, L_b), more rows than keys allowed, empty contexts
@@ -85,7 +93,7 @@ def test_random_full_extend(cuda, case):
         check_attention(out.to(torch.float64).cpu().numpy(), ref, f"case {case} {kern} S={S}")
 
 
-@pytest.mark.parametrize("case", range(24))
+@pytest.mark.parametrize("case", _cases(24))
 def test_random_decode(cuda, case):
     # Steady decode steps, fused and unfused, the tensor-map and the gather
     # producers, page sizes 1 (flat) to 48, batches 1 to 40, 1 to 16 splits.
