@@ -9,12 +9,15 @@
 // A CTA owns 128 query rows of one (request, KV head): 128 / G new tokens x
 // the G query heads of the group, row r = (token r / G, head r % G), so a key
 // tile is read once for the whole group.  Per 128-key tile:
-//   S = Q K^T   tcgen05.mma M = 128, N = 128, K = D in steps of 16.  Q and the
-//               tile's K sit K-major in shared memory with the 128-byte
-//               swizzle ([64-column half][rows][128 B]); S lands in one of
-//               three 128-column TMEM buffers, so later tiles' products run
-//               while this tile's softmax reads its own.  (N = 128: measured,
-//               an N = 64 MMA runs at about half the tensor rate.)
+//   S = Q K^T   tcgen05.mma M = 128, N = 128, K = D in steps of 16.  Q is the
+//               A operand from TMEM (D / 2 columns of bf16 pairs a row, stored
+//               by the softmax warps), which leaves shared memory to a
+//               3-stage K ring; the tile's K sits K-major in shared memory
+//               with the 128-byte swizzle ([64-column half][rows][128 B]); S
+//               lands in one of two 128-column TMEM buffers, so the next
+//               tile's product runs while this tile's softmax reads its own.
+//               (N = 128: measured, an N = 64 MMA runs at about half the
+//               tensor rate.)
 //   softmax     two threads per row, 64 keys each: a thread loads its half
 //               row of S from TMEM (tcgen05.ld), applies the causal mask,
 //               swaps its partial maximum with the other half's thread
@@ -33,8 +36,8 @@
 // reference, so the result is unchanged.
 //
 // Warps: 0 and 10 issue the tensor-map boxes of each tile's K and V (per
-// 16-token page piece one box per 64-column half) into a 2-stage K ring and a
-// 3-stage V ring; 1 issues every tile's Q K^T and 11 every P V (each from one
+// 16-token page piece one box per 64-column half) into 3-stage K and V
+// rings; 1 issues every tile's Q K^T and 11 every P V (each from one
 // lane chosen by elect.sync while the whole warp runs the loop), tracking
 // their completion with tcgen05.commit on mbarriers; 2-9 load Q, run the
 // softmax (two warps per TMEM lane quarter, 64 keys of a tile each) and write
@@ -52,16 +55,17 @@ namespace {
 
 constexpr int kUM = 128;          // query rows per CTA (TMEM lanes)
 constexpr int kUN = 128;          // keys per tile (N of Q K^T: the MMA's full rate)
-constexpr int kUKStages = 2;      // K ring: a tile's K is free once its Q K^T is done
+constexpr int kUKStages = 3;      // K ring: a tile's K is free once its Q K^T is done
 constexpr int kUVStages = 3;      // V ring: free once the tile's P V is done
-constexpr int kUSBufs = 3;        // S / P buffers in TMEM
+constexpr int kUSBufs = 2;        // S / P buffers in TMEM
 constexpr int kUSoftWarps = 8;    // two per TMEM lane quarter, 64 keys of a tile each
 // warps: K loader, Q K^T issuer, softmax, V loader, P V issuer
 constexpr int kUThreads = (4 + kUSoftWarps) * 32;
 constexpr int kUVWarp = 2 + kUSoftWarps;
 constexpr int kUPVWarp = 3 + kUSoftWarps;
-constexpr int kUTmemCols = 512;   // three S buffers of 128 columns, O of D <= 128
+constexpr int kUTmemCols = 512;   // two S buffers of 128 columns, O of D <= 128, Q of D / 2
 constexpr int kUOCol = kUSBufs * kUN;  // O's first column
+constexpr int kUQCol = kUOCol + 128;   // Q's first column: bf16 pairs, D / 2 columns
 constexpr float kURescale = 8.f;  // raise a row's reference max only past this (log2)
 constexpr int kUSortMax = 256;    // (query block, split, request) triples ordered by cost
 
@@ -69,16 +73,15 @@ template <int D>
 struct UCfg {
   static constexpr int HALVES = D / 64;
   static constexpr int KSTEPS = D / 16;
-  static constexpr int QHALF = kUM * 128;   // one 64-column half of Q
   static constexpr int KVHALF = kUN * 128;  // one half of a tile's K (or V)
   static constexpr int KBYTES = HALVES * KVHALF;  // a tile's K (or V)
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + HALVES * QHALF;
+  static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + kUKStages * KBYTES;
   static constexpr int SMEM = OFF_V + kUVStages * KBYTES + 1024;  // + alignment slack
   static constexpr uint32_t PIECE_TX = HALVES * 16 * 128;  // K (or V) of 16 tokens
   static_assert(D == 64 || D == 128, "one or two 64-column halves");
-  static_assert(D <= kUTmemCols - kUOCol, "O fits the allocation");
+  static_assert(D <= kUQCol - kUOCol, "O fits below Q");
+  static_assert(kUQCol + D / 2 <= kUTmemCols, "Q fits the allocation");
   static_assert(SMEM + 8192 <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -105,16 +108,8 @@ __host__ __device__ constexpr uint32_t umma_idesc(int M, int N, int b_mn_major) 
 // Measured: an MMA stream issued from a lone divergent lane ran 3x slower
 // while other warps of its SM sub-partition kept the issue slots busy (the
 // softmax warps here); issued this way it ran within 2 % of its rate alone.
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                     int accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// As umma, with the A operand (M x 16, bf16 pairs per 32-bit column) in TMEM.
+// Both products take their A operand (M x 16, bf16 pairs per 32-bit column)
+// from TMEM and B from a shared-memory descriptor.
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                         uint32_t idesc, int accumulate) {
   asm volatile(
@@ -487,7 +482,6 @@ __global__ void __launch_bounds__(kUThreads, 1)
     constexpr uint32_t kIdO = umma_idesc(kUM, D, 1);    // O += P V: V MN-major
     // descriptors of Q and of stage 0's K and V; every other operand is one
     // of these plus a byte offset (in 16-byte units, inside the start field)
-    const uint64_t dq = umma_desc(sbase + C::OFF_Q, 16, 1024);
     const uint64_t dk = umma_desc(sbase + C::OFF_K, 16, 1024);
     const uint64_t dv = umma_desc(sbase + C::OFF_V, C::KVHALF, 1024);
     int k = 0, ul = 0;
@@ -514,11 +508,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
           const uint64_t ks0 = (uint64_t)((s * C::KBYTES) >> 4);
 #pragma unroll
           for (int ks = 0; ks < C::KSTEPS; ++ks) {
-            // k-step ks: half ks / 4, 32 bytes further per step inside the row
-            constexpr int kQH = C::QHALF, kKH = C::KVHALF;
-            const uint64_t qo = (uint64_t)(((ks >> 2) * kQH + (ks & 3) * 32) >> 4);
-            const uint64_t ko = (uint64_t)(((ks >> 2) * kKH + (ks & 3) * 32) >> 4);
-            umma(tmem + b * kUN, dq + qo, dk + ks0 + ko, kIdS, ks > 0);
+            // k-step ks: Q's columns 8 ks .. 8 ks + 7 (16 dims as bf16 pairs);
+            // K's half ks / 4, 32 bytes further per step inside the rows
+            const uint64_t ko = (uint64_t)(((ks >> 2) * C::KVHALF + (ks & 3) * 32) >> 4);
+            umma_ts(tmem + b * kUN, tmem + kUQCol + ks * 8, dk + ks0 + ko, kIdS, ks > 0);
           }
           umma_commit(&s_full[b]);
           umma_commit(&k_empty[s]);
@@ -573,26 +566,34 @@ __global__ void __launch_bounds__(kUThreads, 1)
       if (lane == 0) mbar_arrive(&xbar[wq]);
       return wait(&xbar[wq], (xphase++) & 1);
     };
-    // half hf of this thread's row of a unit's Q into the K-major Q tile
-    // (swizzled; zeros past the unit's tokens), by 16-byte cp.async
-    auto q_copy = [&](const XUnit &y) {
+    // half hf of this thread's row of a unit's Q (zeros past the unit's
+    // tokens), the row's D / 4 columns of bf16 pairs in Q's TMEM columns
+    auto q_src = [&](const XUnit &y, bool &vy) -> const uint4 * {
       const int iy = y.j * TQ + row / G;
-      const bool vy = iy < y.n;
+      vy = iy < y.n;
       const long long qy = vy ? (long long)(y.q0 + iy) * Hq + y.g * G + row % G : 0;
-      const uint16_t *src = static_cast<const uint16_t *>(a.q) + qy * D;
-#pragma unroll
-      for (int c = hf * (D / 16); c < (hf + 1) * (D / 16); ++c)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                         sbase + C::OFF_Q + (c >> 3) * C::QHALF + row * 128 +
-                         (((c & 7) ^ (row & 7)) << 4)),
-                     "l"(src + c * 8), "r"(vy ? 16 : 0)
-                     : "memory");
-      asm volatile("cp.async.commit_group;" ::: "memory");
+      return reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + qy * D +
+                                             hf * (D / 2));
     };
-    // the copies landed, visible to the tensor cores: arrive on q_full
+    auto q_stage = [&](const XUnit &y) {
+      bool vy;
+      const uint4 *src = q_src(y, vy);
+      uint32_t r[D / 4];
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        const uint4 v = vy ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        r[4 * c] = v.x;
+        r[4 * c + 1] = v.y;
+        r[4 * c + 2] = v.z;
+        r[4 * c + 3] = v.w;
+      }
+      if constexpr (D == 128) tmem_st32(trow + kUQCol + hf * (D / 4), r);
+      else tmem_st16(trow + kUQCol + hf * (D / 4), r);
+    };
+    // the stores landed, ordered before the tensor cores' reads: arrive on q_full
     auto q_publish = [&]() {
-      asm volatile("cp.async.wait_all;" ::: "memory");
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full);
     };
@@ -611,14 +612,15 @@ __global__ void __launch_bounds__(kUThreads, 1)
       bool ok = true;
       if (T > 0) {
         if (!q_pre) {
-          q_copy(x);
+          q_stage(x);
           q_publish();
         }
         // consumed here: a unit without tiles in between keeps it for the
         // next unit that has some
         q_pre = false;
       }
-      bool pre = false;  // the next unit's Q is being copied
+      bool pre = false;  // the next unit has tiles: its Q is staged behind this unit's last P
+      XUnit y;
       for (int t = 0; t < T && ok; ++t) {
         const int kk = k + t, b = kk % kUSBufs;
         const int t0 = x.k0 + t * kUN + hf * KH;  // this thread's first key
@@ -628,14 +630,16 @@ __global__ void __launch_bounds__(kUThreads, 1)
         }
         tc_fence_after();
         if (t == T - 1) {
-          // Every Q K^T of the unit is done: the next unit's Q goes into the Q
-          // tile now, behind this tile's softmax, and is published with its
-          // P, so the next unit's Q K^T overlaps this unit's epilogue.
-          XUnit y;
+          // Every Q K^T of the unit is done: the next unit's Q rows are
+          // fetched into L2 now, stored into Q's columns behind this tile's
+          // P and published, so the next unit's Q K^T overlaps this unit's
+          // epilogue.
           for (int uj = ui + 1, u2; !pre && (u2 = unit_of(uj)) >= 0; ++uj) {
             y = xunit(a, u2, TQ, jmax);
             if (y.live && unit_tiles(y) > 0) {
-              q_copy(y);
+              bool vy;
+              const uint4 *src = q_src(y, vy);
+              if (vy) asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
               pre = true;
             }
           }
@@ -761,6 +765,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[b]);
         if (pre) {
+          q_stage(y);
           q_publish();
           q_pre = true;
         }
@@ -818,7 +823,6 @@ __global__ void __launch_bounds__(kUThreads, 1)
       if (!quarter_sync()) break;
       k += T;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");  // a Q copy an abort left in flight
   }
 
   tc_fence_before();
