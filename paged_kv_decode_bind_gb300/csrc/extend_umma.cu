@@ -317,9 +317,10 @@ __global__ void __launch_bounds__(kUThreads, 1)
       mbar_init(&s_full[i], 1);    // commit after the tile's Q K^T
       // commit after the tile's P V (P read from the buffer, O holds the tile);
       // the softmax waits here for O too.  One barrier per buffer: waiting
-      // on the P V of tile kk, the barrier's previous phase (tile kk - 3) is
-      // always complete, so a parity wait cannot pass early, as it could on a
-      // single barrier two phases behind once Q K^T runs ahead.
+      // on the P V of tile kk, the barrier's previous phase (tile kk - 2) is
+      // complete and its next (tile kk + 2) needs a P not yet written, so a
+      // parity wait cannot pass early, as it could on a single barrier two
+      // phases behind once Q K^T runs ahead.
       mbar_init(&buf_free[i], 1);
     }
     mbar_init(&q_full, kUSoftWarps);  // the softmax warps have written Q
@@ -469,7 +470,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
     // ------------------------------------------------------------ MMA ----
     // Two issuing warps, so that neither kind of product waits behind the
     // other's barriers: warp 1 issues every tile's S = Q K^T as soon as its K
-    // has landed and its S / P buffer is free (the P V of the tile three
+    // has landed and its S / P buffer is free (the P V of the tile two
     // before is done); the P V warp issues O += P V as soon as the softmax
     // has written the tile's P and its V has landed.  The tensor pipe takes
     // both streams; each warp's commits track its own products.
