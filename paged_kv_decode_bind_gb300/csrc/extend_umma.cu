@@ -481,8 +481,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
     };
     constexpr uint32_t kIdS = umma_idesc(kUM, kUN, 0);  // S = Q K^T: both K-major
     constexpr uint32_t kIdO = umma_idesc(kUM, D, 1);    // O += P V: V MN-major
-    // descriptors of Q and of stage 0's K and V; every other operand is one
-    // of these plus a byte offset (in 16-byte units, inside the start field)
+    // descriptors of stage 0's K and V; every other shared-memory operand is
+    // one of these plus a byte offset (in 16-byte units, inside the start
+    // field)
     const uint64_t dk = umma_desc(sbase + C::OFF_K, 16, 1024);
     const uint64_t dv = umma_desc(sbase + C::OFF_V, C::KVHALF, 1024);
     int k = 0, ul = 0;
